@@ -1,0 +1,77 @@
+"""CPU oracle for the tensor-parallel GEMM: the plain definition in fp64.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import this
+module; only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg
+of ``bench.py`` use it.  It shares no code with the device path.
+
+What every schedule computes ("Distributed GEMM", CUTLASS example 65 README,
+section "Getting started": the ``--m --n --k --l --alpha --beta`` problem,
+checked against "a single-device GEMM")::
+
+    D[l, i, j] = alpha * sum_k A[l, i, k] * B[l, k, j] + beta * C[l, i, j]
+
+Layouts (the pages do not fix them; this is the reading the device path
+implements): A is (L, M, K) row-major; B is stored as (L, N, K), i.e. its
+transpose, K innermost ("TN"); C and D are (L, M, N) row-major.
+
+The bf16 inputs are widened exactly to fp64 and the sum is taken in fp64 by
+one library matrix product (numpy ``matmul`` on float64), then scaled and
+offset elementwise.  When ``beta == 0`` C is not read at all (BLAS
+convention; the pages are silent), so NaNs in C do not reach D.
+
+Parity status: pinned (tests/test_oracle_pins.py: brute-force triple loop,
+closed forms, the statistical mean printed on the all_gather+matmul blog
+page, schedule invariance).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """Exact widening of bf16 bit patterns (uint16/int16) to float64."""
+    b = np.asarray(bits)
+    u = b.astype(np.uint16).astype(np.uint32) << np.uint32(16)
+    return u.view(np.float32).astype(np.float64)
+
+
+def gemm(A: np.ndarray, B_nk: np.ndarray, C, alpha: float, beta: float) -> np.ndarray:
+    """``alpha * A @ B + beta * C`` in fp64.
+
+    A: (L, M, K); B_nk: (L, N, K) (B stored transposed); C: (L, M, N) or
+    ``None`` (only allowed when ``beta == 0``).  All float64.  Returns (L, M, N).
+    """
+    A = np.asarray(A, dtype=np.float64)
+    B_nk = np.asarray(B_nk, dtype=np.float64)
+    if A.ndim != 3 or B_nk.ndim != 3:
+        raise ValueError("A and B must be 3-D (L, rows, K)")
+    L, M, K = A.shape
+    if B_nk.shape[0] != L or B_nk.shape[2] != K:
+        raise ValueError(f"shape mismatch A{A.shape} B{B_nk.shape}")
+    D = np.float64(alpha) * np.matmul(A, np.swapaxes(B_nk, 1, 2))
+    if beta != 0.0:
+        if C is None:
+            raise ValueError("beta != 0 needs C")
+        D = D + np.float64(beta) * np.asarray(C, dtype=np.float64)
+    return D
+
+
+def gemm_entries(A_rows: np.ndarray, B_rows: np.ndarray, C_block, alpha: float,
+                 beta: float) -> np.ndarray:
+    """The same definition on a sample: rows i of A against rows j of B.
+
+    A_rows: (R, K) fp64 rows of A (any batch), B_rows: (S, K) fp64 rows of the
+    stored (N, K) B of the same batch, C_block: (R, S) or ``None``.  Returns
+    the (R, S) block ``D[rows, cols]``.  Used to check outputs of problems too
+    large to evaluate in full.
+    """
+    D = np.float64(alpha) * (np.asarray(A_rows, np.float64) @ np.asarray(B_rows, np.float64).T)
+    if beta != 0.0:
+        D = D + np.float64(beta) * np.asarray(C_block, dtype=np.float64)
+    return D
+
+
+def flops(m: int, n: int, k: int, l: int) -> float:
+    """Algorithmic flop count of the whole problem: 2*M*N*K*L."""
+    return 2.0 * m * n * k * l

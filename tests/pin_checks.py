@@ -1,0 +1,213 @@
+"""Checks that pin the CPU oracle to facts outside itself.
+
+Each check takes the oracle functions as arguments and raises
+``AssertionError`` when they disagree with the fact it encodes.
+``test_oracle_pins.py`` runs them on the real oracle;
+``test_oracle_mutations.py`` runs them on oracles with planted mistakes and
+expects at least one check to fail for every mistake.
+"""
+
+from __future__ import annotations
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+
+from reduce_scatter_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _bits_to_f64(bits):
+    return synth.bf16_bits_to_f32_np(bits).astype(np.float64)
+
+
+def _rand(seed, stream, shape, dist=("uniform", -1.0, 1.0)):
+    return _bits_to_f64(synth.tensor_bits_np(seed, stream, shape, dist))
+
+
+def _int_valued(seed, stream, shape, lo=-8, hi=8):
+    """Small integers (exact in bf16); products and sums stay exact in fp64."""
+    rng = np.random.default_rng(seed * 131 + stream)
+    return rng.integers(lo, hi + 1, size=shape).astype(np.float64)
+
+
+def brute_gemm(A, B_nk, C, alpha, beta):
+    """Triple loop in Python floats (fp64), written apart from the oracle."""
+    L, M, K = A.shape
+    N = B_nk.shape[1]
+    D = [[[0.0] * N for _ in range(M)] for _ in range(L)]
+    for l in range(L):
+        for i in range(M):
+            for j in range(N):
+                acc = 0.0
+                for kk in range(K):
+                    acc += float(A[l, i, kk]) * float(B_nk[l, j, kk])
+                v = float(alpha) * acc
+                if beta != 0.0:
+                    v = v + float(beta) * float(C[l, i, j])
+                D[l][i][j] = v
+    return np.array(D, dtype=np.float64)
+
+
+# ----------------------------------------------------------------- gemm pins
+
+BRUTE_SHAPES = [(1, 1, 1, 1), (1, 3, 5, 7), (2, 4, 3, 9), (1, 8, 16, 5), (3, 2, 6, 4)]
+
+
+def check_brute_force_exact(gemm):
+    """Integer-valued inputs: every order of summation is exact, so equal bits."""
+    for idx, (L, M, N, K) in enumerate(BRUTE_SHAPES):
+        for alpha, beta in [(1.0, 0.0), (0.5, 1.0), (-2.0, 0.25), (0.0, 3.0)]:
+            A = _int_valued(idx, 1, (L, M, K))
+            B = _int_valued(idx, 2, (L, N, K))
+            C = _int_valued(idx, 3, (L, M, N))
+            got = gemm(A, B, C, alpha, beta)
+            want = brute_gemm(A, B, C, alpha, beta)
+            assert got.shape == want.shape, (got.shape, want.shape)
+            assert np.array_equal(got, want), (L, M, N, K, alpha, beta)
+
+
+def check_brute_force_random(gemm):
+    """bf16 uniform inputs: agreement within the fp64 summation error bound."""
+    for idx, (L, M, N, K) in enumerate(BRUTE_SHAPES):
+        A = _rand(100 + idx, 1, (L, M, K))
+        B = _rand(100 + idx, 2, (L, N, K))
+        C = _rand(100 + idx, 3, (L, M, N))
+        got = gemm(A, B, C, 0.75, -1.5)
+        want = brute_gemm(A, B, C, 0.75, -1.5)
+        # |error| <= gamma_K * sum|a||b| with gamma_K ~ K * 2^-53, plus the scaling steps.
+        bound = (K + 4) * 2.0 ** -52 * (np.abs(A) @ np.abs(np.swapaxes(B, 1, 2)) * 0.75 + 1.5 * np.abs(C) + 1.0)
+        assert np.all(np.abs(got - want) <= bound)
+
+
+def check_closed_forms(gemm):
+    L, M, N = 2, 5, 7
+    for K in (1, 16, 256, 8192):
+        ones_a = np.ones((L, M, K))
+        ones_b = np.ones((L, N, K))
+        C = _int_valued(7, 3, (L, M, N))
+        # all-ones: D = K * alpha + beta * C
+        D = gemm(ones_a, ones_b, C, 1.0, 0.0)
+        assert np.array_equal(D, np.full((L, M, N), float(K)))
+        D = gemm(ones_a, ones_b, C, 0.5, 1.0)
+        assert np.array_equal(D, 0.5 * K + C)
+    # identity B (N = K): D = alpha * A + beta * C
+    K = 12
+    A = _rand(8, 1, (L, M, K))
+    C = _rand(8, 3, (L, M, K))
+    eye = np.broadcast_to(np.eye(K), (L, K, K)).copy()
+    assert np.array_equal(gemm(A, eye, None, 1.0, 0.0), A)
+    assert np.array_equal(gemm(A, eye, C, 2.0, 0.5), 2.0 * A + 0.5 * C)
+    # one-hot B: column n of D is column perm[n] of A
+    N, K = 9, 6
+    A = _rand(9, 1, (L, M, K))
+    perm = np.array([3, 0, 5, 5, 1, 2, 4, 0, 3])
+    onehot = np.zeros((L, N, K))
+    onehot[:, np.arange(N), perm] = 1.0
+    D = gemm(A, onehot, None, 1.0, 0.0)
+    assert np.array_equal(D, A[:, :, perm])
+    # alpha = 0 leaves beta * C; beta = 0 ignores NaNs in C
+    Cn = np.full((L, M, N), np.nan)
+    D = gemm(A, onehot, Cn, 1.0, 0.0)
+    assert not np.any(np.isnan(D))
+    Cr = _rand(9, 3, (L, M, N))
+    assert np.array_equal(gemm(A, onehot, Cr, 0.0, 1.5), 1.5 * Cr)
+
+
+def check_printed_mean(gemm):
+    """The blog's printed output.mean() for U[0,1) inputs with K = 8192."""
+    with open(os.path.join(GOLDEN, "blog_allgather_matmul_mean.json")) as f:
+        g = json.load(f)
+    K = g["gemm"]["k"]
+    M, N = 96, 80
+    dist = ("uniform", 0.0, 1.0)
+    A = _bits_to_f64(synth.tensor_bits_np(1, 1, (1, M, K), dist))
+    B = _bits_to_f64(synth.tensor_bits_np(1, 2, (1, N, K), dist))
+    mean = float(gemm(A, B, None, 1.0, 0.0).mean())
+    # Standard error of the mean of M*N entries that share rows and columns:
+    # var(D_ij) = K * (E[a^2]E[b^2] - E[a]^2E[b]^2) = K * (1/9 - 1/16); rows and
+    # columns are shared, so take the conservative sqrt(var / min(M, N)) * 3
+    # plus the 2048-vs-printed gap.
+    se = math.sqrt(K * (1.0 / 9 - 1.0 / 16) / min(M, N))
+    assert abs(mean - g["printed_mean"]) <= 3 * se + abs(g["printed_mean"] - K / 4), (mean, se)
+    # a dropped or doubled factor would move the mean by K/4 or more
+    assert abs(mean - K / 4) < K / 64
+
+
+# ------------------------------------------------------------- schedule pins
+
+
+def check_schedule_invariance(run_schedule, gemm, schedules):
+    """Every schedule and TP gives the unsharded D (the torch module's
+    fallbacks define each fused op as collective-then-matmul)."""
+    for P in (1, 2, 4, 8):
+        L, M, N, K = 2, 2 * P, 3 * P, 4 * P
+        A = _int_valued(P, 1, (L, M, K))
+        B = _int_valued(P, 2, (L, N, K))
+        C = _int_valued(P, 3, (L, M, N))
+        for alpha, beta in [(1.0, 0.0), (0.5, 1.0), (2.0, -0.5)]:
+            want = gemm(A, B, C, alpha, beta)
+            for sched in schedules:
+                got = run_schedule(sched, A, B, C, alpha, beta, P)
+                assert np.array_equal(got, want), (sched, P, alpha, beta)
+        # random bf16 inputs: equal up to fp64 rounding of the RS partial sums
+        A = _rand(P, 1, (L, M, K))
+        B = _rand(P, 2, (L, N, K))
+        C = _rand(P, 3, (L, M, N))
+        want = gemm(A, B, C, 0.5, 1.0)
+        for sched in schedules:
+            got = run_schedule(sched, A, B, C, 0.5, 1.0, P)
+            assert np.allclose(got, want, rtol=0, atol=1e-12 * (np.abs(want).max() + 1)), (sched, P)
+
+
+def check_rotation_tables(slab_index, step_blocks, schedules):
+    """Rotation invariants the pages' loops fix, for P = 1..8:
+
+    * each rank handles every shard / slab exactly once;
+    * at every step the P ranks handle P distinct shards / slabs;
+    * AG: step 0 consumes the local shard (no wait for a transfer);
+    * RS: the last step ends on the owner's slab ("own chunk last"), and the
+      partial of slab j moves from rank r at step s to rank r - 1 at step s+1
+      (a ring, so each hand-off is one neighbour transfer);
+    * the blocks of all (rank, step) pairs tile the (M, N, K) volume exactly once.
+    """
+    ag = schedules[:2]
+    for P in range(1, 9):
+        for sched in schedules:
+            for r in range(P):
+                js = [slab_index(sched, P, r, s) for s in range(P)]
+                assert sorted(js) == list(range(P)), (sched, P, r, js)
+            for s in range(P):
+                js = [slab_index(sched, P, r, s) for r in range(P)]
+                assert sorted(js) == list(range(P)), (sched, P, s)
+            if sched in ag:
+                assert all(slab_index(sched, P, r, 0) == r for r in range(P))
+            else:
+                assert all(slab_index(sched, P, r, P - 1) == r for r in range(P))
+                for s in range(P - 1):
+                    for r in range(P):
+                        j = slab_index(sched, P, r, s)
+                        assert slab_index(sched, P, (r - 1) % P, s + 1) == j
+            m, n, k = 2 * P, 3 * P, 5 * P
+            cover = np.zeros((m, n, k), dtype=np.int64)
+            for r in range(P):
+                for s in range(P):
+                    b = step_blocks(sched, m, n, k, P, r, s)
+                    cover[b["rows"], b["cols"], b["k"]] += 1
+            assert np.all(cover == 1), (sched, P)
+
+
+def check_printed_local_sizes(local_problem, schedule_ag_a):
+    with open(os.path.join(GOLDEN, "pr1907_distgemm_printout.json")) as f:
+        g = json.load(f)
+    for run in g["runs"]:
+        m, n, k, l = run["problem"]
+        assert tuple(local_problem(schedule_ag_a, m, n, k, l, run["tp"])) == tuple(run["local_problem"])
+
+
+def all_shapes():
+    return list(itertools.product([1, 2], [1, 3], [2, 5]))

@@ -1,0 +1,119 @@
+"""Plant plausible mistakes in copies of the oracle (on the CPU) and check
+that the pins catch every one of them."""
+
+import numpy as np
+import pytest
+
+from oracle import gemm as og
+from oracle import schedules as osch
+from tests import pin_checks as pc
+
+
+def _fails(fn, *args):
+    try:
+        fn(*args)
+    except AssertionError:
+        return True
+    return False
+
+
+def gemm_drop_beta(A, B, C, alpha, beta):
+    return og.gemm(A, B, C, alpha, 0.0)
+
+
+def gemm_no_transpose(A, B, C, alpha, beta):
+    # treats the stored (N, K) B as (K, N) when it can
+    L, M, K = A.shape
+    Bt = np.reshape(B, (B.shape[0], K, -1)) if B.size == L * K * B.shape[1] else B
+    D = alpha * np.matmul(A, Bt)
+    return D + (beta * C if beta != 0 else 0)
+
+
+def gemm_beta_on_alpha(A, B, C, alpha, beta):
+    D = np.matmul(A, np.swapaxes(B, 1, 2))
+    return alpha * (D + (beta * C if beta != 0 else 0))
+
+
+def gemm_half_k(A, B, C, alpha, beta):
+    K = A.shape[2]
+    h = max(1, K // 2)
+    return og.gemm(A[:, :, :h], B[:, :, :h], C, alpha, beta)
+
+
+def gemm_reads_c_when_beta0(A, B, C, alpha, beta):
+    D = alpha * np.matmul(A, np.swapaxes(B, 1, 2))
+    return D + (beta * C if C is not None else 0)
+
+
+GEMM_MUTANTS = [gemm_drop_beta, gemm_no_transpose, gemm_beta_on_alpha, gemm_half_k,
+                gemm_reads_c_when_beta0]
+
+
+@pytest.mark.parametrize("mutant", GEMM_MUTANTS, ids=lambda f: f.__name__)
+def test_gemm_mutants_caught(mutant):
+    checks = [pc.check_brute_force_exact, pc.check_brute_force_random, pc.check_closed_forms,
+              pc.check_printed_mean]
+    assert any(_fails(c, mutant) for c in checks)
+
+
+def _rs_beta_every_step(sched, A, B, C, alpha, beta, P):
+    if sched not in (osch.RS_TILING_A_ROTATING_C, osch.RS_TILING_B_ROTATING_C):
+        return osch.run_schedule(sched, A, B, C, alpha, beta, P)
+    # re-adds beta*C at every hop of the rotating partial
+    D = osch.run_schedule(sched, A, B, C, alpha, beta, P)
+    return D + (P - 1) * beta * np.asarray(C, np.float64) if beta != 0 else D
+
+
+def _ag_b_wrong_cols(sched, A, B, C, alpha, beta, P):
+    if sched != osch.AG_ROTATING_B or P == 1:
+        return osch.run_schedule(sched, A, B, C, alpha, beta, P)
+    D = osch.run_schedule(sched, A, B, C, alpha, beta, P)
+    n = D.shape[2] // P
+    return np.concatenate([D[:, :, n:], D[:, :, :n]], axis=2)  # slabs written to the wrong place
+
+
+def _rs_drops_last_rank(sched, A, B, C, alpha, beta, P):
+    if sched not in (osch.RS_TILING_A_ROTATING_C,) or P == 1:
+        return osch.run_schedule(sched, A, B, C, alpha, beta, P)
+    k = A.shape[2] // P
+    A2 = np.array(A, np.float64)
+    A2[:, :, (P - 1) * k:] = 0.0
+    return osch.run_schedule(sched, A2, B, C, alpha, beta, P)
+
+
+@pytest.mark.parametrize("mutant", [_rs_beta_every_step, _ag_b_wrong_cols, _rs_drops_last_rank],
+                         ids=lambda f: f.__name__)
+def test_schedule_mutants_caught(mutant):
+    assert _fails(pc.check_schedule_invariance, mutant, og.gemm, osch.SCHEDULES)
+
+
+def _slab_ag_not_local_first(sched, P, r, s):
+    if sched in (osch.AG_ROTATING_A, osch.AG_ROTATING_B):
+        return (r + s + 1) % P
+    return osch.slab_index(sched, P, r, s)
+
+
+def _slab_rs_wrong_ring(sched, P, r, s):
+    if sched in (osch.RS_TILING_A_ROTATING_C, osch.RS_TILING_B_ROTATING_C):
+        return (r - s - 1) % P  # partial hops to r+1: owner still last, but not the ring the pages use
+    return osch.slab_index(sched, P, r, s)
+
+
+def _slab_rs_owner_first(sched, P, r, s):
+    if sched in (osch.RS_TILING_A_ROTATING_C, osch.RS_TILING_B_ROTATING_C):
+        return (r + s) % P
+    return osch.slab_index(sched, P, r, s)
+
+
+@pytest.mark.parametrize("mutant", [_slab_ag_not_local_first, _slab_rs_wrong_ring, _slab_rs_owner_first],
+                         ids=lambda f: f.__name__)
+def test_rotation_mutants_caught(mutant):
+    def blocks(sched, m, n, k, P, r, s):
+        return osch.step_blocks(sched, m, n, k, P, r, s)
+    assert _fails(pc.check_rotation_tables, mutant, blocks, osch.SCHEDULES)
+
+
+def test_local_size_mutant_caught():
+    def wrong(sched, m, n, k, l, P):
+        return (m // P, n, k // P, l)
+    assert _fails(pc.check_printed_local_sizes, wrong, osch.AG_ROTATING_A)
