@@ -1,0 +1,393 @@
+#!/usr/bin/env python
+"""Benchmark of the communication-fused TP GEMM on GB300.
+
+``python bench.py --gpus N --steps K --warmup W [--workload NAME] [--impl dg|reference]``
+
+One step = one fused run of the whole problem (every virtual rank, every
+rotation step, all shard transfers) on one GPU.  With N > 1 (torchrun, one
+process per GPU) every GPU runs its own replica of the problem: the path is
+emulated on one GPU and has no exchange between GPUs, so scaling is weak and
+``value`` is the sum over replicas (N x flops / slowest rank's time).
+
+Prints one JSON line (rank 0).  ``metric``/``unit``: TFLOP/s of the fused
+run; ``roofline``: the fused kernel against the measured dense-bf16 peak;
+``copy_hidden_fraction``: clamp((t_copy + t_gemm - t_fused) / t_copy, 0, 1)
+with t_copy = t_serial - t_gemm; ``e2e``: the same metric with inputs copied
+from pinned host memory and D copied back inside the timed region;
+``cpu_baseline``: the CPU oracle on a bounded sample of the same problem.
+
+``--impl reference`` times the CPU oracle (the slow reference program) on the
+same workload and prints its own line (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from reduce_scatter_gb300 import configs  # noqa: E402
+
+METRIC = "fused TP-GEMM TFLOP/s and % of GB300 BF16 peak; copy-hidden fraction"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAK_TFLOPS = 1900.0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["dg", "reference"], default="dg")
+    ap.add_argument("--workload", choices=sorted(configs.WORKLOADS), default=configs.DEFAULT)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-modes", action="store_true", help="skip the GEMM_ONLY / SERIAL timings")
+    ap.add_argument("--cpu-sample-rows", type=int, default=1024)
+    ap.add_argument("--cpu-sample-cols", type=int, default=4096)
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------- helpers
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"bf16_tflops": FALLBACK_PEAK_TFLOPS}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("dg_kernel.cuh", "dg_geom.h"):
+        with open(os.path.join(ROOT, "reduce_scatter_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(workload)
+    if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return ent.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = open("/tmp/dg_clocks_%d.csv" % os.getpid(), "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.out is not None:
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or self.out is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(loaded), "reasons": reasons}
+
+
+def cpu_oracle_sample(w, rows: int, cols: int):
+    """Time the CPU oracle on rows x cols entries of D (all of K)."""
+    import numpy as np
+
+    from oracle import gemm as og
+    from reduce_scatter_gb300 import synth
+
+    LM, LN = w.l * w.m, w.l * w.n
+    rows = min(rows, LM)
+    cols = min(cols, w.n)
+    rows = min(rows, w.m)
+    ridx = np.linspace(0, w.m - 1, rows).astype(np.int64)   # spread over every shard of batch 0
+    batch = 0
+    cidx = np.linspace(0, w.n - 1, cols).astype(np.int64)
+    a = og.bf16_bits_to_f64(synth.rows_bits_np(w.seed, synth.STREAM_A, (LM, w.k), ridx, w.dist_a))
+    b = og.bf16_bits_to_f64(synth.rows_bits_np(w.seed, synth.STREAM_B, (LN, w.k), cidx, w.dist_b))
+    c = None
+    if w.beta != 0:
+        crow = synth.rows_bits_np(w.seed, synth.STREAM_C, (LM, w.n), ridx, w.dist_c)[:, cidx - batch * w.n]
+        c = og.bf16_bits_to_f64(crow)
+    t0 = time.perf_counter()
+    og.gemm_entries(a, b, c, w.alpha, w.beta)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * cols * w.k
+    try:
+        from threadpoolctl import threadpool_info
+
+        cores = max((i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"),
+                    default=os.cpu_count())
+    except Exception:
+        cores = os.cpu_count()
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "seconds": dt,
+            "sample": f"{rows} rows x {cols} columns of D (all K={w.k}) of {w.name}, fp64 numpy matmul; "
+                      f"{flops:.3e} flop"}
+
+
+# ------------------------------------------------------------------ dg arm
+
+
+def make_inputs(w, device):
+    import torch
+
+    from reduce_scatter_gb300 import synth
+
+    A = synth.tensor_bits_torch(w.seed, synth.STREAM_A, (w.l, w.m, w.k), w.dist_a, device=device).view(torch.bfloat16)
+    B = synth.tensor_bits_torch(w.seed, synth.STREAM_B, (w.l, w.n, w.k), w.dist_b, device=device).view(torch.bfloat16)
+    C = None
+    if w.beta != 0:
+        C = synth.tensor_bits_torch(w.seed, synth.STREAM_C, (w.l, w.m, w.n), w.dist_c, device=device).view(torch.bfloat16)
+    return A, B, C
+
+
+def timed_loop(run, steps, warmup, stream, flush=None):
+    """Per-step CUDA events on ``stream``; returns mean ms per step."""
+    import torch
+
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for s, e in ev:
+        if flush is not None:
+            flush()
+        s.record(stream)
+        run()
+        e.record(stream)
+    torch.cuda.synchronize()
+    return sum(s.elapsed_time(e) for s, e in ev) / steps
+
+
+def run_dg(args, rank, world, dist):
+    import torch
+
+    from reduce_scatter_gb300 import dg
+
+    w = configs.WORKLOADS[args.workload]
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    A, B, C = make_inputs(w, dev)
+    D = torch.empty((w.l, w.m, w.n), dtype=torch.bfloat16, device=dev)
+    plan = dg.Plan(w.m, w.n, w.k, w.l, w.tp, w.schedule, w.alpha, w.beta)
+    ws = torch.zeros(max(plan.workspace_bytes(), 256), dtype=torch.uint8, device=dev)
+    main = torch.cuda.current_stream(dev)
+    copy = torch.cuda.Stream(dev)
+    in_bytes = A.numel() * 2 + B.numel() * 2 + (C.numel() * 2 if C is not None else 0)
+    flush_buf = None
+    if in_bytes < 2 * L2_BYTES:
+        flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = (lambda: flush_buf.fill_(1.0)) if flush_buf is not None else None
+
+    def run():
+        plan.run(A, B, C, D, ws, main, copy)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    # correctness guard before timing: one run, device status must be clean
+    run()
+    plan.check(ws, main)
+
+    barrier()
+    with ClockSampler(local) as clk:
+        barrier()
+        ms_fused = timed_loop(run, args.steps, args.warmup, main, flush)
+        barrier()
+    plan.check(ws, main)
+    clocks = clk.summary()
+
+    ms_gemm = ms_serial = None
+    if not args.no_modes and w.schedule in (dg.AG_ROTATING_A, dg.AG_ROTATING_B) and w.tp > 1:
+        plan.set_mode(dg.MODE_GEMM_ONLY)
+        ms_gemm = timed_loop(run, max(3, args.steps // 2), 2, main, flush)
+        plan.set_mode(dg.MODE_SERIAL)
+        ms_serial = timed_loop(run, max(3, args.steps // 2), 2, main, flush)
+        plan.set_mode(dg.MODE_FUSED)
+        plan.check(ws, main)
+
+    e2e = None
+    if not args.no_e2e:
+        A_h = A.cpu().pin_memory()
+        B_h = B.cpu().pin_memory()
+        C_h = C.cpu().pin_memory() if C is not None else None
+        D_h = torch.empty(D.shape, dtype=D.dtype).pin_memory()
+
+        def run_e2e():
+            A.copy_(A_h, non_blocking=True)
+            B.copy_(B_h, non_blocking=True)
+            if C is not None:
+                C.copy_(C_h, non_blocking=True)
+            plan.run(A, B, C, D, ws, main, copy)
+            D_h.copy_(D, non_blocking=True)
+
+        e2e_steps = max(2, min(args.steps, 5))
+        ms_e2e = timed_loop(run_e2e, e2e_steps, 1, main)
+        plan.check(ws, main)
+        e2e = {"value": None, "unit": "TFLOP/s", "ms_per_step": ms_e2e, "steps": e2e_steps,
+               "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": D.numel() * 2}
+
+    # max over ranks
+    vals = torch.tensor([ms_fused, ms_gemm or 0.0, ms_serial or 0.0, (e2e or {}).get("ms_per_step", 0.0)],
+                        dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    ms_fused, ms_gemm_m, ms_serial_m, ms_e2e = vals.tolist()
+    if rank != 0:
+        return None
+    ms_gemm = ms_gemm_m if ms_gemm is not None else None
+    ms_serial = ms_serial_m if ms_serial is not None else None
+
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK_TFLOPS))
+    per_gpu = w.flops / (ms_fused * 1e-3) / 1e12
+    value = world * per_gpu
+    hidden = None
+    if ms_gemm is not None and ms_serial is not None:
+        t_copy = ms_serial - ms_gemm
+        hidden = max(0.0, min(1.0, (t_copy + ms_gemm - ms_fused) / t_copy)) if t_copy > 0 else None
+    if e2e is not None:
+        e2e["ms_per_step"] = ms_e2e
+        e2e["value"] = world * w.flops / (ms_e2e * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_fused, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded SplitMix64 inputs with the workload's distributions)",
+        "config": dict(w.describe(), parallelism=f"tp{w.tp} virtual ranks on 1 GPU" + (
+            f", {world} replicas" if world > 1 else ""),
+            l2="flushed between steps" if flush is not None else "inputs larger than L2 (no flush)"),
+        "pct_of_peak": round(100.0 * per_gpu / peak, 2),
+        "ms_gemm_only": None if ms_gemm is None else round(ms_gemm, 4),
+        "ms_serial": None if ms_serial is None else round(ms_serial, 4),
+        "copy_hidden_fraction": None if hidden is None else round(hidden, 4),
+        "fused_over_gemm_only": None if ms_gemm is None else round(ms_fused / ms_gemm, 4),
+        "roofline": {"bound": "tensor", "achieved": round(per_gpu, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(per_gpu / peak, 4), "peak_source": f"{peak_kind} bf16 burst",
+                     "frac_of_sustained": round(per_gpu / float(peaks.get("bf16_tflops_sustained", peak)), 4),
+                     "traffic": recorded_traffic(w.name), "kernel": "dg::dg_gemm_kernel"},
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+        "e2e": e2e,
+    }
+    return line
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    w = configs.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        steps = []
+        for _ in range(max(1, args.warmup)):
+            cpu_oracle_sample(w, max(64, args.cpu_sample_rows // 4), max(256, args.cpu_sample_cols // 4))
+        for _ in range(args.steps):
+            steps.append(cpu_oracle_sample(w, max(64, args.cpu_sample_rows // 4), max(256, args.cpu_sample_cols // 4)))
+        secs = sum(s["seconds"] for s in steps) / len(steps)
+        val = sum(s["value"] for s in steps) / len(steps)
+        line = {"impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": w.describe(),
+                "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": steps[0]["cores"],
+                                 "kind": "oracle", "sample": steps[0]["sample"]},
+                "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+
+        backend = "nccl"
+        tdist.init_process_group(backend=backend)
+        dist = tdist
+    line = run_dg(args, rank, world, dist)
+    if line is not None:
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_oracle_sample(w, args.cpu_sample_rows, args.cpu_sample_cols)
+            line["cpu_baseline"].pop("seconds", None)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

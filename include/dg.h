@@ -1,0 +1,185 @@
+/*
+ * dg.h -- C ABI of the communication-fused tensor-parallel GEMM on one GB300.
+ *
+ * What it computes ("Distributed GEMM", CUTLASS example 65 README, section
+ * "Getting started": the m, n, k, l (batch), alpha, beta problem):
+ *
+ *     D[l] = alpha * A[l] * B[l] + beta * C[l]          for l in [0, L)
+ *
+ * split over TP virtual ranks with one of the four schedules that README lists
+ * under "Trying out other schedules".  All TP ranks are emulated on ONE GPU:
+ * each rank's shards are views or receive slots in device memory, transfers
+ * between ranks are copy-engine cudaMemcpyAsync calls on a side stream that
+ * each publish a ready flag, and one persistent kernel runs every rank's steps
+ * in rotation order, waiting on a shard's flag before it loads that shard.
+ *
+ * Layouts (the pages do not fix them):
+ *   A  bf16, L x M x K, row-major (K innermost)
+ *   B  bf16, stored transposed: L x N x K, row-major (K innermost)
+ *   C  bf16, L x M x N, row-major (read only when beta != 0)
+ *   D  bf16, L x M x N, row-major
+ * Every batch is densely packed after the previous one.  bf16 values are
+ * passed as raw 16-bit patterns (dg_bf16_t).
+ *
+ * Shape rules: m, n, k, l >= 0; tp in {1, 2, 4, 8}; K % 8 == 0 and N % 8 == 0
+ * (16-byte row pitch for the tensor-memory-access unit); the sharded extent
+ * divides by tp (AG-RotatingA: M and N; AG-RotatingB: M and N;
+ * RS-TilingA: M and K; RS-TilingB: N and K) and, for the RS schedules,
+ * (K / tp) % 8 == 0.  Shards need not be multiples of the tile.
+ *
+ * Ownership: the caller owns A, B, C, D, the workspace and both streams.  The
+ * plan owns only host state (geometry, events, cached tensor maps).  A
+ * workspace belongs to one plan at a time; the first run of a plan with a
+ * given workspace clears the workspace's flag words on the main stream.
+ *
+ * Errors: every int-returning call returns DG_OK (0) or a negative dg_status;
+ * dg_last_error() gives a message for the calling thread.
+ */
+#ifndef DG_H_
+#define DG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t dg_bf16_t;
+typedef struct dg_plan_s* dg_plan_t;
+
+/* The four schedules ("Distributed GEMM", CUTLASS example 65 README, section
+ * "Trying out other schedules").  P = tp, rank r, step s:
+ *   AG_ROTATING_A: rank r owns D[:, N_r]; step s computes D[M_j, N_r] with the
+ *                  received A shard j = (r + s) mod P.
+ *   AG_ROTATING_B: rank r owns D[M_r, :]; step s computes D[M_r, N_j] with the
+ *                  received B shard j = (r + s) mod P.
+ *   RS_TILING_A_ROTATING_C: rank r holds K-slab K_r; step s adds
+ *                  alpha * A[M_j, K_r] B[K_r, :] into the rotating partial of
+ *                  M-slab j = (r + s + 1) mod P, whose source at step 0 is
+ *                  beta * C; the last step (j = r) writes D[M_r, :].
+ *   RS_TILING_B_ROTATING_C: the same with N-slabs D[:, N_j].
+ * The rotation follows _pipelined_all_gather_and_consume and
+ * _pipelined_produce_and_all2all in torch/distributed/_symmetric_memory. */
+enum dg_schedule {
+  DG_AG_ROTATING_A = 0,
+  DG_AG_ROTATING_B = 1,
+  DG_RS_TILING_A_ROTATING_C = 2,
+  DG_RS_TILING_B_ROTATING_C = 3
+};
+
+/* Run modes (how the AG shard transfers are issued):
+ *   FUSED:     transfers on the copy stream, overlapped with the kernel, which
+ *              waits per shard chunk on its ready flag.
+ *   GEMM_ONLY: no transfers and no flag waits; the receive slots must already
+ *              hold the shards (e.g. from an earlier FUSED run with the same A
+ *              and B).  Measures the kernel alone.
+ *   SERIAL:    all transfers on the main stream, then the kernel ("copy, then
+ *              GEMM").  For the RS schedules SERIAL runs the non-fused
+ *              baseline: one GEMM per rank into its own fp32 partial, then a
+ *              separate reduction kernel; its workspace is larger (size the
+ *              workspace after selecting the mode).
+ * FUSED and GEMM_ONLY are the same kernel for the RS schedules (they move no
+ * shards; the rotating partial lives in the workspace). */
+enum dg_mode { DG_MODE_FUSED = 0, DG_MODE_GEMM_ONLY = 1, DG_MODE_SERIAL = 2 };
+
+enum dg_status {
+  DG_OK = 0,
+  DG_ERR_ARG = -1,         /* null/misaligned pointer, bad enum, negative extent */
+  DG_ERR_SHAPE = -2,       /* extent not divisible by tp, or K/N pitch rule broken */
+  DG_ERR_UNSUPPORTED = -3, /* device or driver lacks a needed feature */
+  DG_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed */
+  DG_ERR_TIMEOUT = -5,     /* a ready-flag wait ran out (device status word) */
+  DG_ERR_HANG = -6,        /* an internal pipeline wait ran out; the kernel bailed out */
+  DG_ERR_STATE = -7        /* call not valid in the plan's current state */
+};
+
+/* Options for dg_set_option. */
+enum dg_option {
+  DG_OPT_TIMEOUT_MS = 0,      /* ready-flag wait limit, ms (default 2000) */
+  DG_OPT_CHUNK_TILES = 1,     /* tiles per shard transfer chunk (0 = auto, >= 2 MiB) */
+  DG_OPT_FAULT_SKIP_FLAG = 2, /* test hook: drop the ready-flag write with this
+                                 enqueue index (-1 = none, default) */
+  DG_OPT_FAULT_DELAY_MS = 3,  /* test hook: hold the copy stream this long
+                                 before the first transfer (default 0) */
+  DG_OPT_GRID = 4,            /* persistent grid size (0 = one CTA per SM) */
+  DG_OPT_COPY_STREAMS = 5     /* reserved: number of copy streams (1) */
+};
+
+/* Plan geometry and workspace layout, for callers and tests. */
+typedef struct dg_plan_info {
+  int64_t m, n, k, l;
+  int32_t tp, schedule;
+  int64_t local_m, local_n, local_k; /* per-rank, per-step GEMM extents */
+  int32_t tile_m, tile_n, tile_k;
+  int64_t tiles_m, tiles_n;          /* tiles per (step, rank, batch) block */
+  int64_t total_tiles;               /* all ranks, all steps */
+  int64_t chunk_tiles, chunks_per_shard;
+  int64_t n_flags;                   /* flag words in the workspace */
+  size_t ws_bytes;
+  size_t off_status, off_flags, off_slots, off_partial, off_serial;
+  size_t slot_bytes;                 /* one receive slot (one shard, one batch) */
+  int64_t copies_per_run;            /* transfer enqueues per FUSED/SERIAL run */
+} dg_plan_info;
+
+/* One tile of the step-major rotation order (host decoder, for tests). */
+typedef struct dg_tile {
+  int32_t step, rank, slab, batch;
+  int32_t a_map, b_map;     /* tensor map index: AG 0 = home, 1 = receive slots;
+                               RS = rank (its K-slab) */
+  int64_t a_row, b_row;     /* first row loaded from that map */
+  int64_t out_row, out_col; /* first D (or partial) element: row in L*M, column in N */
+  int32_t rows_valid, cols_valid;
+  int32_t k_blocks;
+  int64_t flag;             /* AG ready-flag index (-1 = local shard) */
+  int64_t tile_flag;        /* RS rotating-partial flag index (-1 = none) */
+  int32_t src;              /* epilogue source: 0 none, 1 beta*C, 2 rotating partial */
+  int32_t dst;              /* 0 = D (bf16), 1 = rotating partial (fp32) */
+} dg_tile;
+
+/* Validate a problem and build a plan.  Host only: no CUDA call is made, so
+ * this works without a GPU.  alpha/beta as in the README's --alpha/--beta. */
+int dg_plan(dg_plan_t* out, int64_t m, int64_t n, int64_t k, int64_t l, int tp, int schedule,
+            float alpha, float beta);
+
+/* Workspace bytes the plan needs in its current mode (0 is possible). */
+size_t dg_workspace_bytes(dg_plan_t plan);
+
+/* Select the run mode for later dg_run calls (dg_mode). */
+int dg_run_mode(dg_plan_t plan, int mode);
+
+/* Set a dg_option. */
+int dg_set_option(dg_plan_t plan, int option, int64_t value);
+
+/* Enqueue one run.  A, B, D, workspace: device pointers, 16-byte aligned
+ * (workspace 256-byte aligned), workspace of dg_workspace_bytes(plan) bytes.
+ * C may be NULL iff beta == 0.  main_stream / copy_stream: cudaStream_t
+ * handles (copy_stream may equal main_stream; it is used only in FUSED mode
+ * of the AG schedules).  Asynchronous: returns after enqueueing; the work is
+ * ordered after prior work on main_stream and later work on main_stream is
+ * ordered after all of it (copies included).  Device-side failures are
+ * reported by dg_check. */
+int dg_run(dg_plan_t plan, const dg_bf16_t* A, const dg_bf16_t* B, const dg_bf16_t* C,
+           dg_bf16_t* D, void* workspace, void* main_stream, void* copy_stream);
+
+/* Synchronize `stream` and read the workspace status word of the plan's last
+ * run: DG_OK, DG_ERR_TIMEOUT or DG_ERR_HANG (with the flag index in the
+ * message), or DG_ERR_CUDA on a CUDA error. */
+int dg_check(dg_plan_t plan, void* workspace, void* stream);
+
+/* Geometry and workspace layout. */
+int dg_plan_info_get(dg_plan_t plan, dg_plan_info* info);
+
+/* Decode tile t (0 <= t < total_tiles) of the rotation order on the host. */
+int dg_plan_tile(dg_plan_t plan, int64_t t, dg_tile* out);
+
+void dg_destroy(dg_plan_t plan);
+
+/* Message of the calling thread's last error ("" if none). */
+const char* dg_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DG_H_ */

@@ -1,0 +1,71 @@
+"""Named workloads: the problem sizes, schedules and input distributions of
+the pages' benchmarks, as synthetic inputs.
+
+* ``ag_a_tp2_256``: AllGather RotatingA, TP=2, 256^3 (latency / parity case).
+* ``ag_a_tp2_blog``: the all_gather+matmul blog's 8192^2-per-rank,
+  world_size=2 shape (gathered M = 16384, N = K = 8192), U[0,1) inputs
+  (the blog uses torch.rand), here in bf16.
+* ``ag_a_tp8_pr``: the Distributed GEMM pull request's TP=8 benchmark,
+  16384 x 106496 x 16384; activations N(0,1), weights N(0,0.02).
+* ``rs_a_tp8``: ReduceScatter TilingA RotatingC, TP=8, 16384 x 8192 x 28672
+  (K split 8 x 3584); A N(0,1), B N(0,0.02).
+* ``ag_b_tp4_batched`` / ``rs_b_tp4_batched``: RotatingB / TilingB RotatingC,
+  TP=4, 8192 x 53248 x 8192, L=2, alpha=0.5, beta=1, C N(0,1).
+
+A is the activation (M x K), B the weight stored N x K, C the epilogue input.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+U11 = ("uniform", -1.0, 1.0)
+U01 = ("uniform", 0.0, 1.0)
+N1 = ("normal", 0.0, 1.0)
+N002 = ("normal", 0.0, 0.02)
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    schedule: int
+    tp: int
+    m: int
+    n: int
+    k: int
+    l: int = 1
+    alpha: float = 1.0
+    beta: float = 0.0
+    dist_a: tuple = U11
+    dist_b: tuple = U11
+    dist_c: tuple = N1
+    seed: int = 1
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.m * self.n * self.k * self.l
+
+    def describe(self) -> dict:
+        from . import dg
+
+        return {"workload": self.name, "schedule": dg.SCHEDULE_NAMES[self.schedule], "tp": self.tp,
+                "m": self.m, "n": self.n, "k": self.k, "l": self.l, "alpha": self.alpha, "beta": self.beta,
+                "dist_a": list(self.dist_a), "dist_b": list(self.dist_b),
+                "dist_c": list(self.dist_c) if self.beta else None, "seed": self.seed}
+
+
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("ag_a_tp2_256", 0, 2, 256, 256, 256, dist_a=U11, dist_b=U11),
+        Workload("ag_a_tp2_blog", 0, 2, 16384, 8192, 8192, dist_a=U01, dist_b=U01),
+        Workload("ag_a_tp8_pr", 0, 8, 16384, 106496, 16384, dist_a=N1, dist_b=N002),
+        Workload("rs_a_tp8", 2, 8, 16384, 8192, 28672, dist_a=N1, dist_b=N002),
+        Workload("ag_b_tp4_batched", 1, 4, 8192, 53248, 8192, l=2, alpha=0.5, beta=1.0, dist_a=N1,
+                 dist_b=N002, dist_c=N1),
+        Workload("rs_b_tp4_batched", 3, 4, 8192, 53248, 8192, l=2, alpha=0.5, beta=1.0, dist_a=N1,
+                 dist_b=N002, dist_c=N1),
+    ]
+}
+
+DEFAULT = "ag_a_tp8_pr"

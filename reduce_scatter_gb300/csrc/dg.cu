@@ -1,0 +1,576 @@
+// dg.cu -- C ABI (include/dg.h): planner, workspace layout, tensor maps,
+// copy-engine shard mover and the launch of the persistent kernel.
+//
+// Emulation of TP ranks on one GPU ("Distributed GEMM", CUTLASS pull request
+// #1907 description: point-to-point transfers, "a memcopy branch" beside the
+// GEMM kernels, which only add barriers at their start, leaving the SMs to the
+// GEMM and the copy engine to communication):
+//   * rank r's home shards are views of the caller's A / B;
+//   * rank r's receive slot for step s >= 1 is a workspace region; the copy
+//     stream fills it with cudaMemcpyAsync (device to device, copy engine) in
+//     chunks and after each chunk writes the run's epoch into that chunk's
+//     ready flag with a stream memory operation (no SM involved);
+//   * one persistent kernel runs every rank's steps in rotation order and its
+//     producer waits on a chunk's flag before loading from the slot.
+// The RS schedules move no shards on one GPU: the rotating partial X_j lives
+// in the workspace and each tile's hand-off from step s to s + 1 is a release
+// / acquire on a per-tile flag.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <chrono>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <thread>
+#include <unordered_map>
+
+#include "dg.h"
+#include "dg_kernel.cuh"
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(DG_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define DG_CUDA(call)                                   \
+  do {                                                  \
+    cudaError_t e_ = (call);                            \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+  } while (0)
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+typedef CUresult (*WriteValue32Fn)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+
+struct Driver {
+  EncodeTiledFn encode = nullptr;
+  WriteValue32Fn write32 = nullptr;
+};
+
+int get_driver(Driver* d) {
+  static std::mutex mu;
+  static Driver cached;
+  static bool done = false;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!done) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return fail(DG_ERR_UNSUPPORTED, "driver entry point cuTensorMapEncodeTiled not found");
+    cached.encode = reinterpret_cast<EncodeTiledFn>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return fail(DG_ERR_UNSUPPORTED, "driver entry point cuStreamWriteValue32 not found");
+    cached.write32 = reinterpret_cast<WriteValue32Fn>(fn);
+    done = true;
+  }
+  *d = cached;
+  return DG_OK;
+}
+
+// Workspace -> owning plan, so a workspace reused by another plan gets its
+// flag words cleared before its epochs are trusted.
+std::mutex g_ws_mu;
+std::unordered_map<const void*, uint64_t> g_ws_owner;
+uint64_t g_next_plan_id = 1;
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+struct dg_plan_s {
+  dg::Geom g{};
+  int64_t m = 0, n = 0, k = 0, l = 0;
+  int tp = 1, schedule = 0;
+  float alpha = 1.f, beta = 0.f;
+  int mode = DG_MODE_FUSED;
+  int64_t timeout_ms = 2000;
+  int64_t chunk_tiles_req = 0;
+  int64_t fault_skip = -1;
+  int64_t fault_delay_ms = 0;
+  int64_t grid_req = 0;
+  uint64_t id = 0;
+  uint32_t epoch = 0;
+  bool serial_ws = false;
+  // layout
+  int64_t n_flags = 0;
+  size_t off_status = 0, off_flags = 0, off_slots = 0, off_partial = 0, off_serial = 0;
+  size_t slot_bytes = 0, ws_bytes_base = 0, ws_bytes_serial = 0;
+  int64_t copies = 0;
+  // runtime state
+  bool rt = false;
+  int device = -1;
+  int num_sms = 0;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  dg::KParams kp;
+  const void* map_key[3] = {nullptr, nullptr, nullptr};
+  int n_maps = 0;
+};
+
+namespace {
+
+bool is_ag(int s) { return s == DG_AG_ROTATING_A || s == DG_AG_ROTATING_B; }
+
+int layout(dg_plan_s* p) {
+  dg::Geom& g = p->g;
+  const int64_t P = p->tp;
+  g.sched = p->schedule;
+  g.P = (int32_t)P;
+  g.M = p->m;
+  g.N = p->n;
+  g.K = p->k;
+  g.L = p->l;
+  g.BM = dg::BM;
+  g.BN = dg::BN;
+  g.BK = dg::BK;
+  g.group_m = 16;
+  g.beta_nonzero = p->beta != 0.f;
+  switch (p->schedule) {
+    case DG_AG_ROTATING_A:
+      g.blk_m = p->m / P, g.blk_n = p->n / P, g.shard = p->m / P, g.Ks = p->k;
+      break;
+    case DG_AG_ROTATING_B:
+      g.blk_m = p->m / P, g.blk_n = p->n / P, g.shard = p->n / P, g.Ks = p->k;
+      break;
+    case DG_RS_TILING_A_ROTATING_C:
+      g.blk_m = p->m / P, g.blk_n = p->n, g.shard = 0, g.Ks = p->k / P;
+      break;
+    default:
+      g.blk_m = p->m, g.blk_n = p->n / P, g.shard = 0, g.Ks = p->k / P;
+      break;
+  }
+  g.tiles_m = dg::cdiv(g.blk_m, g.BM);
+  g.tiles_n = dg::cdiv(g.blk_n, g.BN);
+  g.tiles_block = g.L * g.tiles_m * g.tiles_n;
+  g.total_tiles = P * P * g.tiles_block;
+  g.chunk_tiles = 1;
+  g.nchunks = 0;
+  p->n_flags = 0;
+  p->copies = 0;
+  if (is_ag(p->schedule)) {
+    const int64_t rot_tiles = p->schedule == DG_AG_ROTATING_A ? g.tiles_m : g.tiles_n;
+    const int64_t tile_rows = p->schedule == DG_AG_ROTATING_A ? g.BM : g.BN;
+    int64_t ct = p->chunk_tiles_req;
+    if (ct <= 0) {
+      const int64_t bytes = tile_rows * std::max<int64_t>(p->k, 1) * 2;
+      ct = std::max<int64_t>(1, dg::cdiv(int64_t(2) << 20, bytes));
+    }
+    g.chunk_tiles = std::max<int64_t>(1, std::min<int64_t>(ct, std::max<int64_t>(rot_tiles, 1)));
+    g.nchunks = dg::cdiv(rot_tiles, g.chunk_tiles);
+    if (P > 1) {
+      p->n_flags = P * (P - 1) * g.L * g.nchunks;
+      p->copies = p->n_flags;
+    }
+  } else if (P > 1) {
+    p->n_flags = g.L * P * g.tiles_m * g.tiles_n;
+  }
+  p->off_status = 0;
+  p->off_flags = 256;
+  size_t off = round_up(p->off_flags + (size_t)p->n_flags * 4, 1024);
+  p->off_slots = off;
+  p->slot_bytes = is_ag(p->schedule) ? (size_t)g.shard * (size_t)p->k * 2 : 0;
+  if (is_ag(p->schedule) && P > 1) off = round_up(off + (size_t)(P * (P - 1) * g.L) * p->slot_bytes, 1024);
+  p->off_partial = off;
+  if (!is_ag(p->schedule) && P > 1) off = round_up(off + (size_t)(g.L * p->m * p->n) * 4, 1024);
+  p->off_serial = off;
+  p->ws_bytes_base = off;
+  p->ws_bytes_serial = off;
+  if (!is_ag(p->schedule))
+    p->ws_bytes_serial = round_up(off + (size_t)(P * g.L * p->m * p->n) * 4, 1024);
+  return DG_OK;
+}
+
+int rt_init(dg_plan_s* p) {
+  if (p->rt) return DG_OK;
+  int dev = 0;
+  DG_CUDA(cudaGetDevice(&dev));
+  int major = 0, minor = 0;
+  DG_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+  DG_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
+  if (major != 10)
+    return fail(DG_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a", dev,
+                major, minor);
+  DG_CUDA(cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, dev));
+  DG_CUDA(cudaFuncSetAttribute(dg::dg_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)dg::SMEM_BYTES));
+  DG_CUDA(cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming));
+  DG_CUDA(cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming));
+  p->device = dev;
+  p->rt = true;
+  return DG_OK;
+}
+
+int encode_map(const Driver& drv, CUtensorMap* map, const void* base, int64_t inner, int64_t rows,
+               int64_t pitch_elems, int box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)pitch_elems * 2};
+  cuuint32_t box[2] = {(cuuint32_t)dg::BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = drv.encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(DG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for %lld x %lld pitch %lld", (int)r,
+                (long long)inner, (long long)rows, (long long)pitch_elems);
+  return DG_OK;
+}
+
+int build_maps(dg_plan_s* p, const Driver& drv, const void* A, const void* B, uint8_t* ws) {
+  if (p->map_key[0] == A && p->map_key[1] == B && p->map_key[2] == ws) return DG_OK;
+  std::memset(p->kp.tmA, 0, sizeof(p->kp.tmA));
+  std::memset(p->kp.tmB, 0, sizeof(p->kp.tmB));
+  const dg::Geom& g = p->g;
+  const int64_t P = p->tp;
+  int rc = DG_OK;
+  p->n_maps = 0;
+  if (p->k > 0) {
+    if (is_ag(p->schedule)) {
+      rc = encode_map(drv, &p->kp.tmA[0], A, p->k, g.L * p->m, p->k, dg::BM);
+      if (rc) return rc;
+      rc = encode_map(drv, &p->kp.tmB[0], B, p->k, g.L * p->n, p->k, dg::BN);
+      if (rc) return rc;
+      p->n_maps = 1;
+      if (P > 1) {
+        const int64_t slot_rows = P * (P - 1) * g.L * g.shard;
+        if (p->schedule == DG_AG_ROTATING_A) {
+          rc = encode_map(drv, &p->kp.tmA[1], ws + p->off_slots, p->k, slot_rows, p->k, dg::BM);
+          p->kp.tmB[1] = p->kp.tmB[0];
+        } else {
+          rc = encode_map(drv, &p->kp.tmB[1], ws + p->off_slots, p->k, slot_rows, p->k, dg::BN);
+          p->kp.tmA[1] = p->kp.tmA[0];
+        }
+        if (rc) return rc;
+        p->n_maps = 2;
+      }
+    } else {
+      const auto* a16 = static_cast<const uint16_t*>(A);
+      const auto* b16 = static_cast<const uint16_t*>(B);
+      for (int64_t r = 0; r < P; ++r) {
+        rc = encode_map(drv, &p->kp.tmA[r], a16 + r * g.Ks, g.Ks, g.L * p->m, p->k, dg::BM);
+        if (rc) return rc;
+        rc = encode_map(drv, &p->kp.tmB[r], b16 + r * g.Ks, g.Ks, g.L * p->n, p->k, dg::BN);
+        if (rc) return rc;
+      }
+      p->n_maps = (int)P;
+    }
+  }
+  p->map_key[0] = A;
+  p->map_key[1] = B;
+  p->map_key[2] = ws;
+  return DG_OK;
+}
+
+void CUDART_CB sleep_cb(void* ms) {
+  std::this_thread::sleep_for(std::chrono::milliseconds((int64_t)(intptr_t)ms));
+}
+
+// Shard transfers of every rank and step >= 1, each chunk followed by its
+// ready-flag write, in the order the kernel consumes them.
+int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B, uint8_t* ws,
+                   cudaStream_t st) {
+  const dg::Geom& g = p->g;
+  const int64_t P = p->tp;
+  if (p->fault_delay_ms > 0) DG_CUDA(cudaLaunchHostFunc(st, sleep_cb, (void*)(intptr_t)p->fault_delay_ms));
+  const bool rot_a = p->schedule == DG_AG_ROTATING_A;
+  const auto* home = static_cast<const uint16_t*>(rot_a ? A : B);
+  const int64_t outer = rot_a ? p->m : p->n;  // rows of one batch of the rotated operand
+  const int64_t tile_rows = rot_a ? g.BM : g.BN;
+  const int64_t chunk_rows = g.chunk_tiles * tile_rows;
+  auto* slots = reinterpret_cast<uint16_t*>(ws + p->off_slots);
+  auto* flags = reinterpret_cast<uint32_t*>(ws + p->off_flags);
+  int64_t idx = 0;
+  for (int64_t s = 1; s < P; ++s)
+    for (int64_t r = 0; r < P; ++r) {
+      const int64_t j = (r + s) % P;
+      for (int64_t l = 0; l < g.L; ++l) {
+        const int64_t slot = (r * (P - 1) + (s - 1)) * g.L + l;
+        for (int64_t c = 0; c < g.nchunks; ++c, ++idx) {
+          const int64_t row0 = c * chunk_rows;
+          const int64_t rows = std::min(chunk_rows, g.shard - row0);
+          if (rows > 0) {
+            const uint16_t* src = home + (l * outer + j * g.shard + row0) * p->k;
+            uint16_t* dst = slots + (slot * g.shard + row0) * p->k;
+            DG_CUDA(cudaMemcpyAsync(dst, src, (size_t)(rows * p->k) * 2, cudaMemcpyDeviceToDevice, st));
+          }
+          if (idx != p->fault_skip) {
+            CUresult rc = drv.write32((CUstream)st, (CUdeviceptr)(flags + slot * g.nchunks + c),
+                                      p->epoch, 0);
+            if (rc != CUDA_SUCCESS)
+              return fail(rc == CUDA_ERROR_NOT_SUPPORTED ? DG_ERR_UNSUPPORTED : DG_ERR_CUDA,
+                          "cuStreamWriteValue32 failed (%d)", (int)rc);
+          }
+        }
+      }
+    }
+  return DG_OK;
+}
+
+int launch(dg_plan_s* p, cudaStream_t st, uint32_t wait_flags) {
+  p->kp.wait_flags = wait_flags;
+  int64_t grid = p->grid_req > 0 ? p->grid_req : p->num_sms;
+  grid = std::min<int64_t>(grid, p->g.total_tiles);
+  if (grid <= 0) return DG_OK;
+  dg::dg_gemm_kernel<<<(unsigned)grid, dg::NUM_THREADS, dg::SMEM_BYTES, st>>>(p->kp);
+  DG_CUDA(cudaGetLastError());
+  return DG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dg_last_error(void) { return g_err.c_str(); }
+
+int dg_plan(dg_plan_t* out, int64_t m, int64_t n, int64_t k, int64_t l, int tp, int schedule,
+            float alpha, float beta) {
+  if (!out) return fail(DG_ERR_ARG, "out is NULL");
+  *out = nullptr;
+  if (m < 0 || n < 0 || k < 0 || l < 0) return fail(DG_ERR_ARG, "negative extent");
+  if (tp != 1 && tp != 2 && tp != 4 && tp != 8) return fail(DG_ERR_ARG, "tp must be 1, 2, 4 or 8 (got %d)", tp);
+  if (schedule < 0 || schedule > 3) return fail(DG_ERR_ARG, "unknown schedule %d", schedule);
+  if (k % 8 || n % 8) return fail(DG_ERR_SHAPE, "K and N must be multiples of 8 (K=%lld N=%lld)",
+                                  (long long)k, (long long)n);
+  const bool rs = !is_ag(schedule);
+  const bool need_m = schedule == DG_AG_ROTATING_A || schedule == DG_AG_ROTATING_B ||
+                      schedule == DG_RS_TILING_A_ROTATING_C;
+  const bool need_n = schedule != DG_RS_TILING_A_ROTATING_C;
+  if (need_m && m % tp) return fail(DG_ERR_SHAPE, "M=%lld not divisible by tp=%d", (long long)m, tp);
+  if (need_n && n % tp) return fail(DG_ERR_SHAPE, "N=%lld not divisible by tp=%d", (long long)n, tp);
+  if (rs && k % tp) return fail(DG_ERR_SHAPE, "K=%lld not divisible by tp=%d", (long long)k, tp);
+  if (rs && (k / tp) % 8)
+    return fail(DG_ERR_SHAPE, "K/tp=%lld must be a multiple of 8", (long long)(k / tp));
+  if (l * m > (int64_t(1) << 31) || l * n > (int64_t(1) << 31) || k > (int64_t(1) << 31))
+    return fail(DG_ERR_SHAPE, "extent too large");
+  auto* p = new dg_plan_s();
+  p->m = m, p->n = n, p->k = k, p->l = l;
+  p->tp = tp, p->schedule = schedule;
+  p->alpha = alpha, p->beta = beta;
+  {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    p->id = g_next_plan_id++;
+  }
+  layout(p);
+  *out = p;
+  return DG_OK;
+}
+
+size_t dg_workspace_bytes(dg_plan_t p) {
+  if (!p) return 0;
+  if (p->mode == DG_MODE_SERIAL && !is_ag(p->schedule)) {
+    p->serial_ws = true;
+    return p->ws_bytes_serial;
+  }
+  return p->ws_bytes_base;
+}
+
+int dg_run_mode(dg_plan_t p, int mode) {
+  if (!p) return fail(DG_ERR_ARG, "plan is NULL");
+  if (mode < DG_MODE_FUSED || mode > DG_MODE_SERIAL) return fail(DG_ERR_ARG, "unknown mode %d", mode);
+  p->mode = mode;
+  return DG_OK;
+}
+
+int dg_set_option(dg_plan_t p, int option, int64_t value) {
+  if (!p) return fail(DG_ERR_ARG, "plan is NULL");
+  switch (option) {
+    case DG_OPT_TIMEOUT_MS:
+      if (value <= 0) return fail(DG_ERR_ARG, "timeout must be > 0");
+      p->timeout_ms = value;
+      return DG_OK;
+    case DG_OPT_CHUNK_TILES:
+      if (value < 0) return fail(DG_ERR_ARG, "chunk tiles must be >= 0");
+      p->chunk_tiles_req = value;
+      layout(p);
+      return DG_OK;
+    case DG_OPT_FAULT_SKIP_FLAG:
+      p->fault_skip = value;
+      return DG_OK;
+    case DG_OPT_FAULT_DELAY_MS:
+      if (value < 0) return fail(DG_ERR_ARG, "delay must be >= 0");
+      p->fault_delay_ms = value;
+      return DG_OK;
+    case DG_OPT_GRID:
+      if (value < 0) return fail(DG_ERR_ARG, "grid must be >= 0");
+      p->grid_req = value;
+      return DG_OK;
+    case DG_OPT_COPY_STREAMS:
+      return value == 1 ? DG_OK : fail(DG_ERR_UNSUPPORTED, "one copy stream only");
+    default:
+      return fail(DG_ERR_ARG, "unknown option %d", option);
+  }
+}
+
+int dg_plan_info_get(dg_plan_t p, dg_plan_info* o) {
+  if (!p || !o) return fail(DG_ERR_ARG, "NULL argument");
+  std::memset(o, 0, sizeof(*o));
+  const dg::Geom& g = p->g;
+  o->m = p->m, o->n = p->n, o->k = p->k, o->l = p->l;
+  o->tp = p->tp, o->schedule = p->schedule;
+  o->local_m = g.blk_m, o->local_n = g.blk_n, o->local_k = g.Ks;
+  o->tile_m = g.BM, o->tile_n = g.BN, o->tile_k = g.BK;
+  o->tiles_m = g.tiles_m, o->tiles_n = g.tiles_n;
+  o->total_tiles = g.total_tiles;
+  o->chunk_tiles = g.chunk_tiles, o->chunks_per_shard = g.nchunks;
+  o->n_flags = p->n_flags;
+  o->ws_bytes = dg_workspace_bytes(p);
+  o->off_status = p->off_status, o->off_flags = p->off_flags, o->off_slots = p->off_slots;
+  o->off_partial = p->off_partial, o->off_serial = p->off_serial;
+  o->slot_bytes = p->slot_bytes;
+  o->copies_per_run = p->copies;
+  return DG_OK;
+}
+
+int dg_plan_tile(dg_plan_t p, int64_t t, dg_tile* o) {
+  if (!p || !o) return fail(DG_ERR_ARG, "NULL argument");
+  if (t < 0 || t >= p->g.total_tiles) return fail(DG_ERR_ARG, "tile %lld out of range", (long long)t);
+  const dg::Tile tl = dg::decode_tile(p->g, t);
+  o->step = tl.s, o->rank = tl.r, o->slab = tl.j, o->batch = tl.l;
+  o->a_map = tl.a_map, o->b_map = tl.b_map;
+  o->a_row = tl.a_row, o->b_row = tl.b_row;
+  o->out_row = tl.out_row, o->out_col = tl.out_col;
+  o->rows_valid = tl.rows_valid, o->cols_valid = tl.cols_valid;
+  o->k_blocks = tl.k_blocks;
+  o->flag = tl.flag, o->tile_flag = tl.tile_flag;
+  o->src = tl.src, o->dst = tl.dst;
+  return DG_OK;
+}
+
+int dg_run(dg_plan_t p, const dg_bf16_t* A, const dg_bf16_t* B, const dg_bf16_t* C, dg_bf16_t* D,
+           void* workspace, void* main_stream, void* copy_stream) {
+  if (!p) return fail(DG_ERR_ARG, "plan is NULL");
+  if (p->g.total_tiles == 0) return DG_OK;  // empty output
+  if (!A || !B || !D) return fail(DG_ERR_ARG, "A, B and D must be non-NULL");
+  if (p->beta != 0.f && !C) return fail(DG_ERR_ARG, "C is NULL but beta != 0");
+  auto misaligned = [](const void* q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) & (a - 1)) != 0; };
+  if (misaligned(A, 16) || misaligned(B, 16) || misaligned(D, 16) || (C && misaligned(C, 16)))
+    return fail(DG_ERR_ARG, "A, B, C and D must be 16-byte aligned");
+  const size_t need = dg_workspace_bytes(p);
+  if (need > 0 && (!workspace || misaligned(workspace, 256)))
+    return fail(DG_ERR_ARG, "workspace must be non-NULL and 256-byte aligned");
+  const bool rs_serial = !is_ag(p->schedule) && p->mode == DG_MODE_SERIAL;
+  if (rs_serial) return fail(DG_ERR_UNSUPPORTED, "RS SERIAL baseline not available");
+  int rc = rt_init(p);
+  if (rc) return rc;
+  Driver drv;
+  rc = get_driver(&drv);
+  if (rc) return rc;
+  auto ms = static_cast<cudaStream_t>(main_stream);
+  auto cs = static_cast<cudaStream_t>(copy_stream);
+  auto* ws = static_cast<uint8_t*>(workspace);
+
+  bool clear = false;
+  {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    auto it = g_ws_owner.find(workspace);
+    if (it == g_ws_owner.end() || it->second != p->id) {
+      g_ws_owner[workspace] = p->id;
+      clear = true;
+    }
+  }
+  if ((uint64_t)(p->epoch + 2) * (uint64_t)p->tp >= 0x7FFFFFFFull) clear = true;
+  if (clear) {
+    DG_CUDA(cudaMemsetAsync(ws, 0, p->off_flags + (size_t)p->n_flags * 4, ms));
+    p->epoch = 0;
+  }
+  p->epoch += 1;
+
+  rc = build_maps(p, drv, A, B, ws);
+  if (rc) return rc;
+  dg::KParams& kp = p->kp;
+  kp.g = p->g;
+  kp.C = reinterpret_cast<const __nv_bfloat16*>(C);
+  kp.D = reinterpret_cast<__nv_bfloat16*>(D);
+  kp.X = reinterpret_cast<float*>(ws + p->off_partial);
+  kp.flags = reinterpret_cast<uint32_t*>(ws + p->off_flags);
+  kp.status = reinterpret_cast<unsigned long long*>(ws + p->off_status);
+  kp.epoch = p->epoch;
+  kp.alpha = p->alpha;
+  kp.beta = p->beta;
+  kp.n_maps = p->n_maps;
+  kp.timeout_ns = (uint64_t)p->timeout_ms * 1000000ull;
+  kp.hang_ns = kp.timeout_ns * 4 + 1000000000ull;
+
+  if (is_ag(p->schedule) && p->tp > 1) {
+    int mode = p->mode;
+    if (mode == DG_MODE_FUSED && (cs == ms || cs == nullptr)) mode = DG_MODE_SERIAL;
+    if (mode == DG_MODE_FUSED) {
+      DG_CUDA(cudaEventRecord(p->ev_fork, ms));
+      rc = launch(p, ms, 1);
+      if (rc) return rc;
+      DG_CUDA(cudaStreamWaitEvent(cs, p->ev_fork, 0));
+      rc = enqueue_copies(p, drv, A, B, ws, cs);
+      if (rc) return rc;
+      DG_CUDA(cudaEventRecord(p->ev_join, cs));
+      DG_CUDA(cudaStreamWaitEvent(ms, p->ev_join, 0));
+    } else if (mode == DG_MODE_SERIAL) {
+      rc = enqueue_copies(p, drv, A, B, ws, ms);
+      if (rc) return rc;
+      rc = launch(p, ms, 1);
+      if (rc) return rc;
+    } else {
+      rc = launch(p, ms, 0);
+      if (rc) return rc;
+    }
+  } else {
+    rc = launch(p, ms, 0);
+    if (rc) return rc;
+  }
+  return DG_OK;
+}
+
+int dg_check(dg_plan_t p, void* workspace, void* stream) {
+  if (!p) return fail(DG_ERR_ARG, "plan is NULL");
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  if (!workspace || p->epoch == 0) return DG_OK;
+  unsigned long long st = 0;
+  e = cudaMemcpy(&st, static_cast<uint8_t*>(workspace) + p->off_status, sizeof(st), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
+  if ((uint32_t)(st >> 32) != p->epoch) return DG_OK;
+  const uint32_t code = (uint32_t)(st >> 24) & 0xFF;
+  const uint32_t info = (uint32_t)st & 0xFFFFFF;
+  if (code == dg::DEV_TIMEOUT)
+    return fail(DG_ERR_TIMEOUT, "ready-flag wait ran out (flag %u, run %u)", info, p->epoch);
+  if (code == dg::DEV_HANG)
+    return fail(DG_ERR_HANG, "pipeline wait ran out (barrier 0x%06x, run %u)", info, p->epoch);
+  return fail(DG_ERR_STATE, "unknown device status 0x%llx", st);
+}
+
+void dg_destroy(dg_plan_t p) {
+  if (!p) return;
+  {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    for (auto it = g_ws_owner.begin(); it != g_ws_owner.end();)
+      it = it->second == p->id ? g_ws_owner.erase(it) : std::next(it);
+  }
+  if (p->ev_fork) cudaEventDestroy(p->ev_fork);
+  if (p->ev_join) cudaEventDestroy(p->ev_join);
+  delete p;
+}
+
+}  // extern "C"

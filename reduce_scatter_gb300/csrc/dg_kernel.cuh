@@ -1,0 +1,575 @@
+// dg_kernel.cuh -- persistent tcgen05 GEMM with shard-rotation tile order,
+// flag-gated TMA producer and rotating-partial (RotatingC) epilogue, sm_103a.
+//
+// One CTA per SM, 192 threads:
+//   warp 0      TMA producer: for each tile, waits (acquire, bounded) on the
+//               ready flag of the shard chunk the tile reads, then streams
+//               64-wide K blocks of A (BM x 64) and B (BN x 64) into a ring of
+//               STAGES shared-memory buffers (128-byte swizzle).
+//   warp 1      MMA issuer: allocates 2 x BN TMEM columns (two fp32
+//               accumulators of BM lanes x BN columns), issues
+//               tcgen05.mma.cta_group::1.kind::f16 (bf16 x bf16 -> fp32), four
+//               K=16 instructions per K block, and commits stage release and
+//               accumulator-full barriers.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (each warp owns the 32
+//               TMEM lanes of its warp id mod 4), d = alpha*acc + source, where
+//               the source is beta*C (AG, RS step 0), the rotating fp32 partial
+//               (RS later steps) or nothing; writes bf16 D or the fp32 partial.
+//
+// Ordering across proxies:
+//   copy engine -> shard data, then stream write of the ready flag;
+//   producer: ld.acquire.gpu(flag) -> fence.proxy.async.global -> TMA loads.
+//   RS epilogue: partial stores -> fence (gpu) -> named barrier ->
+//   st.release.gpu(tile flag); the next step's epilogue acquires the flag and
+//   reads the partial with L1-bypassing loads.
+//
+// Every wait is bounded: flag waits by a timeout (on expiry the kernel records
+// DG timeout in the workspace status word and carries on with whatever the
+// buffer holds, so the pipeline drains normally); pipeline barrier waits by a
+// longer limit, after which the kernel records a hang, stops issuing work,
+// waits (bounded) for its own copies and MMAs in flight, frees its TMEM and
+// exits.  Nothing traps.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "dg_geom.h"
+
+namespace dg {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int MAX_MAPS = 9;  // RS: one K-slab map per rank (P <= 8); AG: home + slots
+constexpr int NUM_THREADS = 192;
+constexpr int EPI_THREADS = 128;
+constexpr uint32_t A_BYTES = BM * BK * 2;
+constexpr uint32_t B_BYTES = BN * BK * 2;
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
+constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+
+// Device status word: (epoch << 32) | (code << 24) | (info & 0xffffff).
+constexpr uint32_t DEV_TIMEOUT = 1;  // a ready-flag wait ran out
+constexpr uint32_t DEV_HANG = 2;     // a pipeline wait ran out
+
+struct KParams {
+  CUtensorMap tmA[MAX_MAPS];
+  CUtensorMap tmB[MAX_MAPS];
+  Geom g;
+  const __nv_bfloat16* C;
+  __nv_bfloat16* D;
+  float* X;
+  uint32_t* flags;  // AG chunk flags or RS tile flags
+  unsigned long long* status;
+  uint32_t epoch;
+  uint32_t wait_flags;  // AG: 1 = wait on chunk flags
+  int32_t n_maps;       // tensor maps in use (each of tmA / tmB)
+  float alpha, beta;
+  uint64_t timeout_ns;
+  uint64_t hang_ns;
+};
+
+// ------------------------------------------------------------------ PTX glue
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// tcgen05 ---------------------------------------------------------------
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 lanes x 32 columns of 32-bit: thread i of the warp gets lane (base+i),
+// columns col..col+31.
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile whose rows are
+// 64 bf16 (128 bytes) stored with the 128-byte swizzle, 8-row groups 1024
+// bytes apart (the layout a TMA load with SWIZZLE_128B writes).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address, 16-byte units
+  d |= (uint64_t)1 << 16;                     // leading byte offset (unused here)
+  d |= (uint64_t)(1024 >> 4) << 32;           // stride byte offset: 8-row group pitch
+  d |= (uint64_t)1 << 46;                     // descriptor version (tcgen05)
+  d |= (uint64_t)2 << 61;                     // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+
+// ---------------------------------------------------------------- status
+
+__device__ __forceinline__ bool status_set(const KParams& p) {
+  return (uint32_t)(ld_relaxed_u64(p.status) >> 32) == p.epoch;
+}
+__device__ __forceinline__ bool status_hang(const KParams& p) {
+  unsigned long long v = ld_relaxed_u64(p.status);
+  return (uint32_t)(v >> 32) == p.epoch && ((uint32_t)(v >> 24) & 0xFF) == DEV_HANG;
+}
+// First error of this epoch wins.
+__device__ __noinline__ void status_record(const KParams& p, uint32_t code, uint32_t info) {
+  unsigned long long want =
+      ((unsigned long long)p.epoch << 32) | ((unsigned long long)(code & 0xFF) << 24) | (info & 0xFFFFFF);
+  unsigned long long old = ld_relaxed_u64(p.status);
+  while ((uint32_t)(old >> 32) != p.epoch) {
+    unsigned long long seen = atomicCAS(p.status, old, want);
+    if (seen == old) break;
+    old = seen;
+  }
+}
+
+// Wait until *f >= target.  false if it ran out (status recorded) or an
+// earlier error of this run is already recorded (then it does not wait).
+__device__ __noinline__ bool wait_flag_geq(const KParams& p, const uint32_t* f, uint32_t target,
+                                           uint32_t info) {
+  if (ld_acquire_u32(f) >= target) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t n = 1;; ++n) {
+    if (ld_acquire_u32(f) >= target) return true;
+    if ((n & 31) == 0) {
+      if (status_set(p)) return false;
+      if (globaltimer() - t0 > p.timeout_ns) {
+        status_record(p, DEV_TIMEOUT, info);
+        return false;
+      }
+    }
+    __nanosleep(128);
+  }
+}
+
+// Bounded mbarrier wait.  false: this or another CTA ran out (hang recorded).
+__device__ __forceinline__ bool mbar_wait(const KParams& p, uint32_t bar, uint32_t parity,
+                                          uint32_t info) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = 0;
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 255) == 0) {
+      if (t0 == 0) t0 = globaltimer();
+      if (status_hang(p)) return false;
+      if (globaltimer() - t0 > p.hang_ns) {
+        status_record(p, DEV_HANG, info);
+        return false;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------- epilogue math
+
+struct alignas(16) F4 {
+  float x, y, z, w;
+};
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Source term (beta*C, the fp32 partial, or 0) for 32 consecutive columns of
+// one output row, then d = alpha*acc + src, stored as bf16 D or fp32 partial.
+__device__ __forceinline__ void epilogue_row_chunk(const KParams& p, const Tile& tl, int64_t grow,
+                                                   int64_t gcol, int ncols, float (&acc)[32]) {
+  const int64_t N = p.g.N;
+  const int64_t e0 = grow * N + gcol;  // element offset in C / D / X
+  float src[32];
+  if (tl.src == SRC_C) {
+    const __nv_bfloat16* c = p.C + e0;
+    if (ncols == 32 && (e0 & 7) == 0) {
+      const uint4* c4 = reinterpret_cast<const uint4*>(c);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 v = __ldg(c4 + q);
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          src[q * 8 + 2 * h] = p.beta * bf16_bits_to_f32(w[h] & 0xFFFFu);
+          src[q * 8 + 2 * h + 1] = p.beta * bf16_bits_to_f32(w[h] >> 16);
+        }
+      }
+    } else {
+      const uint16_t* cs = reinterpret_cast<const uint16_t*>(c);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) src[i] = i < ncols ? p.beta * bf16_bits_to_f32(cs[i]) : 0.f;
+    }
+  } else if (tl.src == SRC_X) {
+    const float* x = p.X + e0;
+    if (ncols == 32 && (e0 & 3) == 0) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float4 v = __ldcg(reinterpret_cast<const float4*>(x) + q);
+        src[4 * q] = v.x;
+        src[4 * q + 1] = v.y;
+        src[4 * q + 2] = v.z;
+        src[4 * q + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) src[i] = i < ncols ? __ldcg(x + i) : 0.f;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) src[i] = 0.f;
+  }
+  float out[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) out[i] = fmaf(p.alpha, acc[i], src[i]);
+
+  if (tl.dst == DST_D) {
+    __nv_bfloat16* d = p.D + e0;
+    if (ncols == 32 && (e0 & 7) == 0) {
+      uint4* d4 = reinterpret_cast<uint4*>(d);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 v;
+        v.x = pack_bf16x2(out[8 * q + 0], out[8 * q + 1]);
+        v.y = pack_bf16x2(out[8 * q + 2], out[8 * q + 3]);
+        v.z = pack_bf16x2(out[8 * q + 4], out[8 * q + 5]);
+        v.w = pack_bf16x2(out[8 * q + 6], out[8 * q + 7]);
+        d4[q] = v;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < ncols) d[i] = __float2bfloat16_rn(out[i]);
+    }
+  } else {
+    float* x = p.X + e0;
+    if (ncols == 32 && (e0 & 3) == 0) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        __stcg(reinterpret_cast<float4*>(x) + q,
+               make_float4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < ncols) __stcg(x + i, out[i]);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+
+__global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_constant__ KParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
+  const uint32_t bar_full = smem_u32(bars);
+  const uint32_t bar_empty = smem_u32(bars + STAGES);
+  const uint32_t bar_tfull = smem_u32(bars + 2 * STAGES);
+  const uint32_t bar_tempty = smem_u32(bars + 2 * STAGES + 2);
+  const uint32_t bar_drain = smem_u32(bars + 2 * STAGES + 4);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile uint32_t* s_go = s_tmem + 1;  // [2] epilogue go/abort, by tile parity
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(bar_full + 8 * i, 1);
+      mbar_init(bar_empty + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_tfull + 8 * i, 1);
+      mbar_init(bar_tempty + 8 * i, EPI_THREADS);
+    }
+    mbar_init(bar_drain, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(s_tmem), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+
+  const int64_t T = p.g.total_tiles;
+  const uint32_t smem_base = smem_u32(smem);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      for (int i = 0; i < p.n_maps; ++i) {
+        prefetch_tmap(&p.tmA[i]);
+        prefetch_tmap(&p.tmB[i]);
+      }
+      uint32_t stage = 0, phase = 0;
+      int32_t issued[STAGES];  // parity of the last load issued per stage, -1 none
+      for (int i = 0; i < STAGES; ++i) issued[i] = -1;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < T && ok; t += gridDim.x) {
+        const Tile tl = decode_tile(p.g, t);
+        if (tl.flag >= 0 && p.wait_flags) {
+          wait_flag_geq(p, p.flags + tl.flag, p.epoch, (uint32_t)tl.flag);
+          fence_proxy_async_global();
+        }
+        const CUtensorMap* ma = &p.tmA[tl.a_map];
+        const CUtensorMap* mb = &p.tmB[tl.b_map];
+        for (int kb = 0; kb < tl.k_blocks; ++kb) {
+          if (!mbar_wait(p, bar_empty + 8 * stage, phase ^ 1, 0x100000u | stage)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = bar_full + 8 * stage;
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const uint32_t sa = smem_base + stage * STAGE_BYTES;
+          tma_load_2d(sa, ma, fb, kb * BK, (int32_t)tl.a_row);
+          tma_load_2d(sa + A_BYTES, mb, fb, kb * BK, (int32_t)tl.b_row);
+          issued[stage] = (int32_t)phase;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // drain: every load issued must land before the CTA exits
+        for (int i = 0; i < STAGES; ++i)
+          if (issued[i] >= 0) {
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(bar_full + 8 * i, (uint32_t)issued[i]) &&
+                   globaltimer() - t0 < 200000000ull) {
+            }
+          }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // --------------------------------------------------------------- MMA
+      constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+      uint32_t stage = 0, phase = 0, it = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < T && ok; t += gridDim.x, ++it) {
+        const Tile tl = decode_tile(p.g, t);
+        const uint32_t buf = it & 1, use = it >> 1;
+        if (!mbar_wait(p, bar_tempty + 8 * buf, (use & 1) ^ 1, 0x200000u | buf)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * BN;
+        for (int kb = 0; kb < tl.k_blocks; ++kb) {
+          if (!mbar_wait(p, bar_full + 8 * stage, phase, 0x300000u | stage)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_base + stage * STAGE_BYTES;
+          const uint64_t da = smem_desc_sw128(sa);
+          const uint64_t db = smem_desc_sw128(sa + A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // +32 bytes per K=16 step inside the swizzled 128-byte row
+            tc_mma_bf16(d_tmem, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), IDESC,
+                        (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(bar_empty + 8 * stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(bar_tfull + 8 * buf);
+      }
+      if (!ok) {
+        tc_commit(bar_drain);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(bar_drain, 0) && globaltimer() - t0 < 200000000ull) {
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int et = threadIdx.x - 64;  // 0..127
+    const int q = warp & 3;           // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;    // accumulator row = TMEM lane
+    uint32_t it = 0;
+    for (int64_t t = blockIdx.x; t < T; t += gridDim.x, ++it) {
+      const Tile tl = decode_tile(p.g, t);
+      const uint32_t buf = it & 1, use = it >> 1;
+      if (et == 0) {
+        bool go = mbar_wait(p, bar_tfull + 8 * buf, use & 1, 0x400000u | buf);
+        if (go && tl.tile_flag >= 0 && tl.s > 0) {
+          // partial of this tile from the previous step
+          wait_flag_geq(p, p.flags + tl.tile_flag, p.epoch * (uint32_t)p.g.P + (uint32_t)tl.s - 1,
+                        (uint32_t)tl.tile_flag);
+        }
+        s_go[it & 1] = go ? 1u : 0u;
+      }
+      named_bar_sync(1, EPI_THREADS);
+      if (s_go[it & 1] == 0) break;
+      tc_fence_after();
+      const bool row_ok = row < tl.rows_valid;
+      const int64_t grow = tl.out_row + row;
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        if (c * 32 >= tl.cols_valid) break;  // uniform across the CTA
+        float acc[32];
+        if (tl.k_blocks > 0) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(v[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+        }
+        if (row_ok) {
+          const int ncols = tl.cols_valid - c * 32 < 32 ? tl.cols_valid - c * 32 : 32;
+          epilogue_row_chunk(p, tl, grow, tl.out_col + c * 32, ncols, acc);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar_tempty + 8 * buf);
+      if (tl.tile_flag >= 0 && tl.dst == DST_X) {
+        __threadfence();
+        named_bar_sync(1, EPI_THREADS);
+        if (et == 0) st_release_u32(p.flags + tl.tile_flag, p.epoch * (uint32_t)p.g.P + (uint32_t)tl.s);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace dg

@@ -1,0 +1,217 @@
+"""ctypes binding of the C ABI in ``include/dg.h`` (argument marshalling only).
+
+Every computation runs in ``_lib/libdg.so``.  If the library has not been
+built, importing works but the first call raises ``RuntimeError``: there is
+no fallback path.
+
+Pointers are accepted as ``torch.Tensor`` (its ``data_ptr()``), plain ints or
+``None``; streams as ``torch.cuda.Stream`` or raw ``cudaStream_t`` ints.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libdg.so")
+
+AG_ROTATING_A = 0
+AG_ROTATING_B = 1
+RS_TILING_A_ROTATING_C = 2
+RS_TILING_B_ROTATING_C = 3
+SCHEDULE_NAMES = {
+    AG_ROTATING_A: "AllGather1D_TilingCD_RotatingA",
+    AG_ROTATING_B: "AllGather1D_TilingCD_RotatingB",
+    RS_TILING_A_ROTATING_C: "ReduceScatter1D_TilingA_RotatingC",
+    RS_TILING_B_ROTATING_C: "ReduceScatter1D_TilingB_RotatingC",
+}
+SCHEDULE_BY_NAME = {v: k for k, v in SCHEDULE_NAMES.items()}
+
+MODE_FUSED = 0
+MODE_GEMM_ONLY = 1
+MODE_SERIAL = 2
+
+OK = 0
+ERR_ARG = -1
+ERR_SHAPE = -2
+ERR_UNSUPPORTED = -3
+ERR_CUDA = -4
+ERR_TIMEOUT = -5
+ERR_HANG = -6
+ERR_STATE = -7
+
+OPT_TIMEOUT_MS = 0
+OPT_CHUNK_TILES = 1
+OPT_FAULT_SKIP_FLAG = 2
+OPT_FAULT_DELAY_MS = 3
+OPT_GRID = 4
+OPT_COPY_STREAMS = 5
+
+# Every symbol include/dg.h declares.
+EXPORTS = ("dg_plan", "dg_workspace_bytes", "dg_run_mode", "dg_set_option", "dg_run", "dg_check",
+           "dg_plan_info_get", "dg_plan_tile", "dg_destroy", "dg_last_error")
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [
+        ("m", ctypes.c_int64), ("n", ctypes.c_int64), ("k", ctypes.c_int64), ("l", ctypes.c_int64),
+        ("tp", ctypes.c_int32), ("schedule", ctypes.c_int32),
+        ("local_m", ctypes.c_int64), ("local_n", ctypes.c_int64), ("local_k", ctypes.c_int64),
+        ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("tile_k", ctypes.c_int32),
+        ("tiles_m", ctypes.c_int64), ("tiles_n", ctypes.c_int64),
+        ("total_tiles", ctypes.c_int64),
+        ("chunk_tiles", ctypes.c_int64), ("chunks_per_shard", ctypes.c_int64),
+        ("n_flags", ctypes.c_int64),
+        ("ws_bytes", ctypes.c_size_t),
+        ("off_status", ctypes.c_size_t), ("off_flags", ctypes.c_size_t), ("off_slots", ctypes.c_size_t),
+        ("off_partial", ctypes.c_size_t), ("off_serial", ctypes.c_size_t),
+        ("slot_bytes", ctypes.c_size_t),
+        ("copies_per_run", ctypes.c_int64),
+    ]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class Tile(ctypes.Structure):
+    _fields_ = [
+        ("step", ctypes.c_int32), ("rank", ctypes.c_int32), ("slab", ctypes.c_int32), ("batch", ctypes.c_int32),
+        ("a_map", ctypes.c_int32), ("b_map", ctypes.c_int32),
+        ("a_row", ctypes.c_int64), ("b_row", ctypes.c_int64),
+        ("out_row", ctypes.c_int64), ("out_col", ctypes.c_int64),
+        ("rows_valid", ctypes.c_int32), ("cols_valid", ctypes.c_int32),
+        ("k_blocks", ctypes.c_int32),
+        ("flag", ctypes.c_int64), ("tile_flag", ctypes.c_int64),
+        ("src", ctypes.c_int32), ("dst", ctypes.c_int32),
+    ]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class DGError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"dg error {code}: {msg}")
+        self.code = code
+
+
+_LIB = None
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+        L.dg_plan.argtypes = [ctypes.POINTER(vp), i64, i64, i64, i64, i32, i32, ctypes.c_float, ctypes.c_float]
+        L.dg_plan.restype = i32
+        L.dg_workspace_bytes.argtypes = [vp]
+        L.dg_workspace_bytes.restype = ctypes.c_size_t
+        L.dg_run_mode.argtypes = [vp, i32]
+        L.dg_run_mode.restype = i32
+        L.dg_set_option.argtypes = [vp, i32, i64]
+        L.dg_set_option.restype = i32
+        L.dg_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
+        L.dg_run.restype = i32
+        L.dg_check.argtypes = [vp, vp, vp]
+        L.dg_check.restype = i32
+        L.dg_plan_info_get.argtypes = [vp, ctypes.POINTER(PlanInfo)]
+        L.dg_plan_info_get.restype = i32
+        L.dg_plan_tile.argtypes = [vp, i64, ctypes.POINTER(Tile)]
+        L.dg_plan_tile.restype = i32
+        L.dg_destroy.argtypes = [vp]
+        L.dg_destroy.restype = None
+        L.dg_last_error.argtypes = []
+        L.dg_last_error.restype = ctypes.c_char_p
+        _LIB = L
+    return _LIB
+
+
+def last_error() -> str:
+    return lib().dg_last_error().decode()
+
+
+def _check(rc: int):
+    if rc != OK:
+        raise DGError(rc, last_error())
+    return rc
+
+
+def ptr(x) -> int | None:
+    """Device address of a tensor / int / None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def stream_handle(s) -> int | None:
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+class Plan:
+    """One problem (m, n, k, l, tp, schedule, alpha, beta) behind ``dg_plan``."""
+
+    def __init__(self, m, n, k, l, tp, schedule, alpha=1.0, beta=0.0):
+        if isinstance(schedule, str):
+            schedule = SCHEDULE_BY_NAME[schedule]
+        h = ctypes.c_void_p()
+        _check(lib().dg_plan(ctypes.byref(h), m, n, k, l, tp, schedule, alpha, beta))
+        self._h = h
+        self.m, self.n, self.k, self.l, self.tp, self.schedule = m, n, k, l, tp, schedule
+        self.alpha, self.beta = alpha, beta
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if self._h:
+            lib().dg_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def workspace_bytes(self) -> int:
+        return int(lib().dg_workspace_bytes(self._h))
+
+    def set_mode(self, mode: int):
+        _check(lib().dg_run_mode(self._h, mode))
+
+    def set_option(self, opt: int, value: int):
+        _check(lib().dg_set_option(self._h, opt, value))
+
+    def info(self) -> dict:
+        inf = PlanInfo()
+        _check(lib().dg_plan_info_get(self._h, ctypes.byref(inf)))
+        return inf.as_dict()
+
+    def tile(self, t: int) -> dict:
+        tl = Tile()
+        _check(lib().dg_plan_tile(self._h, t, ctypes.byref(tl)))
+        return tl.as_dict()
+
+    def run(self, A, B, C, D, workspace, main_stream=None, copy_stream=None, raise_on_error=True) -> int:
+        rc = lib().dg_run(self._h, ptr(A), ptr(B), ptr(C), ptr(D), ptr(workspace),
+                          stream_handle(main_stream), stream_handle(copy_stream))
+        if raise_on_error:
+            _check(rc)
+        return rc
+
+    def check(self, workspace, stream=None, raise_on_error=True) -> int:
+        rc = lib().dg_check(self._h, ptr(workspace), stream_handle(stream))
+        if raise_on_error:
+            _check(rc)
+        return rc

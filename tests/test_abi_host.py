@@ -1,0 +1,211 @@
+"""The C ABI without a GPU: the library loads and exports every declared
+symbol; the planner validates shapes; the tile order it decodes visits every
+(output element, K range) exactly once, in the rotation the oracle states."""
+
+import ctypes
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import schedules as osch
+from reduce_scatter_gb300 import dg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SCHED_NAME = {dg.AG_ROTATING_A: osch.AG_ROTATING_A, dg.AG_ROTATING_B: osch.AG_ROTATING_B,
+              dg.RS_TILING_A_ROTATING_C: osch.RS_TILING_A_ROTATING_C,
+              dg.RS_TILING_B_ROTATING_C: osch.RS_TILING_B_ROTATING_C}
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(dg.LIB_PATH):
+        import __graft_entry__
+
+        __graft_entry__.build()
+    return dg.lib()
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "dg.h")) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dg_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert set(names) == set(dg.EXPORTS), names
+    for name in names:
+        assert hasattr(L, name), name
+
+
+def test_struct_sizes_match_header(L):
+    # the ctypes mirrors must have the C layout: probe through the ABI
+    p = dg.Plan(256, 256, 256, 1, 2, dg.AG_ROTATING_A)
+    info = p.info()
+    assert info["m"] == 256 and info["tp"] == 2 and info["schedule"] == 0
+    assert info["ws_bytes"] == p.workspace_bytes()
+
+
+@pytest.mark.parametrize("args,code", [
+    ((-1, 8, 8, 1, 1, 0), dg.ERR_ARG),
+    ((8, 8, 8, 1, 3, 0), dg.ERR_ARG),
+    ((8, 8, 8, 1, 2, 7), dg.ERR_ARG),
+    ((8, 8, 12, 1, 1, 0), dg.ERR_SHAPE),          # K % 8
+    ((8, 12, 8, 1, 1, 0), dg.ERR_SHAPE),          # N % 8
+    ((10, 16, 8, 1, 4, dg.AG_ROTATING_A), dg.ERR_SHAPE),   # M % tp
+    ((10, 16, 8, 1, 4, dg.AG_ROTATING_B), dg.ERR_SHAPE),   # M % tp (B rotates, M still sharded)
+    ((12, 16, 64, 1, 8, dg.RS_TILING_A_ROTATING_C), dg.ERR_SHAPE),  # M % tp
+    ((16, 16, 24, 1, 2, dg.RS_TILING_A_ROTATING_C), dg.ERR_SHAPE),  # (K/tp) % 8
+    ((16, 16, 36, 1, 8, dg.RS_TILING_B_ROTATING_C), dg.ERR_SHAPE),  # K % 8
+])
+def test_plan_rejects(L, args, code):
+    h = ctypes.c_void_p()
+    rc = L.dg_plan(ctypes.byref(h), *args, 1.0, 0.0)
+    assert rc == code
+    assert dg.last_error()
+
+
+def test_null_and_bad_options(L):
+    assert L.dg_plan(None, 8, 8, 8, 1, 1, 0, 1.0, 0.0) == dg.ERR_ARG
+    p = dg.Plan(16, 16, 16, 1, 1, 0)
+    with pytest.raises(dg.DGError):
+        p.set_mode(9)
+    with pytest.raises(dg.DGError):
+        p.set_option(99, 1)
+    with pytest.raises(dg.DGError):
+        p.set_option(dg.OPT_TIMEOUT_MS, 0)
+    with pytest.raises(dg.DGError):
+        p.tile(p.info()["total_tiles"])
+
+
+def test_run_argument_checks_without_gpu(L):
+    # argument checks come before any CUDA call
+    p = dg.Plan(256, 256, 256, 1, 2, dg.AG_ROTATING_A, 1.0, 0.5)
+    assert p.run(16, 16, None, 16, 256, raise_on_error=False) == dg.ERR_ARG  # C NULL with beta != 0
+    p2 = dg.Plan(256, 256, 256, 1, 2, dg.AG_ROTATING_A)
+    assert p2.run(16, 24, None, 16, 256, raise_on_error=False) == dg.ERR_ARG  # misaligned B
+    assert p2.run(None, 16, None, 16, 256, raise_on_error=False) == dg.ERR_ARG
+    assert p2.run(16, 16, None, 16, 128, raise_on_error=False) == dg.ERR_ARG  # workspace alignment
+
+
+def test_empty_problem_is_a_noop(L):
+    for m, n, k, l in [(0, 16, 16, 1), (16, 0, 16, 1), (16, 16, 16, 0)]:
+        p = dg.Plan(m, n, k, l, 1, dg.AG_ROTATING_A)
+        assert p.info()["total_tiles"] == 0
+        assert p.run(None, None, None, None, None, raise_on_error=False) == dg.OK
+
+
+def test_local_sizes_match_pr_printout(L, golden_dir):
+    with open(os.path.join(golden_dir, "pr1907_distgemm_printout.json")) as f:
+        g = json.load(f)
+    for run in g["runs"]:
+        m, n, k, l = run["problem"]
+        info = dg.Plan(m, n, k, l, run["tp"], dg.AG_ROTATING_A).info()
+        assert (info["local_m"], info["local_n"], info["local_k"], info["l"]) == tuple(run["local_problem"])
+
+
+def _simulate(plan, m, n, k, l, tp, sched):
+    """Walk the decoded order; check coverage and rotation against the oracle."""
+    info = plan.info()
+    T = info["total_tiles"]
+    name = SCHED_NAME[sched]
+    cover = np.zeros((l, m, n), dtype=np.int64)    # (output element, k-slab) visits via k ranges
+    kcover = np.zeros((l, m, n, tp if sched >= 2 else 1), dtype=np.int64)
+    last_step = {}
+    prev_block_end = -1
+    for t in range(T):
+        tl = plan.tile(t)
+        s, r, j, b = tl["step"], tl["rank"], tl["slab"], tl["batch"]
+        assert j == osch.slab_index(name, tp, r, s)
+        blk = osch.step_blocks(name, m, n, k, tp, r, s)
+        rows = slice(tl["out_row"] - b * m, tl["out_row"] - b * m + tl["rows_valid"])
+        cols = slice(tl["out_col"], tl["out_col"] + tl["cols_valid"])
+        # the tile lies inside the oracle's block for (r, s)
+        assert blk["rows"].start <= rows.start and rows.stop <= blk["rows"].stop
+        assert blk["cols"].start <= cols.start and cols.stop <= blk["cols"].stop
+        cover[b, rows, cols] += 1
+        if sched >= 2:
+            kcover[b, rows, cols, r] += 1
+            want_src = (1 if info and plan.beta != 0 else 0) if s == 0 else 2
+            assert tl["src"] == want_src
+            assert tl["dst"] == (0 if s == tp - 1 else 1)
+            assert tl["a_map"] == r and tl["b_map"] == r
+            assert tl["k_blocks"] == -(-(k // tp) // 64)
+            key = (b, rows.start, cols.start)
+            assert last_step.get(key, -1) == s - 1, "steps of one tile in order"
+            last_step[key] = s
+        else:
+            assert tl["k_blocks"] == -(-k // 64)
+            local = (blk["recv"] is None)
+            assert (tl["flag"] < 0) == local
+            if sched == dg.AG_ROTATING_A:
+                assert tl["a_map"] == (0 if local else 1)
+                assert tl["b_row"] == b * n + tl["out_col"]
+                if local:
+                    assert tl["a_row"] == tl["out_row"]
+            else:
+                assert tl["b_map"] == (0 if local else 1)
+                assert tl["a_row"] == tl["out_row"]
+            if not local:
+                assert 0 <= tl["flag"] < info["n_flags"]
+        # step-major order
+        blk_id = s * tp + r
+        assert blk_id >= prev_block_end
+        prev_block_end = blk_id
+    if sched >= 2:
+        assert np.all(kcover == 1)
+        assert tp == 1 or all(v == tp - 1 for v in last_step.values())
+    assert np.all(cover == (tp if sched >= 2 else 1))
+
+
+@pytest.mark.parametrize("sched", [0, 1, 2, 3])
+@pytest.mark.parametrize("tp", [1, 2, 4, 8])
+@pytest.mark.parametrize("shape", [(256, 512, 128, 1), (1024, 768, 512, 2), (136, 272, 80, 1)])
+def test_tile_order_simulator(L, sched, tp, shape):
+    m, n, k, l = shape
+    if sched in (2, 3) and (k % tp or (k // tp) % 8):
+        k = 64 * tp
+    if (sched in (0, 1, 2) and m % tp) or (sched != 2 and n % tp):
+        pytest.skip("not divisible")
+    plan = dg.Plan(m, n, k, l, tp, sched, 1.0, 0.5)
+    _simulate(plan, m, n, k, l, tp, sched)
+
+
+def test_ag_flag_indices_follow_copy_order(L):
+    # chunk flags are laid out in the order the copies are enqueued:
+    # step-major, then rank, batch, chunk
+    m, n, k, l, tp = 2048, 1024, 1024, 2, 4
+    plan = dg.Plan(m, n, k, l, tp, dg.AG_ROTATING_A)
+    plan.set_option(dg.OPT_CHUNK_TILES, 2)
+    info = plan.info()
+    nch = info["chunks_per_shard"]
+    assert nch == -(-info["tiles_m"] // 2)
+    seen = set()
+    for t in range(info["total_tiles"]):
+        tl = plan.tile(t)
+        if tl["flag"] < 0:
+            continue
+        s, r, b = tl["step"], tl["rank"], tl["batch"]
+        mt = (tl["a_row"] % (m // tp)) // 128
+        assert tl["flag"] == ((r * (tp - 1) + s - 1) * l + b) * nch + mt // 2
+        seen.add(tl["flag"])
+    assert seen == set(range(info["n_flags"]))
+    assert info["copies_per_run"] == info["n_flags"]
+
+
+def test_workspace_layout_sizes(L):
+    m, n, k, l, tp = 4096, 2048, 1024, 1, 8
+    pa = dg.Plan(m, n, k, l, tp, dg.AG_ROTATING_A).info()
+    assert pa["slot_bytes"] == (m // tp) * k * 2
+    assert pa["ws_bytes"] >= pa["off_slots"] + tp * (tp - 1) * l * pa["slot_bytes"]
+    pr = dg.Plan(m, n, k, l, tp, dg.RS_TILING_A_ROTATING_C)
+    ir = pr.info()
+    assert ir["ws_bytes"] >= ir["off_partial"] + l * m * n * 4
+    pr.set_mode(dg.MODE_SERIAL)
+    assert pr.workspace_bytes() >= ir["off_serial"] + tp * l * m * n * 4
+    p1 = dg.Plan(m, n, k, l, 1, dg.AG_ROTATING_A).info()
+    assert p1["n_flags"] == 0 and p1["copies_per_run"] == 0

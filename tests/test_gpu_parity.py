@@ -1,0 +1,160 @@
+"""Device path against the CPU oracle, through the C ABI, on small problems
+that span several tiles and ragged tails; bit-exactness of the AllGather
+schedules against the unsharded run; run modes; closed forms; edge cases."""
+
+import numpy as np
+import pytest
+import torch
+
+from reduce_scatter_gb300 import dg
+from tests.gpu_common import TOL, Runner, dev_bits, host_inputs, oracle_full, rel_err, to_dev
+
+pytestmark = pytest.mark.gpu
+
+SCHEDS = [dg.AG_ROTATING_A, dg.AG_ROTATING_B, dg.RS_TILING_A_ROTATING_C, dg.RS_TILING_B_ROTATING_C]
+# (m, n, k, l): several tiles; ragged shards and a ragged K block
+SHAPES = [(512, 1024, 512, 1), (392, 776, 320, 2), (1024, 528, 200, 1)]
+
+
+def _shape_ok(sched, m, n, k, tp):
+    if sched in (0, 1, 2) and m % tp:
+        return False
+    if sched != 2 and n % tp:
+        return False
+    if sched >= 2 and (k % tp or (k // tp) % 8):
+        return False
+    return True
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("tp", [1, 2, 4, 8])
+@pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_parity_vs_oracle(sched, tp, shape):
+    m, n, k, l = shape
+    if not _shape_ok(sched, m, n, k, tp):
+        pytest.skip("shape not divisible for this schedule/tp")
+    a, b, c = host_inputs(m, n, k, l, seed=tp + 10 * sched)
+    A, B, C = to_dev(a), to_dev(b), to_dev(c)
+    for alpha, beta in [(1.0, 0.0), (0.5, 1.0)]:
+        r = Runner(m, n, k, l, tp, sched, alpha, beta)
+        D, _ = r.run(A, B, C if beta else None)
+        err = rel_err(D, oracle_full(a, b, c, alpha, beta))
+        assert err <= TOL, (err, alpha, beta)
+        # a second run reuses the workspace: epochs, not memsets, guard the flags
+        D2, _ = r.run(A, B, C if beta else None)
+        assert torch.equal(D.view(torch.int16), D2.view(torch.int16))
+
+
+@pytest.mark.parametrize("sched", [dg.AG_ROTATING_A, dg.AG_ROTATING_B], ids=lambda s: dg.SCHEDULE_NAMES[s])
+@pytest.mark.parametrize("shape", [(1024, 1024, 328, 1), (392, 776, 320, 2)], ids=lambda s: "x".join(map(str, s)))
+def test_allgather_bit_exact_vs_unsharded(sched, shape):
+    m, n, k, l = shape
+    a, b, c = host_inputs(m, n, k, l, seed=3)
+    A, B, C = to_dev(a), to_dev(b), to_dev(c)
+    ref, _ = Runner(m, n, k, l, 1, sched, 0.5, 1.0).run(A, B, C)
+    for tp in (2, 4, 8):
+        if not _shape_ok(sched, m, n, k, tp):
+            continue
+        D, _ = Runner(m, n, k, l, tp, sched, 0.5, 1.0).run(A, B, C)
+        assert torch.equal(D.view(torch.int16), ref.view(torch.int16)), tp
+
+
+def test_rs_tp1_is_the_plain_gemm_bit_for_bit():
+    m, n, k, l = 512, 768, 512, 1
+    a, b, c = host_inputs(m, n, k, l, seed=4)
+    A, B, C = to_dev(a), to_dev(b), to_dev(c)
+    ref, _ = Runner(m, n, k, l, 1, dg.AG_ROTATING_A, 0.75, -0.5).run(A, B, C)
+    for sched in (dg.RS_TILING_A_ROTATING_C, dg.RS_TILING_B_ROTATING_C):
+        D, _ = Runner(m, n, k, l, 1, sched, 0.75, -0.5).run(A, B, C)
+        assert torch.equal(D.view(torch.int16), ref.view(torch.int16))
+
+
+@pytest.mark.parametrize("sched", [dg.AG_ROTATING_A, dg.AG_ROTATING_B], ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_modes_agree(sched):
+    m, n, k, l, tp = 1024, 1024, 512, 1, 4
+    a, b, c = host_inputs(m, n, k, l, seed=5)
+    A, B = to_dev(a), to_dev(b)
+    fused, _ = Runner(m, n, k, l, tp, sched).run(A, B, None)
+    serial, _ = Runner(m, n, k, l, tp, sched, mode=dg.MODE_SERIAL).run(A, B, None)
+    r = Runner(m, n, k, l, tp, sched)
+    r.run(A, B, None)  # fills the receive slots
+    r.plan.set_mode(dg.MODE_GEMM_ONLY)
+    gemm_only, _ = r.run(A, B, None)
+    for D in (serial, gemm_only):
+        assert torch.equal(D.view(torch.int16), fused.view(torch.int16))
+    # copy stream == main stream runs the transfers first
+    r2 = Runner(m, n, k, l, tp, sched)
+    D = torch.empty_like(fused)
+    r2.plan.run(A, B, None, D, r2.ws, r2.main, r2.main)
+    r2.plan.check(r2.ws, r2.main)
+    assert torch.equal(D.view(torch.int16), fused.view(torch.int16))
+
+
+@pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_closed_forms(sched):
+    tp = 4
+    # all ones: D = K * alpha + beta * C, exact
+    for k in (256, 8192):
+        m, n, l = 512, 512, 1
+        A = torch.ones((l, m, k), dtype=torch.bfloat16, device="cuda")
+        B = torch.ones((l, n, k), dtype=torch.bfloat16, device="cuda")
+        C = torch.full((l, m, n), 3.0, dtype=torch.bfloat16, device="cuda")
+        D, _ = Runner(m, n, k, l, tp, sched, 0.5, 2.0).run(A, B, C)
+        assert torch.all(D.float() == 0.5 * k + 6.0)
+    # identity B (N = K): D = A; one-hot B: D[:, n] = A[:, perm[n]]
+    m, k, l = 256, 512, 1
+    a, _, _ = host_inputs(m, k, k, l, seed=6)
+    A = to_dev(a)
+    eye = torch.eye(k, dtype=torch.bfloat16, device="cuda")[None]
+    D, _ = Runner(m, k, k, l, tp, sched).run(A, eye, None)
+    assert torch.equal(D.float(), A.float())  # value equality (+0 == -0)
+    n = 384
+    perm = torch.randint(0, k, (n,), generator=torch.Generator().manual_seed(7))
+    onehot = torch.zeros((1, n, k), dtype=torch.bfloat16)
+    onehot[0, torch.arange(n), perm] = 1.0
+    D, _ = Runner(m, n, k, l, tp, sched).run(A, onehot.cuda(), None)
+    assert torch.equal(D.float(), A[:, :, perm.cuda()].float())
+
+
+@pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_k_zero_gives_beta_c(sched):
+    m, n, k, l, tp = 256, 512, 0, 1, 2
+    c = host_inputs(m, n, 8, l, seed=8)[2]
+    C = to_dev(c)
+    A = torch.empty((16,), dtype=torch.bfloat16, device="cuda")
+    B = torch.empty((16,), dtype=torch.bfloat16, device="cuda")
+    D, _ = Runner(m, n, k, l, tp, sched, 1.0, 0.5).run(A, B, C)
+    assert torch.equal(D.float(), (0.5 * C.float()).to(torch.bfloat16).float())
+
+
+def test_beta_zero_ignores_nan_c():
+    m, n, k, l = 256, 512, 128, 1
+    a, b, c = host_inputs(m, n, k, l, seed=9)
+    A, B = to_dev(a), to_dev(b)
+    Cn = torch.full((l, m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+    for sched in SCHEDS:
+        D, _ = Runner(m, n, k, l, 2, sched, 1.0, 0.0).run(A, B, Cn)
+        assert rel_err(D, oracle_full(a, b, c, 1.0, 0.0)) <= TOL
+
+
+def test_single_row_shards():
+    # tp = 8 with M = 8: one row per shard, 127 of every 128 tile rows masked
+    m, n, k, l, tp = 8, 64, 64, 3, 8
+    a, b, c = host_inputs(m, n, k, l, seed=10)
+    A, B, C = to_dev(a), to_dev(b), to_dev(c)
+    for sched in SCHEDS:
+        if not _shape_ok(sched, m, n, k, tp):
+            continue
+        D, _ = Runner(m, n, k, l, tp, sched, 1.0, 1.0).run(A, B, C)
+        assert rel_err(D, oracle_full(a, b, c, 1.0, 1.0)) <= TOL
+
+
+def test_does_not_write_outside_d():
+    m, n, k, l, tp = 392, 776, 320, 1, 4
+    a, b, c = host_inputs(m, n, k, l, seed=11)
+    A, B = to_dev(a), to_dev(b)
+    for sched in SCHEDS:
+        big = torch.full((l * m * n + 4096,), 7.0, dtype=torch.bfloat16, device="cuda")
+        D = big[2048: 2048 + l * m * n].view(l, m, n)
+        Runner(m, n, k, l, tp, sched).run(A, B, None, D)
+        assert torch.all(big[:2048] == 7.0) and torch.all(big[2048 + l * m * n:] == 7.0)
