@@ -52,6 +52,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-modes", action="store_true", help="skip the GEMM_ONLY / SERIAL timings")
+    ap.add_argument("--mode", choices=["fused", "gemm_only", "serial"], default="fused",
+                    help="mode of the timed loop (gemm_only/serial for profilers that serialize streams)")
     ap.add_argument("--cpu-sample-rows", type=int, default=1024)
     ap.add_argument("--cpu-sample-cols", type=int, default=4096)
     return ap.parse_args(argv)
@@ -247,9 +249,13 @@ def run_dg(args, rank, world, dist):
         if dist is not None:
             dist.barrier()
 
-    # correctness guard before timing: one run, device status must be clean
+    mode = {"fused": dg.MODE_FUSED, "gemm_only": dg.MODE_GEMM_ONLY, "serial": dg.MODE_SERIAL}[args.mode]
+    # correctness guard before timing: one run, device status must be clean.
+    # GEMM_ONLY needs filled receive slots: fill them with a SERIAL run.
+    plan.set_mode(dg.MODE_SERIAL if mode == dg.MODE_GEMM_ONLY else mode)
     run()
     plan.check(ws, main)
+    plan.set_mode(mode)
 
     barrier()
     with ClockSampler(local) as clk:
@@ -260,12 +266,13 @@ def run_dg(args, rank, world, dist):
     clocks = clk.summary()
 
     ms_gemm = ms_serial = None
-    if not args.no_modes and w.schedule in (dg.AG_ROTATING_A, dg.AG_ROTATING_B) and w.tp > 1:
+    if (not args.no_modes and mode == dg.MODE_FUSED and w.schedule in (dg.AG_ROTATING_A, dg.AG_ROTATING_B)
+            and w.tp > 1):
         plan.set_mode(dg.MODE_GEMM_ONLY)
         ms_gemm = timed_loop(run, max(3, args.steps // 2), 2, main, flush)
         plan.set_mode(dg.MODE_SERIAL)
         ms_serial = timed_loop(run, max(3, args.steps // 2), 2, main, flush)
-        plan.set_mode(dg.MODE_FUSED)
+        plan.set_mode(mode)
         plan.check(ws, main)
 
     e2e = None
@@ -324,6 +331,7 @@ def run_dg(args, rank, world, dist):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded SplitMix64 inputs with the workload's distributions)",
+        "mode": args.mode,
         "config": dict(w.describe(), parallelism=f"tp{w.tp} virtual ranks on 1 GPU" + (
             f", {world} replicas" if world > 1 else ""),
             l2="flushed between steps" if flush is not None else "inputs larger than L2 (no flush)"),

@@ -1,0 +1,76 @@
+"""Full-size workloads, in the launch configuration the benchmark times.
+
+The oracle cannot evaluate these problems whole, so:
+* sampled entries D[rows, cols] (rows spread over every shard and batch,
+  columns over every shard) are checked against the oracle evaluated on
+  exactly those rows of A and B, drawn again on the CPU from the same seeded
+  generator;
+* AllGather schedules are compared bit for bit with the unsharded (tp=1) run
+  of the same kernel, since the K order does not change;
+* ReduceScatter schedules are compared with the unsharded run within the
+  tolerance (the K order of the partial sums differs);
+* D holds no NaN (every element written).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import gemm as og
+from reduce_scatter_gb300 import configs, dg, synth
+from tests.gpu_common import TOL, Runner
+
+pytestmark = pytest.mark.gpu
+
+FULL = ["ag_a_tp2_blog", "ag_a_tp8_pr", "rs_a_tp8", "ag_b_tp4_batched", "rs_b_tp4_batched"]
+
+
+def _dev_inputs(w):
+    A = synth.tensor_bits_torch(w.seed, synth.STREAM_A, (w.l, w.m, w.k), w.dist_a, device="cuda").view(torch.bfloat16)
+    B = synth.tensor_bits_torch(w.seed, synth.STREAM_B, (w.l, w.n, w.k), w.dist_b, device="cuda").view(torch.bfloat16)
+    C = None
+    if w.beta != 0:
+        C = synth.tensor_bits_torch(w.seed, synth.STREAM_C, (w.l, w.m, w.n), w.dist_c, device="cuda").view(torch.bfloat16)
+    return A, B, C
+
+
+def _sample_check(w, D, nrows=48, ncols=48):
+    rng = np.random.default_rng(12345)
+    LM = w.l * w.m
+    rows = np.unique(np.concatenate([rng.integers(0, LM, nrows), [0, LM - 1]]))
+    cols = np.unique(np.concatenate([rng.integers(0, w.n, ncols), [0, w.n - 1]]))
+    Dh = D.view(LM, w.n)[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()].float().cpu().numpy()
+    worst = 0.0
+    for b in range(w.l):
+        rs = rows[(rows >= b * w.m) & (rows < (b + 1) * w.m)]
+        if len(rs) == 0:
+            continue
+        a = og.bf16_bits_to_f64(synth.rows_bits_np(w.seed, synth.STREAM_A, (LM, w.k), rs, w.dist_a))
+        bb = og.bf16_bits_to_f64(synth.rows_bits_np(w.seed, synth.STREAM_B, (w.l * w.n, w.k), cols + b * w.n, w.dist_b))
+        c = None
+        if w.beta != 0:
+            c = og.bf16_bits_to_f64(synth.rows_bits_np(w.seed, synth.STREAM_C, (LM, w.n), rs, w.dist_c)[:, cols])
+        want = og.gemm_entries(a, bb, c, w.alpha, w.beta)
+        got = Dh[np.isin(rows, rs)].astype(np.float64)
+        assert not np.any(np.isnan(got))
+        worst = max(worst, float(np.abs(got - want).max() / np.abs(want).max()))
+    assert worst <= TOL, worst
+    return worst
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size(name):
+    w = configs.WORKLOADS[name]
+    A, B, C = _dev_inputs(w)
+    r = Runner(w.m, w.n, w.k, w.l, w.tp, w.schedule, w.alpha, w.beta)
+    D, _ = r.run(A, B, C)
+    assert not torch.isnan(D.float()).any()
+    _sample_check(w, D)
+    del r
+    ref_sched = w.schedule if w.schedule in (dg.AG_ROTATING_A, dg.AG_ROTATING_B) else dg.AG_ROTATING_A
+    ref, _ = Runner(w.m, w.n, w.k, w.l, 1, ref_sched, w.alpha, w.beta).run(A, B, C)
+    if w.schedule in (dg.AG_ROTATING_A, dg.AG_ROTATING_B):
+        assert torch.equal(D.view(torch.int16), ref.view(torch.int16))
+    else:
+        err = (D.float() - ref.float()).abs().max().item() / ref.float().abs().max().item()
+        assert err <= TOL, err
