@@ -483,20 +483,26 @@ int dg_run(dg_plan_t p, const dg_bf16_t* A, const dg_bf16_t* B, const dg_bf16_t*
   auto cs = static_cast<cudaStream_t>(copy_stream);
   auto* ws = static_cast<uint8_t*>(workspace);
 
+  // Epochs grow per plan across all of its workspaces, so flag words left in
+  // any workspace by this plan's earlier runs stay below the current epoch.
+  // A workspace new to this plan starts from zeroed flags.  Only when the
+  // epoch would overflow is it restarted, and then every other workspace of
+  // this plan is forgotten so that it is cleared again on its next use.
   bool clear = false;
+  const bool wrap = (uint64_t)(p->epoch + 2) * (uint64_t)p->tp >= 0x7FFFFFFFull;
   {
     std::lock_guard<std::mutex> lk(g_ws_mu);
+    if (wrap)
+      for (auto it = g_ws_owner.begin(); it != g_ws_owner.end();)
+        it = it->second == p->id ? g_ws_owner.erase(it) : std::next(it);
     auto it = g_ws_owner.find(workspace);
     if (it == g_ws_owner.end() || it->second != p->id) {
       g_ws_owner[workspace] = p->id;
       clear = true;
     }
   }
-  if ((uint64_t)(p->epoch + 2) * (uint64_t)p->tp >= 0x7FFFFFFFull) clear = true;
-  if (clear) {
-    DG_CUDA(cudaMemsetAsync(ws, 0, p->off_flags + (size_t)p->n_flags * 4, ms));
-    p->epoch = 0;
-  }
+  if (clear) DG_CUDA(cudaMemsetAsync(ws, 0, p->off_flags + (size_t)p->n_flags * 4, ms));
+  if (wrap) p->epoch = 0;
   p->epoch += 1;
 
   rc = build_maps(p, drv, A, B, ws);

@@ -75,3 +75,30 @@ def test_workspace_handed_between_plans():
     _poison_slots(r2)
     D, _ = r2.run(A, B, None)
     assert rel_err(D, oracle_full(a, b, c, 1.0, 0.0)) <= TOL
+
+
+def test_plan_alternating_between_workspaces():
+    # one plan, two workspaces used in turn, with another plan on the second
+    # in between: stale flag words in either workspace must never satisfy a
+    # wait of a later run (copies held back, slots poisoned)
+    m, n, k, l, tp = 512, 512, 256, 1, 4
+    a, b, c = host_inputs(m, n, k, l, seed=24)
+    A, B = to_dev(a), to_dev(b)
+    want = oracle_full(a, b, c, 1.0, 0.0)
+    r1 = Runner(m, n, k, l, tp, dg.AG_ROTATING_A)
+    ws_a = r1.ws
+    ws_b = torch.zeros_like(ws_a)
+    for _ in range(4):
+        r1.run(A, B, None)                      # plan 1 on ws_a, epochs 1..4
+    r1.ws = ws_b
+    r1.run(A, B, None)                          # plan 1 on ws_b
+    other = Runner(m, n, k, l, tp, dg.AG_ROTATING_A)
+    other.ws = ws_b
+    for _ in range(8):
+        other.run(A, B, None)                   # another plan pushes ws_b's flags high
+    r1.plan.set_option(dg.OPT_FAULT_DELAY_MS, 30)
+    for ws in (ws_a, ws_b, ws_a):
+        r1.ws = ws
+        _poison_slots(r1)
+        D, _ = r1.run(A, B, None)
+        assert rel_err(D, want) <= TOL
