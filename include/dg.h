@@ -173,6 +173,41 @@ int dg_plan_info_get(dg_plan_t plan, dg_plan_info* info);
 /* Decode tile t (0 <= t < total_tiles) of the rotation order on the host. */
 int dg_plan_tile(dg_plan_t plan, int64_t t, dg_tile* out);
 
+/* No-allocation variant of dg_run.  The pages have no counterpart to this
+ * entry point; it exists for callers that cannot call cudaMalloc (or
+ * anything that allocates device memory) at the point where they run the
+ * GEMM -- for example code inside an application whose device memory is all
+ * owned and budgeted by a host framework, or a plug-in that is not allowed
+ * to grow the process's device footprint after start-up.
+ *
+ * Instead of a caller-supplied workspace it uses one file-scope device array
+ * of DG_STATIC_WORKSPACE_BYTES bytes inside this library.  Every GPU that
+ * loads the library holds that array until the process exits, whether or not
+ * this function is ever called.  The caller still passes A, B, C, D and the
+ * streams exactly as for dg_run.
+ *
+ * Limits and rules:
+ *   - The plan's dg_workspace_bytes() must be <= DG_STATIC_WORKSPACE_BYTES;
+ *     larger plans are rejected with DG_ERR_SHAPE before any GPU work.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address once; make that first call before starting any
+ *     stream capture on that device.
+ *   - All calls in the process share the one array, and it keeps the last
+ *     call's contents.  The flag and status words that must start at zero are
+ *     cleared on the main stream whenever a different plan used the array
+ *     last.  Calls whose GPU work overlaps (on different streams, or from
+ *     several threads) race on the array: serialize them.
+ *   - It makes no device-memory allocation or free (no cudaMalloc/cudaFree,
+ *     no allocating library call).
+ * dg_check(plan, NULL, stream) reports CUDA errors of such a run.  The
+ * device status word (ready-flag wait timeouts) lives in the shared array,
+ * which dg_check cannot read, so this variant does not report timeouts; a
+ * run that timed out leaves D undefined.  Use dg_run with a workspace when
+ * that report is needed. */
+#define DG_STATIC_WORKSPACE_BYTES ((size_t)32 << 20)
+int dg_run_static(dg_plan_t plan, const dg_bf16_t* A, const dg_bf16_t* B, const dg_bf16_t* C,
+                  dg_bf16_t* D, void* main_stream, void* copy_stream);
+
 void dg_destroy(dg_plan_t plan);
 
 /* Message of the calling thread's last error ("" if none). */

@@ -580,3 +580,54 @@ void dg_destroy(dg_plan_t p) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// No-allocation entry point.
+//
+// Some callers cannot allocate device memory where they run the GEMM (their
+// host framework owns and budgets all of it, or they are a plug-in that must
+// not grow the process's device footprint).  For them the workspace can live
+// in this one file-scope device array instead.  Its size is fixed at build
+// time, every GPU that loads this library holds it until the process exits,
+// and all calls share it.
+//
+// In host code `dg_static_workspace` only names a host-side stand-in for the
+// array, not a device address: its device address is looked up once per
+// device with cudaGetSymbolAddress (with that device current) and then
+// passed to the kernel like any caller workspace.
+static __device__ __align__(256) unsigned char dg_static_workspace[DG_STATIC_WORKSPACE_BYTES];
+
+namespace {
+constexpr int kMaxStaticDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxStaticDevices] = {};
+}  // namespace
+
+extern "C" int dg_run_static(dg_plan_t p, const dg_bf16_t* A, const dg_bf16_t* B, const dg_bf16_t* C,
+                             dg_bf16_t* D, void* main_stream, void* copy_stream) {
+  if (!p) return fail(DG_ERR_ARG, "plan is NULL");
+  const size_t need = dg_workspace_bytes(p);
+  if (need > DG_STATIC_WORKSPACE_BYTES)
+    return fail(DG_ERR_SHAPE,
+                "dg_run_static: plan needs %zu workspace bytes, the built-in array holds %zu; "
+                "use dg_run with a caller workspace",
+                need, (size_t)DG_STATIC_WORKSPACE_BYTES);
+  if (p->g.total_tiles == 0) return DG_OK;
+  int dev = 0;
+  DG_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxStaticDevices) return fail(DG_ERR_UNSUPPORTED, "device index %d too large", dev);
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_ptr[dev]) {
+      void* addr = nullptr;
+      cudaError_t e = cudaGetSymbolAddress(&addr, dg_static_workspace);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(dg_static_workspace)");
+      g_static_ptr[dev] = addr;
+    }
+    ws = g_static_ptr[dev];
+  }
+  // The flag and status words that must start at zero are cleared by dg_run
+  // on the main stream whenever another plan used this array last.
+  return dg_run(p, A, B, C, D, ws, main_stream, copy_stream);
+}

@@ -49,7 +49,10 @@ OPT_COPY_STREAMS = 5
 
 # Every symbol include/dg.h declares.
 EXPORTS = ("dg_plan", "dg_workspace_bytes", "dg_run_mode", "dg_set_option", "dg_run", "dg_check",
-           "dg_plan_info_get", "dg_plan_tile", "dg_destroy", "dg_last_error")
+           "dg_plan_info_get", "dg_plan_tile", "dg_destroy", "dg_last_error", "dg_run_static")
+
+# Size of the library's built-in workspace used by dg_run_static.
+STATIC_WORKSPACE_BYTES = 32 << 20
 
 
 class PlanInfo(ctypes.Structure):
@@ -116,6 +119,8 @@ def lib():
         L.dg_set_option.restype = i32
         L.dg_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
         L.dg_run.restype = i32
+        L.dg_run_static.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+        L.dg_run_static.restype = i32
         L.dg_check.argtypes = [vp, vp, vp]
         L.dg_check.restype = i32
         L.dg_plan_info_get.argtypes = [vp, ctypes.POINTER(PlanInfo)]
@@ -206,6 +211,14 @@ class Plan:
     def run(self, A, B, C, D, workspace, main_stream=None, copy_stream=None, raise_on_error=True) -> int:
         rc = lib().dg_run(self._h, ptr(A), ptr(B), ptr(C), ptr(D), ptr(workspace),
                           stream_handle(main_stream), stream_handle(copy_stream))
+        if raise_on_error:
+            _check(rc)
+        return rc
+
+    def run_static(self, A, B, C, D, main_stream=None, copy_stream=None, raise_on_error=True) -> int:
+        """``dg_run_static``: the library's built-in workspace instead of a caller one."""
+        rc = lib().dg_run_static(self._h, ptr(A), ptr(B), ptr(C), ptr(D), stream_handle(main_stream),
+                                 stream_handle(copy_stream))
         if raise_on_error:
             _check(rc)
         return rc
