@@ -102,8 +102,11 @@ enum dg_option {
                                  enqueue index (-1 = none, default) */
   DG_OPT_FAULT_DELAY_MS = 3,  /* test hook: hold the copy stream this long
                                  before the first transfer (default 0) */
-  DG_OPT_GRID = 4,            /* persistent grid size (0 = one CTA per SM) */
-  DG_OPT_COPY_STREAMS = 5     /* reserved: number of copy streams (1) */
+  DG_OPT_GRID = 4,            /* persistent grid size in CTAs (0 = all co-resident) */
+  DG_OPT_COPY_STREAMS = 5,    /* reserved: number of copy streams (1) */
+  DG_OPT_CTA_GROUP = 6        /* tile configuration, before the first run: 2 (default) =
+                                 256 x 256 tiles on an SM pair (tcgen05 cta_group::2),
+                                 1 = 128 x 256 tiles on one SM */
 };
 
 /* Plan geometry and workspace layout, for callers and tests. */

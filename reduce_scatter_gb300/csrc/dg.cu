@@ -113,6 +113,7 @@ struct dg_plan_s {
   int64_t fault_skip = -1;
   int64_t fault_delay_ms = 0;
   int64_t grid_req = 0;
+  int cg = 2;  // CTA group of the tile config: 1 = 128 x 256 per SM, 2 = 256 x 256 per SM pair
   uint64_t id = 0;
   uint32_t epoch = 0;
   bool serial_ws = false;
@@ -125,6 +126,7 @@ struct dg_plan_s {
   bool rt = false;
   int device = -1;
   int num_sms = 0;
+  int max_pairs = 0;  // co-resident CTA pairs of the CG = 2 kernel
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   dg::KParams kp;
   const void* map_key[3] = {nullptr, nullptr, nullptr};
@@ -144,8 +146,8 @@ int layout(dg_plan_s* p) {
   g.N = p->n;
   g.K = p->k;
   g.L = p->l;
-  g.BM = dg::BM;
-  g.BN = dg::BN;
+  g.BM = p->cg == 2 ? dg::Cfg<2>::TILE_M : dg::Cfg<1>::TILE_M;
+  g.BN = dg::TILE_N;
   g.BK = dg::BK;
   g.group_m = 16;
   g.beta_nonzero = p->beta != 0.f;
@@ -186,7 +188,8 @@ int layout(dg_plan_s* p) {
       p->copies = p->n_flags;
     }
   } else if (P > 1) {
-    p->n_flags = g.L * P * g.tiles_m * g.tiles_n;
+    // one flag per tile and CTA of the group (each CTA hands on its own half)
+    p->n_flags = g.L * P * g.tiles_m * g.tiles_n * p->cg;
   }
   p->off_status = 0;
   p->off_flags = 256;
@@ -215,8 +218,26 @@ int rt_init(dg_plan_s* p) {
     return fail(DG_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a", dev,
                 major, minor);
   DG_CUDA(cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, dev));
-  DG_CUDA(cudaFuncSetAttribute(dg::dg_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)dg::SMEM_BYTES));
+  DG_CUDA(cudaFuncSetAttribute(dg::dg_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)dg::Cfg<1>::SMEM_BYTES));
+  DG_CUDA(cudaFuncSetAttribute(dg::dg_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)dg::Cfg<2>::SMEM_BYTES));
+  {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * 256, 1, 1);
+    cfg.blockDim = dim3(dg::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = dg::Cfg<2>::SMEM_BYTES;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int ncl = 0;
+    DG_CUDA(cudaOccupancyMaxActiveClusters(&ncl, dg::dg_gemm_kernel<2>, &cfg));
+    p->max_pairs = ncl;
+  }
   DG_CUDA(cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming));
   DG_CUDA(cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming));
   p->device = dev;
@@ -248,20 +269,23 @@ int build_maps(dg_plan_s* p, const Driver& drv, const void* A, const void* B, ui
   const int64_t P = p->tp;
   int rc = DG_OK;
   p->n_maps = 0;
+  // each CTA loads its own rows of the tile: 128 of A; 256 (CG = 1) or 128 (CG = 2) of B
+  const int a_box = dg::Cfg<1>::A_ROWS;
+  const int b_box = p->cg == 2 ? dg::Cfg<2>::B_ROWS : dg::Cfg<1>::B_ROWS;
   if (p->k > 0) {
     if (is_ag(p->schedule)) {
-      rc = encode_map(drv, &p->kp.tmA[0], A, p->k, g.L * p->m, p->k, dg::BM);
+      rc = encode_map(drv, &p->kp.tmA[0], A, p->k, g.L * p->m, p->k, a_box);
       if (rc) return rc;
-      rc = encode_map(drv, &p->kp.tmB[0], B, p->k, g.L * p->n, p->k, dg::BN);
+      rc = encode_map(drv, &p->kp.tmB[0], B, p->k, g.L * p->n, p->k, b_box);
       if (rc) return rc;
       p->n_maps = 1;
       if (P > 1) {
         const int64_t slot_rows = P * (P - 1) * g.L * g.shard;
         if (p->schedule == DG_AG_ROTATING_A) {
-          rc = encode_map(drv, &p->kp.tmA[1], ws + p->off_slots, p->k, slot_rows, p->k, dg::BM);
+          rc = encode_map(drv, &p->kp.tmA[1], ws + p->off_slots, p->k, slot_rows, p->k, a_box);
           p->kp.tmB[1] = p->kp.tmB[0];
         } else {
-          rc = encode_map(drv, &p->kp.tmB[1], ws + p->off_slots, p->k, slot_rows, p->k, dg::BN);
+          rc = encode_map(drv, &p->kp.tmB[1], ws + p->off_slots, p->k, slot_rows, p->k, b_box);
           p->kp.tmA[1] = p->kp.tmA[0];
         }
         if (rc) return rc;
@@ -271,9 +295,9 @@ int build_maps(dg_plan_s* p, const Driver& drv, const void* A, const void* B, ui
       const auto* a16 = static_cast<const uint16_t*>(A);
       const auto* b16 = static_cast<const uint16_t*>(B);
       for (int64_t r = 0; r < P; ++r) {
-        rc = encode_map(drv, &p->kp.tmA[r], a16 + r * g.Ks, g.Ks, g.L * p->m, p->k, dg::BM);
+        rc = encode_map(drv, &p->kp.tmA[r], a16 + r * g.Ks, g.Ks, g.L * p->m, p->k, a_box);
         if (rc) return rc;
-        rc = encode_map(drv, &p->kp.tmB[r], b16 + r * g.Ks, g.Ks, g.L * p->n, p->k, dg::BN);
+        rc = encode_map(drv, &p->kp.tmB[r], b16 + r * g.Ks, g.Ks, g.L * p->n, p->k, b_box);
         if (rc) return rc;
       }
       p->n_maps = (int)P;
@@ -332,11 +356,31 @@ int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B
 
 int launch(dg_plan_s* p, cudaStream_t st, uint32_t wait_flags) {
   p->kp.wait_flags = wait_flags;
-  int64_t grid = p->grid_req > 0 ? p->grid_req : p->num_sms;
-  grid = std::min<int64_t>(grid, p->g.total_tiles);
-  if (grid <= 0) return DG_OK;
-  dg::dg_gemm_kernel<<<(unsigned)grid, dg::NUM_THREADS, dg::SMEM_BYTES, st>>>(p->kp);
-  DG_CUDA(cudaGetLastError());
+  if (p->cg == 1) {
+    int64_t grid = p->grid_req > 0 ? p->grid_req : p->num_sms;
+    grid = std::min<int64_t>(grid, p->g.total_tiles);
+    if (grid <= 0) return DG_OK;
+    dg::dg_gemm_kernel<1><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1>::SMEM_BYTES, st>>>(p->kp);
+    DG_CUDA(cudaGetLastError());
+    return DG_OK;
+  }
+  // CTA pairs: every pair must be co-resident (RS tiles wait on earlier tiles)
+  int64_t pairs = p->grid_req > 0 ? p->grid_req / 2 : p->max_pairs;
+  pairs = std::min<int64_t>(std::min<int64_t>(pairs, p->max_pairs), p->g.total_tiles);
+  if (pairs <= 0) return p->g.total_tiles > 0 ? fail(DG_ERR_UNSUPPORTED, "no co-resident CTA pair") : DG_OK;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+  cfg.blockDim = dim3(dg::NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = dg::Cfg<2>::SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2>, p->kp));
   return DG_OK;
 }
 
@@ -420,6 +464,12 @@ int dg_set_option(dg_plan_t p, int option, int64_t value) {
       return DG_OK;
     case DG_OPT_COPY_STREAMS:
       return value == 1 ? DG_OK : fail(DG_ERR_UNSUPPORTED, "one copy stream only");
+    case DG_OPT_CTA_GROUP:
+      if (value != 1 && value != 2) return fail(DG_ERR_ARG, "CTA group must be 1 or 2");
+      if (p->epoch != 0) return fail(DG_ERR_STATE, "the tile configuration is fixed after the first run");
+      p->cg = (int)value;
+      layout(p);
+      return DG_OK;
     default:
       return fail(DG_ERR_ARG, "unknown option %d", option);
   }

@@ -1,16 +1,17 @@
 // dg_kernel.cuh -- persistent tcgen05 GEMM with shard-rotation tile order,
 // flag-gated TMA producer and rotating-partial (RotatingC) epilogue, sm_103a.
 //
-// One CTA per SM, 192 threads:
+// One CTA per SM, 192 threads; with CG = 2 the CTAs of a cluster pair share
+// each 256 x 256 tile (the even CTA issues the MMAs for both SMs):
 //   warp 0      TMA producer: for each tile, waits (acquire, bounded) on the
 //               ready flag of the shard chunk the tile reads, then streams
-//               64-wide K blocks of A (BM x 64) and B (BN x 64) into a ring of
-//               STAGES shared-memory buffers (128-byte swizzle).
-//   warp 1      MMA issuer: allocates 2 x BN TMEM columns (two fp32
-//               accumulators of BM lanes x BN columns), issues
-//               tcgen05.mma.cta_group::1.kind::f16 (bf16 x bf16 -> fp32), four
-//               K=16 instructions per K block, and commits stage release and
-//               accumulator-full barriers.
+//               64-wide K blocks of its 128 rows of A and its rows of B into a
+//               ring of shared-memory stages (128-byte swizzle).
+//   warp 1      MMA issuer (even CTA): 2 x 256 TMEM columns per CTA (two fp32
+//               accumulators of 128 lanes x 256 columns), issues
+//               tcgen05.mma.cta_group::{1,2}.kind::f16 (bf16 x bf16 -> fp32),
+//               four K=16 instructions per K block, and commits stage-release
+//               and accumulator-full barriers (to both CTAs of a pair).
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (each warp owns the 32
 //               TMEM lanes of its warp id mod 4), d = alpha*acc + source, where
 //               the source is beta*C (AG, RS step 0), the rotating fp32 partial
@@ -39,18 +40,30 @@
 
 namespace dg {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
 constexpr int MAX_MAPS = 9;  // RS: one K-slab map per rank (P <= 8); AG: home + slots
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_THREADS = 128;
-constexpr uint32_t A_BYTES = BM * BK * 2;
-constexpr uint32_t B_BYTES = BN * BK * 2;
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
-constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int ROWS_PER_CTA = 128;  // accumulator rows (TMEM lanes) per CTA
+constexpr int TILE_N = 256;        // accumulator columns
+constexpr uint32_t TMEM_COLS = 2 * TILE_N;  // two accumulators
+
+// Tile configuration per CTA group.
+//   CG = 1: one SM, tile 128 x 256, tcgen05.mma.cta_group::1 (M=128, N=256).
+//   CG = 2: an SM pair (cluster of 2), tile 256 x 256, tcgen05.mma.cta_group::2
+//           (M=256, N=256) issued by the even CTA; each CTA stages its 128
+//           rows of A and its 128 rows of B, and its TMEM holds its 128 rows.
+template <int CG>
+struct Cfg {
+  static constexpr int TILE_M = 128 * CG;
+  static constexpr int A_ROWS = 128;           // rows of A per CTA and stage
+  static constexpr int B_ROWS = TILE_N / CG;   // rows of (N x K) B per CTA and stage
+  static constexpr uint32_t A_BYTES = A_ROWS * BK * 2;
+  static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = CG == 1 ? 4 : 6;
+  static constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+};
 
 // Device status word: (epoch << 32) | (code << 24) | (info & 0xffffff).
 constexpr uint32_t DEV_TIMEOUT = 1;  // a ready-flag wait ran out
@@ -179,6 +192,68 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uin
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// CTA-pair (cta_group::2) forms -------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+// TMA load into this CTA's shared memory whose completion is counted on an
+// mbarrier of either CTA of the pair (here: the even CTA's).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive (once) on the mbarrier at this offset in every CTA of `mask` when
+// the pair's earlier tcgen05 operations have completed.
+__device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
       : "memory");
 }
 
@@ -376,11 +451,14 @@ __device__ __forceinline__ void epilogue_row_chunk(const KParams& p, const Tile&
 
 // ------------------------------------------------------------------ kernel
 
+template <int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_constant__ KParams p) {
+  using C = Cfg<CG>;
+  constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
   // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
   const uint32_t bar_full = smem_u32(bars);
   const uint32_t bar_empty = smem_u32(bars + STAGES);
@@ -392,6 +470,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // CTA rank inside the pair (0 for CG = 1); the even CTA issues the MMAs.
+  const uint32_t crank = CG == 2 ? cluster_ctarank() : 0u;
+  const bool leader = crank == 0;
+  const int64_t unit = CG == 2 ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;
+  const int64_t nunits = CG == 2 ? (int64_t)(gridDim.x >> 1) : (int64_t)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -400,22 +483,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_tfull + 8 * i, 1);
-      mbar_init(bar_tempty + 8 * i, EPI_THREADS);
+      mbar_init(bar_tempty + 8 * i, 4 * CG);  // one arrival per epilogue warp of the pair
     }
     mbar_init(bar_drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(s_tmem), TMEM_COLS);
-    tmem_relinquish();
+    if (CG == 2) {
+      tmem_alloc_pair(smem_u32(s_tmem), TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(s_tmem), TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  if (CG == 2)
+    cluster_sync_all();  // barriers of both CTAs initialised before any remote arrive
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
 
   const int64_t T = p.g.total_tiles;
   const uint32_t smem_base = smem_u32(smem);
+  bool aborted = false;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -428,7 +521,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
       int32_t issued[STAGES];  // parity of the last load issued per stage, -1 none
       for (int i = 0; i < STAGES; ++i) issued[i] = -1;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < T && ok; t += gridDim.x) {
+      for (int64_t t = unit; t < T && ok; t += nunits) {
         const Tile tl = decode_tile(p.g, t);
         if (tl.flag >= 0 && p.wait_flags) {
           wait_flag_geq(p, p.flags + tl.flag, p.epoch, (uint32_t)tl.flag);
@@ -436,16 +529,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
         }
         const CUtensorMap* ma = &p.tmA[tl.a_map];
         const CUtensorMap* mb = &p.tmB[tl.b_map];
+        const int32_t a_row = (int32_t)(tl.a_row + (int64_t)crank * C::A_ROWS);
+        const int32_t b_row = (int32_t)(tl.b_row + (int64_t)crank * C::B_ROWS);
         for (int kb = 0; kb < tl.k_blocks; ++kb) {
           if (!mbar_wait(p, bar_empty + 8 * stage, phase ^ 1, 0x100000u | stage)) {
             ok = false;
             break;
           }
           const uint32_t fb = bar_full + 8 * stage;
-          mbar_arrive_expect_tx(fb, STAGE_BYTES);
-          const uint32_t sa = smem_base + stage * STAGE_BYTES;
-          tma_load_2d(sa, ma, fb, kb * BK, (int32_t)tl.a_row);
-          tma_load_2d(sa + A_BYTES, mb, fb, kb * BK, (int32_t)tl.b_row);
+          const uint32_t sa = smem_base + stage * C::STAGE_BYTES;
+          if (CG == 2) {
+            const uint32_t fb_lead = mapa_shared(fb, 0);
+            if (leader) mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);  // both CTAs' bytes
+            tma_load_2d_pair(sa, ma, fb_lead, kb * BK, a_row);
+            tma_load_2d_pair(sa + C::A_BYTES, mb, fb_lead, kb * BK, b_row);
+          } else {
+            mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+            tma_load_2d(sa, ma, fb, kb * BK, a_row);
+            tma_load_2d(sa + C::A_BYTES, mb, fb, kb * BK, b_row);
+          }
           issued[stage] = (int32_t)phase;
           if (++stage == STAGES) {
             stage = 0;
@@ -454,23 +556,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
         }
       }
       if (!ok) {
-        // drain: every load issued must land before the CTA exits
-        for (int i = 0; i < STAGES; ++i)
-          if (issued[i] >= 0) {
-            const uint64_t t0 = globaltimer();
-            while (!mbar_try_wait(bar_full + 8 * i, (uint32_t)issued[i]) &&
-                   globaltimer() - t0 < 200000000ull) {
+        aborted = true;
+        if (CG == 1) {
+          // every load issued must land before the CTA exits
+          for (int i = 0; i < STAGES; ++i)
+            if (issued[i] >= 0) {
+              const uint64_t t0 = globaltimer();
+              while (!mbar_try_wait(bar_full + 8 * i, (uint32_t)issued[i]) &&
+                     globaltimer() - t0 < 200000000ull) {
+              }
             }
-          }
+        }
+        // CG = 2: completions are counted on the even CTA's barriers; the
+        // bounded settle below covers loads still in flight.
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       // --------------------------------------------------------------- MMA
-      constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+      constexpr uint32_t IDESC = idesc_bf16_f32(C::TILE_M, TILE_N);
       uint32_t stage = 0, phase = 0, it = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < T && ok; t += gridDim.x, ++it) {
+      for (int64_t t = unit; t < T && ok; t += nunits, ++it) {
         const Tile tl = decode_tile(p.g, t);
         const uint32_t buf = it & 1, use = it >> 1;
         if (!mbar_wait(p, bar_tempty + 8 * buf, (use & 1) ^ 1, 0x200000u | buf)) {
@@ -478,33 +585,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + buf * BN;
+        const uint32_t d_tmem = tmem_base + buf * TILE_N;
         for (int kb = 0; kb < tl.k_blocks; ++kb) {
           if (!mbar_wait(p, bar_full + 8 * stage, phase, 0x300000u | stage)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_base + stage * STAGE_BYTES;
+          const uint32_t sa = smem_base + stage * C::STAGE_BYTES;
           const uint64_t da = smem_desc_sw128(sa);
-          const uint64_t db = smem_desc_sw128(sa + A_BYTES);
+          const uint64_t db = smem_desc_sw128(sa + C::A_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             // +32 bytes per K=16 step inside the swizzled 128-byte row
-            tc_mma_bf16(d_tmem, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), IDESC,
-                        (kb | kk) != 0 ? 1u : 0u);
+            const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+            if (CG == 2)
+              tc_mma_bf16_pair(d_tmem, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), IDESC, acc);
+            else
+              tc_mma_bf16(d_tmem, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), IDESC, acc);
           }
-          tc_commit(bar_empty + 8 * stage);
+          if (CG == 2)
+            tc_commit_pair_mc(bar_empty + 8 * stage, 0x3);
+          else
+            tc_commit(bar_empty + 8 * stage);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        tc_commit(bar_tfull + 8 * buf);
+        if (CG == 2)
+          tc_commit_pair_mc(bar_tfull + 8 * buf, 0x3);
+        else
+          tc_commit(bar_tfull + 8 * buf);
       }
       if (!ok) {
-        tc_commit(bar_drain);
+        aborted = true;
+        if (CG == 2)
+          tc_commit_pair_mc(bar_drain, 0x1);
+        else
+          tc_commit(bar_drain);
         const uint64_t t0 = globaltimer();
         while (!mbar_try_wait(bar_drain, 0) && globaltimer() - t0 < 200000000ull) {
         }
@@ -516,26 +636,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
     const int q = warp & 3;           // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;    // accumulator row = TMEM lane
     uint32_t it = 0;
-    for (int64_t t = blockIdx.x; t < T; t += gridDim.x, ++it) {
+    for (int64_t t = unit; t < T; t += nunits, ++it) {
       const Tile tl = decode_tile(p.g, t);
       const uint32_t buf = it & 1, use = it >> 1;
+      const int64_t tflag = tl.tile_flag >= 0 ? tl.tile_flag * CG + crank : -1;
       if (et == 0) {
         bool go = mbar_wait(p, bar_tfull + 8 * buf, use & 1, 0x400000u | buf);
-        if (go && tl.tile_flag >= 0 && tl.s > 0) {
-          // partial of this tile from the previous step
-          wait_flag_geq(p, p.flags + tl.tile_flag, p.epoch * (uint32_t)p.g.P + (uint32_t)tl.s - 1,
-                        (uint32_t)tl.tile_flag);
+        if (go && tflag >= 0 && tl.s > 0) {
+          // partial of this half tile from the previous step
+          wait_flag_geq(p, p.flags + tflag, p.epoch * (uint32_t)p.g.P + (uint32_t)tl.s - 1,
+                        (uint32_t)tflag);
         }
         s_go[it & 1] = go ? 1u : 0u;
       }
       named_bar_sync(1, EPI_THREADS);
-      if (s_go[it & 1] == 0) break;
+      if (s_go[it & 1] == 0) {
+        aborted = true;
+        break;
+      }
       tc_fence_after();
-      const bool row_ok = row < tl.rows_valid;
-      const int64_t grow = tl.out_row + row;
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN;
+      const int rows_here = tl.rows_valid - (int)crank * ROWS_PER_CTA;
+      const bool row_ok = row < rows_here;
+      const int64_t grow = tl.out_row + (int64_t)crank * ROWS_PER_CTA + row;
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + buf * TILE_N;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < TILE_N / 32; ++c) {
         if (c * 32 >= tl.cols_valid) break;  // uniform across the CTA
         float acc[32];
         if (tl.k_blocks > 0) {
@@ -554,21 +679,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
         }
       }
       tc_fence_before();
-      mbar_arrive(bar_tempty + 8 * buf);
-      if (tl.tile_flag >= 0 && tl.dst == DST_X) {
+      __syncwarp();
+      if (lane == 0) {
+        if (CG == 2)
+          mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * buf, 0));  // the even CTA's barrier
+        else
+          mbar_arrive(bar_tempty + 8 * buf);
+      }
+      if (tflag >= 0 && tl.dst == DST_X) {
         __threadfence();
         named_bar_sync(1, EPI_THREADS);
-        if (et == 0) st_release_u32(p.flags + tl.tile_flag, p.epoch * (uint32_t)p.g.P + (uint32_t)tl.s);
+        if (et == 0) st_release_u32(p.flags + tflag, p.epoch * (uint32_t)p.g.P + (uint32_t)tl.s);
       }
     }
   }
 
+  if (CG == 2 && aborted) {
+    // let loads and MMAs still in flight for this pair land before exit
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 20000000ull) {
+    }
+  }
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  if (CG == 2)
+    cluster_sync_all();  // no remote arrive may target a CTA that has exited
+  else
+    __syncthreads();
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if (CG == 2)
+      tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 

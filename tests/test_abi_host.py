@@ -162,17 +162,23 @@ def _simulate(plan, m, n, k, l, tp, sched):
     assert np.all(cover == (tp if sched >= 2 else 1))
 
 
+@pytest.mark.parametrize("cg", [1, 2])
 @pytest.mark.parametrize("sched", [0, 1, 2, 3])
 @pytest.mark.parametrize("tp", [1, 2, 4, 8])
 @pytest.mark.parametrize("shape", [(256, 512, 128, 1), (1024, 768, 512, 2), (136, 272, 80, 1)])
-def test_tile_order_simulator(L, sched, tp, shape):
+def test_tile_order_simulator(L, sched, tp, shape, cg):
     m, n, k, l = shape
     if sched in (2, 3) and (k % tp or (k // tp) % 8):
         k = 64 * tp
     if (sched in (0, 1, 2) and m % tp) or (sched != 2 and n % tp):
         pytest.skip("not divisible")
     plan = dg.Plan(m, n, k, l, tp, sched, 1.0, 0.5)
+    plan.set_option(dg.OPT_CTA_GROUP, cg)
+    assert plan.info()["tile_m"] == 128 * cg
     _simulate(plan, m, n, k, l, tp, sched)
+    if sched >= 2 and tp > 1:
+        info = plan.info()
+        assert info["n_flags"] == l * tp * info["tiles_m"] * info["tiles_n"] * cg
 
 
 def test_ag_flag_indices_follow_copy_order(L):
@@ -190,7 +196,7 @@ def test_ag_flag_indices_follow_copy_order(L):
         if tl["flag"] < 0:
             continue
         s, r, b = tl["step"], tl["rank"], tl["batch"]
-        mt = (tl["a_row"] % (m // tp)) // 128
+        mt = (tl["a_row"] % (m // tp)) // info["tile_m"]
         assert tl["flag"] == ((r * (tp - 1) + s - 1) * l + b) * nch + mt // 2
         seen.add(tl["flag"])
     assert seen == set(range(info["n_flags"]))

@@ -160,3 +160,20 @@ def test_does_not_write_outside_d():
         D = big[2048: 2048 + l * m * n].view(l, m, n)
         Runner(m, n, k, l, tp, sched).run(A, B, None, D)
         assert torch.all(big[:2048] == 7.0) and torch.all(big[2048 + l * m * n:] == 7.0)
+
+
+@pytest.mark.parametrize("tp", [1, 2, 4, 8])
+@pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_single_sm_tiles_vs_oracle(sched, tp):
+    # the 128 x 256 single-SM tile configuration (DG_OPT_CTA_GROUP = 1)
+    m, n, k, l = 392, 776, 320, 2
+    if not _shape_ok(sched, m, n, k, tp):
+        pytest.skip("shape not divisible for this schedule/tp")
+    a, b, c = host_inputs(m, n, k, l, seed=50 + tp + 10 * sched)
+    A, B, C = to_dev(a), to_dev(b), to_dev(c)
+    r = Runner(m, n, k, l, tp, sched, 0.5, 1.0, options={dg.OPT_CTA_GROUP: 1})
+    D, _ = r.run(A, B, C)
+    assert rel_err(D, oracle_full(a, b, c, 0.5, 1.0)) <= TOL
+    if sched in (dg.AG_ROTATING_A, dg.AG_ROTATING_B) and tp > 1:
+        ref, _ = Runner(m, n, k, l, 1, sched, 0.5, 1.0, options={dg.OPT_CTA_GROUP: 1}).run(A, B, C)
+        assert torch.equal(D.view(torch.int16), ref.view(torch.int16))
