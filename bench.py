@@ -54,6 +54,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-modes", action="store_true", help="skip the GEMM_ONLY / SERIAL timings")
     ap.add_argument("--mode", choices=["fused", "gemm_only", "serial"], default="fused",
                     help="mode of the timed loop (gemm_only/serial for profilers that serialize streams)")
+    ap.add_argument("--copy-streams", type=int, default=0, help="0 = the library default")
     ap.add_argument("--cpu-sample-rows", type=int, default=1024)
     ap.add_argument("--cpu-sample-cols", type=int, default=4096)
     return ap.parse_args(argv)
@@ -233,6 +234,8 @@ def run_dg(args, rank, world, dist):
     A, B, C = make_inputs(w, dev)
     D = torch.empty((w.l, w.m, w.n), dtype=torch.bfloat16, device=dev)
     plan = dg.Plan(w.m, w.n, w.k, w.l, w.tp, w.schedule, w.alpha, w.beta)
+    if args.copy_streams > 0:
+        plan.set_option(dg.OPT_COPY_STREAMS, args.copy_streams)
     ws = torch.zeros(max(plan.workspace_bytes(), 256), dtype=torch.uint8, device=dev)
     main = torch.cuda.current_stream(dev)
     copy = torch.cuda.Stream(dev)

@@ -128,6 +128,12 @@ struct dg_plan_s {
   int num_sms = 0;
   int max_pairs = 0;  // co-resident CTA pairs of the CG = 2 kernel
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  // extra copy streams (FUSED transfers spread round-robin over the caller's
+  // copy stream and these, so that several copy engines move shards at once)
+  int copy_streams = 1;
+  int n_extra = 0;
+  cudaStream_t extra[7] = {};
+  cudaEvent_t extra_done[7] = {};
   dg::KParams kp;
   const void* map_key[3] = {nullptr, nullptr, nullptr};
   int n_maps = 0;
@@ -315,11 +321,25 @@ void CUDART_CB sleep_cb(void* ms) {
 
 // Shard transfers of every rank and step >= 1, each chunk followed by its
 // ready-flag write, in the order the kernel consumes them.
+int ensure_extra_streams(dg_plan_s* p, int want) {
+  while (p->n_extra < want) {
+    DG_CUDA(cudaStreamCreateWithFlags(&p->extra[p->n_extra], cudaStreamNonBlocking));
+    DG_CUDA(cudaEventCreateWithFlags(&p->extra_done[p->n_extra], cudaEventDisableTiming));
+    p->n_extra++;
+  }
+  return DG_OK;
+}
+
+// Shard transfers of every rank and step >= 1, each chunk followed by its
+// ready-flag write on the same stream, in the order the kernel consumes them.
+// Chunks are dealt round-robin over `ns` streams.
 int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B, uint8_t* ws,
-                   cudaStream_t st) {
+                   cudaStream_t* streams, int ns) {
   const dg::Geom& g = p->g;
   const int64_t P = p->tp;
-  if (p->fault_delay_ms > 0) DG_CUDA(cudaLaunchHostFunc(st, sleep_cb, (void*)(intptr_t)p->fault_delay_ms));
+  if (p->fault_delay_ms > 0)
+    for (int i = 0; i < ns; ++i)
+      DG_CUDA(cudaLaunchHostFunc(streams[i], sleep_cb, (void*)(intptr_t)p->fault_delay_ms));
   const bool rot_a = p->schedule == DG_AG_ROTATING_A;
   const auto* home = static_cast<const uint16_t*>(rot_a ? A : B);
   const int64_t outer = rot_a ? p->m : p->n;  // rows of one batch of the rotated operand
@@ -334,6 +354,7 @@ int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B
       for (int64_t l = 0; l < g.L; ++l) {
         const int64_t slot = (r * (P - 1) + (s - 1)) * g.L + l;
         for (int64_t c = 0; c < g.nchunks; ++c, ++idx) {
+          cudaStream_t st = streams[idx % ns];
           const int64_t row0 = c * chunk_rows;
           const int64_t rows = std::min(chunk_rows, g.shard - row0);
           if (rows > 0) {
@@ -463,7 +484,9 @@ int dg_set_option(dg_plan_t p, int option, int64_t value) {
       p->grid_req = value;
       return DG_OK;
     case DG_OPT_COPY_STREAMS:
-      return value == 1 ? DG_OK : fail(DG_ERR_UNSUPPORTED, "one copy stream only");
+      if (value < 1 || value > 8) return fail(DG_ERR_ARG, "copy streams must be 1..8");
+      p->copy_streams = (int)value;
+      return DG_OK;
     case DG_OPT_CTA_GROUP:
       if (value != 1 && value != 2) return fail(DG_ERR_ARG, "CTA group must be 1 or 2");
       if (p->epoch != 0) return fail(DG_ERR_STATE, "the tile configuration is fixed after the first run");
@@ -575,16 +598,26 @@ int dg_run(dg_plan_t p, const dg_bf16_t* A, const dg_bf16_t* B, const dg_bf16_t*
     int mode = p->mode;
     if (mode == DG_MODE_FUSED && (cs == ms || cs == nullptr)) mode = DG_MODE_SERIAL;
     if (mode == DG_MODE_FUSED) {
+      const int ns = p->copy_streams;
+      rc = ensure_extra_streams(p, ns - 1);
+      if (rc) return rc;
+      cudaStream_t streams[8];
+      streams[0] = cs;
+      for (int i = 1; i < ns; ++i) streams[i] = p->extra[i - 1];
       DG_CUDA(cudaEventRecord(p->ev_fork, ms));
       rc = launch(p, ms, 1);
       if (rc) return rc;
-      DG_CUDA(cudaStreamWaitEvent(cs, p->ev_fork, 0));
-      rc = enqueue_copies(p, drv, A, B, ws, cs);
+      for (int i = 0; i < ns; ++i) DG_CUDA(cudaStreamWaitEvent(streams[i], p->ev_fork, 0));
+      rc = enqueue_copies(p, drv, A, B, ws, streams, ns);
       if (rc) return rc;
+      for (int i = 1; i < ns; ++i) {
+        DG_CUDA(cudaEventRecord(p->extra_done[i - 1], streams[i]));
+        DG_CUDA(cudaStreamWaitEvent(cs, p->extra_done[i - 1], 0));
+      }
       DG_CUDA(cudaEventRecord(p->ev_join, cs));
       DG_CUDA(cudaStreamWaitEvent(ms, p->ev_join, 0));
     } else if (mode == DG_MODE_SERIAL) {
-      rc = enqueue_copies(p, drv, A, B, ws, ms);
+      rc = enqueue_copies(p, drv, A, B, ws, &ms, 1);
       if (rc) return rc;
       rc = launch(p, ms, 1);
       if (rc) return rc;
@@ -626,6 +659,10 @@ void dg_destroy(dg_plan_t p) {
   }
   if (p->ev_fork) cudaEventDestroy(p->ev_fork);
   if (p->ev_join) cudaEventDestroy(p->ev_join);
+  for (int i = 0; i < p->n_extra; ++i) {
+    cudaStreamDestroy(p->extra[i]);
+    cudaEventDestroy(p->extra_done[i]);
+  }
   delete p;
 }
 

@@ -102,3 +102,19 @@ def test_plan_alternating_between_workspaces():
         _poison_slots(r1)
         D, _ = r1.run(A, B, None)
         assert rel_err(D, want) <= TOL
+
+
+@pytest.mark.parametrize("ns", [2, 3, 8])
+def test_transfers_over_several_copy_streams(ns):
+    m, n, k, l, tp = 1024, 2048, 512, 2, 4
+    a, b, c = host_inputs(m, n, k, l, seed=25)
+    A, B = to_dev(a), to_dev(b)
+    want = oracle_full(a, b, c, 1.0, 0.0)
+    for sched in (dg.AG_ROTATING_A, dg.AG_ROTATING_B):
+        r = Runner(m, n, k, l, tp, sched, options={dg.OPT_COPY_STREAMS: ns, dg.OPT_FAULT_DELAY_MS: 20,
+                                                   dg.OPT_CHUNK_TILES: 1})
+        _poison_slots(r)
+        D, _ = r.run(A, B, None)
+        assert rel_err(D, want) <= TOL
+        D2, _ = r.run(A, B, None)
+        assert torch.equal(D.view(torch.int16), D2.view(torch.int16))
