@@ -104,8 +104,8 @@ enum dg_option {
                                  before the first transfer (default 0) */
   DG_OPT_GRID = 4,            /* persistent grid size in CTAs (0 = all co-resident) */
   DG_OPT_COPY_STREAMS = 5,    /* FUSED shard transfers spread round-robin over this many
-                                 streams (1..8): the caller's copy stream plus streams the
-                                 plan creates, so several copy engines run at once */
+                                 streams (1..8, default 2): the caller's copy stream plus
+                                 streams the plan creates, so several copy engines run at once */
   DG_OPT_CTA_GROUP = 6        /* tile configuration, before the first run: 2 (default) =
                                  256 x 256 tiles on an SM pair (tcgen05 cta_group::2),
                                  1 = 128 x 256 tiles on one SM */

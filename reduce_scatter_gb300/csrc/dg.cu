@@ -130,7 +130,7 @@ struct dg_plan_s {
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   // extra copy streams (FUSED transfers spread round-robin over the caller's
   // copy stream and these, so that several copy engines move shards at once)
-  int copy_streams = 1;
+  int copy_streams = 2;
   int n_extra = 0;
   cudaStream_t extra[7] = {};
   cudaEvent_t extra_done[7] = {};
