@@ -11,6 +11,8 @@ the pages' benchmarks, as synthetic inputs.
   (K split 8 x 3584); A N(0,1), B N(0,0.02).
 * ``ag_b_tp4_batched`` / ``rs_b_tp4_batched``: RotatingB / TilingB RotatingC,
   TP=4, 8192 x 53248 x 8192, L=2, alpha=0.5, beta=1, C N(0,1).
+* ``rs_b_tp4_quarter``: rs_b_tp4_batched with N / 4 and L = 1, for profiler
+  captures.
 
 A is the activation (M x K), B the weight stored N x K, C the epilogue input.
 """
@@ -64,6 +66,10 @@ WORKLOADS = {
         Workload("ag_b_tp4_batched", 1, 4, 8192, 53248, 8192, l=2, alpha=0.5, beta=1.0, dist_a=N1,
                  dist_b=N002, dist_c=N1),
         Workload("rs_b_tp4_batched", 3, 4, 8192, 53248, 8192, l=2, alpha=0.5, beta=1.0, dist_a=N1,
+                 dist_b=N002, dist_c=N1),
+        # a quarter of rs_b_tp4_batched's N and one batch: small enough (about 1 GB on the
+        # device) for a full profiler capture, same per-tile work
+        Workload("rs_b_tp4_quarter", 3, 4, 8192, 13312, 8192, l=1, alpha=0.5, beta=1.0, dist_a=N1,
                  dist_b=N002, dist_c=N1),
     ]
 }
