@@ -106,9 +106,13 @@ enum dg_option {
   DG_OPT_COPY_STREAMS = 5,    /* FUSED shard transfers spread round-robin over this many
                                  streams (1..8, default 2): the caller's copy stream plus
                                  streams the plan creates, so several copy engines run at once */
-  DG_OPT_CTA_GROUP = 6        /* tile configuration, before the first run: 2 (default) =
+  DG_OPT_CTA_GROUP = 6,       /* tile configuration, before the first run: 2 (default) =
                                  256 x 256 tiles on an SM pair (tcgen05 cta_group::2),
                                  1 = 128 x 256 tiles on one SM */
+  DG_OPT_EPILOGUE = 7         /* epilogue, before the first run: 1 = source and result
+                                 chunks staged in shared memory and moved by TMA (default
+                                 for the RS schedules), 0 = direct per-row global accesses
+                                 (default for the AG schedules, one more operand stage) */
 };
 
 /* Plan geometry and workspace layout, for callers and tests. */

@@ -114,6 +114,7 @@ struct dg_plan_s {
   int64_t fault_delay_ms = 0;
   int64_t grid_req = 0;
   int cg = 2;  // CTA group of the tile config: 1 = 128 x 256 per SM, 2 = 256 x 256 per SM pair
+  int epi = 0;  // epilogue: 0 direct, 1 staged through shared memory with TMA (default for RS)
   uint64_t id = 0;
   uint32_t epoch = 0;
   bool serial_ws = false;
@@ -224,10 +225,14 @@ int rt_init(dg_plan_s* p) {
     return fail(DG_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a", dev,
                 major, minor);
   DG_CUDA(cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, dev));
-  DG_CUDA(cudaFuncSetAttribute(dg::dg_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)dg::Cfg<1>::SMEM_BYTES));
-  DG_CUDA(cudaFuncSetAttribute(dg::dg_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)dg::Cfg<2>::SMEM_BYTES));
+  DG_CUDA(cudaFuncSetAttribute(dg::dg_gemm_kernel<1, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)dg::Cfg<1, 0>::SMEM_BYTES));
+  DG_CUDA(cudaFuncSetAttribute(dg::dg_gemm_kernel<1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)dg::Cfg<1, 1>::SMEM_BYTES));
+  DG_CUDA(cudaFuncSetAttribute(dg::dg_gemm_kernel<2, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)dg::Cfg<2, 0>::SMEM_BYTES));
+  DG_CUDA(cudaFuncSetAttribute(dg::dg_gemm_kernel<2, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)dg::Cfg<2, 1>::SMEM_BYTES));
   {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -237,12 +242,14 @@ int rt_init(dg_plan_s* p) {
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(2 * 256, 1, 1);
     cfg.blockDim = dim3(dg::NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = dg::Cfg<2>::SMEM_BYTES;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int ncl = 0;
-    DG_CUDA(cudaOccupancyMaxActiveClusters(&ncl, dg::dg_gemm_kernel<2>, &cfg));
-    p->max_pairs = ncl;
+    int ncl0 = 0, ncl1 = 0;
+    cfg.dynamicSmemBytes = dg::Cfg<2, 0>::SMEM_BYTES;
+    DG_CUDA(cudaOccupancyMaxActiveClusters(&ncl0, dg::dg_gemm_kernel<2, 0>, &cfg));
+    cfg.dynamicSmemBytes = dg::Cfg<2, 1>::SMEM_BYTES;
+    DG_CUDA(cudaOccupancyMaxActiveClusters(&ncl1, dg::dg_gemm_kernel<2, 1>, &cfg));
+    p->max_pairs = std::min(ncl0, ncl1);
   }
   DG_CUDA(cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming));
   DG_CUDA(cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming));
@@ -267,6 +274,46 @@ int encode_map(const Driver& drv, CUtensorMap* map, const void* base, int64_t in
   return DG_OK;
 }
 
+// Epilogue chunk map: `rows` x `cols` elements (fp32 or bf16) with a row pitch
+// of `cols`, box of 32 columns x 128 rows, swizzle matching the 32-column
+// chunk's row bytes (128 B for fp32, 64 B for bf16).
+int encode_epi_map(const Driver& drv, CUtensorMap* map, const void* base, bool f32, int64_t cols,
+                   int64_t rows) {
+  const int64_t esz = f32 ? 4 : 2;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(cols * esz)};
+  cuuint32_t box[2] = {(cuuint32_t)dg::XCOLS, (cuuint32_t)dg::ROWS_PER_CTA};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = drv.encode(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(DG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for the %s epilogue map %lld x %lld", (int)r,
+                f32 ? "fp32" : "bf16", (long long)rows, (long long)cols);
+  return DG_OK;
+}
+
+// Maps of the staged epilogue (caller pointers may change from run to run).
+int build_epi_maps(dg_plan_s* p, const Driver& drv, const void* C, void* D, uint8_t* ws) {
+  std::memset(&p->kp.tmX, 0, sizeof(CUtensorMap));
+  std::memset(&p->kp.tmC, 0, sizeof(CUtensorMap));
+  std::memset(&p->kp.tmD, 0, sizeof(CUtensorMap));
+  if (p->epi != 1) return DG_OK;
+  const int64_t rows = p->l * p->m;
+  int rc = encode_epi_map(drv, &p->kp.tmD, D, false, p->n, rows);
+  if (rc) return rc;
+  if (C && p->beta != 0.f) {
+    rc = encode_epi_map(drv, &p->kp.tmC, C, false, p->n, rows);
+    if (rc) return rc;
+  }
+  if (!is_ag(p->schedule) && p->tp > 1) {
+    rc = encode_epi_map(drv, &p->kp.tmX, ws + p->off_partial, true, p->n, rows);
+    if (rc) return rc;
+  }
+  return DG_OK;
+}
+
 int build_maps(dg_plan_s* p, const Driver& drv, const void* A, const void* B, uint8_t* ws) {
   if (p->map_key[0] == A && p->map_key[1] == B && p->map_key[2] == ws) return DG_OK;
   std::memset(p->kp.tmA, 0, sizeof(p->kp.tmA));
@@ -278,6 +325,7 @@ int build_maps(dg_plan_s* p, const Driver& drv, const void* A, const void* B, ui
   // each CTA loads its own rows of the tile: 128 of A; 256 (CG = 1) or 128 (CG = 2) of B
   const int a_box = dg::Cfg<1>::A_ROWS;
   const int b_box = p->cg == 2 ? dg::Cfg<2>::B_ROWS : dg::Cfg<1>::B_ROWS;
+  static_assert(dg::Cfg<2, 0>::B_ROWS == dg::Cfg<2, 1>::B_ROWS, "box rows do not depend on the epilogue");
   if (p->k > 0) {
     if (is_ag(p->schedule)) {
       rc = encode_map(drv, &p->kp.tmA[0], A, p->k, g.L * p->m, p->k, a_box);
@@ -381,7 +429,10 @@ int launch(dg_plan_s* p, cudaStream_t st, uint32_t wait_flags) {
     int64_t grid = p->grid_req > 0 ? p->grid_req : p->num_sms;
     grid = std::min<int64_t>(grid, p->g.total_tiles);
     if (grid <= 0) return DG_OK;
-    dg::dg_gemm_kernel<1><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1>::SMEM_BYTES, st>>>(p->kp);
+    if (p->epi == 1)
+      dg::dg_gemm_kernel<1, 1><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 1>::SMEM_BYTES, st>>>(p->kp);
+    else
+      dg::dg_gemm_kernel<1, 0><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 0>::SMEM_BYTES, st>>>(p->kp);
     DG_CUDA(cudaGetLastError());
     return DG_OK;
   }
@@ -397,11 +448,14 @@ int launch(dg_plan_s* p, cudaStream_t st, uint32_t wait_flags) {
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
   cfg.blockDim = dim3(dg::NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = dg::Cfg<2>::SMEM_BYTES;
+  cfg.dynamicSmemBytes = p->epi == 1 ? dg::Cfg<2, 1>::SMEM_BYTES : dg::Cfg<2, 0>::SMEM_BYTES;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2>, p->kp));
+  if (p->epi == 1)
+    DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 1>, p->kp));
+  else
+    DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 0>, p->kp));
   return DG_OK;
 }
 
@@ -435,6 +489,7 @@ int dg_plan(dg_plan_t* out, int64_t m, int64_t n, int64_t k, int64_t l, int tp, 
   p->m = m, p->n = n, p->k = k, p->l = l;
   p->tp = tp, p->schedule = schedule;
   p->alpha = alpha, p->beta = beta;
+  p->epi = is_ag(schedule) ? 0 : 1;
   {
     std::lock_guard<std::mutex> lk(g_ws_mu);
     p->id = g_next_plan_id++;
@@ -486,6 +541,11 @@ int dg_set_option(dg_plan_t p, int option, int64_t value) {
     case DG_OPT_COPY_STREAMS:
       if (value < 1 || value > 8) return fail(DG_ERR_ARG, "copy streams must be 1..8");
       p->copy_streams = (int)value;
+      return DG_OK;
+    case DG_OPT_EPILOGUE:
+      if (value != 0 && value != 1) return fail(DG_ERR_ARG, "epilogue must be 0 (direct) or 1 (staged)");
+      if (p->epoch != 0) return fail(DG_ERR_STATE, "the epilogue is fixed after the first run");
+      p->epi = (int)value;
       return DG_OK;
     case DG_OPT_CTA_GROUP:
       if (value != 1 && value != 2) return fail(DG_ERR_ARG, "CTA group must be 1 or 2");
@@ -579,6 +639,8 @@ int dg_run(dg_plan_t p, const dg_bf16_t* A, const dg_bf16_t* B, const dg_bf16_t*
   p->epoch += 1;
 
   rc = build_maps(p, drv, A, B, ws);
+  if (rc) return rc;
+  rc = build_epi_maps(p, drv, C, D, ws);
   if (rc) return rc;
   dg::KParams& kp = p->kp;
   kp.g = p->g;

@@ -48,12 +48,23 @@ constexpr int ROWS_PER_CTA = 128;  // accumulator rows (TMEM lanes) per CTA
 constexpr int TILE_N = 256;        // accumulator columns
 constexpr uint32_t TMEM_COLS = 2 * TILE_N;  // two accumulators
 
+// Epilogue variants.
+//   EPI = 0 (direct): each thread writes its accumulator row straight to
+//           global memory (and reads its source row the same way).
+//   EPI = 1 (staged): 32-column chunks of the source (beta*C or the fp32
+//           rotating partial) are TMA-loaded into swizzled shared memory ahead
+//           of use, and full destination chunks are staged in shared memory and
+//           TMA-stored, so every global access is a coalesced bulk transfer.
+//           Costs one operand stage of the ring (64 KB of staging).
+constexpr int XCOLS = 32;                            // columns per epilogue chunk
+constexpr uint32_t XBUF = ROWS_PER_CTA * XCOLS * 4;  // 16 KB: one fp32 chunk
+
 // Tile configuration per CTA group.
 //   CG = 1: one SM, tile 128 x 256, tcgen05.mma.cta_group::1 (M=128, N=256).
 //   CG = 2: an SM pair (cluster of 2), tile 256 x 256, tcgen05.mma.cta_group::2
 //           (M=256, N=256) issued by the even CTA; each CTA stages its 128
 //           rows of A and its 128 rows of B, and its TMEM holds its 128 rows.
-template <int CG>
+template <int CG, int EPI = 0>
 struct Cfg {
   static constexpr int TILE_M = 128 * CG;
   static constexpr int A_ROWS = 128;           // rows of A per CTA and stage
@@ -61,8 +72,10 @@ struct Cfg {
   static constexpr uint32_t A_BYTES = A_ROWS * BK * 2;
   static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = CG == 1 ? 4 : 6;
-  static constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int STAGES = CG == 1 ? (EPI ? 3 : 4) : (EPI ? 5 : 6);
+  static constexpr uint32_t STAGING_BYTES = EPI ? 4 * XBUF : 0;  // 2 source + 2 destination chunks
+  static constexpr uint32_t SMEM_BYTES =
+      STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 };
 
 // Device status word: (epoch << 32) | (code << 24) | (info & 0xffffff).
@@ -72,6 +85,9 @@ constexpr uint32_t DEV_HANG = 2;     // a pipeline wait ran out
 struct KParams {
   CUtensorMap tmA[MAX_MAPS];
   CUtensorMap tmB[MAX_MAPS];
+  // staged epilogue: fp32 partial (box 32 x 128, 128B swizzle), bf16 C and D
+  // (box 32 x 128, 64B swizzle)
+  CUtensorMap tmX, tmC, tmD;
   Geom g;
   const __nv_bfloat16* C;
   __nv_bfloat16* D;
@@ -85,6 +101,7 @@ struct KParams {
   uint64_t timeout_ns;
   uint64_t hang_ns;
 };
+static_assert(sizeof(KParams) <= 4096, "kernel parameters must fit the 4 KB parameter space");
 
 // ------------------------------------------------------------------ PTX glue
 
@@ -155,6 +172,35 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
+
+// Generic-proxy writes to shared memory made visible to a following TMA store.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N committed bulk stores still read their shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until at most N committed bulk stores are still incomplete.
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Byte offset inside a 1024-byte-aligned tile written by TMA with the
+// 128-byte (64-byte) swizzle: 16-byte unit bits [4,7) ([4,6)) XOR bits
+// [7,10) ([7,9)) of the linear offset.
+__device__ __forceinline__ uint32_t sw128(uint32_t off) { return off ^ (((off >> 7) & 7u) << 4); }
+__device__ __forceinline__ uint32_t sw64(uint32_t off) { return off ^ (((off >> 7) & 3u) << 4); }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -449,23 +495,102 @@ __device__ __forceinline__ void epilogue_row_chunk(const KParams& p, const Tile&
   }
 }
 
+// Masked direct store of 32 consecutive results of one output row.
+__device__ __forceinline__ void store_row_chunk(const KParams& p, const Tile& tl, int64_t grow,
+                                                int64_t gcol, int ncols, const float (&out)[32]) {
+  const int64_t e0 = grow * p.g.N + gcol;
+  if (tl.dst == DST_D) {
+    __nv_bfloat16* d = p.D + e0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < ncols) d[i] = __float2bfloat16_rn(out[i]);
+  } else {
+    float* x = p.X + e0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < ncols) __stcg(x + i, out[i]);
+  }
+}
+
+// Row `row` (32 values) of a staged source chunk: fp32 with the 128-byte
+// swizzle (the rotating partial) or bf16 with the 64-byte swizzle (C, scaled
+// by beta).
+__device__ __forceinline__ void staged_read_row(const uint8_t* buf, int row, bool f32, float beta,
+                                                float (&src)[32]) {
+  if (f32) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float4 v = *reinterpret_cast<const float4*>(buf + sw128((uint32_t)row * 128u + j * 16u));
+      src[4 * j] = v.x;
+      src[4 * j + 1] = v.y;
+      src[4 * j + 2] = v.z;
+      src[4 * j + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 v = *reinterpret_cast<const uint4*>(buf + sw64((uint32_t)row * 64u + j * 16u));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        src[8 * j + 2 * h] = beta * bf16_bits_to_f32(w[h] & 0xFFFFu);
+        src[8 * j + 2 * h + 1] = beta * bf16_bits_to_f32(w[h] >> 16);
+      }
+    }
+  }
+}
+
+// Row `row` of a staged destination chunk, in the layout its TMA store reads.
+__device__ __forceinline__ void staged_write_row(uint8_t* buf, int row, bool f32, const float (&out)[32]) {
+  if (f32) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<float4*>(buf + sw128((uint32_t)row * 128u + j * 16u)) =
+          make_float4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint4 v;
+      v.x = pack_bf16x2(out[8 * j + 0], out[8 * j + 1]);
+      v.y = pack_bf16x2(out[8 * j + 2], out[8 * j + 3]);
+      v.z = pack_bf16x2(out[8 * j + 4], out[8 * j + 5]);
+      v.w = pack_bf16x2(out[8 * j + 6], out[8 * j + 7]);
+      *reinterpret_cast<uint4*>(buf + sw64((uint32_t)row * 64u + j * 16u)) = v;
+    }
+  }
+}
+
+// TMA load of source chunk c of a tile half into staging buffer (idx & 1).
+__device__ __forceinline__ void staged_load_src(const KParams& p, const Tile& tl, int64_t row0, int c,
+                                                uint32_t idx, uint32_t sbase, uint32_t bar_xfull) {
+  const uint32_t sb = idx & 1;
+  const bool f32 = tl.src == SRC_X;
+  mbar_arrive_expect_tx(bar_xfull + 8 * sb, f32 ? XBUF : XBUF / 2);
+  tma_load_2d(sbase + sb * XBUF, f32 ? &p.tmX : &p.tmC, bar_xfull + 8 * sb,
+              (int32_t)(tl.out_col + c * XCOLS), (int32_t)row0);
+}
+
 // ------------------------------------------------------------------ kernel
 
-template <int CG>
+template <int CG, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_constant__ KParams p) {
-  using C = Cfg<CG>;
+  using C = Cfg<CG, EPI>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
-  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
+  // staged epilogue: source chunks [2] then destination chunks [2], 1024-aligned
+  uint8_t* xsrc = smem + STAGES * C::STAGE_BYTES;
+  uint8_t* xdst = xsrc + 2 * XBUF;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES + C::STAGING_BYTES);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, xfull[2]
   const uint32_t bar_full = smem_u32(bars);
   const uint32_t bar_empty = smem_u32(bars + STAGES);
   const uint32_t bar_tfull = smem_u32(bars + 2 * STAGES);
   const uint32_t bar_tempty = smem_u32(bars + 2 * STAGES + 2);
   const uint32_t bar_drain = smem_u32(bars + 2 * STAGES + 4);
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  const uint32_t bar_xfull = smem_u32(bars + 2 * STAGES + 5);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 7);
   volatile uint32_t* s_go = s_tmem + 1;  // [2] epilogue go/abort, by tile parity
 
   const int warp = threadIdx.x >> 5;
@@ -486,6 +611,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
       mbar_init(bar_tempty + 8 * i, 4 * CG);  // one arrival per epilogue warp of the pair
     }
     mbar_init(bar_drain, 1);
+    mbar_init(bar_xfull, 1);
+    mbar_init(bar_xfull + 8, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -635,17 +762,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
     const int et = threadIdx.x - 64;  // 0..127
     const int q = warp & 3;           // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;    // accumulator row = TMEM lane
+    const uint32_t xsrc_addr = smem_u32(xsrc);
+    const uint32_t xdst_addr = smem_u32(xdst);
+    uint32_t nload = 0;   // staged source chunks loaded so far (buffer idx & 1)
+    uint32_t nstore = 0;  // staged destination chunks stored so far (buffer idx & 1)
     uint32_t it = 0;
     for (int64_t t = unit; t < T; t += nunits, ++it) {
       const Tile tl = decode_tile(p.g, t);
       const uint32_t buf = it & 1, use = it >> 1;
       const int64_t tflag = tl.tile_flag >= 0 ? tl.tile_flag * CG + crank : -1;
+      const int rows_here = tl.rows_valid - (int)crank * ROWS_PER_CTA;
+      const int64_t row0 = tl.out_row + (int64_t)crank * ROWS_PER_CTA;
+      const int nch = (tl.cols_valid + XCOLS - 1) / XCOLS;
+      // Staged tiles need 16-byte aligned TMA column coordinates (8 bf16).
+      const bool staged = EPI == 1 && (tl.out_col & 7) == 0;
+      const bool has_src = staged && tl.src != SRC_NONE;
       if (et == 0) {
         bool go = mbar_wait(p, bar_tfull + 8 * buf, use & 1, 0x400000u | buf);
         if (go && tflag >= 0 && tl.s > 0) {
           // partial of this half tile from the previous step
           wait_flag_geq(p, p.flags + tflag, p.epoch * (uint32_t)p.g.P + (uint32_t)tl.s - 1,
                         (uint32_t)tflag);
+        }
+        if (go && has_src) {
+          fence_proxy_async_global();
+          for (int c = 0; c < nch && c < 2; ++c)
+            staged_load_src(p, tl, row0, c, nload + c, xsrc_addr, bar_xfull);
         }
         s_go[it & 1] = go ? 1u : 0u;
       }
@@ -655,17 +797,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
         break;
       }
       tc_fence_after();
-      const int rows_here = tl.rows_valid - (int)crank * ROWS_PER_CTA;
       const bool row_ok = row < rows_here;
-      const int64_t grow = tl.out_row + (int64_t)crank * ROWS_PER_CTA + row;
+      const int64_t grow = row0 + row;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + buf * TILE_N;
 #pragma unroll 1
-      for (int c = 0; c < TILE_N / 32; ++c) {
-        if (c * 32 >= tl.cols_valid) break;  // uniform across the CTA
+      for (int c = 0; c < nch; ++c) {
         float acc[32];
         if (tl.k_blocks > 0) {
           uint32_t v[32];
-          tmem_ld_32x32b_x32(tbase + c * 32, v);
+          tmem_ld_32x32b_x32(tbase + c * XCOLS, v);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(v[i]);
@@ -673,25 +813,70 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
 #pragma unroll
           for (int i = 0; i < 32; ++i) acc[i] = 0.f;
         }
-        if (row_ok) {
-          const int ncols = tl.cols_valid - c * 32 < 32 ? tl.cols_valid - c * 32 : 32;
-          epilogue_row_chunk(p, tl, grow, tl.out_col + c * 32, ncols, acc);
+        if (c == nch - 1) {
+          // the accumulator has been read: hand the TMEM buffer back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (CG == 2)
+              mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * buf, 0));  // the even CTA's barrier
+            else
+              mbar_arrive(bar_tempty + 8 * buf);
+          }
         }
+        const int ncols = tl.cols_valid - c * XCOLS < XCOLS ? tl.cols_valid - c * XCOLS : XCOLS;
+        if (!staged) {
+          if (row_ok) epilogue_row_chunk(p, tl, grow, tl.out_col + c * XCOLS, ncols, acc);
+          continue;
+        }
+        float src[32];
+        if (has_src) {
+          const uint32_t idx = nload + c, sb = idx & 1;
+          mbar_wait(p, bar_xfull + 8 * sb, (idx >> 1) & 1, 0x500000u | sb);
+          staged_read_row(xsrc + sb * XBUF, row, tl.src == SRC_X, p.beta, src);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) src[i] = 0.f;
+        }
+        float out[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) out[i] = fmaf(p.alpha, acc[i], src[i]);
+        // A whole chunk inside the tile (and inside its shard) goes out by TMA.
+        const bool tma_ok = rows_here >= ROWS_PER_CTA && ncols == XCOLS;
+        // barrier A: every thread is done with the source buffer, and the
+        // store that used this destination buffer two chunks ago has read it
+        if (et == 0 && tma_ok) bulk_wait_read<1>();
+        named_bar_sync(1, EPI_THREADS);
+        if (tma_ok) {
+          const uint32_t db = nstore & 1;
+          staged_write_row(xdst + db * XBUF, row, tl.dst == DST_X, out);
+          fence_proxy_async_smem();
+          named_bar_sync(1, EPI_THREADS);  // barrier B: the chunk is complete in shared memory
+          if (et == 0) {
+            tma_store_2d(tl.dst == DST_X ? &p.tmX : &p.tmD, xdst_addr + db * XBUF,
+                         (int32_t)(tl.out_col + c * XCOLS), (int32_t)row0);
+            bulk_commit();
+          }
+          ++nstore;
+        } else if (row_ok) {
+          store_row_chunk(p, tl, grow, tl.out_col + c * XCOLS, ncols, out);
+        }
+        if (et == 0 && has_src && c + 2 < nch)
+          staged_load_src(p, tl, row0, c + 2, nload + c + 2, xsrc_addr, bar_xfull);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (CG == 2)
-          mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * buf, 0));  // the even CTA's barrier
-        else
-          mbar_arrive(bar_tempty + 8 * buf);
-      }
+      if (has_src) nload += (uint32_t)nch;
       if (tflag >= 0 && tl.dst == DST_X) {
+        // hand the partial on: bulk stores complete, plain stores fenced
+        if (EPI == 1 && et == 0) bulk_wait<0>();
         __threadfence();
         named_bar_sync(1, EPI_THREADS);
-        if (et == 0) st_release_u32(p.flags + tflag, p.epoch * (uint32_t)p.g.P + (uint32_t)tl.s);
+        if (et == 0) {
+          if (EPI == 1) fence_proxy_async_global();
+          st_release_u32(p.flags + tflag, p.epoch * (uint32_t)p.g.P + (uint32_t)tl.s);
+        }
       }
     }
+    if (EPI == 1 && et == 0) bulk_wait<0>();  // no bulk store may outlive the CTA
   }
 
   if (CG == 2 && aborted) {

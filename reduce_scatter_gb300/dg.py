@@ -47,6 +47,7 @@ OPT_FAULT_DELAY_MS = 3
 OPT_GRID = 4
 OPT_COPY_STREAMS = 5
 OPT_CTA_GROUP = 6
+OPT_EPILOGUE = 7
 
 # Every symbol include/dg.h declares.
 EXPORTS = ("dg_plan", "dg_workspace_bytes", "dg_run_mode", "dg_set_option", "dg_run", "dg_check",

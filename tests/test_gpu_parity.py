@@ -177,3 +177,24 @@ def test_single_sm_tiles_vs_oracle(sched, tp):
     if sched in (dg.AG_ROTATING_A, dg.AG_ROTATING_B) and tp > 1:
         ref, _ = Runner(m, n, k, l, 1, sched, 0.5, 1.0, options={dg.OPT_CTA_GROUP: 1}).run(A, B, C)
         assert torch.equal(D.view(torch.int16), ref.view(torch.int16))
+
+
+@pytest.mark.parametrize("epi", [0, 1])
+@pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
+@pytest.mark.parametrize("shape", [(1024, 2048, 512, 2), (392, 776, 320, 2)], ids=lambda s: "x".join(map(str, s)))
+def test_both_epilogues_vs_oracle(sched, epi, shape):
+    # staged (TMA through shared memory) and direct epilogues, every schedule;
+    # the ragged shape mixes staged tiles with tiles whose column offset is not
+    # 16-byte aligned (those fall back to direct accesses)
+    m, n, k, l = shape
+    for tp in (2, 4):
+        if not _shape_ok(sched, m, n, k, tp):
+            continue
+        a, b, c = host_inputs(m, n, k, l, seed=70 + tp + 10 * sched + epi)
+        A, B, C = to_dev(a), to_dev(b), to_dev(c)
+        for alpha, beta in [(1.0, 0.0), (0.5, 1.0)]:
+            r = Runner(m, n, k, l, tp, sched, alpha, beta, options={dg.OPT_EPILOGUE: epi})
+            D, _ = r.run(A, B, C if beta else None)
+            assert rel_err(D, oracle_full(a, b, c, alpha, beta)) <= TOL, (tp, alpha, beta)
+            D2, _ = r.run(A, B, C if beta else None)
+            assert torch.equal(D.view(torch.int16), D2.view(torch.int16))
