@@ -278,6 +278,25 @@ def run_dg(args, rank, world, dist):
         plan.set_mode(mode)
         plan.check(ws, main)
 
+    # the same kernel on the unsharded problem (tp=1), and for the RS
+    # schedules the non-fused baseline (per-rank partial GEMMs, then a
+    # separate reduction kernel)
+    ms_tp1 = ms_nonfused = None
+    if not args.no_modes and mode == dg.MODE_FUSED and w.tp > 1:
+        p1 = dg.Plan(w.m, w.n, w.k, w.l, 1, w.schedule, w.alpha, w.beta)
+        ws1 = torch.zeros(max(p1.workspace_bytes(), 256), dtype=torch.uint8, device=dev)
+        ms_tp1 = timed_loop(lambda: p1.run(A, B, C, D, ws1, main, copy), max(3, args.steps // 2), 2, main, flush)
+        p1.check(ws1, main)
+        del ws1, p1
+        if w.schedule in (dg.RS_TILING_A_ROTATING_C, dg.RS_TILING_B_ROTATING_C):
+            ps = dg.Plan(w.m, w.n, w.k, w.l, w.tp, w.schedule, w.alpha, w.beta)
+            ps.set_mode(dg.MODE_SERIAL)
+            wss = torch.zeros(max(ps.workspace_bytes(), 256), dtype=torch.uint8, device=dev)
+            ms_nonfused = timed_loop(lambda: ps.run(A, B, C, D, wss, main, main), max(3, args.steps // 2), 2,
+                                     main, flush)
+            ps.check(wss, main)
+            del wss, ps
+
     e2e = None
     if not args.no_e2e:
         A_h = A.cpu().pin_memory()
@@ -300,11 +319,13 @@ def run_dg(args, rank, world, dist):
                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": D.numel() * 2}
 
     # max over ranks
-    vals = torch.tensor([ms_fused, ms_gemm or 0.0, ms_serial or 0.0, (e2e or {}).get("ms_per_step", 0.0)],
-                        dtype=torch.float64, device=dev)
+    vals = torch.tensor([ms_fused, ms_gemm or 0.0, ms_serial or 0.0, (e2e or {}).get("ms_per_step", 0.0),
+                         ms_tp1 or 0.0, ms_nonfused or 0.0], dtype=torch.float64, device=dev)
     if dist is not None:
         dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    ms_fused, ms_gemm_m, ms_serial_m, ms_e2e = vals.tolist()
+    ms_fused, ms_gemm_m, ms_serial_m, ms_e2e, ms_tp1_m, ms_nonfused_m = vals.tolist()
+    ms_tp1 = ms_tp1_m if ms_tp1 is not None else None
+    ms_nonfused = ms_nonfused_m if ms_nonfused is not None else None
     if rank != 0:
         return None
     ms_gemm = ms_gemm_m if ms_gemm is not None else None
@@ -343,12 +364,15 @@ def run_dg(args, rank, world, dist):
         "ms_serial": None if ms_serial is None else round(ms_serial, 4),
         "copy_hidden_fraction": None if hidden is None else round(hidden, 4),
         "fused_over_gemm_only": None if ms_gemm is None else round(ms_fused / ms_gemm, 4),
+        "ms_unsharded_tp1": None if ms_tp1 is None else round(ms_tp1, 4),
+        "ms_rs_nonfused_baseline": None if ms_nonfused is None else round(ms_nonfused, 4),
+        "fused_speedup_vs_nonfused": None if ms_nonfused is None else round(ms_nonfused / ms_fused, 4),
         "roofline": {"bound": "tensor", "achieved": round(per_gpu, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(per_gpu / peak, 4), "peak_source": f"{peak_kind} bf16 burst",
                      "frac_of_sustained": round(per_gpu / float(peaks.get("bf16_tflops_sustained", peak)), 4),
                      "traffic": recorded_traffic(w.name), "kernel": "dg::dg_gemm_kernel"},
         "clocks": clocks,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps,  # one dg_gemm_kernel launch per fused step
         "e2e": e2e,
     }
     return line

@@ -136,6 +136,8 @@ struct dg_plan_s {
   cudaStream_t extra[7] = {};
   cudaEvent_t extra_done[7] = {};
   dg::KParams kp;
+  dg::Geom gser{};   // RS SERIAL baseline: per-rank partial GEMMs (SCHED_PARTIAL)
+  dg::KParams kser;  // its kernel parameters
   const void* map_key[3] = {nullptr, nullptr, nullptr};
   int n_maps = 0;
 };
@@ -198,6 +200,15 @@ int layout(dg_plan_s* p) {
     // one flag per tile and CTA of the group (each CTA hands on its own half)
     p->n_flags = g.L * P * g.tiles_m * g.tiles_n * p->cg;
   }
+  // RS SERIAL baseline geometry: every rank's full M x N partial over its K-slab
+  p->gser = g;
+  p->gser.sched = dg::SCHED_PARTIAL;
+  p->gser.blk_m = p->m;
+  p->gser.blk_n = p->n;
+  p->gser.tiles_m = dg::cdiv(p->m, g.BM);
+  p->gser.tiles_n = dg::cdiv(p->n, g.BN);
+  p->gser.tiles_block = g.L * p->gser.tiles_m * p->gser.tiles_n;
+  p->gser.total_tiles = P * p->gser.tiles_block;
   p->off_status = 0;
   p->off_flags = 256;
   size_t off = round_up(p->off_flags + (size_t)p->n_flags * 4, 1024);
@@ -423,23 +434,23 @@ int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B
   return DG_OK;
 }
 
-int launch(dg_plan_s* p, cudaStream_t st, uint32_t wait_flags) {
-  p->kp.wait_flags = wait_flags;
+int launch_kp(dg_plan_s* p, const dg::KParams& kp, cudaStream_t st) {
+  const int64_t tiles = kp.g.total_tiles;
   if (p->cg == 1) {
     int64_t grid = p->grid_req > 0 ? p->grid_req : p->num_sms;
-    grid = std::min<int64_t>(grid, p->g.total_tiles);
+    grid = std::min<int64_t>(grid, tiles);
     if (grid <= 0) return DG_OK;
     if (p->epi == 1)
-      dg::dg_gemm_kernel<1, 1><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 1>::SMEM_BYTES, st>>>(p->kp);
+      dg::dg_gemm_kernel<1, 1><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 1>::SMEM_BYTES, st>>>(kp);
     else
-      dg::dg_gemm_kernel<1, 0><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 0>::SMEM_BYTES, st>>>(p->kp);
+      dg::dg_gemm_kernel<1, 0><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 0>::SMEM_BYTES, st>>>(kp);
     DG_CUDA(cudaGetLastError());
     return DG_OK;
   }
   // CTA pairs: every pair must be co-resident (RS tiles wait on earlier tiles)
   int64_t pairs = p->grid_req > 0 ? p->grid_req / 2 : p->max_pairs;
-  pairs = std::min<int64_t>(std::min<int64_t>(pairs, p->max_pairs), p->g.total_tiles);
-  if (pairs <= 0) return p->g.total_tiles > 0 ? fail(DG_ERR_UNSUPPORTED, "no co-resident CTA pair") : DG_OK;
+  pairs = std::min<int64_t>(std::min<int64_t>(pairs, p->max_pairs), tiles);
+  if (pairs <= 0) return tiles > 0 ? fail(DG_ERR_UNSUPPORTED, "no co-resident CTA pair") : DG_OK;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -453,9 +464,39 @@ int launch(dg_plan_s* p, cudaStream_t st, uint32_t wait_flags) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (p->epi == 1)
-    DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 1>, p->kp));
+    DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 1>, kp));
   else
-    DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 0>, p->kp));
+    DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 0>, kp));
+  return DG_OK;
+}
+
+int launch(dg_plan_s* p, cudaStream_t st, uint32_t wait_flags) {
+  p->kp.wait_flags = wait_flags;
+  return launch_kp(p, p->kp, st);
+}
+
+// Non-fused ReduceScatter baseline ("GEMM, then reduce"): one launch computes
+// every rank's full partial over its K-slab into its own fp32 buffer; a
+// separate kernel sums the partials, adds beta*C and writes bf16 D.
+int run_rs_serial(dg_plan_s* p, const Driver& drv, const void* C, void* D, uint8_t* ws, cudaStream_t st) {
+  p->kser = p->kp;
+  p->kser.g = p->gser;
+  p->kser.X = reinterpret_cast<float*>(ws + p->off_serial);
+  p->kser.wait_flags = 0;
+  std::memset(&p->kser.tmX, 0, sizeof(CUtensorMap));
+  if (p->epi == 1) {
+    int rc = encode_epi_map(drv, &p->kser.tmX, ws + p->off_serial, true, p->n, p->tp * p->l * p->m);
+    if (rc) return rc;
+  }
+  int rc = launch_kp(p, p->kser, st);
+  if (rc) return rc;
+  const int64_t n4 = p->l * p->m * p->n / 4;
+  int64_t blocks = std::min<int64_t>((int64_t)p->num_sms * 8, (n4 + 255) / 256);
+  if (blocks < 1) blocks = 1;
+  dg::dg_reduce_partials_kernel<<<(unsigned)blocks, 256, 0, st>>>(
+      reinterpret_cast<const float*>(ws + p->off_serial), p->tp, n4,
+      reinterpret_cast<const __nv_bfloat16*>(C), p->beta, reinterpret_cast<__nv_bfloat16*>(D));
+  DG_CUDA(cudaGetLastError());
   return DG_OK;
 }
 
@@ -602,11 +643,14 @@ int dg_run(dg_plan_t p, const dg_bf16_t* A, const dg_bf16_t* B, const dg_bf16_t*
   auto misaligned = [](const void* q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) & (a - 1)) != 0; };
   if (misaligned(A, 16) || misaligned(B, 16) || misaligned(D, 16) || (C && misaligned(C, 16)))
     return fail(DG_ERR_ARG, "A, B, C and D must be 16-byte aligned");
-  const size_t need = dg_workspace_bytes(p);
+  // bytes this run uses (no side effect on the plan's SERIAL sizing record)
+  const size_t need =
+      (!is_ag(p->schedule) && p->mode == DG_MODE_SERIAL) ? p->ws_bytes_serial : p->ws_bytes_base;
   if (need > 0 && (!workspace || misaligned(workspace, 256)))
     return fail(DG_ERR_ARG, "workspace must be non-NULL and 256-byte aligned");
   const bool rs_serial = !is_ag(p->schedule) && p->mode == DG_MODE_SERIAL;
-  if (rs_serial) return fail(DG_ERR_UNSUPPORTED, "RS SERIAL baseline not available");
+  if (rs_serial && !p->serial_ws)
+    return fail(DG_ERR_STATE, "RS SERIAL needs the larger workspace: size it with dg_workspace_bytes in SERIAL mode");
   int rc = rt_init(p);
   if (rc) return rc;
   Driver drv;
@@ -656,6 +700,7 @@ int dg_run(dg_plan_t p, const dg_bf16_t* A, const dg_bf16_t* B, const dg_bf16_t*
   kp.timeout_ns = (uint64_t)p->timeout_ms * 1000000ull;
   kp.hang_ns = kp.timeout_ns * 4 + 1000000000ull;
 
+  if (rs_serial) return run_rs_serial(p, drv, C, D, ws, ms);
   if (is_ag(p->schedule) && p->tp > 1) {
     int mode = p->mode;
     if (mode == DG_MODE_FUSED && (cs == ms || cs == nullptr)) mode = DG_MODE_SERIAL;

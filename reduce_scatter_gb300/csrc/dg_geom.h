@@ -29,6 +29,10 @@
 namespace dg {
 
 enum : int { SCHED_AG_A = 0, SCHED_AG_B = 1, SCHED_RS_A = 2, SCHED_RS_B = 3 };
+// Non-fused ReduceScatter baseline: every rank's full partial product over its
+// own K-slab, written to its own fp32 buffer (stacked rank-major); a separate
+// reduction then sums them.  Tile order: rank-major, one step.
+enum : int { SCHED_PARTIAL = 4 };
 enum : int { SRC_NONE = 0, SRC_C = 1, SRC_X = 2 };
 enum : int { DST_D = 0, DST_X = 1 };
 enum : int { MAP_HOME = 0, MAP_SLOT = 1 };
@@ -84,6 +88,7 @@ DG_HD Tile decode_tile(const Geom& g, int64_t t) {
   const int64_t nt = in / gm;
 
   const bool ag = g.sched == SCHED_AG_A || g.sched == SCHED_AG_B;
+  // (SCHED_PARTIAL has one step: total_tiles = P * tiles_block, so s = 0.)
   const int64_t j = ag ? (r + s) % P : (r + s + 1) % P;
   o.s = (int32_t)s;
   o.r = (int32_t)r;
@@ -131,6 +136,15 @@ DG_HD Tile decode_tile(const Geom& g, int64_t t) {
     }
     o.src = g.beta_nonzero ? SRC_C : SRC_NONE;
     o.dst = DST_D;
+  } else if (g.sched == SCHED_PARTIAL) {
+    o.out_row = (r * g.L + l) * g.M + mrow;  // row of the stacked partial buffers
+    o.out_col = ncol;
+    o.a_map = (int32_t)r;
+    o.b_map = (int32_t)r;
+    o.a_row = l * g.M + mrow;
+    o.b_row = l * g.N + ncol;
+    o.src = SRC_NONE;
+    o.dst = DST_X;
   } else {
     // RS: rank r contributes its K-slab to output slab j
     const bool rs_a = g.sched == SCHED_RS_A;

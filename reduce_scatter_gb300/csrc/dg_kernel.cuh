@@ -901,4 +901,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
   }
 }
 
+// Reduction of the non-fused ReduceScatter baseline:
+//   D[e] = bf16( (X_0[e] + X_1[e] + ... + X_{P-1}[e]) + beta * C[e] )
+// over the P stacked fp32 partials (each already scaled by alpha), four
+// elements per thread and iteration, grid-stride.  HBM-bound.
+__global__ void __launch_bounds__(256) dg_reduce_partials_kernel(const float* __restrict__ X, int P,
+                                                                 int64_t n4, const __nv_bfloat16* C,
+                                                                 float beta, __nv_bfloat16* D) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t plane = n4;  // float4 units per partial
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    float4 acc = __ldcs(reinterpret_cast<const float4*>(X) + i);
+    for (int r = 1; r < P; ++r) {
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(X) + r * plane + i);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    if (beta != 0.f) {
+      const uint2 cw = __ldg(reinterpret_cast<const uint2*>(C) + i);
+      acc.x += beta * bf16_bits_to_f32(cw.x & 0xFFFFu);
+      acc.y += beta * bf16_bits_to_f32(cw.x >> 16);
+      acc.z += beta * bf16_bits_to_f32(cw.y & 0xFFFFu);
+      acc.w += beta * bf16_bits_to_f32(cw.y >> 16);
+    }
+    uint2 o;
+    o.x = pack_bf16x2(acc.x, acc.y);
+    o.y = pack_bf16x2(acc.z, acc.w);
+    reinterpret_cast<uint2*>(D)[i] = o;
+  }
+}
+
 }  // namespace dg

@@ -198,3 +198,33 @@ def test_both_epilogues_vs_oracle(sched, epi, shape):
             assert rel_err(D, oracle_full(a, b, c, alpha, beta)) <= TOL, (tp, alpha, beta)
             D2, _ = r.run(A, B, C if beta else None)
             assert torch.equal(D.view(torch.int16), D2.view(torch.int16))
+
+
+@pytest.mark.parametrize("sched", [dg.RS_TILING_A_ROTATING_C, dg.RS_TILING_B_ROTATING_C],
+                         ids=lambda s: dg.SCHEDULE_NAMES[s])
+@pytest.mark.parametrize("epi", [0, 1])
+def test_rs_nonfused_baseline_vs_oracle(sched, epi):
+    # SERIAL on an RS plan: per-rank partial GEMMs, then the separate reduction
+    m, n, k, l, tp = 1024, 1024, 1024, 2, 4
+    a, b, c = host_inputs(m, n, k, l, seed=80 + sched)
+    A, B, C = to_dev(a), to_dev(b), to_dev(c)
+    for alpha, beta in [(1.0, 0.0), (0.5, 1.0)]:
+        plan = dg.Plan(m, n, k, l, tp, sched, alpha, beta)
+        plan.set_option(dg.OPT_EPILOGUE, epi)
+        plan.set_mode(dg.MODE_SERIAL)
+        ws = torch.zeros(plan.workspace_bytes(), dtype=torch.uint8, device="cuda")
+        D = torch.full((l, m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+        main = torch.cuda.current_stream()
+        plan.run(A, B, C if beta else None, D, ws, main, main)
+        plan.check(ws, main)
+        assert rel_err(D, oracle_full(a, b, c, alpha, beta)) <= TOL
+
+
+def test_rs_serial_needs_the_serial_workspace():
+    plan = dg.Plan(256, 256, 256, 1, 2, dg.RS_TILING_A_ROTATING_C)
+    small = plan.workspace_bytes()          # FUSED sizing
+    plan.set_mode(dg.MODE_SERIAL)
+    ws = torch.zeros(small, dtype=torch.uint8, device="cuda")
+    A = torch.zeros((256, 256), dtype=torch.bfloat16, device="cuda")
+    rc = plan.run(A, A, None, torch.empty_like(A), ws, raise_on_error=False)
+    assert rc == dg.ERR_STATE
