@@ -196,11 +196,15 @@ def make_inputs(w, device):
 
     from reduce_scatter_gb300 import synth
 
-    A = synth.tensor_bits_torch(w.seed, synth.STREAM_A, (w.l, w.m, w.k), w.dist_a, device=device).view(torch.bfloat16)
-    B = synth.tensor_bits_torch(w.seed, synth.STREAM_B, (w.l, w.n, w.k), w.dist_b, device=device).view(torch.bfloat16)
+    chunk = 1 << 28  # fewer, larger generator launches
+    A = synth.tensor_bits_torch(w.seed, synth.STREAM_A, (w.l, w.m, w.k), w.dist_a, device=device,
+                                chunk=chunk).view(torch.bfloat16)
+    B = synth.tensor_bits_torch(w.seed, synth.STREAM_B, (w.l, w.n, w.k), w.dist_b, device=device,
+                                chunk=chunk).view(torch.bfloat16)
     C = None
     if w.beta != 0:
-        C = synth.tensor_bits_torch(w.seed, synth.STREAM_C, (w.l, w.m, w.n), w.dist_c, device=device).view(torch.bfloat16)
+        C = synth.tensor_bits_torch(w.seed, synth.STREAM_C, (w.l, w.m, w.n), w.dist_c, device=device,
+                                    chunk=chunk).view(torch.bfloat16)
     return A, B, C
 
 
