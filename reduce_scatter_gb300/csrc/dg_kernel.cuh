@@ -560,6 +560,15 @@ __device__ __forceinline__ void staged_write_row(uint8_t* buf, int row, bool f32
   }
 }
 
+// Hand a rotating-partial half tile to the next step: the bulk stores that
+// wrote it (all issued by this thread) complete, then the flag is released.
+__device__ __forceinline__ void release_partial(const KParams& p, int64_t flag, uint32_t val) {
+  bulk_wait<0>();
+  fence_proxy_async_global();
+  __threadfence();
+  st_release_u32(p.flags + flag, val);
+}
+
 // TMA load of source chunk c of a tile half into staging buffer (idx & 1).
 __device__ __forceinline__ void staged_load_src(const KParams& p, const Tile& tl, int64_t row0, int c,
                                                 uint32_t idx, uint32_t sbase, uint32_t bar_xfull) {
@@ -764,6 +773,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
     const int row = q * 32 + lane;    // accumulator row = TMEM lane
     const uint32_t xsrc_addr = smem_u32(xsrc);
     const uint32_t xdst_addr = smem_u32(xdst);
+    int64_t pend_flag = -1;  // half-tile flag whose release waits for this CTA's bulk stores
+    uint32_t pend_val = 0;
     uint32_t nload = 0;   // staged source chunks loaded so far (buffer idx & 1)
     uint32_t nstore = 0;  // staged destination chunks stored so far (buffer idx & 1)
     uint32_t it = 0;
@@ -778,16 +789,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
       const bool staged = EPI == 1 && (tl.out_col & 7) == 0;
       const bool has_src = staged && tl.src != SRC_NONE;
       if (et == 0) {
-        bool go = mbar_wait(p, bar_tfull + 8 * buf, use & 1, 0x400000u | buf);
-        if (go && tflag >= 0 && tl.s > 0) {
+        // A hand-off this CTA still holds may be the very flag this tile
+        // waits for (same output tile, next step): release it first.
+        if (pend_flag >= 0 && pend_flag == tflag) {
+          release_partial(p, pend_flag, pend_val);
+          pend_flag = -1;
+        }
+        if (tflag >= 0 && tl.s > 0) {
           // partial of this half tile from the previous step
           wait_flag_geq(p, p.flags + tflag, p.epoch * (uint32_t)p.g.P + (uint32_t)tl.s - 1,
                         (uint32_t)tflag);
         }
-        if (go && has_src) {
+        if (has_src) {
+          // the source needs only the previous step: load it while the MMAs run
           fence_proxy_async_global();
           for (int c = 0; c < nch && c < 2; ++c)
             staged_load_src(p, tl, row0, c, nload + c, xsrc_addr, bar_xfull);
+        }
+        bool go = mbar_wait(p, bar_tfull + 8 * buf, use & 1, 0x400000u | buf);
+        if (pend_flag >= 0) {  // the previous tile's bulk stores have long completed
+          release_partial(p, pend_flag, pend_val);
+          pend_flag = -1;
         }
         s_go[it & 1] = go ? 1u : 0u;
       }
@@ -866,16 +888,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
       }
       if (has_src) nload += (uint32_t)nch;
       if (tflag >= 0 && tl.dst == DST_X) {
-        // hand the partial on: bulk stores complete, plain stores fenced
-        if (EPI == 1 && et == 0) bulk_wait<0>();
-        __threadfence();
-        named_bar_sync(1, EPI_THREADS);
-        if (et == 0) {
-          if (EPI == 1) fence_proxy_async_global();
-          st_release_u32(p.flags + tflag, p.epoch * (uint32_t)p.g.P + (uint32_t)tl.s);
+        const uint32_t val = p.epoch * (uint32_t)p.g.P + (uint32_t)tl.s;
+        // every chunk left by TMA store (issued by thread 0 alone)?
+        const bool all_bulk = staged && rows_here >= ROWS_PER_CTA && (tl.cols_valid % XCOLS) == 0;
+        if (all_bulk) {
+          // hand the partial on later, once the bulk stores are surely done
+          pend_flag = tflag;
+          pend_val = val;
+        } else {
+          // plain stores from every thread: fence, gather, release now
+          if (EPI == 1 && et == 0) bulk_wait<0>();
+          __threadfence();
+          named_bar_sync(1, EPI_THREADS);
+          if (et == 0) {
+            if (EPI == 1) fence_proxy_async_global();
+            st_release_u32(p.flags + tflag, val);
+          }
         }
       }
     }
+    if (et == 0 && pend_flag >= 0) release_partial(p, pend_flag, pend_val);
     if (EPI == 1 && et == 0) bulk_wait<0>();  // no bulk store may outlive the CTA
   }
 
