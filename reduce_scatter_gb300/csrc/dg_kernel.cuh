@@ -789,16 +789,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
       const bool staged = EPI == 1 && (tl.out_col & 7) == 0;
       const bool has_src = staged && tl.src != SRC_NONE;
       if (et == 0) {
-        // A hand-off this CTA still holds may be the very flag this tile
-        // waits for (same output tile, next step): release it first.
-        if (pend_flag >= 0 && pend_flag == tflag) {
+        const bool need_flag = tflag >= 0 && tl.s > 0;
+        const uint32_t want = p.epoch * (uint32_t)p.g.P + (uint32_t)tl.s - 1;
+        // Never hold a deferred hand-off while waiting for one: a ring of CTAs
+        // could each wait on the next one's.  If this tile has to wait (its
+        // previous step is not yet handed on, possibly by this very CTA),
+        // release first.
+        if (pend_flag >= 0 && need_flag && ld_acquire_u32(p.flags + tflag) < want) {
           release_partial(p, pend_flag, pend_val);
           pend_flag = -1;
         }
-        if (tflag >= 0 && tl.s > 0) {
+        if (need_flag) {
           // partial of this half tile from the previous step
-          wait_flag_geq(p, p.flags + tflag, p.epoch * (uint32_t)p.g.P + (uint32_t)tl.s - 1,
-                        (uint32_t)tflag);
+          wait_flag_geq(p, p.flags + tflag, want, (uint32_t)tflag);
         }
         if (has_src) {
           // the source needs only the previous step: load it while the MMAs run
