@@ -188,6 +188,27 @@ def cpu_oracle_sample(w, rows: int, cols: int):
                       f"{flops:.3e} flop"}
 
 
+# ------------------------------------------------------------ multi-rank
+
+
+def max_over_ranks(values, dist=None, device=None):
+    """Element-wise maximum of per-rank timings (ms) over all ranks.
+
+    Every rank runs its own replica; the job is as slow as its slowest rank.
+    """
+    import torch
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_tflops(flops_per_replica: float, world: int, ms_slowest: float) -> float:
+    """TFLOP/s of the whole job: every replica's work over the slowest rank's time."""
+    return world * flops_per_replica / (ms_slowest * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ dg arm
 
 
@@ -323,11 +344,9 @@ def run_dg(args, rank, world, dist):
                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": D.numel() * 2}
 
     # max over ranks
-    vals = torch.tensor([ms_fused, ms_gemm or 0.0, ms_serial or 0.0, (e2e or {}).get("ms_per_step", 0.0),
-                         ms_tp1 or 0.0, ms_nonfused or 0.0], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    ms_fused, ms_gemm_m, ms_serial_m, ms_e2e, ms_tp1_m, ms_nonfused_m = vals.tolist()
+    ms_fused, ms_gemm_m, ms_serial_m, ms_e2e, ms_tp1_m, ms_nonfused_m = max_over_ranks(
+        [ms_fused, ms_gemm or 0.0, ms_serial or 0.0, (e2e or {}).get("ms_per_step", 0.0), ms_tp1 or 0.0,
+         ms_nonfused or 0.0], dist, dev)
     ms_tp1 = ms_tp1_m if ms_tp1 is not None else None
     ms_nonfused = ms_nonfused_m if ms_nonfused is not None else None
     if rank != 0:
@@ -338,7 +357,7 @@ def run_dg(args, rank, world, dist):
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK_TFLOPS))
     per_gpu = w.flops / (ms_fused * 1e-3) / 1e12
-    value = world * per_gpu
+    value = whole_job_tflops(w.flops, world, ms_fused)
     hidden = None
     if ms_gemm is not None and ms_serial is not None:
         t_copy = ms_serial - ms_gemm
