@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--mode", choices=["fused", "gemm_only", "serial"], default="fused",
                     help="mode of the timed loop (gemm_only/serial for profilers that serialize streams)")
     ap.add_argument("--copy-streams", type=int, default=0, help="0 = the library default")
+    ap.add_argument("--option", action="append", default=[], metavar="NAME=VALUE",
+                    help="extra plan option, e.g. L2_HINT=9 (names of dg.OPT_*)")
     ap.add_argument("--cpu-sample-rows", type=int, default=1024)
     ap.add_argument("--cpu-sample-cols", type=int, default=4096)
     return ap.parse_args(argv)
@@ -261,6 +263,9 @@ def run_dg(args, rank, world, dist):
     plan = dg.Plan(w.m, w.n, w.k, w.l, w.tp, w.schedule, w.alpha, w.beta)
     if args.copy_streams > 0:
         plan.set_option(dg.OPT_COPY_STREAMS, args.copy_streams)
+    for opt in args.option:
+        name, val = opt.split("=")
+        plan.set_option(getattr(dg, "OPT_" + name.upper()), int(val))
     ws = torch.zeros(max(plan.workspace_bytes(), 256), dtype=torch.uint8, device=dev)
     main = torch.cuda.current_stream(dev)
     copy = torch.cuda.Stream(dev)
@@ -379,6 +384,7 @@ def run_dg(args, rank, world, dist):
         "dtype": "bf16",
         "data": "synthetic (seeded SplitMix64 inputs with the workload's distributions)",
         "mode": args.mode,
+        "options": args.option,
         "config": dict(w.describe(), parallelism=f"tp{w.tp} virtual ranks on 1 GPU" + (
             f", {world} replicas" if world > 1 else ""),
             l2="flushed between steps" if flush is not None else "inputs larger than L2 (no flush)"),

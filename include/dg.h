@@ -109,10 +109,12 @@ enum dg_option {
   DG_OPT_CTA_GROUP = 6,       /* tile configuration, before the first run: 2 (default) =
                                  256 x 256 tiles on an SM pair (tcgen05 cta_group::2),
                                  1 = 128 x 256 tiles on one SM */
-  DG_OPT_EPILOGUE = 7         /* epilogue, before the first run: 1 = source and result
+  DG_OPT_EPILOGUE = 7,        /* epilogue, before the first run: 1 = source and result
                                  chunks staged in shared memory and moved by TMA (default
                                  for the RS schedules), 0 = direct per-row global accesses
                                  (default for the AG schedules, one more operand stage) */
+  DG_OPT_L2_HINT = 8          /* L2 eviction policy of the operand loads: bits 0-1 for A,
+                                 bits 2-3 for B; 0 = none, 1 = evict first, 2 = evict last */
 };
 
 /* Plan geometry and workspace layout, for callers and tests. */

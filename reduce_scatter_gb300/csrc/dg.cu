@@ -115,6 +115,7 @@ struct dg_plan_s {
   int64_t grid_req = 0;
   int cg = 2;  // CTA group of the tile config: 1 = 128 x 256 per SM, 2 = 256 x 256 per SM pair
   int epi = 0;  // epilogue: 0 direct, 1 staged through shared memory with TMA (default for RS)
+  uint32_t l2_hint = 0;  // L2 policy of operand loads (DG_OPT_L2_HINT)
   uint64_t id = 0;
   uint32_t epoch = 0;
   bool serial_ws = false;
@@ -583,6 +584,11 @@ int dg_set_option(dg_plan_t p, int option, int64_t value) {
       if (value < 1 || value > 8) return fail(DG_ERR_ARG, "copy streams must be 1..8");
       p->copy_streams = (int)value;
       return DG_OK;
+    case DG_OPT_L2_HINT:
+      if (value < 0 || value > 15 || (value & 3) == 3 || ((value >> 2) & 3) == 3)
+        return fail(DG_ERR_ARG, "L2 hint: two 2-bit fields (A, B), each 0, 1 or 2");
+      p->l2_hint = (uint32_t)value;
+      return DG_OK;
     case DG_OPT_EPILOGUE:
       if (value != 0 && value != 1) return fail(DG_ERR_ARG, "epilogue must be 0 (direct) or 1 (staged)");
       if (p->epoch != 0) return fail(DG_ERR_STATE, "the epilogue is fixed after the first run");
@@ -697,6 +703,7 @@ int dg_run(dg_plan_t p, const dg_bf16_t* A, const dg_bf16_t* B, const dg_bf16_t*
   kp.alpha = p->alpha;
   kp.beta = p->beta;
   kp.n_maps = p->n_maps;
+  kp.l2_hint = p->l2_hint;
   kp.timeout_ns = (uint64_t)p->timeout_ms * 1000000ull;
   kp.hang_ns = kp.timeout_ns * 4 + 1000000000ull;
 

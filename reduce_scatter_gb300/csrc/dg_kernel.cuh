@@ -97,6 +97,8 @@ struct KParams {
   uint32_t epoch;
   uint32_t wait_flags;  // AG: 1 = wait on chunk flags
   int32_t n_maps;       // tensor maps in use (each of tmA / tmB)
+  uint32_t l2_hint;     // L2 policy of operand loads: bits 0-1 A, bits 2-3 B
+                        // (0 none, 1 evict-first, 2 evict-last)
   float alpha, beta;
   uint64_t timeout_ns;
   uint64_t hang_ns;
@@ -147,6 +149,24 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
+}
+
+// Same loads with an L2 eviction policy (from createpolicy).
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                 int32_t x, int32_t y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t l2_policy(uint32_t kind) {
+  uint64_t pol = 0;
+  if (kind == 1)
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  else
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
@@ -270,6 +290,15 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap* map,
+                                                      uint32_t bar_cluster, int32_t x, int32_t y,
+                                                      uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster), "l"(policy)
       : "memory");
 }
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
@@ -653,6 +682,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
         prefetch_tmap(&p.tmA[i]);
         prefetch_tmap(&p.tmB[i]);
       }
+      const uint32_t hint_a = p.l2_hint & 3u, hint_b = (p.l2_hint >> 2) & 3u;
+      const uint64_t pol_a = hint_a ? l2_policy(hint_a) : 0, pol_b = hint_b ? l2_policy(hint_b) : 0;
       uint32_t stage = 0, phase = 0;
       int32_t issued[STAGES];  // parity of the last load issued per stage, -1 none
       for (int i = 0; i < STAGES; ++i) issued[i] = -1;
@@ -677,12 +708,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           if (CG == 2) {
             const uint32_t fb_lead = mapa_shared(fb, 0);
             if (leader) mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);  // both CTAs' bytes
-            tma_load_2d_pair(sa, ma, fb_lead, kb * BK, a_row);
-            tma_load_2d_pair(sa + C::A_BYTES, mb, fb_lead, kb * BK, b_row);
+            if (hint_a)
+              tma_load_2d_pair_hint(sa, ma, fb_lead, kb * BK, a_row, pol_a);
+            else
+              tma_load_2d_pair(sa, ma, fb_lead, kb * BK, a_row);
+            if (hint_b)
+              tma_load_2d_pair_hint(sa + C::A_BYTES, mb, fb_lead, kb * BK, b_row, pol_b);
+            else
+              tma_load_2d_pair(sa + C::A_BYTES, mb, fb_lead, kb * BK, b_row);
           } else {
             mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-            tma_load_2d(sa, ma, fb, kb * BK, a_row);
-            tma_load_2d(sa + C::A_BYTES, mb, fb, kb * BK, b_row);
+            if (hint_a)
+              tma_load_2d_hint(sa, ma, fb, kb * BK, a_row, pol_a);
+            else
+              tma_load_2d(sa, ma, fb, kb * BK, a_row);
+            if (hint_b)
+              tma_load_2d_hint(sa + C::A_BYTES, mb, fb, kb * BK, b_row, pol_b);
+            else
+              tma_load_2d(sa + C::A_BYTES, mb, fb, kb * BK, b_row);
           }
           issued[stage] = (int32_t)phase;
           if (++stage == STAGES) {

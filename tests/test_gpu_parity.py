@@ -228,3 +228,14 @@ def test_rs_serial_needs_the_serial_workspace():
     A = torch.zeros((256, 256), dtype=torch.bfloat16, device="cuda")
     rc = plan.run(A, A, None, torch.empty_like(A), ws, raise_on_error=False)
     assert rc == dg.ERR_STATE
+
+
+@pytest.mark.parametrize("hint", [2, 6, 9])
+def test_l2_hints_do_not_change_results(hint):
+    m, n, k, l, tp = 1024, 2048, 512, 1, 4
+    a, b, c = host_inputs(m, n, k, l, seed=90)
+    A, B, C = to_dev(a), to_dev(b), to_dev(c)
+    for sched in SCHEDS:
+        ref, _ = Runner(m, n, k, l, tp, sched, 0.5, 1.0).run(A, B, C)
+        D, _ = Runner(m, n, k, l, tp, sched, 0.5, 1.0, options={dg.OPT_L2_HINT: hint}).run(A, B, C)
+        assert torch.equal(D.view(torch.int16), ref.view(torch.int16)), sched
