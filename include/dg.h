@@ -113,8 +113,12 @@ enum dg_option {
                                  chunks staged in shared memory and moved by TMA (default
                                  for the RS schedules), 0 = direct per-row global accesses
                                  (default for the AG schedules, one more operand stage) */
-  DG_OPT_L2_HINT = 8          /* L2 eviction policy of the operand loads: bits 0-1 for A,
+  DG_OPT_L2_HINT = 8,         /* L2 eviction policy of the operand loads: bits 0-1 for A,
                                  bits 2-3 for B; 0 = none, 1 = evict first, 2 = evict last */
+  DG_OPT_WAVE_SYNC = 9        /* 1 = each CTA starts its i-th tile only after every CTA has
+                                 issued the loads of its (i-1)-th (keeps the CTAs that share
+                                 an operand strip in phase for L2 reuse); a zeroed counter
+                                 word per run, memset on the main stream */
 };
 
 /* Plan geometry and workspace layout, for callers and tests. */

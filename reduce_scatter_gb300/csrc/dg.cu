@@ -116,6 +116,7 @@ struct dg_plan_s {
   int cg = 2;  // CTA group of the tile config: 1 = 128 x 256 per SM, 2 = 256 x 256 per SM pair
   int epi = 0;  // epilogue: 0 direct, 1 staged through shared memory with TMA (default for RS)
   uint32_t l2_hint = 0;  // L2 policy of operand loads (DG_OPT_L2_HINT)
+  uint32_t wave_sync = 0;  // DG_OPT_WAVE_SYNC
   uint64_t id = 0;
   uint32_t epoch = 0;
   bool serial_ws = false;
@@ -584,6 +585,10 @@ int dg_set_option(dg_plan_t p, int option, int64_t value) {
       if (value < 1 || value > 8) return fail(DG_ERR_ARG, "copy streams must be 1..8");
       p->copy_streams = (int)value;
       return DG_OK;
+    case DG_OPT_WAVE_SYNC:
+      if (value != 0 && value != 1) return fail(DG_ERR_ARG, "wave sync must be 0 or 1");
+      p->wave_sync = (uint32_t)value;
+      return DG_OK;
     case DG_OPT_L2_HINT:
       if (value < 0 || value > 15 || (value & 3) == 3 || ((value >> 2) & 3) == 3)
         return fail(DG_ERR_ARG, "L2 hint: two 2-bit fields (A, B), each 0, 1 or 2");
@@ -704,6 +709,9 @@ int dg_run(dg_plan_t p, const dg_bf16_t* A, const dg_bf16_t* B, const dg_bf16_t*
   kp.beta = p->beta;
   kp.n_maps = p->n_maps;
   kp.l2_hint = p->l2_hint;
+  kp.wave_sync = p->wave_sync;
+  kp.wave_ctr = reinterpret_cast<uint32_t*>(ws + p->off_status + 64);
+  if (p->wave_sync) DG_CUDA(cudaMemsetAsync(ws + p->off_status + 64, 0, 4, ms));
   kp.timeout_ns = (uint64_t)p->timeout_ms * 1000000ull;
   kp.hang_ns = kp.timeout_ns * 4 + 1000000000ull;
 

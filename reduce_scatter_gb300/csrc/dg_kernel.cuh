@@ -99,6 +99,8 @@ struct KParams {
   int32_t n_maps;       // tensor maps in use (each of tmA / tmB)
   uint32_t l2_hint;     // L2 policy of operand loads: bits 0-1 A, bits 2-3 B
                         // (0 none, 1 evict-first, 2 evict-last)
+  uint32_t wave_sync;   // producers start tile i only after every CTA issued tile i-1
+  uint32_t* wave_ctr;   // per-run counter of tiles whose loads are issued (zeroed per run)
   float alpha, beta;
   uint64_t timeout_ns;
   uint64_t hang_ns;
@@ -181,6 +183,12 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
 
 __device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
@@ -688,8 +696,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
       int32_t issued[STAGES];  // parity of the last load issued per stage, -1 none
       for (int i = 0; i < STAGES; ++i) issued[i] = -1;
       bool ok = true;
-      for (int64_t t = unit; t < T && ok; t += nunits) {
+      uint32_t wave = 0;
+      for (int64_t t = unit; t < T && ok; t += nunits, ++wave) {
         const Tile tl = decode_tile(p.g, t);
+        if (p.wave_sync && wave > 0) {
+          // keep the CTAs in phase so that tiles sharing an operand strip read
+          // it while it is still in L2 (a timing gate only: no data depends on it)
+          const uint32_t want = wave * gridDim.x;
+          const uint64_t t0 = globaltimer();
+          while (ld_relaxed_u32(p.wave_ctr) < want) {
+            if (globaltimer() - t0 > p.timeout_ns) break;
+            __nanosleep(64);
+          }
+        }
         if (tl.flag >= 0 && p.wait_flags) {
           wait_flag_geq(p, p.flags + tl.flag, p.epoch, (uint32_t)tl.flag);
           fence_proxy_async_global();
@@ -733,6 +752,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
             phase ^= 1;
           }
         }
+        if (p.wave_sync) atomicAdd(p.wave_ctr, 1u);
       }
       if (!ok) {
         aborted = true;

@@ -239,3 +239,16 @@ def test_l2_hints_do_not_change_results(hint):
         ref, _ = Runner(m, n, k, l, tp, sched, 0.5, 1.0).run(A, B, C)
         D, _ = Runner(m, n, k, l, tp, sched, 0.5, 1.0, options={dg.OPT_L2_HINT: hint}).run(A, B, C)
         assert torch.equal(D.view(torch.int16), ref.view(torch.int16)), sched
+
+
+@pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_wave_sync_does_not_change_results(sched):
+    m, n, k, l, tp = 2048, 4096, 512, 1, 4
+    a, b, c = host_inputs(m, n, k, l, seed=91)
+    A, B, C = to_dev(a), to_dev(b), to_dev(c)
+    ref, _ = Runner(m, n, k, l, tp, sched, 0.5, 1.0).run(A, B, C)
+    r = Runner(m, n, k, l, tp, sched, 0.5, 1.0, options={dg.OPT_WAVE_SYNC: 1, dg.OPT_TIMEOUT_MS: 1000})
+    for _ in range(2):
+        D, rc = r.run(A, B, C)
+        assert rc == dg.OK
+        assert torch.equal(D.view(torch.int16), ref.view(torch.int16))
