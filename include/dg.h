@@ -117,8 +117,10 @@ enum dg_option {
                                  bits 2-3 for B; 0 = none, 1 = evict first, 2 = evict last */
   DG_OPT_WAVE_SYNC = 9        /* 1 = each CTA starts its i-th tile only after every CTA has
                                  issued the loads of its (i-1)-th (keeps the CTAs that share
-                                 an operand strip in phase for L2 reuse); a zeroed counter
-                                 word per run, memset on the main stream */
+                                 an operand strip in phase for L2 reuse; one counter word
+                                 memset on the main stream per run), 0 = off, -1 (default) =
+                                 on for AG plans whose per-wave operand strips exceed about
+                                 96 MiB */
 };
 
 /* Plan geometry and workspace layout, for callers and tests. */

@@ -116,7 +116,7 @@ struct dg_plan_s {
   int cg = 2;  // CTA group of the tile config: 1 = 128 x 256 per SM, 2 = 256 x 256 per SM pair
   int epi = 0;  // epilogue: 0 direct, 1 staged through shared memory with TMA (default for RS)
   uint32_t l2_hint = 0;  // L2 policy of operand loads (DG_OPT_L2_HINT)
-  uint32_t wave_sync = 0;  // DG_OPT_WAVE_SYNC
+  int wave_sync = -1;  // DG_OPT_WAVE_SYNC: -1 auto, 0 off, 1 on
   uint64_t id = 0;
   uint32_t epoch = 0;
   bool serial_ws = false;
@@ -225,6 +225,23 @@ int layout(dg_plan_s* p) {
   if (!is_ag(p->schedule))
     p->ws_bytes_serial = round_up(off + (size_t)(P * g.L * p->m * p->n) * 4, 1024);
   return DG_OK;
+}
+
+// Wave gate (auto): AG plans whose wave of co-resident tiles touches more
+// full-K operand strips than about three quarters of L2 holds.  Tiles that
+// share a strip then drift apart by more than its L2 lifetime unless the CTAs
+// start each wave together.
+bool wave_sync_on(const dg_plan_s* p) {
+  if (p->wave_sync >= 0) return p->wave_sync == 1;
+  if (!is_ag(p->schedule)) return false;
+  const dg::Geom& g = p->g;
+  const int64_t units = p->cg == 2 ? p->max_pairs : p->num_sms;
+  if (units <= 0 || g.tiles_m <= 0) return false;
+  const double wm = (double)std::min<int64_t>(g.group_m, g.tiles_m);
+  const double wn = std::min((double)g.tiles_n * g.L, (double)units / wm);
+  const double strip = (double)g.BN * (double)p->k * 2.0;  // 256 rows x K x bf16
+  const double footprint = (wm + wn) * strip;
+  return footprint > 96.0 * 1024 * 1024;
 }
 
 int rt_init(dg_plan_s* p) {
@@ -586,8 +603,8 @@ int dg_set_option(dg_plan_t p, int option, int64_t value) {
       p->copy_streams = (int)value;
       return DG_OK;
     case DG_OPT_WAVE_SYNC:
-      if (value != 0 && value != 1) return fail(DG_ERR_ARG, "wave sync must be 0 or 1");
-      p->wave_sync = (uint32_t)value;
+      if (value < -1 || value > 1) return fail(DG_ERR_ARG, "wave sync must be -1 (auto), 0 or 1");
+      p->wave_sync = (int)value;
       return DG_OK;
     case DG_OPT_L2_HINT:
       if (value < 0 || value > 15 || (value & 3) == 3 || ((value >> 2) & 3) == 3)
@@ -709,9 +726,9 @@ int dg_run(dg_plan_t p, const dg_bf16_t* A, const dg_bf16_t* B, const dg_bf16_t*
   kp.beta = p->beta;
   kp.n_maps = p->n_maps;
   kp.l2_hint = p->l2_hint;
-  kp.wave_sync = p->wave_sync;
+  kp.wave_sync = wave_sync_on(p) ? 1u : 0u;
   kp.wave_ctr = reinterpret_cast<uint32_t*>(ws + p->off_status + 64);
-  if (p->wave_sync) DG_CUDA(cudaMemsetAsync(ws + p->off_status + 64, 0, 4, ms));
+  if (kp.wave_sync) DG_CUDA(cudaMemsetAsync(ws + p->off_status + 64, 0, 4, ms));
   kp.timeout_ns = (uint64_t)p->timeout_ms * 1000000ull;
   kp.hang_ns = kp.timeout_ns * 4 + 1000000000ull;
 
