@@ -75,3 +75,45 @@ def gemm_entries(A_rows: np.ndarray, B_rows: np.ndarray, C_block, alpha: float,
 def flops(m: int, n: int, k: int, l: int) -> float:
     """Algorithmic flop count of the whole problem: 2*M*N*K*L."""
     return 2.0 * m * n * k * l
+
+
+# ------------------------------------------------------------ scaled fp8 GEMM
+#
+# The scaled variants on the pages (fused_all_gather_scaled_matmul and
+# fused_scaled_matmul_reduce_scatter in torch/distributed/_symmetric_memory,
+# which call aten._scaled_mm with A_scale and B_scale) multiply the fp8 product
+# by the per-tensor scales:  D = alpha * scale_a * scale_b * (A B) + beta * C.
+# Here in fp64 on the exactly decoded fp8 values.
+
+# OCP fp8 formats: (mantissa bits, exponent bias); e4m3 is the "fn" variant
+# (no infinities; S.1111.111 is NaN), e5m2 is IEEE-like (infinities, NaNs).
+_FP8 = {"e4m3": (3, 7), "e5m2": (2, 15)}
+
+
+def fp8_bits_to_f64(bits, fmt: str) -> np.ndarray:
+    """Exact value of each fp8 code (uint8) in float64."""
+    man, bias = _FP8[fmt]
+    b = np.asarray(bits).astype(np.int64) & 0xFF
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    exp_field = (b >> man) & ((1 << (7 - man)) - 1)
+    mant = b & ((1 << man) - 1)
+    sub = np.ldexp(mant.astype(np.float64), 1 - bias - man)
+    nrm = np.ldexp(1.0 + mant / float(1 << man), exp_field - bias)
+    val = sign * np.where(exp_field == 0, sub, nrm)
+    top = (1 << (7 - man)) - 1
+    if fmt == "e4m3":
+        val = np.where((exp_field == top) & (mant == (1 << man) - 1), np.nan, val)
+    else:
+        val = np.where((exp_field == top) & (mant == 0), sign * np.inf, val)
+        val = np.where((exp_field == top) & (mant != 0), np.nan, val)
+    return val
+
+
+def scaled_gemm(A, B_nk, C, alpha: float, beta: float, scale_a: float, scale_b: float) -> np.ndarray:
+    """alpha * scale_a * scale_b * A @ B + beta * C in fp64 (A, B already decoded)."""
+    A = np.asarray(A, dtype=np.float64)
+    B_nk = np.asarray(B_nk, dtype=np.float64)
+    D = (np.float64(alpha) * np.float64(scale_a) * np.float64(scale_b)) * np.matmul(A, np.swapaxes(B_nk, 1, 2))
+    if beta != 0.0:
+        D = D + np.float64(beta) * np.asarray(C, dtype=np.float64)
+    return D

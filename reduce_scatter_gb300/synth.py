@@ -238,3 +238,138 @@ def bf16_view(t):
     import torch
 
     return t.view(torch.bfloat16)
+
+
+# ------------------------------------------------------------------- fp8 inputs
+#
+# fp8 tensors are the same seeded fp32 draws rounded to an OCP fp8 format:
+# e4m3 (the "fn" variant: bias 7, 3 mantissa bits, no infinities, largest
+# finite 448) or e5m2 (bias 15, 2 mantissa bits, largest finite 57344).
+# Rounding is to nearest, ties to even, on the value's own quantum (the
+# subnormal quantum below the smallest normal); magnitudes beyond the largest
+# finite value saturate to it.  All steps are exact float64 arithmetic on
+# powers of two, so the numpy and torch versions give the same bits.
+
+FP8_FORMATS = {"e4m3": (3, 7, 448.0), "e5m2": (2, 15, 57344.0)}
+
+
+def f32_to_fp8_bits_np(x: np.ndarray, fmt: str) -> np.ndarray:
+    man, bias, top = FP8_FORMATS[fmt]
+    v = np.asarray(x, dtype=np.float32).astype(np.float64)
+    sign = np.signbit(v)
+    a = np.minimum(np.abs(v), top)
+    _, e = np.frexp(np.where(a > 0, a, 1.0))          # a = f * 2**e, f in [0.5, 1)
+    E = np.maximum(e - 1, 1 - bias)                  # exponent of the value's binade
+    quantum = np.ldexp(1.0, E - man)
+    q = np.minimum(np.rint(a / quantum) * quantum, top)
+    _, e2 = np.frexp(np.where(q > 0, q, 1.0))
+    E2 = e2 - 1
+    normal = q >= np.ldexp(1.0, 1 - bias)
+    sub_code = np.rint(q / np.ldexp(1.0, 1 - bias - man))
+    mant = np.rint((q / np.ldexp(1.0, E2) - 1.0) * (1 << man))
+    norm_code = (E2 + bias) * (1 << man) + mant
+    code = np.where(normal, norm_code, sub_code).astype(np.int64)
+    code = np.where(q == 0, 0, code)
+    return (code | (sign.astype(np.int64) << 7)).astype(np.uint8)
+
+
+def fp8_bits_to_f32_np(bits: np.ndarray, fmt: str) -> np.ndarray:
+    """Decode (finite codes only; used by the generator's own checks)."""
+    man, bias, _ = FP8_FORMATS[fmt]
+    b = np.asarray(bits, dtype=np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    ef = (b >> man) & ((1 << (7 - man)) - 1)
+    mf = b & ((1 << man) - 1)
+    val = np.where(ef == 0, np.ldexp(mf.astype(np.float64), 1 - bias - man),
+                   np.ldexp(1.0 + mf / (1 << man), ef - bias))
+    return (sign * val).astype(np.float32)
+
+
+def _f32_to_fp8_bits_t(v, fmt: str):
+    import torch
+
+    man, bias, top = FP8_FORMATS[fmt]
+    v = v.to(torch.float32).to(torch.float64)
+    sign = torch.signbit(v)
+    a = torch.clamp(v.abs(), max=top)
+    _, e = torch.frexp(torch.where(a > 0, a, torch.ones_like(a)))
+    E = torch.clamp(e - 1, min=1 - bias).to(torch.float64)
+    quantum = torch.pow(2.0, E - man)
+    q = torch.clamp(torch.round(a / quantum) * quantum, max=top)
+    _, e2 = torch.frexp(torch.where(q > 0, q, torch.ones_like(q)))
+    E2 = (e2 - 1).to(torch.float64)
+    normal = q >= 2.0 ** (1 - bias)
+    sub_code = torch.round(q / 2.0 ** (1 - bias - man))
+    mant = torch.round((q / torch.pow(2.0, E2) - 1.0) * (1 << man))
+    norm_code = (E2 + bias) * (1 << man) + mant
+    code = torch.where(normal, norm_code, sub_code).to(torch.int64)
+    code = torch.where(q == 0, torch.zeros_like(code), code)
+    code = code | (sign.to(torch.int64) << 7)
+    return code.to(torch.uint8)
+
+
+def _draw_f32_np(seed, stream, idx, dist):
+    """fp32 value of a draw before its final rounding (uniform or normal)."""
+    kind = dist[0]
+    if kind == "uniform":
+        lo, hi = float(dist[1]), float(dist[2])
+        z = raw_np(stream_key(seed, stream), idx)
+        u = (z >> np.uint64(40)).astype(np.float64) * (2.0 ** -24)
+        return (lo + (hi - lo) * u).astype(np.float32)
+    if kind == "normal":
+        mean, std = float(dist[1]), float(dist[2])
+        i = np.asarray(idx, dtype=np.uint64)
+        key = stream_key(seed, stream)
+        z1 = raw_np(key, i * np.uint64(2))
+        z2 = raw_np(key, i * np.uint64(2) + np.uint64(1))
+        u1 = ((z1 >> np.uint64(40)).astype(np.float64) + 1.0) * (2.0 ** -24)
+        u2 = (z2 >> np.uint64(40)).astype(np.float64) * (2.0 ** -24)
+        n = np.sqrt(-2.0 * np.log(u1)) * np.cos((2.0 * math.pi) * u2)
+        return (mean + std * n).astype(np.float32)
+    raise ValueError(f"unknown distribution {dist!r}")
+
+
+def tensor_fp8_bits_np(seed: int, stream: int, shape: tuple, dist: tuple, fmt: str) -> np.ndarray:
+    n = int(np.prod(shape)) if len(shape) else 1
+    return f32_to_fp8_bits_np(_draw_f32_np(seed, stream, np.arange(n, dtype=np.uint64), dist), fmt).reshape(shape)
+
+
+def rows_fp8_bits_np(seed: int, stream: int, shape: tuple, rows: np.ndarray, dist: tuple, fmt: str) -> np.ndarray:
+    cols = int(shape[-1])
+    rows = np.asarray(rows, dtype=np.uint64)
+    idx = rows[:, None] * np.uint64(cols) + np.arange(cols, dtype=np.uint64)[None, :]
+    return f32_to_fp8_bits_np(_draw_f32_np(seed, stream, idx.reshape(-1), dist), fmt).reshape(len(rows), cols)
+
+
+def _draw_f32_t(seed: int, stream: int, idx, dist: tuple):
+    import torch
+
+    key = stream_key(seed, stream)
+    kind = dist[0]
+    if kind == "uniform":
+        lo, hi = float(dist[1]), float(dist[2])
+        u = _lsr(_raw_t(key, idx), 40).to(torch.float64) * (2.0 ** -24)
+        return (lo + (hi - lo) * u).to(torch.float32)
+    if kind == "normal":
+        mean, std = float(dist[1]), float(dist[2])
+        u1 = (_lsr(_raw_t(key, idx * 2), 40).to(torch.float64) + 1.0) * (2.0 ** -24)
+        u2 = _lsr(_raw_t(key, idx * 2 + 1), 40).to(torch.float64) * (2.0 ** -24)
+        n = torch.sqrt(-2.0 * torch.log(u1)) * torch.cos((2.0 * math.pi) * u2)
+        return (mean + std * n).to(torch.float32)
+    raise ValueError(f"unknown distribution {dist!r}")
+
+
+def tensor_fp8_bits_torch(seed: int, stream: int, shape: tuple, dist: tuple, fmt: str, device="cpu",
+                          chunk: int = 1 << 26):
+    """Same bits as :func:`tensor_fp8_bits_np`, as a uint8 torch tensor on ``device``."""
+    import torch
+
+    n = 1
+    for d in shape:
+        n *= int(d)
+    out = torch.empty(n, dtype=torch.uint8, device=device)
+    for start in range(0, n, chunk):
+        stop = min(n, start + chunk)
+        idx = torch.arange(start, stop, dtype=torch.int64, device=device)
+        out[start:stop] = _f32_to_fp8_bits_t(_draw_f32_t(seed, stream, idx, dist), fmt)
+    return out.view(*shape)

@@ -117,3 +117,10 @@ def test_local_size_mutant_caught():
     def wrong(sched, m, n, k, l, P):
         return (m // P, n, k // P, l)
     assert _fails(pc.check_printed_local_sizes, wrong, osch.AG_ROTATING_A)
+
+
+def test_scaled_gemm_mutant_caught():
+    def drops_scale_b(A, B, C, alpha, beta, sa, sb):
+        return og.scaled_gemm(A, B, C, alpha, beta, sa, 1.0)
+    ones_a, ones_b = np.ones((1, 3, 64)), np.ones((1, 2, 64))
+    assert not np.all(drops_scale_b(ones_a, ones_b, None, 1.0, 0.0, 3.0, 0.5) == 64 * 1.5)

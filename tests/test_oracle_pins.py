@@ -63,3 +63,36 @@ def test_flops_matches_printed_tflops():
         m, n, k, l = run["problem"]
         per_gpu = og.flops(m, n, k, l) / (run["avg_runtime_ms"] * 1e-3) / run["tp"] / 1e12
         assert abs(per_gpu - run["tflops_per_gpu"]) < 0.01
+
+
+def test_fp8_decode_matches_torch_for_every_code():
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    for fmt, tdt in (("e4m3", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)):
+        ours = og.fp8_bits_to_f64(codes, fmt)
+        theirs = torch.from_numpy(codes).view(tdt).to(torch.float64).numpy()
+        assert np.array_equal(np.isnan(ours), np.isnan(theirs))
+        ok = ~np.isnan(ours)
+        assert np.array_equal(ours[ok], theirs[ok])
+
+
+def test_fp8_format_facts():
+    # OCP 8-bit floating point formats: largest finite, one, smallest subnormal
+    e4 = og.fp8_bits_to_f64(np.array([0x7E, 0x38, 0x01, 0x08, 0xFE, 0x7F]), "e4m3")
+    assert e4[:5].tolist() == [448.0, 1.0, 2.0 ** -9, 2.0 ** -6, -448.0] and np.isnan(e4[5])
+    e5 = og.fp8_bits_to_f64(np.array([0x7B, 0x3C, 0x01, 0x04, 0x7C]), "e5m2")
+    assert e5.tolist() == [57344.0, 1.0, 2.0 ** -16, 2.0 ** -14, np.inf]
+
+
+def test_scaled_gemm_pins():
+    # brute force with integer inputs and power-of-two scales: exact
+    L, M, N, K = 2, 3, 4, 5
+    A = pc._int_valued(1, 1, (L, M, K))
+    B = pc._int_valued(1, 2, (L, N, K))
+    C = pc._int_valued(1, 3, (L, M, N))
+    got = og.scaled_gemm(A, B, C, 0.5, 2.0, 4.0, 0.25)
+    want = pc.brute_gemm(A, B, C, 0.5, 2.0)  # 0.5 * 4 * 0.25 = 0.5
+    assert np.array_equal(got, want)
+    # all ones: D = K * alpha * scale_a * scale_b
+    ones_a, ones_b = np.ones((1, 3, 64)), np.ones((1, 2, 64))
+    assert np.all(og.scaled_gemm(ones_a, ones_b, None, 1.0, 0.0, 3.0, 0.5) == 64 * 1.5)

@@ -56,3 +56,31 @@ def test_normal_moments():
     v = synth.bf16_bits_to_f32_np(synth.tensor_bits_np(3, 2, (200000,), ("normal", 0.0, 0.02))).astype(np.float64)
     assert abs(v.mean()) < 0.001
     assert abs(v.std() - 0.02) < 0.0005
+
+
+@pytest.mark.parametrize("fmt,tdt", [("e4m3", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)])
+def test_fp8_quantizer_matches_torch_casts_in_range(fmt, tdt):
+    top = synth.FP8_FORMATS[fmt][2]
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.normal(0, 1, 20000), rng.normal(0, 0.02, 20000), rng.normal(0, 100, 5000),
+                        rng.uniform(-top, top, 5000), [0.0, -0.0, top, -top, 2.0 ** -9, 2.0 ** -10,
+                                                       2.0 ** -17, 1.0625, 1.1875]]).astype(np.float32)
+    x = x[np.abs(x) <= top]
+    ours = synth.f32_to_fp8_bits_np(x, fmt)
+    theirs = torch.from_numpy(x).to(tdt).view(torch.uint8).numpy()
+    assert np.array_equal(ours, theirs)
+    # saturation beyond the largest finite value (torch gives NaN there instead)
+    assert synth.f32_to_fp8_bits_np(np.array([1e6, -1e6], np.float32), fmt).tolist() == \
+        synth.f32_to_fp8_bits_np(np.array([top, -top], np.float32), fmt).tolist()
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("dist", [("normal", 0.0, 1.0), ("normal", 0.0, 0.02), ("uniform", -1.0, 1.0)])
+def test_fp8_numpy_and_torch_agree(fmt, dist):
+    shape = (2, 31, 77)
+    a = synth.tensor_fp8_bits_np(4, 1, shape, dist, fmt)
+    b = synth.tensor_fp8_bits_torch(4, 1, shape, dist, fmt, chunk=999).numpy()
+    assert np.array_equal(a, b)
+    rows = np.array([0, 5, 61])
+    sub = synth.rows_fp8_bits_np(4, 1, shape, rows, dist, fmt)
+    assert np.array_equal(sub, a.reshape(62, 77)[rows])
