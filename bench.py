@@ -167,14 +167,20 @@ def cpu_oracle_sample(w, rows: int, cols: int):
     ridx = np.linspace(0, w.m - 1, rows).astype(np.int64)   # spread over every shard of batch 0
     batch = 0
     cidx = np.linspace(0, w.n - 1, cols).astype(np.int64)
-    a = og.bf16_bits_to_f64(synth.rows_bits_np(w.seed, synth.STREAM_A, (LM, w.k), ridx, w.dist_a))
-    b = og.bf16_bits_to_f64(synth.rows_bits_np(w.seed, synth.STREAM_B, (LN, w.k), cidx, w.dist_b))
+    if w.in_type == "bf16":
+        a = og.bf16_bits_to_f64(synth.rows_bits_np(w.seed, synth.STREAM_A, (LM, w.k), ridx, w.dist_a))
+        b = og.bf16_bits_to_f64(synth.rows_bits_np(w.seed, synth.STREAM_B, (LN, w.k), cidx, w.dist_b))
+    else:
+        a = og.fp8_bits_to_f64(synth.rows_fp8_bits_np(w.seed, synth.STREAM_A, (LM, w.k), ridx, w.dist_a,
+                                                      w.in_type), w.in_type)
+        b = og.fp8_bits_to_f64(synth.rows_fp8_bits_np(w.seed, synth.STREAM_B, (LN, w.k), cidx, w.dist_b,
+                                                      w.in_type), w.in_type)
     c = None
     if w.beta != 0:
         crow = synth.rows_bits_np(w.seed, synth.STREAM_C, (LM, w.n), ridx, w.dist_c)[:, cidx - batch * w.n]
         c = og.bf16_bits_to_f64(crow)
     t0 = time.perf_counter()
-    og.gemm_entries(a, b, c, w.alpha, w.beta)
+    og.gemm_entries(a, b, c, w.alpha * w.scale_a * w.scale_b, w.beta)
     dt = time.perf_counter() - t0
     flops = 2.0 * rows * cols * w.k
     try:
@@ -220,10 +226,16 @@ def make_inputs(w, device):
     from reduce_scatter_gb300 import synth
 
     chunk = 1 << 28  # fewer, larger generator launches
-    A = synth.tensor_bits_torch(w.seed, synth.STREAM_A, (w.l, w.m, w.k), w.dist_a, device=device,
-                                chunk=chunk).view(torch.bfloat16)
-    B = synth.tensor_bits_torch(w.seed, synth.STREAM_B, (w.l, w.n, w.k), w.dist_b, device=device,
-                                chunk=chunk).view(torch.bfloat16)
+    if w.in_type == "bf16":
+        A = synth.tensor_bits_torch(w.seed, synth.STREAM_A, (w.l, w.m, w.k), w.dist_a, device=device,
+                                    chunk=chunk).view(torch.bfloat16)
+        B = synth.tensor_bits_torch(w.seed, synth.STREAM_B, (w.l, w.n, w.k), w.dist_b, device=device,
+                                    chunk=chunk).view(torch.bfloat16)
+    else:  # fp8 bytes
+        A = synth.tensor_fp8_bits_torch(w.seed, synth.STREAM_A, (w.l, w.m, w.k), w.dist_a, w.in_type,
+                                        device=device, chunk=chunk)
+        B = synth.tensor_fp8_bits_torch(w.seed, synth.STREAM_B, (w.l, w.n, w.k), w.dist_b, w.in_type,
+                                        device=device, chunk=chunk)
     C = None
     if w.beta != 0:
         C = synth.tensor_bits_torch(w.seed, synth.STREAM_C, (w.l, w.m, w.n), w.dist_c, device=device,
@@ -260,7 +272,8 @@ def run_dg(args, rank, world, dist):
     torch.cuda.set_device(dev)
     A, B, C = make_inputs(w, dev)
     D = torch.empty((w.l, w.m, w.n), dtype=torch.bfloat16, device=dev)
-    plan = dg.Plan(w.m, w.n, w.k, w.l, w.tp, w.schedule, w.alpha, w.beta)
+    plan = dg.Plan(w.m, w.n, w.k, w.l, w.tp, w.schedule, w.alpha, w.beta, w.in_type, w.in_type, w.scale_a,
+                   w.scale_b)
     if args.copy_streams > 0:
         plan.set_option(dg.OPT_COPY_STREAMS, args.copy_streams)
     for opt in args.option:
@@ -269,7 +282,8 @@ def run_dg(args, rank, world, dist):
     ws = torch.zeros(max(plan.workspace_bytes(), 256), dtype=torch.uint8, device=dev)
     main = torch.cuda.current_stream(dev)
     copy = torch.cuda.Stream(dev)
-    in_bytes = A.numel() * 2 + B.numel() * 2 + (C.numel() * 2 if C is not None else 0)
+    in_bytes = (A.numel() * A.element_size() + B.numel() * B.element_size()
+                + (C.numel() * 2 if C is not None else 0))
     flush_buf = None
     if in_bytes < 2 * L2_BYTES:
         flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
@@ -313,13 +327,15 @@ def run_dg(args, rank, world, dist):
     # separate reduction kernel)
     ms_tp1 = ms_nonfused = None
     if not args.no_modes and mode == dg.MODE_FUSED and w.tp > 1:
-        p1 = dg.Plan(w.m, w.n, w.k, w.l, 1, w.schedule, w.alpha, w.beta)
+        p1 = dg.Plan(w.m, w.n, w.k, w.l, 1, w.schedule, w.alpha, w.beta, w.in_type, w.in_type, w.scale_a,
+                     w.scale_b)
         ws1 = torch.zeros(max(p1.workspace_bytes(), 256), dtype=torch.uint8, device=dev)
         ms_tp1 = timed_loop(lambda: p1.run(A, B, C, D, ws1, main, copy), max(3, args.steps // 2), 2, main, flush)
         p1.check(ws1, main)
         del ws1, p1
         if w.schedule in (dg.RS_TILING_A_ROTATING_C, dg.RS_TILING_B_ROTATING_C):
-            ps = dg.Plan(w.m, w.n, w.k, w.l, w.tp, w.schedule, w.alpha, w.beta)
+            ps = dg.Plan(w.m, w.n, w.k, w.l, w.tp, w.schedule, w.alpha, w.beta, w.in_type, w.in_type,
+                         w.scale_a, w.scale_b)
             ps.set_mode(dg.MODE_SERIAL)
             wss = torch.zeros(max(ps.workspace_bytes(), 256), dtype=torch.uint8, device=dev)
             ms_nonfused = timed_loop(lambda: ps.run(A, B, C, D, wss, main, main), max(3, args.steps // 2), 2,
@@ -361,6 +377,12 @@ def run_dg(args, rank, world, dist):
 
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK_TFLOPS))
+    peak_sust = float(peaks.get("bf16_tflops_sustained", peak))
+    peak_note = peak_kind + " bf16 burst"
+    if w.in_type != "bf16":
+        # fp8 dense peak: the measured bf16 peak x the nominal fp8 / bf16 ratio (4.5 / 2.25)
+        peak, peak_sust = 2.0 * peak, 2.0 * peak_sust
+        peak_note = peak_kind + " bf16 burst x 2 (nominal fp8 / bf16 dense ratio)"
     per_gpu = w.flops / (ms_fused * 1e-3) / 1e12
     value = whole_job_tflops(w.flops, world, ms_fused)
     hidden = None
@@ -381,7 +403,7 @@ def run_dg(args, rank, world, dist):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "bf16" if w.in_type == "bf16" else w.in_type + " inputs, fp32 accumulation, bf16 output",
         "data": "synthetic (seeded SplitMix64 inputs with the workload's distributions)",
         "mode": args.mode,
         "options": args.option,
@@ -397,8 +419,8 @@ def run_dg(args, rank, world, dist):
         "ms_rs_nonfused_baseline": None if ms_nonfused is None else round(ms_nonfused, 4),
         "fused_speedup_vs_nonfused": None if ms_nonfused is None else round(ms_nonfused / ms_fused, 4),
         "roofline": {"bound": "tensor", "achieved": round(per_gpu, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(per_gpu / peak, 4), "peak_source": f"{peak_kind} bf16 burst",
-                     "frac_of_sustained": round(per_gpu / float(peaks.get("bf16_tflops_sustained", peak)), 4),
+                     "frac": round(per_gpu / peak, 4), "peak_source": peak_note,
+                     "frac_of_sustained": round(per_gpu / peak_sust, 4),
                      "traffic": recorded_traffic(w.name), "kernel": "dg::dg_gemm_kernel"},
         "clocks": clocks,
         "gpu_launches": args.steps,  # one dg_gemm_kernel launch per fused step

@@ -83,6 +83,12 @@ enum dg_schedule {
  * shards; the rotating partial lives in the workspace). */
 enum dg_mode { DG_MODE_FUSED = 0, DG_MODE_GEMM_ONLY = 1, DG_MODE_SERIAL = 2 };
 
+/* Input element types of A and B (C and D are always bf16).  fp8 follows the
+ * OCP 8-bit formats: E4M3 is the variant without infinities (largest finite
+ * 448), E5M2 the IEEE-like one (largest finite 57344); both are passed as raw
+ * bytes. */
+enum dg_type { DG_TYPE_BF16 = 0, DG_TYPE_E4M3 = 1, DG_TYPE_E5M2 = 2 };
+
 enum dg_status {
   DG_OK = 0,
   DG_ERR_ARG = -1,         /* null/misaligned pointer, bad enum, negative extent */
@@ -137,6 +143,8 @@ typedef struct dg_plan_info {
   size_t off_status, off_flags, off_slots, off_partial, off_serial;
   size_t slot_bytes;                 /* one receive slot (one shard, one batch) */
   int64_t copies_per_run;            /* transfer enqueues per FUSED/SERIAL run */
+  int32_t a_type, b_type;            /* dg_type of A and B */
+  int32_t elem_bytes;                /* bytes per A / B element (2 bf16, 1 fp8) */
 } dg_plan_info;
 
 /* One tile of the step-major rotation order (host decoder, for tests). */
@@ -159,6 +167,19 @@ typedef struct dg_tile {
 int dg_plan(dg_plan_t* out, int64_t m, int64_t n, int64_t k, int64_t l, int tp, int schedule,
             float alpha, float beta);
 
+/* The scaled variant: A and B of dg_type a_type / b_type (both bf16, or both
+ * fp8 in either format) with per-tensor scales, after the scaled all-gather /
+ * reduce-scatter matmuls of torch/distributed/_symmetric_memory
+ * (fused_all_gather_scaled_matmul and fused_scaled_matmul_reduce_scatter,
+ * which pass A_scale and B_scale to a scaled matmul):
+ *     D = alpha * scale_a * scale_b * A * B + beta * C
+ * The three factors are folded into one fp32 multiplier (alpha*scale_a*scale_b
+ * rounded to fp32) applied to the fp32 accumulator.  For fp8 inputs K must be
+ * a multiple of 16 (and K/tp for the RS schedules); each K block holds 128
+ * elements.  dg_plan is this call with bf16 inputs and unit scales. */
+int dg_plan_scaled(dg_plan_t* out, int64_t m, int64_t n, int64_t k, int64_t l, int tp, int schedule,
+                   float alpha, float beta, int a_type, int b_type, float scale_a, float scale_b);
+
 /* Workspace bytes the plan needs in its current mode (0 is possible). */
 size_t dg_workspace_bytes(dg_plan_t plan);
 
@@ -168,7 +189,8 @@ int dg_run_mode(dg_plan_t plan, int mode);
 /* Set a dg_option. */
 int dg_set_option(dg_plan_t plan, int option, int64_t value);
 
-/* Enqueue one run.  A, B, D, workspace: device pointers, 16-byte aligned
+/* Enqueue one run.  A and B hold the plan's input type (bf16 or fp8 bytes).
+ * A, B, D, workspace: device pointers, 16-byte aligned
  * (workspace 256-byte aligned), workspace of dg_workspace_bytes(plan) bytes.
  * C may be NULL iff beta == 0.  main_stream / copy_stream: cudaStream_t
  * handles (copy_stream may equal main_stream; it is used only in FUSED mode
@@ -176,7 +198,7 @@ int dg_set_option(dg_plan_t plan, int option, int64_t value);
  * ordered after prior work on main_stream and later work on main_stream is
  * ordered after all of it (copies included).  Device-side failures are
  * reported by dg_check. */
-int dg_run(dg_plan_t plan, const dg_bf16_t* A, const dg_bf16_t* B, const dg_bf16_t* C,
+int dg_run(dg_plan_t plan, const void* A, const void* B, const dg_bf16_t* C,
            dg_bf16_t* D, void* workspace, void* main_stream, void* copy_stream);
 
 /* Synchronize `stream` and read the workspace status word of the plan's last

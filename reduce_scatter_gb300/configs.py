@@ -13,6 +13,9 @@ the pages' benchmarks, as synthetic inputs.
   TP=4, 8192 x 53248 x 8192, L=2, alpha=0.5, beta=1, C N(0,1).
 * ``rs_b_tp4_quarter``: rs_b_tp4_batched with N / 4 and L = 1, for profiler
   captures.
+* ``ag_a_tp8_pr_e4m3`` / ``rs_a_tp8_e4m3``: the TP=8 problems with e4m3
+  operands (the scaled variant): both drawn N(0,1) and rounded to e4m3, the
+  weight's 0.02 standard deviation carried by scale_b.
 
 A is the activation (M x K), B the weight stored N x K, C the epilogue input.
 """
@@ -42,6 +45,9 @@ class Workload:
     dist_b: tuple = U11
     dist_c: tuple = N1
     seed: int = 1
+    in_type: str = "bf16"  # A and B element type: bf16, e4m3 or e5m2
+    scale_a: float = 1.0
+    scale_b: float = 1.0
 
     @property
     def flops(self) -> float:
@@ -53,7 +59,8 @@ class Workload:
         return {"workload": self.name, "schedule": dg.SCHEDULE_NAMES[self.schedule], "tp": self.tp,
                 "m": self.m, "n": self.n, "k": self.k, "l": self.l, "alpha": self.alpha, "beta": self.beta,
                 "dist_a": list(self.dist_a), "dist_b": list(self.dist_b),
-                "dist_c": list(self.dist_c) if self.beta else None, "seed": self.seed}
+                "dist_c": list(self.dist_c) if self.beta else None, "seed": self.seed,
+                "in_type": self.in_type, "scale_a": self.scale_a, "scale_b": self.scale_b}
 
 
 WORKLOADS = {
@@ -67,6 +74,11 @@ WORKLOADS = {
                  dist_b=N002, dist_c=N1),
         Workload("rs_b_tp4_batched", 3, 4, 8192, 53248, 8192, l=2, alpha=0.5, beta=1.0, dist_a=N1,
                  dist_b=N002, dist_c=N1),
+        # fp8 versions of the TP=8 workloads: e4m3 operands drawn N(0,1), the weight's
+        # N(0,0.02) scale carried by the per-tensor scale_b
+        Workload("ag_a_tp8_pr_e4m3", 0, 8, 16384, 106496, 16384, dist_a=N1, dist_b=N1, in_type="e4m3",
+                 scale_b=0.02),
+        Workload("rs_a_tp8_e4m3", 2, 8, 16384, 8192, 28672, dist_a=N1, dist_b=N1, in_type="e4m3", scale_b=0.02),
         # a quarter of rs_b_tp4_batched's N and one batch: small enough (about 1 GB on the
         # device) for a full profiler capture, same per-tile work
         Workload("rs_b_tp4_quarter", 3, 4, 8192, 13312, 8192, l=1, alpha=0.5, beta=1.0, dist_a=N1,

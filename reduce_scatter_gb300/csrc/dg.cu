@@ -107,6 +107,9 @@ struct dg_plan_s {
   int64_t m = 0, n = 0, k = 0, l = 0;
   int tp = 1, schedule = 0;
   float alpha = 1.f, beta = 0.f;
+  int a_type = DG_TYPE_BF16, b_type = DG_TYPE_BF16;  // input element types
+  int esz = 2;                                       // bytes per A / B element
+  float scale_a = 1.f, scale_b = 1.f;                // per-tensor scales (scaled GEMM)
   int mode = DG_MODE_FUSED;
   int64_t timeout_ms = 2000;
   int64_t chunk_tiles_req = 0;
@@ -159,7 +162,7 @@ int layout(dg_plan_s* p) {
   g.L = p->l;
   g.BM = p->cg == 2 ? dg::Cfg<2>::TILE_M : dg::Cfg<1>::TILE_M;
   g.BN = dg::TILE_N;
-  g.BK = dg::BK;
+  g.BK = dg::KROW_BYTES / p->esz;  // 64 bf16 or 128 fp8 elements: 128 bytes per row
   g.group_m = 16;
   g.beta_nonzero = p->beta != 0.f;
   switch (p->schedule) {
@@ -189,7 +192,7 @@ int layout(dg_plan_s* p) {
     const int64_t tile_rows = p->schedule == DG_AG_ROTATING_A ? g.BM : g.BN;
     int64_t ct = p->chunk_tiles_req;
     if (ct <= 0) {
-      const int64_t bytes = tile_rows * std::max<int64_t>(p->k, 1) * 2;
+      const int64_t bytes = tile_rows * std::max<int64_t>(p->k, 1) * p->esz;
       ct = std::max<int64_t>(1, dg::cdiv(int64_t(2) << 20, bytes));
     }
     g.chunk_tiles = std::max<int64_t>(1, std::min<int64_t>(ct, std::max<int64_t>(rot_tiles, 1)));
@@ -215,7 +218,7 @@ int layout(dg_plan_s* p) {
   p->off_flags = 256;
   size_t off = round_up(p->off_flags + (size_t)p->n_flags * 4, 1024);
   p->off_slots = off;
-  p->slot_bytes = is_ag(p->schedule) ? (size_t)g.shard * (size_t)p->k * 2 : 0;
+  p->slot_bytes = is_ag(p->schedule) ? (size_t)g.shard * (size_t)p->k * (size_t)p->esz : 0;
   if (is_ag(p->schedule) && P > 1) off = round_up(off + (size_t)(P * (P - 1) * g.L) * p->slot_bytes, 1024);
   p->off_partial = off;
   if (!is_ag(p->schedule) && P > 1) off = round_up(off + (size_t)(g.L * p->m * p->n) * 4, 1024);
@@ -255,14 +258,18 @@ int rt_init(dg_plan_s* p) {
     return fail(DG_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a", dev,
                 major, minor);
   DG_CUDA(cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, dev));
-  DG_CUDA(cudaFuncSetAttribute(dg::dg_gemm_kernel<1, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)dg::Cfg<1, 0>::SMEM_BYTES));
-  DG_CUDA(cudaFuncSetAttribute(dg::dg_gemm_kernel<1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)dg::Cfg<1, 1>::SMEM_BYTES));
-  DG_CUDA(cudaFuncSetAttribute(dg::dg_gemm_kernel<2, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)dg::Cfg<2, 0>::SMEM_BYTES));
-  DG_CUDA(cudaFuncSetAttribute(dg::dg_gemm_kernel<2, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)dg::Cfg<2, 1>::SMEM_BYTES));
+#define DG_SMEM_ATTR(CG, EPI, F8)                                                                  \
+  DG_CUDA(cudaFuncSetAttribute(dg::dg_gemm_kernel<CG, EPI, F8>,                                   \
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dg::Cfg<CG, EPI>::SMEM_BYTES))
+  DG_SMEM_ATTR(1, 0, 0);
+  DG_SMEM_ATTR(1, 1, 0);
+  DG_SMEM_ATTR(2, 0, 0);
+  DG_SMEM_ATTR(2, 1, 0);
+  DG_SMEM_ATTR(1, 0, 1);
+  DG_SMEM_ATTR(1, 1, 1);
+  DG_SMEM_ATTR(2, 0, 1);
+  DG_SMEM_ATTR(2, 1, 1);
+#undef DG_SMEM_ATTR
   {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -276,9 +283,9 @@ int rt_init(dg_plan_s* p) {
     cfg.numAttrs = 1;
     int ncl0 = 0, ncl1 = 0;
     cfg.dynamicSmemBytes = dg::Cfg<2, 0>::SMEM_BYTES;
-    DG_CUDA(cudaOccupancyMaxActiveClusters(&ncl0, dg::dg_gemm_kernel<2, 0>, &cfg));
+    DG_CUDA(cudaOccupancyMaxActiveClusters(&ncl0, dg::dg_gemm_kernel<2, 0, 0>, &cfg));
     cfg.dynamicSmemBytes = dg::Cfg<2, 1>::SMEM_BYTES;
-    DG_CUDA(cudaOccupancyMaxActiveClusters(&ncl1, dg::dg_gemm_kernel<2, 1>, &cfg));
+    DG_CUDA(cudaOccupancyMaxActiveClusters(&ncl1, dg::dg_gemm_kernel<2, 1, 0>, &cfg));
     p->max_pairs = std::min(ncl0, ncl1);
   }
   DG_CUDA(cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming));
@@ -288,13 +295,17 @@ int rt_init(dg_plan_s* p) {
   return DG_OK;
 }
 
+// Operand map: `rows` rows of `inner` elements (row pitch `pitch_elems`), box
+// of one 128-byte K block x `box_rows` rows, 128-byte swizzle.  esz = 2 (bf16)
+// or 1 (fp8, moved as bytes).
 int encode_map(const Driver& drv, CUtensorMap* map, const void* base, int64_t inner, int64_t rows,
-               int64_t pitch_elems, int box_rows) {
+               int64_t pitch_elems, int box_rows, int esz) {
   cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)pitch_elems * 2};
-  cuuint32_t box[2] = {(cuuint32_t)dg::BK, (cuuint32_t)box_rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(pitch_elems * esz)};
+  cuuint32_t box[2] = {(cuuint32_t)(dg::KROW_BYTES / esz), (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = drv.encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+  CUresult r = drv.encode(map, esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                          const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -358,30 +369,30 @@ int build_maps(dg_plan_s* p, const Driver& drv, const void* A, const void* B, ui
   static_assert(dg::Cfg<2, 0>::B_ROWS == dg::Cfg<2, 1>::B_ROWS, "box rows do not depend on the epilogue");
   if (p->k > 0) {
     if (is_ag(p->schedule)) {
-      rc = encode_map(drv, &p->kp.tmA[0], A, p->k, g.L * p->m, p->k, a_box);
+      rc = encode_map(drv, &p->kp.tmA[0], A, p->k, g.L * p->m, p->k, a_box, p->esz);
       if (rc) return rc;
-      rc = encode_map(drv, &p->kp.tmB[0], B, p->k, g.L * p->n, p->k, b_box);
+      rc = encode_map(drv, &p->kp.tmB[0], B, p->k, g.L * p->n, p->k, b_box, p->esz);
       if (rc) return rc;
       p->n_maps = 1;
       if (P > 1) {
         const int64_t slot_rows = P * (P - 1) * g.L * g.shard;
         if (p->schedule == DG_AG_ROTATING_A) {
-          rc = encode_map(drv, &p->kp.tmA[1], ws + p->off_slots, p->k, slot_rows, p->k, a_box);
+          rc = encode_map(drv, &p->kp.tmA[1], ws + p->off_slots, p->k, slot_rows, p->k, a_box, p->esz);
           p->kp.tmB[1] = p->kp.tmB[0];
         } else {
-          rc = encode_map(drv, &p->kp.tmB[1], ws + p->off_slots, p->k, slot_rows, p->k, b_box);
+          rc = encode_map(drv, &p->kp.tmB[1], ws + p->off_slots, p->k, slot_rows, p->k, b_box, p->esz);
           p->kp.tmA[1] = p->kp.tmA[0];
         }
         if (rc) return rc;
         p->n_maps = 2;
       }
     } else {
-      const auto* a16 = static_cast<const uint16_t*>(A);
-      const auto* b16 = static_cast<const uint16_t*>(B);
+      const auto* a8 = static_cast<const uint8_t*>(A);  // byte addressing: K-slab offsets
+      const auto* b8 = static_cast<const uint8_t*>(B);
       for (int64_t r = 0; r < P; ++r) {
-        rc = encode_map(drv, &p->kp.tmA[r], a16 + r * g.Ks, g.Ks, g.L * p->m, p->k, a_box);
+        rc = encode_map(drv, &p->kp.tmA[r], a8 + r * g.Ks * p->esz, g.Ks, g.L * p->m, p->k, a_box, p->esz);
         if (rc) return rc;
-        rc = encode_map(drv, &p->kp.tmB[r], b16 + r * g.Ks, g.Ks, g.L * p->n, p->k, b_box);
+        rc = encode_map(drv, &p->kp.tmB[r], b8 + r * g.Ks * p->esz, g.Ks, g.L * p->n, p->k, b_box, p->esz);
         if (rc) return rc;
       }
       p->n_maps = (int)P;
@@ -419,11 +430,12 @@ int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B
     for (int i = 0; i < ns; ++i)
       DG_CUDA(cudaLaunchHostFunc(streams[i], sleep_cb, (void*)(intptr_t)p->fault_delay_ms));
   const bool rot_a = p->schedule == DG_AG_ROTATING_A;
-  const auto* home = static_cast<const uint16_t*>(rot_a ? A : B);
+  const auto* home = static_cast<const uint8_t*>(rot_a ? A : B);
+  const int64_t row_bytes = p->k * p->esz;
   const int64_t outer = rot_a ? p->m : p->n;  // rows of one batch of the rotated operand
   const int64_t tile_rows = rot_a ? g.BM : g.BN;
   const int64_t chunk_rows = g.chunk_tiles * tile_rows;
-  auto* slots = reinterpret_cast<uint16_t*>(ws + p->off_slots);
+  auto* slots = ws + p->off_slots;
   auto* flags = reinterpret_cast<uint32_t*>(ws + p->off_flags);
   int64_t idx = 0;
   for (int64_t s = 1; s < P; ++s)
@@ -436,9 +448,9 @@ int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B
           const int64_t row0 = c * chunk_rows;
           const int64_t rows = std::min(chunk_rows, g.shard - row0);
           if (rows > 0) {
-            const uint16_t* src = home + (l * outer + j * g.shard + row0) * p->k;
-            uint16_t* dst = slots + (slot * g.shard + row0) * p->k;
-            DG_CUDA(cudaMemcpyAsync(dst, src, (size_t)(rows * p->k) * 2, cudaMemcpyDeviceToDevice, st));
+            const uint8_t* src = home + (l * outer + j * g.shard + row0) * row_bytes;
+            uint8_t* dst = slots + (slot * g.shard + row0) * row_bytes;
+            DG_CUDA(cudaMemcpyAsync(dst, src, (size_t)(rows * row_bytes), cudaMemcpyDeviceToDevice, st));
           }
           if (idx != p->fault_skip) {
             CUresult rc = drv.write32((CUstream)st, (CUdeviceptr)(flags + slot * g.nchunks + c),
@@ -459,10 +471,15 @@ int launch_kp(dg_plan_s* p, const dg::KParams& kp, cudaStream_t st) {
     int64_t grid = p->grid_req > 0 ? p->grid_req : p->num_sms;
     grid = std::min<int64_t>(grid, tiles);
     if (grid <= 0) return DG_OK;
-    if (p->epi == 1)
-      dg::dg_gemm_kernel<1, 1><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 1>::SMEM_BYTES, st>>>(kp);
+    const bool f8 = p->esz == 1;
+    if (p->epi == 1 && f8)
+      dg::dg_gemm_kernel<1, 1, 1><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 1>::SMEM_BYTES, st>>>(kp);
+    else if (p->epi == 1)
+      dg::dg_gemm_kernel<1, 1, 0><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 1>::SMEM_BYTES, st>>>(kp);
+    else if (f8)
+      dg::dg_gemm_kernel<1, 0, 1><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 0>::SMEM_BYTES, st>>>(kp);
     else
-      dg::dg_gemm_kernel<1, 0><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 0>::SMEM_BYTES, st>>>(kp);
+      dg::dg_gemm_kernel<1, 0, 0><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 0>::SMEM_BYTES, st>>>(kp);
     DG_CUDA(cudaGetLastError());
     return DG_OK;
   }
@@ -482,10 +499,15 @@ int launch_kp(dg_plan_s* p, const dg::KParams& kp, cudaStream_t st) {
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (p->epi == 1)
-    DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 1>, kp));
+  const bool f8 = p->esz == 1;
+  if (p->epi == 1 && f8)
+    DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 1, 1>, kp));
+  else if (p->epi == 1)
+    DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 1, 0>, kp));
+  else if (f8)
+    DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 0, 1>, kp));
   else
-    DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 0>, kp));
+    DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 0, 0>, kp));
   return DG_OK;
 }
 
@@ -525,15 +547,22 @@ extern "C" {
 
 const char* dg_last_error(void) { return g_err.c_str(); }
 
-int dg_plan(dg_plan_t* out, int64_t m, int64_t n, int64_t k, int64_t l, int tp, int schedule,
-            float alpha, float beta) {
+int dg_plan_scaled(dg_plan_t* out, int64_t m, int64_t n, int64_t k, int64_t l, int tp, int schedule,
+                   float alpha, float beta, int a_type, int b_type, float scale_a, float scale_b) {
   if (!out) return fail(DG_ERR_ARG, "out is NULL");
   *out = nullptr;
   if (m < 0 || n < 0 || k < 0 || l < 0) return fail(DG_ERR_ARG, "negative extent");
   if (tp != 1 && tp != 2 && tp != 4 && tp != 8) return fail(DG_ERR_ARG, "tp must be 1, 2, 4 or 8 (got %d)", tp);
   if (schedule < 0 || schedule > 3) return fail(DG_ERR_ARG, "unknown schedule %d", schedule);
-  if (k % 8 || n % 8) return fail(DG_ERR_SHAPE, "K and N must be multiples of 8 (K=%lld N=%lld)",
-                                  (long long)k, (long long)n);
+  auto known = [](int t) { return t == DG_TYPE_BF16 || t == DG_TYPE_E4M3 || t == DG_TYPE_E5M2; };
+  if (!known(a_type) || !known(b_type)) return fail(DG_ERR_ARG, "unknown input type (%d, %d)", a_type, b_type);
+  if ((a_type == DG_TYPE_BF16) != (b_type == DG_TYPE_BF16))
+    return fail(DG_ERR_UNSUPPORTED, "A and B must both be bf16 or both fp8");
+  const int esz = a_type == DG_TYPE_BF16 ? 2 : 1;
+  const int64_t kq = 16 / esz;  // K elements per 16 bytes (TMA row pitch and K-slab starts)
+  if (k % kq || n % 8)
+    return fail(DG_ERR_SHAPE, "K must be a multiple of %lld and N of 8 (K=%lld N=%lld)", (long long)kq,
+                (long long)k, (long long)n);
   const bool rs = !is_ag(schedule);
   const bool need_m = schedule == DG_AG_ROTATING_A || schedule == DG_AG_ROTATING_B ||
                       schedule == DG_RS_TILING_A_ROTATING_C;
@@ -541,14 +570,16 @@ int dg_plan(dg_plan_t* out, int64_t m, int64_t n, int64_t k, int64_t l, int tp, 
   if (need_m && m % tp) return fail(DG_ERR_SHAPE, "M=%lld not divisible by tp=%d", (long long)m, tp);
   if (need_n && n % tp) return fail(DG_ERR_SHAPE, "N=%lld not divisible by tp=%d", (long long)n, tp);
   if (rs && k % tp) return fail(DG_ERR_SHAPE, "K=%lld not divisible by tp=%d", (long long)k, tp);
-  if (rs && (k / tp) % 8)
-    return fail(DG_ERR_SHAPE, "K/tp=%lld must be a multiple of 8", (long long)(k / tp));
+  if (rs && (k / tp) % kq)
+    return fail(DG_ERR_SHAPE, "K/tp=%lld must be a multiple of %lld", (long long)(k / tp), (long long)kq);
   if (l * m > (int64_t(1) << 31) || l * n > (int64_t(1) << 31) || k > (int64_t(1) << 31))
     return fail(DG_ERR_SHAPE, "extent too large");
   auto* p = new dg_plan_s();
   p->m = m, p->n = n, p->k = k, p->l = l;
   p->tp = tp, p->schedule = schedule;
   p->alpha = alpha, p->beta = beta;
+  p->a_type = a_type, p->b_type = b_type, p->esz = esz;
+  p->scale_a = scale_a, p->scale_b = scale_b;
   p->epi = is_ag(schedule) ? 0 : 1;
   {
     std::lock_guard<std::mutex> lk(g_ws_mu);
@@ -557,6 +588,11 @@ int dg_plan(dg_plan_t* out, int64_t m, int64_t n, int64_t k, int64_t l, int tp, 
   layout(p);
   *out = p;
   return DG_OK;
+}
+
+int dg_plan(dg_plan_t* out, int64_t m, int64_t n, int64_t k, int64_t l, int tp, int schedule,
+            float alpha, float beta) {
+  return dg_plan_scaled(out, m, n, k, l, tp, schedule, alpha, beta, DG_TYPE_BF16, DG_TYPE_BF16, 1.f, 1.f);
 }
 
 size_t dg_workspace_bytes(dg_plan_t p) {
@@ -644,6 +680,7 @@ int dg_plan_info_get(dg_plan_t p, dg_plan_info* o) {
   o->off_partial = p->off_partial, o->off_serial = p->off_serial;
   o->slot_bytes = p->slot_bytes;
   o->copies_per_run = p->copies;
+  o->a_type = p->a_type, o->b_type = p->b_type, o->elem_bytes = p->esz;
   return DG_OK;
 }
 
@@ -662,7 +699,7 @@ int dg_plan_tile(dg_plan_t p, int64_t t, dg_tile* o) {
   return DG_OK;
 }
 
-int dg_run(dg_plan_t p, const dg_bf16_t* A, const dg_bf16_t* B, const dg_bf16_t* C, dg_bf16_t* D,
+int dg_run(dg_plan_t p, const void* A, const void* B, const dg_bf16_t* C, dg_bf16_t* D,
            void* workspace, void* main_stream, void* copy_stream) {
   if (!p) return fail(DG_ERR_ARG, "plan is NULL");
   if (p->g.total_tiles == 0) return DG_OK;  // empty output
@@ -722,8 +759,15 @@ int dg_run(dg_plan_t p, const dg_bf16_t* A, const dg_bf16_t* B, const dg_bf16_t*
   kp.flags = reinterpret_cast<uint32_t*>(ws + p->off_flags);
   kp.status = reinterpret_cast<unsigned long long*>(ws + p->off_status);
   kp.epoch = p->epoch;
-  kp.alpha = p->alpha;
+  // scaled GEMM: alpha * scale_a * scale_b folded into one fp32 factor
+  kp.alpha = p->alpha * p->scale_a * p->scale_b;
   kp.beta = p->beta;
+  {
+    const int tm = p->cg == 2 ? dg::Cfg<2>::TILE_M : dg::Cfg<1>::TILE_M;
+    const uint32_t fa = p->esz == 1 ? (p->a_type == DG_TYPE_E5M2 ? 1u : 0u) : 1u;
+    const uint32_t fb = p->esz == 1 ? (p->b_type == DG_TYPE_E5M2 ? 1u : 0u) : 1u;
+    kp.idesc = dg::idesc_f32acc(tm, dg::TILE_N, fa, fb);
+  }
   kp.n_maps = p->n_maps;
   kp.l2_hint = p->l2_hint;
   kp.wave_sync = wave_sync_on(p) ? 1u : 0u;

@@ -40,7 +40,8 @@
 
 namespace dg {
 
-constexpr int BK = 64;
+constexpr int BK = 64;            // K elements per block for bf16 inputs (128 for fp8)
+constexpr int KROW_BYTES = 128;   // bytes of one operand row per K block (the 128B swizzle span)
 constexpr int MAX_MAPS = 9;  // RS: one K-slab map per rank (P <= 8); AG: home + slots
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_THREADS = 128;
@@ -69,8 +70,8 @@ struct Cfg {
   static constexpr int TILE_M = 128 * CG;
   static constexpr int A_ROWS = 128;           // rows of A per CTA and stage
   static constexpr int B_ROWS = TILE_N / CG;   // rows of (N x K) B per CTA and stage
-  static constexpr uint32_t A_BYTES = A_ROWS * BK * 2;
-  static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;
+  static constexpr uint32_t A_BYTES = A_ROWS * KROW_BYTES;
+  static constexpr uint32_t B_BYTES = B_ROWS * KROW_BYTES;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = CG == 1 ? (EPI ? 3 : 4) : (EPI ? 5 : 6);
   static constexpr uint32_t STAGING_BYTES = EPI ? 4 * XBUF : 0;  // 2 source + 2 destination chunks
@@ -97,6 +98,7 @@ struct KParams {
   uint32_t epoch;
   uint32_t wait_flags;  // AG: 1 = wait on chunk flags
   int32_t n_maps;       // tensor maps in use (each of tmA / tmB)
+  uint32_t idesc;       // tcgen05 instruction descriptor (operand formats, M, N)
   uint32_t l2_hint;     // L2 policy of operand loads: bits 0-1 A, bits 2-3 B
                         // (0 none, 1 evict-first, 2 evict-last)
   uint32_t wave_sync;   // producers start tile i only after every CTA issued tile i-1
@@ -340,6 +342,27 @@ __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t mask) {
       : "memory");
 }
 
+// fp8 operands (e4m3 / e5m2, formats in the instruction descriptor), fp32
+// accumulator; one instruction covers K = 32 (32 bytes of each operand row).
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // 32 lanes x 32 columns of 32-bit: thread i of the warp gets lane (base+i),
 // columns col..col+31.
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&v)[32]) {
@@ -372,12 +395,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+// Instruction descriptor: fp32 accumulator (bits 4-5 = 1), A format at bits
+// 7-9 and B format at bits 10-12 (kind::f16: bf16 = 1; kind::f8f6f4:
+// e4m3 = 0, e5m2 = 1), both operands K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int m, int n, uint32_t a_fmt, uint32_t b_fmt) {
+  return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | ((uint32_t)(n >> 3) << 17) |
          ((uint32_t)(m >> 4) << 24);
 }
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) { return idesc_f32acc(m, n, 1, 1); }
 
 // ---------------------------------------------------------------- status
 
@@ -618,7 +643,7 @@ __device__ __forceinline__ void staged_load_src(const KParams& p, const Tile& tl
 
 // ------------------------------------------------------------------ kernel
 
-template <int CG, int EPI>
+template <int CG, int EPI, int F8>
 __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_constant__ KParams p) {
   using C = Cfg<CG, EPI>;
   constexpr int STAGES = C::STAGES;
@@ -690,6 +715,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
         prefetch_tmap(&p.tmA[i]);
         prefetch_tmap(&p.tmB[i]);
       }
+      const int32_t kblk = p.g.BK;  // K elements per block: 128 bytes of a row
       const uint32_t hint_a = p.l2_hint & 3u, hint_b = (p.l2_hint >> 2) & 3u;
       const uint64_t pol_a = hint_a ? l2_policy(hint_a) : 0, pol_b = hint_b ? l2_policy(hint_b) : 0;
       uint32_t stage = 0, phase = 0;
@@ -728,23 +754,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
             const uint32_t fb_lead = mapa_shared(fb, 0);
             if (leader) mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);  // both CTAs' bytes
             if (hint_a)
-              tma_load_2d_pair_hint(sa, ma, fb_lead, kb * BK, a_row, pol_a);
+              tma_load_2d_pair_hint(sa, ma, fb_lead, kb * kblk, a_row, pol_a);
             else
-              tma_load_2d_pair(sa, ma, fb_lead, kb * BK, a_row);
+              tma_load_2d_pair(sa, ma, fb_lead, kb * kblk, a_row);
             if (hint_b)
-              tma_load_2d_pair_hint(sa + C::A_BYTES, mb, fb_lead, kb * BK, b_row, pol_b);
+              tma_load_2d_pair_hint(sa + C::A_BYTES, mb, fb_lead, kb * kblk, b_row, pol_b);
             else
-              tma_load_2d_pair(sa + C::A_BYTES, mb, fb_lead, kb * BK, b_row);
+              tma_load_2d_pair(sa + C::A_BYTES, mb, fb_lead, kb * kblk, b_row);
           } else {
             mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
             if (hint_a)
-              tma_load_2d_hint(sa, ma, fb, kb * BK, a_row, pol_a);
+              tma_load_2d_hint(sa, ma, fb, kb * kblk, a_row, pol_a);
             else
-              tma_load_2d(sa, ma, fb, kb * BK, a_row);
+              tma_load_2d(sa, ma, fb, kb * kblk, a_row);
             if (hint_b)
-              tma_load_2d_hint(sa + C::A_BYTES, mb, fb, kb * BK, b_row, pol_b);
+              tma_load_2d_hint(sa + C::A_BYTES, mb, fb, kb * kblk, b_row, pol_b);
             else
-              tma_load_2d(sa + C::A_BYTES, mb, fb, kb * BK, b_row);
+              tma_load_2d(sa + C::A_BYTES, mb, fb, kb * kblk, b_row);
           }
           issued[stage] = (int32_t)phase;
           if (++stage == STAGES) {
@@ -773,7 +799,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // --------------------------------------------------------------- MMA
-      constexpr uint32_t IDESC = idesc_bf16_f32(C::TILE_M, TILE_N);
+      const uint32_t IDESC = p.idesc;
       uint32_t stage = 0, phase = 0, it = 0;
       bool ok = true;
       for (int64_t t = unit; t < T && ok; t += nunits, ++it) {
@@ -795,13 +821,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           const uint64_t da = smem_desc_sw128(sa);
           const uint64_t db = smem_desc_sw128(sa + C::A_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            // +32 bytes per K=16 step inside the swizzled 128-byte row
+          for (int kk = 0; kk < KROW_BYTES / 32; ++kk) {
+            // +32 bytes per instruction inside the swizzled 128-byte row
+            // (K = 16 bf16 or K = 32 fp8)
             const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
-            if (CG == 2)
-              tc_mma_bf16_pair(d_tmem, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), IDESC, acc);
-            else
-              tc_mma_bf16(d_tmem, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), IDESC, acc);
+            const uint64_t ad = da + (uint64_t)(2 * kk), bd = db + (uint64_t)(2 * kk);
+            if (F8) {
+              if (CG == 2)
+                tc_mma_f8_pair(d_tmem, ad, bd, IDESC, acc);
+              else
+                tc_mma_f8(d_tmem, ad, bd, IDESC, acc);
+            } else {
+              if (CG == 2)
+                tc_mma_bf16_pair(d_tmem, ad, bd, IDESC, acc);
+              else
+                tc_mma_bf16(d_tmem, ad, bd, IDESC, acc);
+            }
           }
           if (CG == 2)
             tc_commit_pair_mc(bar_empty + 8 * stage, 0x3);

@@ -27,6 +27,12 @@ SCHEDULE_NAMES = {
 }
 SCHEDULE_BY_NAME = {v: k for k, v in SCHEDULE_NAMES.items()}
 
+TYPE_BF16 = 0
+TYPE_E4M3 = 1
+TYPE_E5M2 = 2
+TYPE_NAMES = {TYPE_BF16: "bf16", TYPE_E4M3: "e4m3", TYPE_E5M2: "e5m2"}
+TYPE_BY_NAME = {v: k for k, v in TYPE_NAMES.items()}
+
 MODE_FUSED = 0
 MODE_GEMM_ONLY = 1
 MODE_SERIAL = 2
@@ -53,7 +59,8 @@ OPT_WAVE_SYNC = 9
 
 # Every symbol include/dg.h declares.
 EXPORTS = ("dg_plan", "dg_workspace_bytes", "dg_run_mode", "dg_set_option", "dg_run", "dg_check",
-           "dg_plan_info_get", "dg_plan_tile", "dg_destroy", "dg_last_error", "dg_run_static")
+           "dg_plan_info_get", "dg_plan_tile", "dg_destroy", "dg_last_error", "dg_run_static",
+           "dg_plan_scaled")
 
 # Size of the library's built-in workspace used by dg_run_static.
 STATIC_WORKSPACE_BYTES = 32 << 20
@@ -74,6 +81,7 @@ class PlanInfo(ctypes.Structure):
         ("off_partial", ctypes.c_size_t), ("off_serial", ctypes.c_size_t),
         ("slot_bytes", ctypes.c_size_t),
         ("copies_per_run", ctypes.c_int64),
+        ("a_type", ctypes.c_int32), ("b_type", ctypes.c_int32), ("elem_bytes", ctypes.c_int32),
     ]
 
     def as_dict(self):
@@ -115,6 +123,9 @@ def lib():
         i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
         L.dg_plan.argtypes = [ctypes.POINTER(vp), i64, i64, i64, i64, i32, i32, ctypes.c_float, ctypes.c_float]
         L.dg_plan.restype = i32
+        L.dg_plan_scaled.argtypes = [ctypes.POINTER(vp), i64, i64, i64, i64, i32, i32, ctypes.c_float,
+                                     ctypes.c_float, i32, i32, ctypes.c_float, ctypes.c_float]
+        L.dg_plan_scaled.restype = i32
         L.dg_workspace_bytes.argtypes = [vp]
         L.dg_workspace_bytes.restype = ctypes.c_size_t
         L.dg_run_mode.argtypes = [vp, i32]
@@ -169,11 +180,19 @@ def stream_handle(s) -> int | None:
 class Plan:
     """One problem (m, n, k, l, tp, schedule, alpha, beta) behind ``dg_plan``."""
 
-    def __init__(self, m, n, k, l, tp, schedule, alpha=1.0, beta=0.0):
+    def __init__(self, m, n, k, l, tp, schedule, alpha=1.0, beta=0.0, a_type=TYPE_BF16, b_type=TYPE_BF16,
+                 scale_a=1.0, scale_b=1.0):
         if isinstance(schedule, str):
             schedule = SCHEDULE_BY_NAME[schedule]
+        a_type = TYPE_BY_NAME.get(a_type, a_type)
+        b_type = TYPE_BY_NAME.get(b_type, b_type)
         h = ctypes.c_void_p()
-        _check(lib().dg_plan(ctypes.byref(h), m, n, k, l, tp, schedule, alpha, beta))
+        if a_type == TYPE_BF16 and b_type == TYPE_BF16 and scale_a == 1.0 and scale_b == 1.0:
+            _check(lib().dg_plan(ctypes.byref(h), m, n, k, l, tp, schedule, alpha, beta))
+        else:
+            _check(lib().dg_plan_scaled(ctypes.byref(h), m, n, k, l, tp, schedule, alpha, beta, a_type, b_type,
+                                        scale_a, scale_b))
+        self.a_type, self.b_type, self.scale_a, self.scale_b = a_type, b_type, scale_a, scale_b
         self._h = h
         self.m, self.n, self.k, self.l, self.tp, self.schedule = m, n, k, l, tp, schedule
         self.alpha, self.beta = alpha, beta

@@ -29,11 +29,24 @@ def dev_bits(t: torch.Tensor) -> np.ndarray:
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
+def host_inputs_fp8(m, n, k, l, seed=1, fmt_a="e4m3", fmt_b="e4m3", da=("normal", 0.0, 1.0),
+                    db=("normal", 0.0, 1.0), dc=UNIFORM):
+    a = synth.tensor_fp8_bits_np(seed, synth.STREAM_A, (l, m, k), da, fmt_a)
+    b = synth.tensor_fp8_bits_np(seed, synth.STREAM_B, (l, n, k), db, fmt_b)
+    c = synth.tensor_bits_np(seed, synth.STREAM_C, (l, m, n), dc)
+    return a, b, c
+
+
+def to_dev_u8(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits)).cuda()
+
+
 class Runner:
     """A plan, its workspace and two streams."""
 
-    def __init__(self, m, n, k, l, tp, sched, alpha=1.0, beta=0.0, mode=dg.MODE_FUSED, options=None):
-        self.plan = dg.Plan(m, n, k, l, tp, sched, alpha, beta)
+    def __init__(self, m, n, k, l, tp, sched, alpha=1.0, beta=0.0, mode=dg.MODE_FUSED, options=None,
+                 a_type=dg.TYPE_BF16, b_type=dg.TYPE_BF16, scale_a=1.0, scale_b=1.0):
+        self.plan = dg.Plan(m, n, k, l, tp, sched, alpha, beta, a_type, b_type, scale_a, scale_b)
         self.plan.set_mode(mode)
         for opt, val in (options or {}).items():
             self.plan.set_option(opt, val)
@@ -53,6 +66,11 @@ class Runner:
 def oracle_full(a, b, c, alpha, beta):
     return og.gemm(og.bf16_bits_to_f64(a), og.bf16_bits_to_f64(b),
                    og.bf16_bits_to_f64(c) if beta != 0 else None, alpha, beta)
+
+
+def oracle_fp8(a, b, c, fmt_a, fmt_b, alpha, beta, scale_a, scale_b):
+    return og.scaled_gemm(og.fp8_bits_to_f64(a, fmt_a), og.fp8_bits_to_f64(b, fmt_b),
+                          og.bf16_bits_to_f64(c) if beta != 0 else None, alpha, beta, scale_a, scale_b)
 
 
 def rel_err(D: torch.Tensor, want: np.ndarray) -> float:

@@ -215,3 +215,23 @@ def test_workspace_layout_sizes(L):
     assert pr.workspace_bytes() >= ir["off_serial"] + tp * l * m * n * 4
     p1 = dg.Plan(m, n, k, l, 1, dg.AG_ROTATING_A).info()
     assert p1["n_flags"] == 0 and p1["copies_per_run"] == 0
+
+
+def test_scaled_plan_rules(L):
+    h = ctypes.c_void_p()
+    # mixed 16-bit / 8-bit operands are refused; unknown types too
+    assert L.dg_plan_scaled(ctypes.byref(h), 64, 64, 64, 1, 1, 0, 1.0, 0.0, dg.TYPE_BF16, dg.TYPE_E4M3,
+                            1.0, 1.0) == dg.ERR_UNSUPPORTED
+    assert L.dg_plan_scaled(ctypes.byref(h), 64, 64, 64, 1, 1, 0, 1.0, 0.0, 7, 7, 1.0, 1.0) == dg.ERR_ARG
+    # fp8 rows need 16-byte pitch: K % 16, and (K/tp) % 16 for RS
+    assert L.dg_plan_scaled(ctypes.byref(h), 64, 64, 40, 1, 1, 0, 1.0, 0.0, dg.TYPE_E4M3, dg.TYPE_E4M3,
+                            1.0, 1.0) == dg.ERR_SHAPE
+    assert L.dg_plan_scaled(ctypes.byref(h), 64, 64, 64, 1, 8, 2, 1.0, 0.0, dg.TYPE_E4M3, dg.TYPE_E4M3,
+                            1.0, 1.0) == dg.ERR_SHAPE
+    p = dg.Plan(1024, 1024, 640, 1, 4, dg.AG_ROTATING_A, a_type="e4m3", b_type="e5m2", scale_b=0.5)
+    info = p.info()
+    assert (info["a_type"], info["b_type"], info["elem_bytes"]) == (dg.TYPE_E4M3, dg.TYPE_E5M2, 1)
+    assert info["slot_bytes"] == (1024 // 4) * 640          # one byte per element
+    assert p.tile(0)["k_blocks"] == 5                        # 128 fp8 elements per K block
+    pb = dg.Plan(1024, 1024, 640, 1, 4, dg.AG_ROTATING_A).info()
+    assert pb["elem_bytes"] == 2 and pb["slot_bytes"] == 2 * info["slot_bytes"]
