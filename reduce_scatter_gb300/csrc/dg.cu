@@ -242,7 +242,7 @@ bool wave_sync_on(const dg_plan_s* p) {
   if (units <= 0 || g.tiles_m <= 0) return false;
   const double wm = (double)std::min<int64_t>(g.group_m, g.tiles_m);
   const double wn = std::min((double)g.tiles_n * g.L, (double)units / wm);
-  const double strip = (double)g.BN * (double)p->k * 2.0;  // 256 rows x K x bf16
+  const double strip = (double)g.BN * (double)p->k * (double)p->esz;  // 256 rows x K elements
   const double footprint = (wm + wn) * strip;
   return footprint > 96.0 * 1024 * 1024;
 }
