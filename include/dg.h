@@ -121,6 +121,13 @@ enum dg_option {
                                  (default for the AG schedules, one more operand stage) */
   DG_OPT_L2_HINT = 8,         /* L2 eviction policy of the operand loads: bits 0-1 for A,
                                  bits 2-3 for B; 0 = none, 1 = evict first, 2 = evict last */
+  DG_OPT_RS_CE_PARTIALS = 10, /* RS plans with tp > 1, before the first run: 1 = hand the
+                                 rotating partial from rank to rank by copy-engine transfers
+                                 (each rank writes a send buffer; the copy streams wait on
+                                 per-band completion counts, copy into the next rank's
+                                 double-buffered receive buffer and publish a ready flag),
+                                 0 (default) = the next rank reads the partial in place.
+                                 Needs a copy stream distinct from the main stream. */
   DG_OPT_WAVE_SYNC = 9        /* 1 = each CTA starts its i-th tile only after every CTA has
                                  issued the loads of its (i-1)-th (keeps the CTAs that share
                                  an operand strip in phase for L2 reuse; one counter word

@@ -61,10 +61,12 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 typedef CUresult (*WriteValue32Fn)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+typedef CUresult (*WaitValue32Fn)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
 
 struct Driver {
   EncodeTiledFn encode = nullptr;
   WriteValue32Fn write32 = nullptr;
+  WaitValue32Fn wait32 = nullptr;
 };
 
 int get_driver(Driver* d) {
@@ -86,6 +88,12 @@ int get_driver(Driver* d) {
         q != cudaDriverEntryPointSuccess || !fn)
       return fail(DG_ERR_UNSUPPORTED, "driver entry point cuStreamWriteValue32 not found");
     cached.write32 = reinterpret_cast<WriteValue32Fn>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuStreamWaitValue32", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return fail(DG_ERR_UNSUPPORTED, "driver entry point cuStreamWaitValue32 not found");
+    cached.wait32 = reinterpret_cast<WaitValue32Fn>(fn);
     done = true;
   }
   *d = cached;
@@ -117,6 +125,8 @@ struct dg_plan_s {
   int64_t fault_delay_ms = 0;
   int64_t grid_req = 0;
   int cg = 2;  // CTA group of the tile config: 1 = 128 x 256 per SM, 2 = 256 x 256 per SM pair
+  bool cep = false;  // RS: hand partials on by copy-engine transfers (DG_OPT_RS_CE_PARTIALS)
+  size_t off_done = 0, off_send = 0, off_recv = 0;
   int epi = 0;  // epilogue: 0 direct, 1 staged through shared memory with TMA (default for RS)
   uint32_t l2_hint = 0;  // L2 policy of operand loads (DG_OPT_L2_HINT)
   int wave_sync = -1;  // DG_OPT_WAVE_SYNC: -1 auto, 0 off, 1 on
@@ -201,10 +211,14 @@ int layout(dg_plan_s* p) {
       p->n_flags = P * (P - 1) * g.L * g.nchunks;
       p->copies = p->n_flags;
     }
+  } else if (P > 1 && p->cep) {
+    // copy-engine hand-off: one ready flag per (receiving rank, step, batch, band)
+    p->n_flags = P * P * g.L * g.tiles_m;
   } else if (P > 1) {
     // one flag per tile and CTA of the group (each CTA hands on its own half)
     p->n_flags = g.L * P * g.tiles_m * g.tiles_n * p->cg;
   }
+  g.ce_partials = p->cep ? 1 : 0;
   // RS SERIAL baseline geometry: every rank's full M x N partial over its K-slab
   p->gser = g;
   p->gser.sched = dg::SCHED_PARTIAL;
@@ -221,7 +235,20 @@ int layout(dg_plan_s* p) {
   p->slot_bytes = is_ag(p->schedule) ? (size_t)g.shard * (size_t)p->k * (size_t)p->esz : 0;
   if (is_ag(p->schedule) && P > 1) off = round_up(off + (size_t)(P * (P - 1) * g.L) * p->slot_bytes, 1024);
   p->off_partial = off;
-  if (!is_ag(p->schedule) && P > 1) off = round_up(off + (size_t)(g.L * p->m * p->n) * 4, 1024);
+  p->off_done = p->off_send = p->off_recv = off;
+  if (!is_ag(p->schedule) && P > 1 && p->cep) {
+    // done counters (per rank, step, batch, band), send buffers (one slab per
+    // rank) and double-buffered receive buffers
+    const size_t slab = (size_t)(g.L * g.blk_m * g.blk_n) * 4;
+    p->off_done = off;
+    off = round_up(off + (size_t)(P * P * g.L * g.tiles_m) * 4, 1024);
+    p->off_send = off;
+    off = round_up(off + (size_t)P * slab, 1024);
+    p->off_recv = off;
+    off = round_up(off + (size_t)(2 * P) * slab, 1024);
+  } else if (!is_ag(p->schedule) && P > 1) {
+    off = round_up(off + (size_t)(g.L * p->m * p->n) * 4, 1024);
+  }
   p->off_serial = off;
   p->ws_bytes_base = off;
   p->ws_bytes_serial = off;
@@ -348,7 +375,15 @@ int build_epi_maps(dg_plan_s* p, const Driver& drv, const void* C, void* D, uint
     rc = encode_epi_map(drv, &p->kp.tmC, C, false, p->n, rows);
     if (rc) return rc;
   }
-  if (!is_ag(p->schedule) && p->tp > 1) {
+  std::memset(&p->kp.tmS, 0, sizeof(CUtensorMap));
+  std::memset(&p->kp.tmR, 0, sizeof(CUtensorMap));
+  if (!is_ag(p->schedule) && p->tp > 1 && p->cep) {
+    const dg::Geom& g = p->g;
+    rc = encode_epi_map(drv, &p->kp.tmS, ws + p->off_send, true, g.blk_n, p->tp * g.L * g.blk_m);
+    if (rc) return rc;
+    rc = encode_epi_map(drv, &p->kp.tmR, ws + p->off_recv, true, g.blk_n, 2 * p->tp * g.L * g.blk_m);
+    if (rc) return rc;
+  } else if (!is_ag(p->schedule) && p->tp > 1) {
     rc = encode_epi_map(drv, &p->kp.tmX, ws + p->off_partial, true, p->n, rows);
     if (rc) return rc;
   }
@@ -516,6 +551,84 @@ int launch(dg_plan_s* p, cudaStream_t st, uint32_t wait_flags) {
   return launch_kp(p, p->kp, st);
 }
 
+// ReduceScatter with copy-engine hand-off of the rotating partial (the
+// "memcopy branch" form of RotatingC).  Rank r writes its step-s partial to
+// its send buffer S_r; the kernel counts, per (rank, step, batch, band of 256
+// rows), the half tiles written; a copy stream waits until the band is
+// complete (and until the receiver has finished reading the same receive
+// slot two steps earlier), copies it into the receiving rank's
+// double-buffered receive buffer R_{r-1}[(s+1) & 1] and writes the band's
+// ready flag, which rank r-1's epilogue waits on at step s+1.  The copies are
+// enqueued step-major, so a copy waits only for tiles of its own step or the
+// one before, and every tile only for copies of the step before.
+int run_rs_ce(dg_plan_s* p, const Driver& drv, uint8_t* ws, cudaStream_t ms, cudaStream_t cs) {
+  const dg::Geom& g = p->g;
+  const int64_t P = p->tp, L = g.L, TM = g.tiles_m;
+  const size_t ndone = (size_t)(P * P * L * TM);
+  DG_CUDA(cudaMemsetAsync(ws + p->off_done, 0, ndone * 4, ms));
+  const int ns = p->copy_streams;
+  int rc = ensure_extra_streams(p, ns - 1);
+  if (rc) return rc;
+  cudaStream_t streams[8];
+  streams[0] = cs;
+  for (int i = 1; i < ns; ++i) streams[i] = p->extra[i - 1];
+  DG_CUDA(cudaEventRecord(p->ev_fork, ms));
+  rc = launch(p, ms, 0);
+  if (rc) return rc;
+  for (int i = 0; i < ns; ++i) DG_CUDA(cudaStreamWaitEvent(streams[i], p->ev_fork, 0));
+  if (p->fault_delay_ms > 0)
+    for (int i = 0; i < ns; ++i)
+      DG_CUDA(cudaLaunchHostFunc(streams[i], sleep_cb, (void*)(intptr_t)p->fault_delay_ms));
+  auto* done = reinterpret_cast<uint32_t*>(ws + p->off_done);
+  auto* flags = reinterpret_cast<uint32_t*>(ws + p->off_flags);
+  const uint32_t target = (uint32_t)(g.tiles_n * p->cg);  // half tiles per band
+  const size_t row_bytes = (size_t)g.blk_n * 4;
+  auto idx = [&](int64_t q, int64_t s, int64_t l, int64_t b) { return ((q * P + s) * L + l) * TM + b; };
+  auto check = [&](CUresult r, const char* what) {
+    return r == CUDA_SUCCESS ? DG_OK
+                             : fail(r == CUDA_ERROR_NOT_SUPPORTED ? DG_ERR_UNSUPPORTED : DG_ERR_CUDA, "%s failed (%d)",
+                                    what, (int)r);
+  };
+  int64_t n = 0;
+  for (int64_t s = 0; s + 1 < P; ++s)
+    for (int64_t r = 0; r < P; ++r) {
+      const int64_t q = (r + P - 1) % P;  // the ring neighbour that adds the next K-slab
+      for (int64_t l = 0; l < L; ++l)
+        for (int64_t b = 0; b < TM; ++b, ++n) {
+          cudaStream_t st = streams[n % ns];
+          rc = check(drv.wait32((CUstream)st, (CUdeviceptr)(done + idx(r, s, l, b)), target,
+                                CU_STREAM_WAIT_VALUE_GEQ),
+                     "cuStreamWaitValue32");
+          if (rc) return rc;
+          if (s >= 1) {
+            rc = check(drv.wait32((CUstream)st, (CUdeviceptr)(done + idx(q, s - 1, l, b)), target,
+                                  CU_STREAM_WAIT_VALUE_GEQ),
+                       "cuStreamWaitValue32");
+            if (rc) return rc;
+          }
+          const int64_t rows = std::min<int64_t>(g.BM, g.blk_m - b * g.BM);
+          const uint8_t* src = ws + p->off_send + (size_t)((r * L + l) * g.blk_m + b * g.BM) * row_bytes;
+          uint8_t* dst = ws + p->off_recv + (size_t)(((2 * q + ((s + 1) & 1)) * L + l) * g.blk_m + b * g.BM) * row_bytes;
+          DG_CUDA(cudaMemcpyAsync(dst, src, (size_t)rows * row_bytes, cudaMemcpyDeviceToDevice, st));
+          if (n != p->fault_skip) {
+            rc = check(drv.write32((CUstream)st, (CUdeviceptr)(flags + idx(q, s + 1, l, b)), p->epoch, 0),
+                       "cuStreamWriteValue32");
+            if (rc) return rc;
+          }
+        }
+    }
+  // After the kernel, raise every count: no copy-stream wait outlives a kernel
+  // that stopped early (in a normal run every copy has already run by then).
+  DG_CUDA(cudaMemsetAsync(ws + p->off_done, 0x7F, ndone * 4, ms));
+  for (int i = 1; i < ns; ++i) {
+    DG_CUDA(cudaEventRecord(p->extra_done[i - 1], streams[i]));
+    DG_CUDA(cudaStreamWaitEvent(cs, p->extra_done[i - 1], 0));
+  }
+  DG_CUDA(cudaEventRecord(p->ev_join, cs));
+  DG_CUDA(cudaStreamWaitEvent(ms, p->ev_join, 0));
+  return DG_OK;
+}
+
 // Non-fused ReduceScatter baseline ("GEMM, then reduce"): one launch computes
 // every rank's full partial over its K-slab into its own fp32 buffer; a
 // separate kernel sums the partials, adds beta*C and writes bf16 D.
@@ -637,6 +750,19 @@ int dg_set_option(dg_plan_t p, int option, int64_t value) {
     case DG_OPT_COPY_STREAMS:
       if (value < 1 || value > 8) return fail(DG_ERR_ARG, "copy streams must be 1..8");
       p->copy_streams = (int)value;
+      return DG_OK;
+    case DG_OPT_RS_CE_PARTIALS:
+      if (value != 0 && value != 1) return fail(DG_ERR_ARG, "RS copy-engine hand-off must be 0 or 1");
+      if (p->epoch != 0) return fail(DG_ERR_STATE, "the hand-off is fixed after the first run");
+      if (value == 1) {
+        if (is_ag(p->schedule) || p->tp < 2)
+          return fail(DG_ERR_UNSUPPORTED, "copy-engine hand-off is for RS plans with tp > 1");
+        if (p->schedule == DG_RS_TILING_B_ROTATING_C && (p->n / p->tp) % 8)
+          return fail(DG_ERR_UNSUPPORTED, "copy-engine hand-off needs N/tp %% 8 == 0");
+        p->epi = 1;  // the hand-off runs through the staged epilogue
+      }
+      p->cep = value == 1;
+      layout(p);
       return DG_OK;
     case DG_OPT_WAVE_SYNC:
       if (value < -1 || value > 1) return fail(DG_ERR_ARG, "wave sync must be -1 (auto), 0 or 1");
@@ -770,6 +896,8 @@ int dg_run(dg_plan_t p, const void* A, const void* B, const dg_bf16_t* C, dg_bf1
   }
   kp.n_maps = p->n_maps;
   kp.l2_hint = p->l2_hint;
+  kp.done = reinterpret_cast<uint32_t*>(ws + p->off_done);
+  kp.S = reinterpret_cast<float*>(ws + p->off_send);
   kp.wave_sync = wave_sync_on(p) ? 1u : 0u;
   kp.wave_ctr = reinterpret_cast<uint32_t*>(ws + p->off_status + 64);
   if (kp.wave_sync) DG_CUDA(cudaMemsetAsync(ws + p->off_status + 64, 0, 4, ms));
@@ -777,6 +905,11 @@ int dg_run(dg_plan_t p, const void* A, const void* B, const dg_bf16_t* C, dg_bf1
   kp.hang_ns = kp.timeout_ns * 4 + 1000000000ull;
 
   if (rs_serial) return run_rs_serial(p, drv, C, D, ws, ms);
+  if (!is_ag(p->schedule) && p->tp > 1 && p->cep) {
+    if (cs == ms || cs == nullptr)
+      return fail(DG_ERR_ARG, "copy-engine hand-off needs a copy stream distinct from the main stream");
+    return run_rs_ce(p, drv, ws, ms, cs);
+  }
   if (is_ag(p->schedule) && p->tp > 1) {
     int mode = p->mode;
     if (mode == DG_MODE_FUSED && (cs == ms || cs == nullptr)) mode = DG_MODE_SERIAL;

@@ -51,6 +51,7 @@ struct Geom {
   int64_t chunk_tiles;      // AG: tiles of the rotated dim per transfer chunk
   int64_t nchunks;          // AG: chunks per shard
   int32_t beta_nonzero;
+  int32_t ce_partials;  // RS: partials handed on by copy-engine transfers between rank buffers
 };
 
 struct Tile {
@@ -63,6 +64,11 @@ struct Tile {
   int64_t flag;       // AG chunk flag, -1 if local
   int64_t tile_flag;  // RS tile flag, -1 if none
   int32_t src, dst;
+  // RS with copy-engine hand-off: position in the rank's send / receive buffers
+  int32_t band;       // tile row (m-tile) inside the slab
+  int64_t xs_row;     // first row in the send buffer (rank-major, slab-local rows)
+  int64_t xr_row;     // first row in the receive buffer of this step (double-buffered)
+  int64_t x_col;      // first column inside the slab
 };
 
 DG_HD int64_t dg_min64(int64_t a, int64_t b) { return a < b ? a : b; }
@@ -97,6 +103,8 @@ DG_HD Tile decode_tile(const Geom& g, int64_t t) {
   o.k_blocks = (int32_t)cdiv(g.Ks, g.BK);
   o.flag = -1;
   o.tile_flag = -1;
+  o.band = 0;
+  o.xs_row = o.xr_row = o.x_col = 0;
   const int64_t mrow = mt * g.BM;  // inside the block
   const int64_t ncol = nt * g.BN;
   o.rows_valid = (int32_t)dg_min64(g.BM, g.blk_m - mrow);
@@ -158,7 +166,11 @@ DG_HD Tile decode_tile(const Geom& g, int64_t t) {
     o.b_row = l * g.N + o.out_col;
     const int64_t tiles_slab = g.tiles_m * g.tiles_n;
     const int64_t tf = ((l * P + j) * tiles_slab) + mt * g.tiles_n + nt;
-    o.tile_flag = P > 1 ? tf : -1;
+    o.tile_flag = P > 1 && !g.ce_partials ? tf : -1;
+    o.band = (int32_t)mt;
+    o.x_col = ncol;
+    o.xs_row = (r * g.L + l) * g.blk_m + mrow;
+    o.xr_row = ((2 * r + (s & 1)) * g.L + l) * g.blk_m + mrow;
     o.src = s == 0 ? (g.beta_nonzero ? SRC_C : SRC_NONE) : SRC_X;
     o.dst = s == P - 1 ? DST_D : DST_X;
   }

@@ -89,6 +89,11 @@ struct KParams {
   // staged epilogue: fp32 partial (box 32 x 128, 128B swizzle), bf16 C and D
   // (box 32 x 128, 64B swizzle)
   CUtensorMap tmX, tmC, tmD;
+  // RS with copy-engine hand-off: rank send buffers and (double-buffered)
+  // receive buffers, fp32, slab-local rows and columns
+  CUtensorMap tmS, tmR;
+  uint32_t* done;       // per (rank, step, batch, band): half-tiles written to the send buffer
+  float* S;             // send buffers (plain-store address of tmS)
   Geom g;
   const __nv_bfloat16* C;
   __nv_bfloat16* D;
@@ -557,17 +562,16 @@ __device__ __forceinline__ void epilogue_row_chunk(const KParams& p, const Tile&
   }
 }
 
-// Masked direct store of 32 consecutive results of one output row.
+// Masked direct store of 32 consecutive results of one output row (D at
+// (grow, gcol); the partial at `x`).
 __device__ __forceinline__ void store_row_chunk(const KParams& p, const Tile& tl, int64_t grow,
-                                                int64_t gcol, int ncols, const float (&out)[32]) {
-  const int64_t e0 = grow * p.g.N + gcol;
+                                                int64_t gcol, int ncols, const float (&out)[32], float* x) {
   if (tl.dst == DST_D) {
-    __nv_bfloat16* d = p.D + e0;
+    __nv_bfloat16* d = p.D + grow * p.g.N + gcol;
 #pragma unroll
     for (int i = 0; i < 32; ++i)
       if (i < ncols) d[i] = __float2bfloat16_rn(out[i]);
   } else {
-    float* x = p.X + e0;
 #pragma unroll
     for (int i = 0; i < 32; ++i)
       if (i < ncols) __stcg(x + i, out[i]);
@@ -631,14 +635,19 @@ __device__ __forceinline__ void release_partial(const KParams& p, int64_t flag, 
   st_release_u32(p.flags + flag, val);
 }
 
-// TMA load of source chunk c of a tile half into staging buffer (idx & 1).
+// TMA load of source chunk c of a tile half into staging buffer (idx & 1):
+// the rotating partial (fp32, map `xmap` at column x_col0 / row x_row0) or
+// beta*C (bf16, at the tile's output position).
 __device__ __forceinline__ void staged_load_src(const KParams& p, const Tile& tl, int64_t row0, int c,
-                                                uint32_t idx, uint32_t sbase, uint32_t bar_xfull) {
+                                                uint32_t idx, uint32_t sbase, uint32_t bar_xfull,
+                                                const CUtensorMap* xmap, int64_t x_col0, int64_t x_row0) {
   const uint32_t sb = idx & 1;
   const bool f32 = tl.src == SRC_X;
   mbar_arrive_expect_tx(bar_xfull + 8 * sb, f32 ? XBUF : XBUF / 2);
-  tma_load_2d(sbase + sb * XBUF, f32 ? &p.tmX : &p.tmC, bar_xfull + 8 * sb,
-              (int32_t)(tl.out_col + c * XCOLS), (int32_t)row0);
+  if (f32)
+    tma_load_2d(sbase + sb * XBUF, xmap, bar_xfull + 8 * sb, (int32_t)(x_col0 + c * XCOLS), (int32_t)x_row0);
+  else
+    tma_load_2d(sbase + sb * XBUF, &p.tmC, bar_xfull + 8 * sb, (int32_t)(tl.out_col + c * XCOLS), (int32_t)row0);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -886,7 +895,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
       // Staged tiles need 16-byte aligned TMA column coordinates (8 bf16).
       const bool staged = EPI == 1 && (tl.out_col & 7) == 0;
       const bool has_src = staged && tl.src != SRC_NONE;
+      // Where the rotating partial is read and written: the shared partial X
+      // (in-place hand-off), or, with copy-engine hand-off, this rank's receive
+      // and send buffers.
+      const bool cep = p.g.ce_partials != 0;
+      const CUtensorMap* src_map = cep ? &p.tmR : &p.tmX;
+      const CUtensorMap* xdst_map = cep ? &p.tmS : &p.tmX;
+      const int64_t src_col0 = cep ? tl.x_col : tl.out_col;
+      const int64_t src_row0 = cep ? tl.xr_row + (int64_t)crank * ROWS_PER_CTA : row0;
+      const int64_t xd_col0 = cep ? tl.x_col : tl.out_col;
+      const int64_t xd_row0 = cep ? tl.xs_row + (int64_t)crank * ROWS_PER_CTA : row0;
+      const int64_t xd_pitch = cep ? p.g.blk_n : p.g.N;
       if (et == 0) {
+        if (cep && tl.s > 0) {
+          const int64_t P = p.g.P;
+          // the partial this step adds to has arrived in this rank's receive buffer
+          const int64_t fsrc = ((tl.r * P + tl.s) * p.g.L + tl.l) * p.g.tiles_m + tl.band;
+          wait_flag_geq(p, p.flags + fsrc, p.epoch, (uint32_t)fsrc);
+          if (tl.dst == DST_X) {
+            // the send buffer's previous contents have been copied out
+            const int64_t fsnd = ((((tl.r + P - 1) % P) * P + tl.s) * p.g.L + tl.l) * p.g.tiles_m + tl.band;
+            wait_flag_geq(p, p.flags + fsnd, p.epoch, (uint32_t)fsnd);
+          }
+        }
         const bool need_flag = tflag >= 0 && tl.s > 0;
         const uint32_t want = p.epoch * (uint32_t)p.g.P + (uint32_t)tl.s - 1;
         // Never hold a deferred hand-off while waiting for one: a ring of CTAs
@@ -905,7 +936,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           // the source needs only the previous step: load it while the MMAs run
           fence_proxy_async_global();
           for (int c = 0; c < nch && c < 2; ++c)
-            staged_load_src(p, tl, row0, c, nload + c, xsrc_addr, bar_xfull);
+            staged_load_src(p, tl, row0, c, nload + c, xsrc_addr, bar_xfull, src_map, src_col0, src_row0);
         }
         bool go = mbar_wait(p, bar_tfull + 8 * buf, use & 1, 0x400000u | buf);
         if (pend_flag >= 0) {  // the previous tile's bulk stores have long completed
@@ -976,18 +1007,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           fence_proxy_async_smem();
           named_bar_sync(1, EPI_THREADS);  // barrier B: the chunk is complete in shared memory
           if (et == 0) {
-            tma_store_2d(tl.dst == DST_X ? &p.tmX : &p.tmD, xdst_addr + db * XBUF,
-                         (int32_t)(tl.out_col + c * XCOLS), (int32_t)row0);
+            if (tl.dst == DST_X)
+              tma_store_2d(xdst_map, xdst_addr + db * XBUF, (int32_t)(xd_col0 + c * XCOLS), (int32_t)xd_row0);
+            else
+              tma_store_2d(&p.tmD, xdst_addr + db * XBUF, (int32_t)(tl.out_col + c * XCOLS), (int32_t)row0);
             bulk_commit();
           }
           ++nstore;
         } else if (row_ok) {
-          store_row_chunk(p, tl, grow, tl.out_col + c * XCOLS, ncols, out);
+          float* xp = nullptr;  // the partial's plain-store address (send buffer or X)
+          if (tl.dst == DST_X) xp = (cep ? p.S : p.X) + (xd_row0 + row) * xd_pitch + xd_col0 + c * XCOLS;
+          store_row_chunk(p, tl, grow, tl.out_col + c * XCOLS, ncols, out, xp);
         }
         if (et == 0 && has_src && c + 2 < nch)
-          staged_load_src(p, tl, row0, c + 2, nload + c + 2, xsrc_addr, bar_xfull);
+          staged_load_src(p, tl, row0, c + 2, nload + c + 2, xsrc_addr, bar_xfull, src_map, src_col0, src_row0);
       }
       if (has_src) nload += (uint32_t)nch;
+      if (cep && tl.dst == DST_X) {
+        // count this half tile as written to the send buffer: its bulk and
+        // plain stores complete and fenced first (the copy stream waits on it)
+        if (et == 0) bulk_wait<0>();
+        __threadfence();
+        named_bar_sync(1, EPI_THREADS);
+        if (et == 0) {
+          fence_proxy_async_global();
+          __threadfence();
+          const int64_t fd = ((tl.r * p.g.P + tl.s) * p.g.L + tl.l) * p.g.tiles_m + tl.band;
+          atomicAdd(p.done + fd, 1u);
+        }
+      }
       if (tflag >= 0 && tl.dst == DST_X) {
         const uint32_t val = p.epoch * (uint32_t)p.g.P + (uint32_t)tl.s;
         // every chunk left by TMA store (issued by thread 0 alone)?

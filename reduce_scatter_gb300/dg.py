@@ -56,6 +56,7 @@ OPT_CTA_GROUP = 6
 OPT_EPILOGUE = 7
 OPT_L2_HINT = 8
 OPT_WAVE_SYNC = 9
+OPT_RS_CE_PARTIALS = 10
 
 # Every symbol include/dg.h declares.
 EXPORTS = ("dg_plan", "dg_workspace_bytes", "dg_run_mode", "dg_set_option", "dg_run", "dg_check",

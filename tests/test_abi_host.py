@@ -235,3 +235,21 @@ def test_scaled_plan_rules(L):
     assert p.tile(0)["k_blocks"] == 5                        # 128 fp8 elements per K block
     pb = dg.Plan(1024, 1024, 640, 1, 4, dg.AG_ROTATING_A).info()
     assert pb["elem_bytes"] == 2 and pb["slot_bytes"] == 2 * info["slot_bytes"]
+
+
+def test_ce_handoff_option_rules(L):
+    p = dg.Plan(512, 512, 512, 1, 2, dg.AG_ROTATING_A)
+    with pytest.raises(dg.DGError):
+        p.set_option(dg.OPT_RS_CE_PARTIALS, 1)          # AG plan
+    p = dg.Plan(512, 1000, 512, 1, 8, dg.RS_TILING_B_ROTATING_C)
+    with pytest.raises(dg.DGError):
+        p.set_option(dg.OPT_RS_CE_PARTIALS, 1)          # N/tp = 125, not a multiple of 8
+    q = dg.Plan(2048, 1024, 1024, 2, 4, dg.RS_TILING_A_ROTATING_C)
+    before = q.workspace_bytes()
+    q.set_option(dg.OPT_RS_CE_PARTIALS, 1)
+    info = q.info()
+    slab = 2 * (2048 // 4) * 1024 * 4
+    assert info["ws_bytes"] >= 3 * 4 * slab // 1 and info["ws_bytes"] > before
+    assert info["n_flags"] == 4 * 4 * 2 * info["tiles_m"]
+    for t in range(info["total_tiles"]):
+        assert q.tile(t)["tile_flag"] == -1                # hand-offs go through the copy engine
