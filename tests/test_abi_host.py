@@ -253,3 +253,17 @@ def test_ce_handoff_option_rules(L):
     assert info["n_flags"] == 4 * 4 * 2 * info["tiles_m"]
     for t in range(info["total_tiles"]):
         assert q.tile(t)["tile_flag"] == -1                # hand-offs go through the copy engine
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_tile_order_simulator_random(L, i):
+    rng = np.random.default_rng(500 + i)
+    sched = int(rng.integers(0, 4))
+    tp = int(rng.choice([1, 2, 4, 8]))
+    l = int(rng.integers(1, 3))
+    m = int(rng.integers(1, 6)) * 8 * tp
+    n = int(rng.integers(1, 9)) * 8 * tp
+    k = int(rng.integers(1, 5)) * 64 * tp
+    plan = dg.Plan(m, n, k, l, tp, sched, 1.0, 0.5 if rng.integers(0, 2) else 0.0)
+    plan.set_option(dg.OPT_CTA_GROUP, int(rng.integers(1, 3)))
+    _simulate(plan, m, n, k, l, tp, sched)

@@ -1,0 +1,59 @@
+"""A seeded random sweep over the configuration space against the CPU oracle:
+schedule, TP, tile configuration, epilogue, input type, RS hand-off, batch,
+alpha / beta / scales and ragged shapes (within the shape rules)."""
+
+import numpy as np
+import pytest
+
+from reduce_scatter_gb300 import dg
+from tests.gpu_common import (TOL, Runner, host_inputs, host_inputs_fp8, oracle_fp8, oracle_full, rel_err, to_dev,
+                              to_dev_u8)
+
+pytestmark = pytest.mark.gpu
+
+TYPES = [("bf16", "bf16"), ("e4m3", "e4m3"), ("e5m2", "e5m2"), ("e4m3", "e5m2")]
+TCODE = {"bf16": dg.TYPE_BF16, "e4m3": dg.TYPE_E4M3, "e5m2": dg.TYPE_E5M2}
+
+
+def _case(i):
+    rng = np.random.default_rng(1000 + i)
+    sched = int(rng.integers(0, 4))
+    tp = int(rng.choice([1, 2, 4, 8]))
+    ta, tb = TYPES[int(rng.integers(0, len(TYPES)))]
+    kq = 8 if ta == "bf16" else 16                     # K granule (16-byte rows)
+    l = int(rng.integers(1, 4))
+    m = int(rng.integers(1, 9)) * 8 * tp if sched in (0, 1, 2) else int(rng.integers(8, 700))
+    n = int(rng.integers(1, 13)) * 8 * (tp if sched != 2 else 1)
+    if sched >= 2:
+        k = int(rng.integers(1, 7)) * kq * tp
+    else:
+        k = int(rng.integers(1, 50)) * kq
+    if sched == 3 and (n // tp) % 8:
+        n = 8 * tp * max(1, n // (8 * tp))
+    cep = sched >= 2 and tp > 1 and (sched == 2 or (n // tp) % 8 == 0) and bool(rng.integers(0, 2))
+    opts = {dg.OPT_CTA_GROUP: int(rng.integers(1, 3)), dg.OPT_EPILOGUE: 1 if cep else int(rng.integers(0, 2))}
+    if cep:
+        opts[dg.OPT_RS_CE_PARTIALS] = 1
+    alpha = float(rng.choice([1.0, 0.5, -1.25]))
+    beta = float(rng.choice([0.0, 1.0, 0.75]))
+    sa, sb = (1.0, 1.0) if ta == "bf16" else (float(rng.choice([1.0, 0.5])), float(rng.choice([1.0, 0.03125])))
+    return sched, tp, m, n, k, l, ta, tb, alpha, beta, sa, sb, opts
+
+
+@pytest.mark.parametrize("i", range(48))
+def test_random_configuration(i):
+    sched, tp, m, n, k, l, ta, tb, alpha, beta, sa, sb, opts = _case(i)
+    if ta == "bf16":
+        a, b, c = host_inputs(m, n, k, l, seed=2000 + i)
+        A, B = to_dev(a), to_dev(b)
+        want = oracle_full(a, b, c, alpha, beta)
+    else:
+        a, b, c = host_inputs_fp8(m, n, k, l, seed=2000 + i, fmt_a=ta, fmt_b=tb)
+        A, B = to_dev_u8(a), to_dev_u8(b)
+        want = oracle_fp8(a, b, c, ta, tb, alpha, beta, sa, sb)
+    C = to_dev(c)
+    r = Runner(m, n, k, l, tp, sched, alpha, beta, options=opts, a_type=TCODE[ta], b_type=TCODE[tb],
+               scale_a=sa, scale_b=sb)
+    D, _ = r.run(A, B, C if beta else None)
+    err = rel_err(D, want)
+    assert err <= TOL, (err, sched, tp, m, n, k, l, ta, tb, opts)
