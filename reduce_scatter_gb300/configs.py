@@ -13,6 +13,8 @@ the pages' benchmarks, as synthetic inputs.
   TP=4, 8192 x 53248 x 8192, L=2, alpha=0.5, beta=1, C N(0,1).
 * ``rs_b_tp4_quarter``: rs_b_tp4_batched with N / 4 and L = 1, for profiler
   captures.
+* ``ag_a_tp8_pr_small``: ag_a_tp8_pr with M / 2 and N / 8, for profiler
+  captures of the headline kernel.
 * ``ag_a_tp8_pr_e4m3`` / ``rs_a_tp8_e4m3``: the TP=8 problems with e4m3
   operands (the scaled variant): both drawn N(0,1) and rounded to e4m3, the
   weight's 0.02 standard deviation carried by scale_b.
@@ -74,6 +76,9 @@ WORKLOADS = {
                  dist_b=N002, dist_c=N1),
         Workload("rs_b_tp4_batched", 3, 4, 8192, 53248, 8192, l=2, alpha=0.5, beta=1.0, dist_a=N1,
                  dist_b=N002, dist_c=N1),
+        # ag_a_tp8_pr with M / 2 and N / 8: the same full-K (16384) tiles and wave regime,
+        # about 2.6 GB on the device, for full profiler captures
+        Workload("ag_a_tp8_pr_small", 0, 8, 8192, 13312, 16384, dist_a=N1, dist_b=N002),
         # fp8 versions of the TP=8 workloads: e4m3 operands drawn N(0,1), the weight's
         # N(0,0.02) scale carried by the per-tensor scale_b
         Workload("ag_a_tp8_pr_e4m3", 0, 8, 16384, 106496, 16384, dist_a=N1, dist_b=N1, in_type="e4m3",
