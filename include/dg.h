@@ -116,9 +116,10 @@ enum dg_option {
                                  256 x 256 tiles on an SM pair (tcgen05 cta_group::2),
                                  1 = 128 x 256 tiles on one SM */
   DG_OPT_EPILOGUE = 7,        /* epilogue, before the first run: 1 = source and result
-                                 chunks staged in shared memory and moved by TMA (default
-                                 for the RS schedules), 0 = direct per-row global accesses
-                                 (default for the AG schedules, one more operand stage) */
+                                 chunks staged in shared memory and moved by TMA (default for
+                                 the RS schedules, fp8 inputs and K >= 16384), 0 = direct
+                                 per-row global accesses (one more operand stage; default for
+                                 bf16 AG plans with K < 16384) */
   DG_OPT_L2_HINT = 8,         /* L2 eviction policy of the operand loads: bits 0-1 for A,
                                  bits 2-3 for B; 0 = none, 1 = evict first, 2 = evict last */
   DG_OPT_RS_CE_PARTIALS = 10, /* RS plans with tp > 1, before the first run: 1 = hand the

@@ -693,7 +693,9 @@ int dg_plan_scaled(dg_plan_t* out, int64_t m, int64_t n, int64_t k, int64_t l, i
   p->alpha = alpha, p->beta = beta;
   p->a_type = a_type, p->b_type = b_type, p->esz = esz;
   p->scale_a = scale_a, p->scale_b = scale_b;
-  p->epi = is_ag(schedule) ? 0 : 1;
+  // staged epilogue by default for RS, for fp8 and for long K (where a tile's
+  // mainloop is long and one fewer operand stage costs least); direct otherwise
+  p->epi = (!is_ag(schedule) || esz == 1 || k >= 16384) ? 1 : 0;
   {
     std::lock_guard<std::mutex> lk(g_ws_mu);
     p->id = g_next_plan_id++;
