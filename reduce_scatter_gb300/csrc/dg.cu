@@ -222,6 +222,7 @@ int layout(dg_plan_s* p) {
   // RS SERIAL baseline geometry: every rank's full M x N partial over its K-slab
   p->gser = g;
   p->gser.sched = dg::SCHED_PARTIAL;
+  p->gser.ce_partials = 0;  // the baseline writes its own partial buffers, no hand-off
   p->gser.blk_m = p->m;
   p->gser.blk_n = p->n;
   p->gser.tiles_m = dg::cdiv(p->m, g.BM);

@@ -79,3 +79,19 @@ def test_ce_handoff_needs_a_separate_copy_stream():
     A = torch.zeros((512, 512), dtype=torch.bfloat16, device="cuda")
     s = torch.cuda.current_stream()
     assert p.run(A, A, None, torch.empty_like(A), ws, s, s, raise_on_error=False) == dg.ERR_ARG
+
+
+@pytest.mark.parametrize("sched", RS, ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_serial_baseline_unaffected_by_ce_option(sched):
+    m, n, k, l, tp = 1024, 1024, 1024, 1, 4
+    a, b, c = host_inputs(m, n, k, l, seed=112)
+    A, B, C = to_dev(a), to_dev(b), to_dev(c)
+    plan = dg.Plan(m, n, k, l, tp, sched, 0.5, 1.0)
+    plan.set_option(dg.OPT_RS_CE_PARTIALS, 1)
+    plan.set_mode(dg.MODE_SERIAL)
+    ws = torch.zeros(plan.workspace_bytes(), dtype=torch.uint8, device="cuda")
+    D = torch.full((l, m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+    main = torch.cuda.current_stream()
+    plan.run(A, B, C, D, ws, main, main)
+    plan.check(ws, main)
+    assert rel_err(D, oracle_full(a, b, c, 0.5, 1.0)) <= TOL
