@@ -1060,8 +1060,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
     if (EPI == 1 && et == 0) bulk_wait<0>();  // no bulk store may outlive the CTA
   }
 
-  if (CG == 2 && aborted) {
-    // let loads and MMAs still in flight for this pair land before exit
+  if (aborted) {
+    // let loads (operand stages, staged epilogue sources) and MMAs still in
+    // flight for this CTA or pair land before exit
     const uint64_t t0 = globaltimer();
     while (globaltimer() - t0 < 20000000ull) {
     }
