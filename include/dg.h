@@ -103,7 +103,7 @@ enum dg_status {
 /* Options for dg_set_option. */
 enum dg_option {
   DG_OPT_TIMEOUT_MS = 0,      /* ready-flag wait limit, ms (default 2000) */
-  DG_OPT_CHUNK_TILES = 1,     /* tiles per shard transfer chunk (0 = auto, >= 2 MiB) */
+  DG_OPT_CHUNK_TILES = 1,     /* tiles per shard transfer chunk (0 = auto, >= 16 MiB) */
   DG_OPT_FAULT_SKIP_FLAG = 2, /* test hook: drop the ready-flag write with this
                                  enqueue index (-1 = none, default) */
   DG_OPT_FAULT_DELAY_MS = 3,  /* test hook: hold the copy stream this long
