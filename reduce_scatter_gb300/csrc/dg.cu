@@ -127,7 +127,7 @@ struct dg_plan_s {
   int cg = 2;  // CTA group of the tile config: 1 = 128 x 256 per SM, 2 = 256 x 256 per SM pair
   bool cep = false;  // RS: hand partials on by copy-engine transfers (DG_OPT_RS_CE_PARTIALS)
   size_t off_done = 0, off_send = 0, off_recv = 0;
-  int epi = 0;  // epilogue: 0 direct, 1 staged through shared memory with TMA (default for RS)
+  int epi = 0;  // epilogue: 0 direct, 1 staged through shared memory with TMA (default: RS, fp8, K >= 16384)
   uint32_t l2_hint = 0;  // L2 policy of operand loads (DG_OPT_L2_HINT)
   int wave_sync = -1;  // DG_OPT_WAVE_SYNC: -1 auto, 0 off, 1 on
   uint64_t id = 0;
