@@ -21,7 +21,9 @@ convention; the pages are silent), so NaNs in C do not reach D.
 
 Parity status: pinned (tests/test_oracle_pins.py: brute-force triple loop,
 closed forms, the statistical mean printed on the all_gather+matmul blog
-page, schedule invariance).
+page, schedule invariance; ``fused_gemm``: a loop-by-loop restatement of the
+torch module's per-rank composition, closed forms, schedule invariance with
+a bias and both reduce ops).
 """
 
 from __future__ import annotations
@@ -115,5 +117,50 @@ def scaled_gemm(A, B_nk, C, alpha: float, beta: float, scale_a: float, scale_b: 
     B_nk = np.asarray(B_nk, dtype=np.float64)
     D = (np.float64(alpha) * np.float64(scale_a) * np.float64(scale_b)) * np.matmul(A, np.swapaxes(B_nk, 1, 2))
     if beta != 0.0:
+        D = D + np.float64(beta) * np.asarray(C, dtype=np.float64)
+    return D
+
+
+# ------------------------------------------------- bias and the reduce op
+#
+# The scaled fused ops of torch/distributed/_symmetric_memory/__init__.py take
+# a per-column ``bias`` that aten._scaled_mm adds to every rank's product, and
+# fused_matmul_reduce_scatter reduces the ranks' products with ``reduce_op``
+# "sum" (torch.sum over ranks) or "avg" (torch.mean over ranks).  Their
+# reference compositions (_fused_all_gather_scaled_matmul_fallback and
+# _fused_scaled_matmul_reduce_scatter_fallback: one _scaled_mm per rank, then
+# all-gather / reduce_scatter_tensor) fix what the result is.  In the
+# reduce-scatter ops every rank adds the bias before the reduction; the ranks'
+# K-slabs partition K, so sum_r A_r B_r = A B and
+#
+#   all-gather:            D = alpha A B + bias + beta C
+#   reduce-scatter, sum:   D = alpha A B + P bias + beta C
+#   reduce-scatter, avg:   D = (alpha A B + P bias) / P + beta C
+#
+# beta C belongs to the CUTLASS problem (``--beta``), not to the torch ops; it
+# enters once, after the reduction.
+
+
+def fused_gemm(A, B_nk, C, alpha: float, beta: float, *, P: int = 1, reduce_op=None,
+               bias=None) -> np.ndarray:
+    """The fused op's result in fp64, from its composition above.
+
+    ``reduce_op`` None for the all-gather ops, "sum" or "avg" for the
+    reduce-scatter ops over ``P`` ranks; ``bias`` None or an (N,) vector added
+    to each output row of every rank's product.  A, B_nk, C as in ``gemm``.
+    """
+    if reduce_op not in (None, "sum", "avg"):
+        raise ValueError(f"reduce_op must be None, 'sum' or 'avg', got {reduce_op!r}")
+    A = np.asarray(A, dtype=np.float64)
+    B_nk = np.asarray(B_nk, dtype=np.float64)
+    D = np.float64(alpha) * np.matmul(A, np.swapaxes(B_nk, 1, 2))
+    if bias is not None:
+        copies = 1 if reduce_op is None else P
+        D = D + np.float64(copies) * np.asarray(bias, dtype=np.float64)
+    if reduce_op == "avg":
+        D = D / np.float64(P)
+    if beta != 0.0:
+        if C is None:
+            raise ValueError("beta != 0 needs C")
         D = D + np.float64(beta) * np.asarray(C, dtype=np.float64)
     return D

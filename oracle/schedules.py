@@ -101,18 +101,26 @@ def step_blocks(schedule: str, m: int, n: int, k: int, P: int, r: int, s: int) -
 
 
 def run_schedule(schedule: str, A: np.ndarray, B_nk: np.ndarray, C, alpha: float,
-                 beta: float, P: int) -> np.ndarray:
+                 beta: float, P: int, *, bias=None, reduce_op: str = "sum") -> np.ndarray:
     """D assembled from what every virtual rank computes at every step (fp64).
 
     For the RS schedules the partial X_j is carried from step to step exactly
     as the rotation prescribes; D receives X_j from the step that ends on the
-    slab's owner.
+    slab's owner.  ``bias`` (N,), if given, enters every block a rank
+    computes (each rank's product carries it, as aten._scaled_mm adds it in
+    the torch module's compositions); ``reduce_op`` "avg" weighs each rank's
+    contribution to a rotating partial by 1/P, so the finished partial is
+    the mean over ranks (torch.mean in ``_fused_matmul_reduce_scatter_impl``),
+    beta C still entering once.
     """
+    if reduce_op not in ("sum", "avg"):
+        raise ValueError(f"reduce_op must be 'sum' or 'avg', got {reduce_op!r}")
     A = np.asarray(A, np.float64)
     B_nk = np.asarray(B_nk, np.float64)
     L, m, k = A.shape
     n = B_nk.shape[1]
     Cf = None if C is None else np.asarray(C, np.float64)
+    bv = None if bias is None else np.asarray(bias, np.float64)
     D = np.full((L, m, n), np.nan)
     if schedule in (AG_ROTATING_A, AG_ROTATING_B):
         for s in range(P):
@@ -120,11 +128,14 @@ def run_schedule(schedule: str, A: np.ndarray, B_nk: np.ndarray, C, alpha: float
                 b = step_blocks(schedule, m, n, k, P, r, s)
                 rows, cols = b["rows"], b["cols"]
                 blk = np.float64(alpha) * np.matmul(A[:, rows, :], np.swapaxes(B_nk[:, cols, :], 1, 2))
+                if bv is not None:
+                    blk = blk + bv[cols]
                 if beta != 0.0:
                     blk = blk + np.float64(beta) * Cf[:, rows, cols]
                 D[:, rows, cols] = blk
         return D
     # ReduceScatter: one rotating partial per output slab.
+    weight = np.float64(1.0) if reduce_op == "sum" else np.float64(1.0) / np.float64(P)
     X = {}
     for s in range(P):
         for r in range(P):
@@ -132,6 +143,9 @@ def run_schedule(schedule: str, A: np.ndarray, B_nk: np.ndarray, C, alpha: float
             b = step_blocks(schedule, m, n, k, P, r, s)
             rows, cols, ks = b["rows"], b["cols"], b["k"]
             part = np.float64(alpha) * np.matmul(A[:, rows, ks], np.swapaxes(B_nk[:, cols, ks], 1, 2))
+            if bv is not None:
+                part = part + bv[cols]
+            part = weight * part
             if s == 0:
                 src = np.float64(beta) * Cf[:, rows, cols] if beta != 0.0 else 0.0
             else:

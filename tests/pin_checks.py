@@ -211,3 +211,99 @@ def check_printed_local_sizes(local_problem, schedule_ag_a):
 
 def all_shapes():
     return list(itertools.product([1, 2], [1, 3], [2, 5]))
+
+
+# ------------------------------------------------ bias and reduce-op pins
+
+
+def brute_fused(A, B_nk, C, alpha, beta, P, reduce_op, bias):
+    """The torch module's composition by loops, written apart from the oracle:
+    each rank r takes the product over its own K-slab (all of K for the
+    all-gather ops, reduce_op None), scales it by alpha and adds the bias (one
+    aten._scaled_mm per rank); the ranks' results are summed or averaged;
+    beta * C enters once."""
+    L, M, K = A.shape
+    N = B_nk.shape[1]
+    ranks = 1 if reduce_op is None else P
+    w = K // ranks
+    D = np.zeros((L, M, N))
+    for l in range(L):
+        for i in range(M):
+            for j in range(N):
+                total = 0.0
+                for r in range(ranks):
+                    acc = 0.0
+                    for kk in range(r * w, (r + 1) * w):
+                        acc += float(A[l, i, kk]) * float(B_nk[l, j, kk])
+                    v = float(alpha) * acc
+                    if bias is not None:
+                        v += float(bias[j])
+                    total += v
+                if reduce_op == "avg":
+                    total /= P
+                if beta != 0.0:
+                    total += float(beta) * float(C[l, i, j])
+                D[l, i, j] = total
+    return D
+
+
+def check_bias_reduce_brute_force(fused_gemm):
+    """Integer-valued inputs, P a power of two: every result is exact."""
+    for idx, (L, M, N) in enumerate([(1, 3, 5), (2, 4, 3)]):
+        for P in (1, 2, 4):
+            K = 2 * P
+            A = _int_valued(40 + idx, 1, (L, M, K))
+            B = _int_valued(40 + idx, 2, (L, N, K))
+            C = _int_valued(40 + idx, 3, (L, M, N))
+            bias = _int_valued(40 + idx, 4, (N,))
+            for op in (None, "sum", "avg"):
+                for alpha, beta, bv in [(1.0, 0.0, bias), (0.5, 1.0, bias), (2.0, -0.5, None)]:
+                    got = fused_gemm(A, B, C, alpha, beta, P=P, reduce_op=op, bias=bv)
+                    want = brute_fused(A, B, C, alpha, beta, P, op, bv)
+                    assert np.array_equal(got, want), (L, M, N, P, op, alpha, beta, bv is None)
+
+
+def check_bias_reduce_closed_forms(fused_gemm):
+    L, M, N, K, P = 2, 3, 4, 8, 4
+    bias = _int_valued(50, 4, (N,))
+    C = _int_valued(50, 3, (L, M, N))
+    zeros_a = np.zeros((L, M, K))
+    B = _int_valued(50, 2, (L, N, K))
+    # A = 0: only the bias copies and beta * C remain
+    assert np.array_equal(fused_gemm(zeros_a, B, C, 1.0, 0.0, P=P, reduce_op=None, bias=bias),
+                          np.broadcast_to(bias, (L, M, N)))
+    assert np.array_equal(fused_gemm(zeros_a, B, C, 1.0, 0.5, P=P, reduce_op="sum", bias=bias),
+                          P * bias + 0.5 * C)
+    assert np.array_equal(fused_gemm(zeros_a, B, C, 1.0, 0.5, P=P, reduce_op="avg", bias=bias),
+                          bias + 0.5 * C)
+    # all-ones operands: alpha K plus the bias (AG), P bias (sum); avg is sum / P
+    ones_a, ones_b = np.ones((L, M, K)), np.ones((L, N, K))
+    assert np.array_equal(fused_gemm(ones_a, ones_b, None, 0.5, 0.0, P=P, reduce_op=None, bias=bias),
+                          np.broadcast_to(0.5 * K + bias, (L, M, N)))
+    s = fused_gemm(ones_a, ones_b, None, 0.5, 0.0, P=P, reduce_op="sum", bias=bias)
+    assert np.array_equal(s, np.broadcast_to(0.5 * K + P * bias, (L, M, N)))
+    assert np.array_equal(fused_gemm(ones_a, ones_b, None, 0.5, 0.0, P=P, reduce_op="avg", bias=bias), s / P)
+    # no bias and no reduction: the plain definition
+    A = _rand(51, 1, (L, M, K))
+    Br = _rand(51, 2, (L, N, K))
+    plain = np.float64(0.75) * np.matmul(A, np.swapaxes(Br, 1, 2)) + 1.5 * C
+    assert np.array_equal(fused_gemm(A, Br, C, 0.75, 1.5), plain)
+
+
+def check_schedule_bias_reduce(run_schedule, fused_gemm, schedules):
+    """Every schedule and TP, with a bias and both reduce ops, gives the
+    composition's result (exact on integer inputs)."""
+    for P in (1, 2, 4, 8):
+        L, M, N, K = 2, 2 * P, 3 * P, 4 * P
+        A = _int_valued(60 + P, 1, (L, M, K))
+        B = _int_valued(60 + P, 2, (L, N, K))
+        C = _int_valued(60 + P, 3, (L, M, N))
+        bias = _int_valued(60 + P, 4, (N,))
+        for sched in schedules[:2]:
+            got = run_schedule(sched, A, B, C, 0.5, 1.0, P, bias=bias)
+            assert np.array_equal(got, fused_gemm(A, B, C, 0.5, 1.0, P=P, reduce_op=None, bias=bias)), (sched, P)
+        for sched in schedules[2:]:
+            for op in ("sum", "avg"):
+                got = run_schedule(sched, A, B, C, 0.5, 1.0, P, bias=bias, reduce_op=op)
+                want = fused_gemm(A, B, C, 0.5, 1.0, P=P, reduce_op=op, bias=bias)
+                assert np.array_equal(got, want), (sched, P, op)

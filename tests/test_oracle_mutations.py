@@ -124,3 +124,56 @@ def test_scaled_gemm_mutant_caught():
         return og.scaled_gemm(A, B, C, alpha, beta, sa, 1.0)
     ones_a, ones_b = np.ones((1, 3, 64)), np.ones((1, 2, 64))
     assert not np.all(drops_scale_b(ones_a, ones_b, None, 1.0, 0.0, 3.0, 0.5) == 64 * 1.5)
+
+
+# ------------------------------------------------ bias and the reduce op
+
+def _fused_bias_once(A, B, C, alpha, beta, *, P=1, reduce_op=None, bias=None):
+    # the reduce-scatter bias added once instead of once per rank
+    return og.fused_gemm(A, B, C, alpha, beta, P=P, reduce_op=reduce_op, bias=None) + \
+        (0.0 if bias is None else (bias / P if reduce_op == "avg" else bias))
+
+
+def _fused_drops_bias(A, B, C, alpha, beta, *, P=1, reduce_op=None, bias=None):
+    return og.fused_gemm(A, B, C, alpha, beta, P=P, reduce_op=reduce_op, bias=None)
+
+
+def _fused_avg_divides_c(A, B, C, alpha, beta, *, P=1, reduce_op=None, bias=None):
+    D = og.fused_gemm(A, B, C, alpha, 0.0, P=P, reduce_op=reduce_op, bias=bias)
+    if beta != 0.0:
+        D = D + (beta * C / P if reduce_op == "avg" else beta * C)
+    return D
+
+
+def _fused_avg_ignored(A, B, C, alpha, beta, *, P=1, reduce_op=None, bias=None):
+    return og.fused_gemm(A, B, C, alpha, beta, P=P, reduce_op="sum" if reduce_op == "avg" else reduce_op,
+                         bias=bias)
+
+
+@pytest.mark.parametrize("mutant", [_fused_bias_once, _fused_drops_bias, _fused_avg_divides_c, _fused_avg_ignored],
+                         ids=lambda f: f.__name__)
+def test_fused_gemm_mutants_caught(mutant):
+    checks = [pc.check_bias_reduce_brute_force, pc.check_bias_reduce_closed_forms]
+    assert any(_fails(c, mutant) for c in checks)
+
+
+def _sched_bias_first_step_only(sched, A, B, C, alpha, beta, P, *, bias=None, reduce_op="sum"):
+    # the rotating partial picks up the bias at step 0 only
+    if sched in (osch.RS_TILING_A_ROTATING_C, osch.RS_TILING_B_ROTATING_C) and bias is not None:
+        D = osch.run_schedule(sched, A, B, C, alpha, beta, P, reduce_op=reduce_op)
+        return D + (bias / P if reduce_op == "avg" else bias)
+    return osch.run_schedule(sched, A, B, C, alpha, beta, P, bias=bias, reduce_op=reduce_op)
+
+
+def _sched_avg_weights_product_only(sched, A, B, C, alpha, beta, P, *, bias=None, reduce_op="sum"):
+    # avg divides the products but not the bias copies
+    if sched in (osch.RS_TILING_A_ROTATING_C, osch.RS_TILING_B_ROTATING_C) and reduce_op == "avg" and bias is not None:
+        D = osch.run_schedule(sched, A, B, C, alpha, beta, P, reduce_op="avg")
+        return D + P * bias
+    return osch.run_schedule(sched, A, B, C, alpha, beta, P, bias=bias, reduce_op=reduce_op)
+
+
+@pytest.mark.parametrize("mutant", [_sched_bias_first_step_only, _sched_avg_weights_product_only],
+                         ids=lambda f: f.__name__)
+def test_schedule_bias_mutants_caught(mutant):
+    assert _fails(pc.check_schedule_bias_reduce, mutant, og.fused_gemm, osch.SCHEDULES)

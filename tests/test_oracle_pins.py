@@ -96,3 +96,15 @@ def test_scaled_gemm_pins():
     # all ones: D = K * alpha * scale_a * scale_b
     ones_a, ones_b = np.ones((1, 3, 64)), np.ones((1, 2, 64))
     assert np.all(og.scaled_gemm(ones_a, ones_b, None, 1.0, 0.0, 3.0, 0.5) == 64 * 1.5)
+
+
+def test_bias_and_reduce_op_brute_force():
+    pc.check_bias_reduce_brute_force(og.fused_gemm)
+
+
+def test_bias_and_reduce_op_closed_forms():
+    pc.check_bias_reduce_closed_forms(og.fused_gemm)
+
+
+def test_every_schedule_with_bias_and_reduce_op():
+    pc.check_schedule_bias_reduce(osch.run_schedule, og.fused_gemm, osch.SCHEDULES)
