@@ -14,10 +14,11 @@
  * in rotation order, waiting on a shard's flag before it loads that shard.
  *
  * Layouts (the pages do not fix them):
- *   A  bf16, L x M x K, row-major (K innermost)
- *   B  bf16, stored transposed: L x N x K, row-major (K innermost)
+ *   A  bf16 (or fp8, dg_plan_scaled), L x M x K, row-major (K innermost)
+ *   B  bf16 (or fp8), stored transposed: L x N x K, row-major (K innermost)
  *   C  bf16, L x M x N, row-major (read only when beta != 0)
- *   D  bf16, L x M x N, row-major
+ *   D  bf16 (or fp32, DG_OPT_OUT_TYPE), L x M x N, row-major
+ *   bias  bf16, N values (dg_run_ex only; optional)
  * Every batch is densely packed after the previous one.  bf16 values are
  * passed as raw 16-bit patterns (dg_bf16_t).
  *
@@ -83,11 +84,20 @@ enum dg_schedule {
  * shards; the rotating partial lives in the workspace). */
 enum dg_mode { DG_MODE_FUSED = 0, DG_MODE_GEMM_ONLY = 1, DG_MODE_SERIAL = 2 };
 
-/* Input element types of A and B (C and D are always bf16).  fp8 follows the
- * OCP 8-bit formats: E4M3 is the variant without infinities (largest finite
- * 448), E5M2 the IEEE-like one (largest finite 57344); both are passed as raw
- * bytes. */
-enum dg_type { DG_TYPE_BF16 = 0, DG_TYPE_E4M3 = 1, DG_TYPE_E5M2 = 2 };
+/* Element types.  A and B: BF16, E4M3 or E5M2 (C and the bias are always
+ * bf16).  D: BF16 (default) or F32 (DG_OPT_OUT_TYPE), after the out_dtype
+ * argument of the scaled fused ops in torch/distributed/_symmetric_memory.
+ * fp8 follows the OCP 8-bit formats: E4M3 is the variant without infinities
+ * (largest finite 448), E5M2 the IEEE-like one (largest finite 57344); both
+ * are passed as raw bytes. */
+enum dg_type { DG_TYPE_BF16 = 0, DG_TYPE_E4M3 = 1, DG_TYPE_E5M2 = 2, DG_TYPE_F32 = 3 };
+
+/* How the RS schedules combine the ranks' products (reduce_op of
+ * fused_matmul_reduce_scatter in torch/distributed/_symmetric_memory: "sum"
+ * is torch.sum over ranks, "avg" torch.mean).  With AVG every rank's product
+ * and bias enter with weight 1/tp (exact, tp being a power of two); beta * C
+ * still enters once. */
+enum dg_reduce_op { DG_REDUCE_SUM = 0, DG_REDUCE_AVG = 1 };
 
 enum dg_status {
   DG_OK = 0,
@@ -129,12 +139,16 @@ enum dg_option {
                                  double-buffered receive buffer and publish a ready flag),
                                  0 (default) = the next rank reads the partial in place.
                                  Needs a copy stream distinct from the main stream. */
-  DG_OPT_WAVE_SYNC = 9        /* 1 = each CTA starts its i-th tile only after every CTA has
+  DG_OPT_WAVE_SYNC = 9,       /* 1 = each CTA starts its i-th tile only after every CTA has
                                  issued the loads of its (i-1)-th (keeps the CTAs that share
                                  an operand strip in phase for L2 reuse; one counter word
                                  memset on the main stream per run), 0 = off, -1 (default) =
                                  on for AG plans whose per-wave operand strips exceed about
                                  96 MiB */
+  DG_OPT_OUT_TYPE = 11,       /* element type of D: DG_TYPE_BF16 (default) or DG_TYPE_F32
+                                 (fp32 D runs through dg_run_ex) */
+  DG_OPT_REDUCE_OP = 12       /* RS plans: dg_reduce_op, DG_REDUCE_SUM (default) or
+                                 DG_REDUCE_AVG; AG plans accept only SUM */
 };
 
 /* Plan geometry and workspace layout, for callers and tests. */
@@ -153,6 +167,8 @@ typedef struct dg_plan_info {
   int64_t copies_per_run;            /* transfer enqueues per FUSED/SERIAL run */
   int32_t a_type, b_type;            /* dg_type of A and B */
   int32_t elem_bytes;                /* bytes per A / B element (2 bf16, 1 fp8) */
+  int32_t out_type;                  /* dg_type of D */
+  int32_t reduce_op;                 /* dg_reduce_op */
 } dg_plan_info;
 
 /* One tile of the step-major rotation order (host decoder, for tests). */
@@ -167,7 +183,7 @@ typedef struct dg_tile {
   int64_t flag;             /* AG ready-flag index (-1 = local shard) */
   int64_t tile_flag;        /* RS rotating-partial flag index (-1 = none) */
   int32_t src;              /* epilogue source: 0 none, 1 beta*C, 2 rotating partial */
-  int32_t dst;              /* 0 = D (bf16), 1 = rotating partial (fp32) */
+  int32_t dst;              /* 0 = D (the plan's output type), 1 = rotating partial (fp32) */
 } dg_tile;
 
 /* Validate a problem and build a plan.  Host only: no CUDA call is made, so
@@ -208,6 +224,25 @@ int dg_set_option(dg_plan_t plan, int option, int64_t value);
  * reported by dg_check. */
 int dg_run(dg_plan_t plan, const void* A, const void* B, const dg_bf16_t* C,
            dg_bf16_t* D, void* workspace, void* main_stream, void* copy_stream);
+
+/* dg_run with the epilogue extras of the scaled fused ops in
+ * torch/distributed/_symmetric_memory (fused_all_gather_scaled_matmul and
+ * fused_scaled_matmul_reduce_scatter pass bias and out_dtype to a scaled
+ * matmul on every rank):
+ *   bias  NULL, or N bf16 values (16-byte aligned) added to every row of
+ *         every rank's product.  The AG schedules therefore add it once; the
+ *         RS schedules once per rank before the reduction (tp copies with
+ *         DG_REDUCE_SUM, their mean -- one copy -- with DG_REDUCE_AVG), as
+ *         the module's reference composition (a scaled matmul with the bias
+ *         on each rank, then reduce_scatter_tensor) does.
+ *   D     elements of the plan's output type (DG_OPT_OUT_TYPE): bf16 or fp32.
+ * The epilogue computes fmaf(alpha', acc, src) + w * bias in fp32, with
+ * alpha' = alpha * scale_a * scale_b * w and w = 1 (or 1/tp for AVG), then
+ * rounds to D's type.  Everything else is as for dg_run, which is this call
+ * with bias = NULL on a bf16-output plan (dg_run refuses fp32-output plans
+ * with DG_ERR_STATE). */
+int dg_run_ex(dg_plan_t plan, const void* A, const void* B, const dg_bf16_t* C, const dg_bf16_t* bias,
+              void* D, void* workspace, void* main_stream, void* copy_stream);
 
 /* Synchronize `stream` and read the workspace status word of the plan's last
  * run: DG_OK, DG_ERR_TIMEOUT or DG_ERR_HANG (with the flag index in the

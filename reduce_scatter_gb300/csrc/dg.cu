@@ -118,6 +118,8 @@ struct dg_plan_s {
   int a_type = DG_TYPE_BF16, b_type = DG_TYPE_BF16;  // input element types
   int esz = 2;                                       // bytes per A / B element
   float scale_a = 1.f, scale_b = 1.f;                // per-tensor scales (scaled GEMM)
+  int out_type = DG_TYPE_BF16;                       // element type of D (DG_OPT_OUT_TYPE)
+  int reduce_op = DG_REDUCE_SUM;                     // RS: sum or mean over ranks (DG_OPT_REDUCE_OP)
   int mode = DG_MODE_FUSED;
   int64_t timeout_ms = 2000;
   int64_t chunk_tiles_req = 0;
@@ -372,7 +374,7 @@ int build_epi_maps(dg_plan_s* p, const Driver& drv, const void* C, void* D, uint
   std::memset(&p->kp.tmD, 0, sizeof(CUtensorMap));
   if (p->epi != 1) return DG_OK;
   const int64_t rows = p->l * p->m;
-  int rc = encode_epi_map(drv, &p->kp.tmD, D, false, p->n, rows);
+  int rc = encode_epi_map(drv, &p->kp.tmD, D, p->out_type == DG_TYPE_F32, p->n, rows);
   if (rc) return rc;
   if (C && p->beta != 0.f) {
     rc = encode_epi_map(drv, &p->kp.tmC, C, false, p->n, rows);
@@ -634,7 +636,7 @@ int run_rs_ce(dg_plan_s* p, const Driver& drv, uint8_t* ws, cudaStream_t ms, cud
 
 // Non-fused ReduceScatter baseline ("GEMM, then reduce"): one launch computes
 // every rank's full partial over its K-slab into its own fp32 buffer; a
-// separate kernel sums the partials, adds beta*C and writes bf16 D.
+// separate kernel sums the partials, adds beta*C and writes D.
 int run_rs_serial(dg_plan_s* p, const Driver& drv, const void* C, void* D, uint8_t* ws, cudaStream_t st) {
   p->kser = p->kp;
   p->kser.g = p->gser;
@@ -652,7 +654,7 @@ int run_rs_serial(dg_plan_s* p, const Driver& drv, const void* C, void* D, uint8
   if (blocks < 1) blocks = 1;
   dg::dg_reduce_partials_kernel<<<(unsigned)blocks, 256, 0, st>>>(
       reinterpret_cast<const float*>(ws + p->off_serial), p->tp, n4,
-      reinterpret_cast<const __nv_bfloat16*>(C), p->beta, reinterpret_cast<__nv_bfloat16*>(D));
+      reinterpret_cast<const __nv_bfloat16*>(C), p->beta, D, p->out_type == DG_TYPE_F32 ? 1 : 0);
   DG_CUDA(cudaGetLastError());
   return DG_OK;
 }
@@ -783,6 +785,18 @@ int dg_set_option(dg_plan_t p, int option, int64_t value) {
       if (p->epoch != 0) return fail(DG_ERR_STATE, "the epilogue is fixed after the first run");
       p->epi = (int)value;
       return DG_OK;
+    case DG_OPT_OUT_TYPE:
+      if (value != DG_TYPE_BF16 && value != DG_TYPE_F32)
+        return fail(DG_ERR_ARG, "output type must be DG_TYPE_BF16 or DG_TYPE_F32");
+      p->out_type = (int)value;
+      return DG_OK;
+    case DG_OPT_REDUCE_OP:
+      if (value != DG_REDUCE_SUM && value != DG_REDUCE_AVG)
+        return fail(DG_ERR_ARG, "reduce op must be DG_REDUCE_SUM or DG_REDUCE_AVG");
+      if (value == DG_REDUCE_AVG && is_ag(p->schedule))
+        return fail(DG_ERR_UNSUPPORTED, "the reduce op applies to the RS schedules");
+      p->reduce_op = (int)value;
+      return DG_OK;
     case DG_OPT_CTA_GROUP:
       if (value != 1 && value != 2) return fail(DG_ERR_ARG, "CTA group must be 1 or 2");
       if (p->epoch != 0) return fail(DG_ERR_STATE, "the tile configuration is fixed after the first run");
@@ -812,6 +826,7 @@ int dg_plan_info_get(dg_plan_t p, dg_plan_info* o) {
   o->slot_bytes = p->slot_bytes;
   o->copies_per_run = p->copies;
   o->a_type = p->a_type, o->b_type = p->b_type, o->elem_bytes = p->esz;
+  o->out_type = p->out_type, o->reduce_op = p->reduce_op;
   return DG_OK;
 }
 
@@ -833,12 +848,20 @@ int dg_plan_tile(dg_plan_t p, int64_t t, dg_tile* o) {
 int dg_run(dg_plan_t p, const void* A, const void* B, const dg_bf16_t* C, dg_bf16_t* D,
            void* workspace, void* main_stream, void* copy_stream) {
   if (!p) return fail(DG_ERR_ARG, "plan is NULL");
+  if (p->out_type != DG_TYPE_BF16) return fail(DG_ERR_STATE, "the plan writes fp32 D: run it with dg_run_ex");
+  return dg_run_ex(p, A, B, C, nullptr, D, workspace, main_stream, copy_stream);
+}
+
+int dg_run_ex(dg_plan_t p, const void* A, const void* B, const dg_bf16_t* C, const dg_bf16_t* bias, void* D,
+              void* workspace, void* main_stream, void* copy_stream) {
+  if (!p) return fail(DG_ERR_ARG, "plan is NULL");
   if (p->g.total_tiles == 0) return DG_OK;  // empty output
   if (!A || !B || !D) return fail(DG_ERR_ARG, "A, B and D must be non-NULL");
   if (p->beta != 0.f && !C) return fail(DG_ERR_ARG, "C is NULL but beta != 0");
   auto misaligned = [](const void* q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) & (a - 1)) != 0; };
-  if (misaligned(A, 16) || misaligned(B, 16) || misaligned(D, 16) || (C && misaligned(C, 16)))
-    return fail(DG_ERR_ARG, "A, B, C and D must be 16-byte aligned");
+  if (misaligned(A, 16) || misaligned(B, 16) || misaligned(D, 16) || (C && misaligned(C, 16)) ||
+      (bias && misaligned(bias, 16)))
+    return fail(DG_ERR_ARG, "A, B, C, D and bias must be 16-byte aligned");
   // bytes this run uses (no side effect on the plan's SERIAL sizing record)
   const size_t need =
       (!is_ag(p->schedule) && p->mode == DG_MODE_SERIAL) ? p->ws_bytes_serial : p->ws_bytes_base;
@@ -885,13 +908,19 @@ int dg_run(dg_plan_t p, const void* A, const void* B, const dg_bf16_t* C, dg_bf1
   dg::KParams& kp = p->kp;
   kp.g = p->g;
   kp.C = reinterpret_cast<const __nv_bfloat16*>(C);
-  kp.D = reinterpret_cast<__nv_bfloat16*>(D);
+  kp.D = D;
+  kp.bias = reinterpret_cast<const __nv_bfloat16*>(bias);
+  kp.out_f32 = p->out_type == DG_TYPE_F32 ? 1u : 0u;
   kp.X = reinterpret_cast<float*>(ws + p->off_partial);
   kp.flags = reinterpret_cast<uint32_t*>(ws + p->off_flags);
   kp.status = reinterpret_cast<unsigned long long*>(ws + p->off_status);
   kp.epoch = p->epoch;
-  // scaled GEMM: alpha * scale_a * scale_b folded into one fp32 factor
-  kp.alpha = p->alpha * p->scale_a * p->scale_b;
+  // scaled GEMM: alpha * scale_a * scale_b folded into one fp32 factor; the
+  // mean over ranks weighs every rank's product and bias by 1/P (exact: P is a
+  // power of two)
+  const float w = p->reduce_op == DG_REDUCE_AVG ? 1.f / (float)p->tp : 1.f;
+  kp.alpha = p->alpha * p->scale_a * p->scale_b * w;
+  kp.bias_scale = w;
   kp.beta = p->beta;
   {
     const int tm = p->cg == 2 ? dg::Cfg<2>::TILE_M : dg::Cfg<1>::TILE_M;

@@ -86,8 +86,9 @@ constexpr uint32_t DEV_HANG = 2;     // a pipeline wait ran out
 struct KParams {
   CUtensorMap tmA[MAX_MAPS];
   CUtensorMap tmB[MAX_MAPS];
-  // staged epilogue: fp32 partial (box 32 x 128, 128B swizzle), bf16 C and D
-  // (box 32 x 128, 64B swizzle)
+  // staged epilogue: fp32 partial (box 32 x 128, 128B swizzle), bf16 C
+  // (box 32 x 128, 64B swizzle), D in its output type (bf16 like C, fp32 like
+  // the partial)
   CUtensorMap tmX, tmC, tmD;
   // RS with copy-engine hand-off: rank send buffers and (double-buffered)
   // receive buffers, fp32, slab-local rows and columns
@@ -96,7 +97,8 @@ struct KParams {
   float* S;             // send buffers (plain-store address of tmS)
   Geom g;
   const __nv_bfloat16* C;
-  __nv_bfloat16* D;
+  void* D;                    // bf16, or fp32 when out_f32
+  const __nv_bfloat16* bias;  // per-column bias (N values), or null
   float* X;
   uint32_t* flags;  // AG chunk flags or RS tile flags
   unsigned long long* status;
@@ -109,6 +111,8 @@ struct KParams {
   uint32_t wave_sync;   // producers start tile i only after every CTA issued tile i-1
   uint32_t* wave_ctr;   // per-run counter of tiles whose loads are issued (zeroed per run)
   float alpha, beta;
+  float bias_scale;  // weight of the bias in every epilogue pass (1, or 1/P for the mean)
+  uint32_t out_f32;  // D is fp32
   uint64_t timeout_ns;
   uint64_t hang_ns;
 };
@@ -480,8 +484,46 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// out += bias_scale * bias[gcol + i] for the ncols valid columns (the bias is
+// shared by every row; all threads of the warp read the same bytes).
+__device__ __forceinline__ void add_bias(const KParams& p, int64_t gcol, int ncols, float (&out)[32]) {
+  const __nv_bfloat16* b = p.bias + gcol;
+  if (ncols == 32 && (gcol & 7) == 0) {
+    const uint4* b4 = reinterpret_cast<const uint4*>(b);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = __ldg(b4 + q);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        out[q * 8 + 2 * h] = fmaf(p.bias_scale, bf16_bits_to_f32(w[h] & 0xFFFFu), out[q * 8 + 2 * h]);
+        out[q * 8 + 2 * h + 1] = fmaf(p.bias_scale, bf16_bits_to_f32(w[h] >> 16), out[q * 8 + 2 * h + 1]);
+      }
+    }
+  } else {
+    const uint16_t* bs = reinterpret_cast<const uint16_t*>(b);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < ncols) out[i] = fmaf(p.bias_scale, bf16_bits_to_f32(__ldg(bs + i)), out[i]);
+  }
+}
+
+// Plain stores of 32 consecutive fp32 values (the ncols valid ones).
+__device__ __forceinline__ void store_f32_row(float* x, int ncols, const float (&out)[32], bool vec) {
+  if (vec) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      __stcg(reinterpret_cast<float4*>(x) + q, make_float4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < ncols) __stcg(x + i, out[i]);
+  }
+}
+
 // Source term (beta*C, the fp32 partial, or 0) for 32 consecutive columns of
-// one output row, then d = alpha*acc + src, stored as bf16 D or fp32 partial.
+// one output row, then d = alpha*acc + src (+ the bias), stored as D (bf16 or
+// fp32) or as the fp32 partial.
 __device__ __forceinline__ void epilogue_row_chunk(const KParams& p, const Tile& tl, int64_t grow,
                                                    int64_t gcol, int ncols, float (&acc)[32]) {
   const int64_t N = p.g.N;
@@ -528,9 +570,12 @@ __device__ __forceinline__ void epilogue_row_chunk(const KParams& p, const Tile&
   float out[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) out[i] = fmaf(p.alpha, acc[i], src[i]);
+  if (p.bias) add_bias(p, gcol, ncols, out);
 
-  if (tl.dst == DST_D) {
-    __nv_bfloat16* d = p.D + e0;
+  if (tl.dst == DST_D && p.out_f32) {
+    store_f32_row(static_cast<float*>(p.D) + e0, ncols, out, ncols == 32 && (e0 & 3) == 0);
+  } else if (tl.dst == DST_D) {
+    __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.D) + e0;
     if (ncols == 32 && (e0 & 7) == 0) {
       uint4* d4 = reinterpret_cast<uint4*>(d);
 #pragma unroll
@@ -548,17 +593,7 @@ __device__ __forceinline__ void epilogue_row_chunk(const KParams& p, const Tile&
         if (i < ncols) d[i] = __float2bfloat16_rn(out[i]);
     }
   } else {
-    float* x = p.X + e0;
-    if (ncols == 32 && (e0 & 3) == 0) {
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        __stcg(reinterpret_cast<float4*>(x) + q,
-               make_float4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]));
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < ncols) __stcg(x + i, out[i]);
-    }
+    store_f32_row(p.X + e0, ncols, out, ncols == 32 && (e0 & 3) == 0);
   }
 }
 
@@ -566,8 +601,10 @@ __device__ __forceinline__ void epilogue_row_chunk(const KParams& p, const Tile&
 // (grow, gcol); the partial at `x`).
 __device__ __forceinline__ void store_row_chunk(const KParams& p, const Tile& tl, int64_t grow,
                                                 int64_t gcol, int ncols, const float (&out)[32], float* x) {
-  if (tl.dst == DST_D) {
-    __nv_bfloat16* d = p.D + grow * p.g.N + gcol;
+  if (tl.dst == DST_D && p.out_f32) {
+    store_f32_row(static_cast<float*>(p.D) + grow * p.g.N + gcol, ncols, out, false);
+  } else if (tl.dst == DST_D) {
+    __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.D) + grow * p.g.N + gcol;
 #pragma unroll
     for (int i = 0; i < 32; ++i)
       if (i < ncols) d[i] = __float2bfloat16_rn(out[i]);
@@ -995,6 +1032,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
         float out[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) out[i] = fmaf(p.alpha, acc[i], src[i]);
+        if (p.bias) add_bias(p, tl.out_col + c * XCOLS, ncols, out);
         // A whole chunk inside the tile (and inside its shard) goes out by TMA.
         const bool tma_ok = rows_here >= ROWS_PER_CTA && ncols == XCOLS;
         // barrier A: every thread is done with the source buffer, and the
@@ -1003,7 +1041,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
         named_bar_sync(1, EPI_THREADS);
         if (tma_ok) {
           const uint32_t db = nstore & 1;
-          staged_write_row(xdst + db * XBUF, row, tl.dst == DST_X, out);
+          staged_write_row(xdst + db * XBUF, row, tl.dst == DST_X || p.out_f32 != 0, out);
           fence_proxy_async_smem();
           named_bar_sync(1, EPI_THREADS);  // barrier B: the chunk is complete in shared memory
           if (et == 0) {
@@ -1084,12 +1122,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
 }
 
 // Reduction of the non-fused ReduceScatter baseline:
-//   D[e] = bf16( (X_0[e] + X_1[e] + ... + X_{P-1}[e]) + beta * C[e] )
-// over the P stacked fp32 partials (each already scaled by alpha), four
-// elements per thread and iteration, grid-stride.  HBM-bound.
+//   D[e] = (X_0[e] + X_1[e] + ... + X_{P-1}[e]) + beta * C[e]   (bf16 or fp32 D)
+// over the P stacked fp32 partials (each already scaled by alpha and carrying
+// its bias), four elements per thread and iteration, grid-stride.  HBM-bound.
 __global__ void __launch_bounds__(256) dg_reduce_partials_kernel(const float* __restrict__ X, int P,
                                                                  int64_t n4, const __nv_bfloat16* C,
-                                                                 float beta, __nv_bfloat16* D) {
+                                                                 float beta, void* D, int out_f32) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t plane = n4;  // float4 units per partial
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
@@ -1108,10 +1146,14 @@ __global__ void __launch_bounds__(256) dg_reduce_partials_kernel(const float* __
       acc.z += beta * bf16_bits_to_f32(cw.y & 0xFFFFu);
       acc.w += beta * bf16_bits_to_f32(cw.y >> 16);
     }
-    uint2 o;
-    o.x = pack_bf16x2(acc.x, acc.y);
-    o.y = pack_bf16x2(acc.z, acc.w);
-    reinterpret_cast<uint2*>(D)[i] = o;
+    if (out_f32) {
+      reinterpret_cast<float4*>(D)[i] = acc;
+    } else {
+      uint2 o;
+      o.x = pack_bf16x2(acc.x, acc.y);
+      o.y = pack_bf16x2(acc.z, acc.w);
+      reinterpret_cast<uint2*>(D)[i] = o;
+    }
   }
 }
 

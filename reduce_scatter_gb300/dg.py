@@ -30,8 +30,13 @@ SCHEDULE_BY_NAME = {v: k for k, v in SCHEDULE_NAMES.items()}
 TYPE_BF16 = 0
 TYPE_E4M3 = 1
 TYPE_E5M2 = 2
-TYPE_NAMES = {TYPE_BF16: "bf16", TYPE_E4M3: "e4m3", TYPE_E5M2: "e5m2"}
+TYPE_F32 = 3  # output (D) only
+TYPE_NAMES = {TYPE_BF16: "bf16", TYPE_E4M3: "e4m3", TYPE_E5M2: "e5m2", TYPE_F32: "f32"}
 TYPE_BY_NAME = {v: k for k, v in TYPE_NAMES.items()}
+
+REDUCE_SUM = 0
+REDUCE_AVG = 1
+REDUCE_BY_NAME = {"sum": REDUCE_SUM, "avg": REDUCE_AVG}
 
 MODE_FUSED = 0
 MODE_GEMM_ONLY = 1
@@ -57,11 +62,13 @@ OPT_EPILOGUE = 7
 OPT_L2_HINT = 8
 OPT_WAVE_SYNC = 9
 OPT_RS_CE_PARTIALS = 10
+OPT_OUT_TYPE = 11
+OPT_REDUCE_OP = 12
 
 # Every symbol include/dg.h declares.
 EXPORTS = ("dg_plan", "dg_workspace_bytes", "dg_run_mode", "dg_set_option", "dg_run", "dg_check",
            "dg_plan_info_get", "dg_plan_tile", "dg_destroy", "dg_last_error", "dg_run_static",
-           "dg_plan_scaled")
+           "dg_plan_scaled", "dg_run_ex")
 
 # Size of the library's built-in workspace used by dg_run_static.
 STATIC_WORKSPACE_BYTES = 32 << 20
@@ -83,6 +90,7 @@ class PlanInfo(ctypes.Structure):
         ("slot_bytes", ctypes.c_size_t),
         ("copies_per_run", ctypes.c_int64),
         ("a_type", ctypes.c_int32), ("b_type", ctypes.c_int32), ("elem_bytes", ctypes.c_int32),
+        ("out_type", ctypes.c_int32), ("reduce_op", ctypes.c_int32),
     ]
 
     def as_dict(self):
@@ -135,6 +143,8 @@ def lib():
         L.dg_set_option.restype = i32
         L.dg_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
         L.dg_run.restype = i32
+        L.dg_run_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.dg_run_ex.restype = i32
         L.dg_run_static.argtypes = [vp, vp, vp, vp, vp, vp, vp]
         L.dg_run_static.restype = i32
         L.dg_check.argtypes = [vp, vp, vp]
@@ -179,10 +189,14 @@ def stream_handle(s) -> int | None:
 
 
 class Plan:
-    """One problem (m, n, k, l, tp, schedule, alpha, beta) behind ``dg_plan``."""
+    """One problem (m, n, k, l, tp, schedule, alpha, beta) behind ``dg_plan``.
+
+    ``out_type`` (TYPE_BF16 / TYPE_F32 or "bf16" / "f32") and ``reduce_op``
+    (REDUCE_SUM / REDUCE_AVG or "sum" / "avg") are set through
+    ``dg_set_option`` right after planning."""
 
     def __init__(self, m, n, k, l, tp, schedule, alpha=1.0, beta=0.0, a_type=TYPE_BF16, b_type=TYPE_BF16,
-                 scale_a=1.0, scale_b=1.0):
+                 scale_a=1.0, scale_b=1.0, out_type=TYPE_BF16, reduce_op=REDUCE_SUM):
         if isinstance(schedule, str):
             schedule = SCHEDULE_BY_NAME[schedule]
         a_type = TYPE_BY_NAME.get(a_type, a_type)
@@ -195,6 +209,12 @@ class Plan:
                                         scale_a, scale_b))
         self.a_type, self.b_type, self.scale_a, self.scale_b = a_type, b_type, scale_a, scale_b
         self._h = h
+        self.out_type = TYPE_BY_NAME.get(out_type, out_type)
+        self.reduce_op = REDUCE_BY_NAME.get(reduce_op, reduce_op)
+        if self.out_type != TYPE_BF16:
+            self.set_option(OPT_OUT_TYPE, self.out_type)
+        if self.reduce_op != REDUCE_SUM:
+            self.set_option(OPT_REDUCE_OP, self.reduce_op)
         self.m, self.n, self.k, self.l, self.tp, self.schedule = m, n, k, l, tp, schedule
         self.alpha, self.beta = alpha, beta
 
@@ -235,6 +255,14 @@ class Plan:
     def run(self, A, B, C, D, workspace, main_stream=None, copy_stream=None, raise_on_error=True) -> int:
         rc = lib().dg_run(self._h, ptr(A), ptr(B), ptr(C), ptr(D), ptr(workspace),
                           stream_handle(main_stream), stream_handle(copy_stream))
+        if raise_on_error:
+            _check(rc)
+        return rc
+
+    def run_ex(self, A, B, C, bias, D, workspace, main_stream=None, copy_stream=None, raise_on_error=True) -> int:
+        """``dg_run_ex``: an optional per-column bf16 bias; D of the plan's output type."""
+        rc = lib().dg_run_ex(self._h, ptr(A), ptr(B), ptr(C), ptr(bias), ptr(D), ptr(workspace),
+                             stream_handle(main_stream), stream_handle(copy_stream))
         if raise_on_error:
             _check(rc)
         return rc

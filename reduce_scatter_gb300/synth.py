@@ -50,6 +50,7 @@ _U64 = (1 << 64) - 1
 STREAM_A = 1
 STREAM_B = 2
 STREAM_C = 3
+STREAM_BIAS = 4
 
 
 def _mix64_int(z: int) -> int:

@@ -267,3 +267,24 @@ def test_tile_order_simulator_random(L, i):
     plan = dg.Plan(m, n, k, l, tp, sched, 1.0, 0.5 if rng.integers(0, 2) else 0.0)
     plan.set_option(dg.OPT_CTA_GROUP, int(rng.integers(1, 3)))
     _simulate(plan, m, n, k, l, tp, sched)
+
+
+def test_output_type_and_reduce_op_rules(L):
+    p = dg.Plan(256, 256, 256, 1, 2, dg.AG_ROTATING_A)
+    with pytest.raises(dg.DGError):
+        p.set_option(dg.OPT_OUT_TYPE, dg.TYPE_E4M3)        # fp8 D is not built
+    with pytest.raises(dg.DGError):
+        p.set_option(dg.OPT_REDUCE_OP, dg.REDUCE_AVG)      # AG plans have no reduction
+    p.set_option(dg.OPT_REDUCE_OP, dg.REDUCE_SUM)
+    p.set_option(dg.OPT_OUT_TYPE, dg.TYPE_F32)
+    info = p.info()
+    assert (info["out_type"], info["reduce_op"]) == (dg.TYPE_F32, dg.REDUCE_SUM)
+    # dg_run writes bf16 D only: an fp32-output plan is refused before any CUDA call
+    assert p.run(16, 16, None, 16, 256, raise_on_error=False) == dg.ERR_STATE
+    # dg_run_ex checks the bias alignment with the other pointers
+    assert p.run_ex(16, 16, None, 24, 16, 256, raise_on_error=False) == dg.ERR_ARG
+    q = dg.Plan(256, 256, 256, 1, 4, dg.RS_TILING_B_ROTATING_C, out_type="f32", reduce_op="avg")
+    info = q.info()
+    assert (info["out_type"], info["reduce_op"]) == (dg.TYPE_F32, dg.REDUCE_AVG)
+    with pytest.raises(dg.DGError):
+        q.set_option(dg.OPT_REDUCE_OP, 2)

@@ -1,62 +1,156 @@
-"""The torch-op front end: argument checks on CPU, and on the GPU the same
-results as the C ABI (bit for bit) and as torch's matmul (within tolerance)."""
+"""The torch-op front end (the fused-op signatures of the torch symmetric-memory
+module over the C ABI): argument rules and layouts on CPU; on the GPU the same
+bits as the C ABI on the flattened problem, and torch's matmul within
+tolerance."""
 
 import numpy as np
 import pytest
 import torch
 
 from reduce_scatter_gb300 import dg, ops
-from tests.gpu_common import TOL, Runner, host_inputs, to_dev
+from tests.gpu_common import TOL, Runner
 
 
 def test_argument_checks_on_cpu():
     a = torch.zeros((64, 32), dtype=torch.bfloat16)
+    w = torch.zeros((48, 32), dtype=torch.bfloat16)           # (N, K) weight
     with pytest.raises(ValueError):
-        ops.fused_all_gather_matmul(a, a.t(), 2, gather_dim=2)
+        ops.fused_all_gather_matmul(a, [w.t()], 1, 2)          # gather along K
     with pytest.raises(ValueError):
-        ops.fused_matmul_reduce_scatter(a, a.t(), 2, reduce_op="avg")
+        ops.fused_all_gather_matmul(a, [w.t()], 0, 2, rotate="C")
     with pytest.raises(ValueError):
-        ops.fused_all_gather_matmul(a, a.t(), 2)  # not CUDA tensors
+        ops.fused_all_gather_matmul(a, [w.t()], 0, 2)          # not CUDA tensors
+    with pytest.raises(ValueError):
+        ops.fused_all_gather_matmul(a[:63], [w.t()], 0, 2)     # 63 rows over 2 ranks
+    with pytest.raises(ValueError):
+        ops.fused_matmul_reduce_scatter(a, w.t(), "max", 0, 2)
+    with pytest.raises(ValueError):
+        ops.fused_matmul_reduce_scatter(a, w.t(), "sum", 2, 2)  # no such dimension
+    with pytest.raises(ValueError):
+        ops.fused_all_gather_scaled_matmul(a, [w.t()], 1.0, [1.0, 1.0], 0, 2)   # list lengths
+    with pytest.raises(ValueError):
+        ops.fused_all_gather_scaled_matmul(a, [w.t()], 1.0, [1.0], 0, 2, result_scales=[torch.ones(())])
+    with pytest.raises(ValueError):
+        ops.fused_scaled_matmul_reduce_scatter(a, w.t(), 1.0, 1.0, "sum", 0, 2, result_scale=1.0)
+    with pytest.raises(ValueError):
+        ops._out_type(torch.float16)
     with pytest.raises(TypeError):
         ops._in_type(torch.zeros(2, dtype=torch.float32))
-    w = torch.zeros((48, 32), dtype=torch.bfloat16)          # (N, K) weight
-    assert ops._k_major_b(w.t().unsqueeze(0)).data_ptr() == w.data_ptr()   # used in place
+    with pytest.raises(ValueError):
+        ops._scale(torch.ones(2))
+    assert ops._k_major_b(w.t()).data_ptr() == w.data_ptr()    # used in place
+    assert ops._k_major_b(w.t().contiguous()).is_contiguous()
+
+
+def test_layouts_on_cpu():
+    # rank r's shard of the gathered / scattered dimension is the r-th block of rows
+    t = torch.arange(2 * 8 * 3 * 4, dtype=torch.float32).view(2, 8, 3, 4)
+    A2, lead = ops._rows(t, 1, "gather_dim", 4)
+    assert lead == [8, 2, 3] and A2.shape == (48, 4)
+    assert torch.equal(A2[:12], t[:, 0:2].movedim(1, 0).reshape(12, 4))   # rank 0: rows 0..1 of dim 1
+    D = ops._unflatten(A2, lead, 1)
+    assert torch.equal(D, t)
+    sched, A2, lead, dim = ops._rs_layout(t, 3, 4)        # last dimension: N-slabs
+    assert sched == dg.RS_TILING_B_ROTATING_C and dim is None and lead == [2, 8, 3]
+    sched, A2, lead, dim = ops._rs_layout(t, 2, 3)
+    assert sched == dg.RS_TILING_A_ROTATING_C and dim == 2
+    for d in range(4):
+        r = ops.restride_A_shard_for_fused_all_gather_matmul(t, d)
+        assert torch.equal(r, t) and r.movedim(d, 0).is_contiguous()
+        r = ops.restride_A_for_fused_matmul_reduce_scatter(t, d)
+        assert torch.equal(r, t) and r.movedim(d, 0).is_contiguous()
+
+
+def _randn(shape, seed, dtype=torch.bfloat16, std=1.0):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    return (torch.randn(shape, device="cuda", generator=g) * std).to(dtype)
+
+
+def _rel(got, want):
+    return ((got.double() - want).abs().max() / want.abs().max()).item()
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("sched,kw", [(dg.AG_ROTATING_A, dict(gather_dim=0)), (dg.AG_ROTATING_B, dict(gather_dim=1)),
-                                      (dg.RS_TILING_A_ROTATING_C, dict(scatter_dim=0)),
-                                      (dg.RS_TILING_B_ROTATING_C, dict(scatter_dim=1))])
-def test_ops_match_the_abi_and_torch(sched, kw):
-    m, n, k, l, tp = 1024, 768, 512, 2, 4
-    a, b, c = host_inputs(m, n, k, l, seed=60 + sched)
-    A, Bnk, C = to_dev(a), to_dev(b), to_dev(c)
-    B = Bnk.transpose(1, 2)                                   # torch layout (L, K, N), a view
-    ref, _ = Runner(m, n, k, l, tp, sched, 0.5, 1.0).run(A, Bnk, C)
-    fn = ops.fused_all_gather_matmul if sched <= 1 else ops.fused_matmul_reduce_scatter
-    D = fn(A, B, tp, alpha=0.5, beta=1.0, C=C, **kw)
+@pytest.mark.parametrize("rotate", ["A", "B"])
+@pytest.mark.parametrize("gather_dim", [0, 1])
+def test_all_gather_matmul_multi_b(rotate, gather_dim):
+    tp = 4
+    A = _randn((4, 256, 512), 1)                      # (batch, seq, hidden): all ranks' shards
+    Ws = [_randn((768, 512), 2, std=0.05), _randn((256, 512), 3, std=0.05)]   # (N, K) weights
+    Bs = [W.t() for W in Ws]                          # torch layout (K, N), K-major views
+    Ag, outs = ops.fused_all_gather_matmul(A, Bs, gather_dim, tp, rotate=rotate)
     torch.cuda.synchronize()
-    assert torch.equal(D.view(torch.int16), ref.view(torch.int16))
-    want = (0.5 * torch.matmul(A.double(), B.double()) + C.double()).float()
-    err = (D.float() - want).abs().max().item() / want.abs().max().item()
-    assert err <= TOL
-    # a B that is not a transposed K-major view is copied once, same result
-    D2 = fn(A, B.contiguous(), tp, alpha=0.5, beta=1.0, C=C, **kw)
-    torch.cuda.synchronize()
-    assert torch.equal(D2.view(torch.int16), ref.view(torch.int16))
+    assert Ag is A and len(outs) == 2
+    sched = dg.AG_ROTATING_A if rotate == "A" else dg.AG_ROTATING_B
+    A2 = A.movedim(gather_dim, 0).reshape(-1, 512).contiguous()
+    for W, B, D in zip(Ws, Bs, outs):
+        assert D.shape == (4, 256, W.shape[0])
+        want = torch.matmul(A.double(), B.double())
+        assert _rel(D, want) <= TOL
+        # the same bits as the C ABI on the flattened problem
+        ref, _ = Runner(A2.shape[0], W.shape[0], 512, 1, tp, sched).run(A2.unsqueeze(0), W.unsqueeze(0), None)
+        flat = D.movedim(gather_dim, 0).reshape(-1, W.shape[0])
+        assert torch.equal(flat.view(torch.int16), ref[0].view(torch.int16))
 
 
 @pytest.mark.gpu
-def test_scaled_ops_fp8():
+def test_all_gather_matmul_alpha_beta_c():
+    tp = 2
+    A = _randn((512, 256), 4)
+    W = _randn((384, 256), 5, std=0.05)
+    C = _randn((512, 384), 6)
+    _, (D,) = ops.fused_all_gather_matmul(A, [W.t()], 0, tp, alpha=0.5, beta=1.0, Cs=[C])
+    want = 0.5 * torch.matmul(A.double(), W.double().t()) + C.double()
+    assert _rel(D, want) <= TOL
+    # a B that is not a K-major view is copied once: same bits
+    _, (D2,) = ops.fused_all_gather_matmul(A, [W.t().contiguous()], 0, tp, alpha=0.5, beta=1.0, Cs=[C])
+    assert torch.equal(D.view(torch.int16), D2.view(torch.int16))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("reduce_op", ["sum", "avg"])
+@pytest.mark.parametrize("scatter_dim", [0, 1, 2])
+def test_matmul_reduce_scatter(scatter_dim, reduce_op):
+    tp = 4
+    A = _randn((4, 256, 1024), 7)                     # all ranks' K-slabs along the last dimension
+    W = _randn((512, 1024), 8, std=0.05)
+    D = ops.fused_matmul_reduce_scatter(A, W.t(), reduce_op, scatter_dim, tp)
+    assert D.shape == (4, 256, 512)
+    want = torch.matmul(A.double(), W.double().t()) / (tp if reduce_op == "avg" else 1)
+    assert _rel(D, want) <= TOL
+    # rank r's slab of scatter_dim is the r-th block: per-rank K-slab products reduce to it
+    r = 1
+    sl = [slice(None)] * 3
+    sl[scatter_dim] = slice(r * D.shape[scatter_dim] // tp, (r + 1) * D.shape[scatter_dim] // tp)
+    parts = sum(torch.matmul(A[..., q * 256:(q + 1) * 256].double(), W[:, q * 256:(q + 1) * 256].double().t())
+                for q in range(tp))
+    if reduce_op == "avg":
+        parts = parts / tp
+    assert _rel(D[tuple(sl)], parts[tuple(sl)]) <= TOL
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("reduce_op", ["sum", "avg"])
+def test_scaled_ops_fp8_bias_f32(reduce_op):
     if not hasattr(torch, "float8_e4m3fn"):
         pytest.skip("no float8 in this torch")
-    m, n, k, tp = 1024, 1024, 512, 4
-    A = (torch.randn((m, k), device="cuda", generator=torch.Generator("cuda").manual_seed(1))).to(torch.float8_e4m3fn)
-    W = (torch.randn((n, k), device="cuda", generator=torch.Generator("cuda").manual_seed(2))).to(torch.float8_e4m3fn)
+    tp = 4
+    A = _randn((2, 512, 512), 9, dtype=torch.float32).to(torch.float8_e4m3fn)
+    W = _randn((1024, 512), 10, dtype=torch.float32).to(torch.float8_e4m3fn)
+    bias = _randn((1024,), 11)
     sa, sb = torch.tensor(0.5, device="cuda"), 0.25
-    want = (torch.matmul(A.double(), W.double().t()) * 0.125).float()
-    for fn, kw in ((ops.fused_all_gather_scaled_matmul, {}), (ops.fused_scaled_matmul_reduce_scatter, {})):
-        D = fn(A, W.t(), sa, sb, tp, **kw)
-        torch.cuda.synchronize()
-        err = (D.float().squeeze(0) - want).abs().max().item() / want.abs().max().item()
-        assert err <= TOL
+    prod = torch.matmul(A.double(), W.double().t()) * 0.125
+    _, (D,) = ops.fused_all_gather_scaled_matmul(A, [W.t()], sa, [sb], 1, tp, biases=[bias],
+                                                 out_dtypes=[torch.float32])
+    assert D.dtype == torch.float32 and D.shape == (2, 512, 1024)
+    assert _rel(D, prod + bias.double()) <= 5e-4
+    Dr = ops.fused_scaled_matmul_reduce_scatter(A, W.t(), sa, sb, reduce_op, 1, tp, bias=bias,
+                                                out_dtype=torch.float32)
+    want = prod + tp * bias.double()
+    if reduce_op == "avg":
+        want = want / tp
+    assert _rel(Dr, want) <= 5e-4
+    # bf16 output is the fp32 result rounded
+    Db = ops.fused_scaled_matmul_reduce_scatter(A, W.t(), sa, sb, reduce_op, 1, tp, bias=bias)
+    assert Db.dtype == torch.bfloat16
+    assert torch.equal(Db.view(torch.int16), Dr.to(torch.bfloat16).view(torch.int16))
