@@ -9,8 +9,8 @@
  * split over TP virtual ranks with one of the four schedules that README lists
  * under "Trying out other schedules".  All TP ranks are emulated on ONE GPU:
  * each rank's shards are views or receive slots in device memory, transfers
- * between ranks are copy-engine cudaMemcpyAsync calls on a side stream that
- * each publish a ready flag, and one persistent kernel runs every rank's steps
+ * between ranks are copy-engine (two-dimensional device-to-device) copies on
+ * side streams that each publish a ready flag, and one persistent kernel runs every rank's steps
  * in rotation order, waiting on a shard's flag before it loads that shard.
  *
  * Layouts (the pages do not fix them):
@@ -147,8 +147,21 @@ enum dg_option {
                                  96 MiB */
   DG_OPT_OUT_TYPE = 11,       /* element type of D: DG_TYPE_BF16 (default) or DG_TYPE_F32
                                  (fp32 D runs through dg_run_ex) */
-  DG_OPT_REDUCE_OP = 12       /* RS plans: dg_reduce_op, DG_REDUCE_SUM (default) or
+  DG_OPT_REDUCE_OP = 12,      /* RS plans: dg_reduce_op, DG_REDUCE_SUM (default) or
                                  DG_REDUCE_AVG; AG plans accept only SUM */
+  DG_OPT_COPY_PACE = 13,      /* AG FUSED runs with tp > 2: 1 = the shard transfers of step
+                                 s >= 2 start only once the kernel has reached step s - 1
+                                 (progress words the producers set; copy streams wait on them),
+                                 so each step's transfers overlap the previous step's GEMM
+                                 instead of all running at the start; 0 = all transfers are
+                                 issued at once; -1 (default) = on */
+  DG_OPT_COPY_KIND = 14       /* how shard and partial transfers are issued: 0 (default) =
+                                 two-dimensional device-to-device copies, which run on a copy
+                                 engine beside a kernel that fills every SM; 1 = one-dimensional
+                                 cudaMemcpyAsync, which on GB300 runs as a copy kernel on SMs
+                                 and so only progresses where the GEMM kernel leaves an SM
+                                 registers to spare (faster, ~3.2 TB/s against ~1-1.8 TB/s,
+                                 but it competes with the GEMM for SMs) */
 };
 
 /* Plan geometry and workspace layout, for callers and tests. */

@@ -7,9 +7,10 @@
 // GEMM and the copy engine to communication):
 //   * rank r's home shards are views of the caller's A / B;
 //   * rank r's receive slot for step s >= 1 is a workspace region; the copy
-//     stream fills it with cudaMemcpyAsync (device to device, copy engine) in
-//     chunks and after each chunk writes the run's epoch into that chunk's
-//     ready flag with a stream memory operation (no SM involved);
+//     streams fill it in chunks with two-dimensional device-to-device copies,
+//     which run on a copy engine, and after each chunk write the run's epoch
+//     into that chunk's ready flag with a stream memory operation (no SM
+//     involved);
 //   * one persistent kernel runs every rank's steps in rotation order and its
 //     producer waits on a chunk's flag before loading from the slot.
 // The RS schedules move no shards on one GPU: the rotating partial X_j lives
@@ -108,6 +109,10 @@ uint64_t g_next_plan_id = 1;
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Layout of the 256-byte status area: [0, 8) status word, [64, 68) wave
+// counter, [128, 128 + 4 * tp) copy-pacing progress words.
+constexpr size_t kProgressOffset = 128;
+
 }  // namespace
 
 struct dg_plan_s {
@@ -132,6 +137,8 @@ struct dg_plan_s {
   int epi = 0;  // epilogue: 0 direct, 1 staged through shared memory with TMA (default: RS, fp8, K >= 16384)
   uint32_t l2_hint = 0;  // L2 policy of operand loads (DG_OPT_L2_HINT)
   int wave_sync = -1;  // DG_OPT_WAVE_SYNC: -1 auto, 0 off, 1 on
+  int copy_pace = -1;  // DG_OPT_COPY_PACE: -1 auto, 0 off, 1 on
+  int copy_kind = 0;   // DG_OPT_COPY_KIND: 0 copy engine (2D copies), 1 one-dimensional cudaMemcpyAsync
   uint64_t id = 0;
   uint32_t epoch = 0;
   bool serial_ws = false;
@@ -444,6 +451,20 @@ int build_maps(dg_plan_s* p, const Driver& drv, const void* A, const void* B, ui
   return DG_OK;
 }
 
+// Device-to-device transfer of `rows` contiguous rows of `row_bytes` bytes on
+// a copy engine.  Issued as a two-dimensional copy: a one-dimensional
+// device-to-device cudaMemcpyAsync runs as a copy kernel on the SMs, which can
+// only start where the persistent GEMM kernel leaves registers free (measured
+// on GB300: such copies stall until the kernel exits when it holds 47 K of an
+// SM's 64 K registers, and move 3.2 TB/s when they get SMs), while the
+// two-dimensional form runs on a copy engine beside a kernel that fills every
+// SM (1.8 TB/s per copy).
+// DG_OPT_COPY_KIND = 1 selects the one-dimensional form instead.
+cudaError_t ce_copy(void* dst, const void* src, size_t row_bytes, size_t rows, cudaStream_t st, int kind) {
+  if (kind == 1) return cudaMemcpyAsync(dst, src, row_bytes * rows, cudaMemcpyDeviceToDevice, st);
+  return cudaMemcpy2DAsync(dst, row_bytes, src, row_bytes, row_bytes, rows, cudaMemcpyDeviceToDevice, st);
+}
+
 void CUDART_CB sleep_cb(void* ms) {
   std::this_thread::sleep_for(std::chrono::milliseconds((int64_t)(intptr_t)ms));
 }
@@ -463,7 +484,8 @@ int ensure_extra_streams(dg_plan_s* p, int want) {
 // ready-flag write on the same stream, in the order the kernel consumes them.
 // Chunks are dealt round-robin over `ns` streams.
 int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B, uint8_t* ws,
-                   cudaStream_t* streams, int ns) {
+                   cudaStream_t* streams, int ns, bool pace) {
+  auto* progress = reinterpret_cast<uint32_t*>(ws + p->off_status + kProgressOffset);
   const dg::Geom& g = p->g;
   const int64_t P = p->tp;
   if (p->fault_delay_ms > 0)
@@ -478,7 +500,16 @@ int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B
   auto* slots = ws + p->off_slots;
   auto* flags = reinterpret_cast<uint32_t*>(ws + p->off_flags);
   int64_t idx = 0;
-  for (int64_t s = 1; s < P; ++s)
+  for (int64_t s = 1; s < P; ++s) {
+    if (pace && s >= 2)
+      // step s's shards move while the kernel computes step s - 1
+      for (int i = 0; i < ns; ++i) {
+        CUresult rc = drv.wait32((CUstream)streams[i], (CUdeviceptr)(progress + (s - 1)), 1u,
+                                 CU_STREAM_WAIT_VALUE_GEQ);
+        if (rc != CUDA_SUCCESS)
+          return fail(rc == CUDA_ERROR_NOT_SUPPORTED ? DG_ERR_UNSUPPORTED : DG_ERR_CUDA,
+                      "cuStreamWaitValue32 failed (%d)", (int)rc);
+      }
     for (int64_t r = 0; r < P; ++r) {
       const int64_t j = (r + s) % P;
       for (int64_t l = 0; l < g.L; ++l) {
@@ -490,7 +521,7 @@ int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B
           if (rows > 0) {
             const uint8_t* src = home + (l * outer + j * g.shard + row0) * row_bytes;
             uint8_t* dst = slots + (slot * g.shard + row0) * row_bytes;
-            DG_CUDA(cudaMemcpyAsync(dst, src, (size_t)(rows * row_bytes), cudaMemcpyDeviceToDevice, st));
+            DG_CUDA(ce_copy(dst, src, (size_t)row_bytes, (size_t)rows, st, p->copy_kind));
           }
           if (idx != p->fault_skip) {
             CUresult rc = drv.write32((CUstream)st, (CUdeviceptr)(flags + slot * g.nchunks + c),
@@ -502,6 +533,7 @@ int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B
         }
       }
     }
+  }
   return DG_OK;
 }
 
@@ -550,6 +582,10 @@ int launch_kp(dg_plan_s* p, const dg::KParams& kp, cudaStream_t st) {
     DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 0, 0>, kp));
   return DG_OK;
 }
+
+// Pacing of the AG shard transfers: the copies of step s >= 2 wait until the
+// kernel has reached step s - 1 (progress words in the status area).
+bool copy_pace_on(const dg_plan_s* p) { return p->copy_pace != 0; }
 
 int launch(dg_plan_s* p, cudaStream_t st, uint32_t wait_flags) {
   p->kp.wait_flags = wait_flags;
@@ -614,7 +650,7 @@ int run_rs_ce(dg_plan_s* p, const Driver& drv, uint8_t* ws, cudaStream_t ms, cud
           const int64_t rows = std::min<int64_t>(g.BM, g.blk_m - b * g.BM);
           const uint8_t* src = ws + p->off_send + (size_t)((r * L + l) * g.blk_m + b * g.BM) * row_bytes;
           uint8_t* dst = ws + p->off_recv + (size_t)(((2 * q + ((s + 1) & 1)) * L + l) * g.blk_m + b * g.BM) * row_bytes;
-          DG_CUDA(cudaMemcpyAsync(dst, src, (size_t)rows * row_bytes, cudaMemcpyDeviceToDevice, st));
+          DG_CUDA(ce_copy(dst, src, row_bytes, (size_t)rows, st, p->copy_kind));
           if (n != p->fault_skip) {
             rc = check(drv.write32((CUstream)st, (CUdeviceptr)(flags + idx(q, s + 1, l, b)), p->epoch, 0),
                        "cuStreamWriteValue32");
@@ -770,6 +806,14 @@ int dg_set_option(dg_plan_t p, int option, int64_t value) {
       }
       p->cep = value == 1;
       layout(p);
+      return DG_OK;
+    case DG_OPT_COPY_KIND:
+      if (value != 0 && value != 1) return fail(DG_ERR_ARG, "copy kind must be 0 (copy engine) or 1 (1D memcpy)");
+      p->copy_kind = (int)value;
+      return DG_OK;
+    case DG_OPT_COPY_PACE:
+      if (value < -1 || value > 1) return fail(DG_ERR_ARG, "copy pacing must be -1 (auto), 0 or 1");
+      p->copy_pace = (int)value;
       return DG_OK;
     case DG_OPT_WAVE_SYNC:
       if (value < -1 || value > 1) return fail(DG_ERR_ARG, "wave sync must be -1 (auto), 0 or 1");
@@ -935,6 +979,10 @@ int dg_run_ex(dg_plan_t p, const void* A, const void* B, const dg_bf16_t* C, con
   kp.wave_sync = wave_sync_on(p) ? 1u : 0u;
   kp.wave_ctr = reinterpret_cast<uint32_t*>(ws + p->off_status + 64);
   if (kp.wave_sync) DG_CUDA(cudaMemsetAsync(ws + p->off_status + 64, 0, 4, ms));
+  const bool pace = copy_pace_on(p) && is_ag(p->schedule) && p->tp > 2 && p->mode == DG_MODE_FUSED && cs != ms &&
+                    cs != nullptr;
+  kp.progress = pace ? reinterpret_cast<uint32_t*>(ws + p->off_status + kProgressOffset) : nullptr;
+  if (pace) DG_CUDA(cudaMemsetAsync(ws + p->off_status + kProgressOffset, 0, (size_t)p->tp * 4, ms));
   kp.timeout_ns = (uint64_t)p->timeout_ms * 1000000ull;
   kp.hang_ns = kp.timeout_ns * 4 + 1000000000ull;
 
@@ -958,8 +1006,11 @@ int dg_run_ex(dg_plan_t p, const void* A, const void* B, const dg_bf16_t* C, con
       rc = launch(p, ms, 1);
       if (rc) return rc;
       for (int i = 0; i < ns; ++i) DG_CUDA(cudaStreamWaitEvent(streams[i], p->ev_fork, 0));
-      rc = enqueue_copies(p, drv, A, B, ws, streams, ns);
+      rc = enqueue_copies(p, drv, A, B, ws, streams, ns, pace);
       if (rc) return rc;
+      // Release every pacing wait still pending (a kernel that stopped early
+      // never reaches the later steps): no copy-stream wait outlives the kernel.
+      if (pace) DG_CUDA(cudaMemsetAsync(ws + p->off_status + kProgressOffset, 0x01, (size_t)p->tp * 4, ms));
       for (int i = 1; i < ns; ++i) {
         DG_CUDA(cudaEventRecord(p->extra_done[i - 1], streams[i]));
         DG_CUDA(cudaStreamWaitEvent(cs, p->extra_done[i - 1], 0));
@@ -967,7 +1018,7 @@ int dg_run_ex(dg_plan_t p, const void* A, const void* B, const dg_bf16_t* C, con
       DG_CUDA(cudaEventRecord(p->ev_join, cs));
       DG_CUDA(cudaStreamWaitEvent(ms, p->ev_join, 0));
     } else if (mode == DG_MODE_SERIAL) {
-      rc = enqueue_copies(p, drv, A, B, ws, &ms, 1);
+      rc = enqueue_copies(p, drv, A, B, ws, &ms, 1, false);
       if (rc) return rc;
       rc = launch(p, ms, 1);
       if (rc) return rc;

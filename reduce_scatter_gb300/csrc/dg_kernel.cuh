@@ -110,6 +110,7 @@ struct KParams {
                         // (0 none, 1 evict-first, 2 evict-last)
   uint32_t wave_sync;   // producers start tile i only after every CTA issued tile i-1
   uint32_t* wave_ctr;   // per-run counter of tiles whose loads are issued (zeroed per run)
+  uint32_t* progress;   // AG copy pacing: progress[s] set to 1 once a producer reaches step s, or null
   float alpha, beta;
   float bias_scale;  // weight of the bias in every epilogue pass (1, or 1/P for the mean)
   uint32_t out_f32;  // D is fp32
@@ -196,6 +197,9 @@ __device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -769,8 +773,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
       for (int i = 0; i < STAGES; ++i) issued[i] = -1;
       bool ok = true;
       uint32_t wave = 0;
+      int32_t step_seen = -1;
       for (int64_t t = unit; t < T && ok; t += nunits, ++wave) {
         const Tile tl = decode_tile(p.g, t);
+        if (p.progress && tl.s != step_seen) {
+          // the copies of step s + 1 may start now (paced shard transfers);
+          // set before any wait of this step, so it never depends on them
+          step_seen = tl.s;
+          st_relaxed_u32(p.progress + tl.s, 1u);
+        }
         if (p.wave_sync && wave > 0) {
           // keep the CTAs in phase so that tiles sharing an operand strip read
           // it while it is still in L2 (a timing gate only: no data depends on it)

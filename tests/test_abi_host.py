@@ -288,3 +288,20 @@ def test_output_type_and_reduce_op_rules(L):
     assert (info["out_type"], info["reduce_op"]) == (dg.TYPE_F32, dg.REDUCE_AVG)
     with pytest.raises(dg.DGError):
         q.set_option(dg.OPT_REDUCE_OP, 2)
+
+
+def test_copy_pace_option_rules(L):
+    p = dg.Plan(512, 512, 512, 1, 4, dg.AG_ROTATING_A)
+    for v in (-1, 0, 1):
+        p.set_option(dg.OPT_COPY_PACE, v)
+    for v in (-2, 2):
+        with pytest.raises(dg.DGError):
+            p.set_option(dg.OPT_COPY_PACE, v)
+
+
+def test_copy_kind_option_rules(L):
+    p = dg.Plan(512, 512, 512, 1, 4, dg.AG_ROTATING_A)
+    p.set_option(dg.OPT_COPY_KIND, 1)
+    p.set_option(dg.OPT_COPY_KIND, 0)
+    with pytest.raises(dg.DGError):
+        p.set_option(dg.OPT_COPY_KIND, 2)

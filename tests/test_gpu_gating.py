@@ -138,3 +138,44 @@ def test_rs_grid_equal_to_step_distance(sched, tp):
     D, rc = r.run(A, B, C, check=False)
     assert rc == dg.OK, dg.last_error()
     assert rel_err(D, oracle_full(a, b, c, 0.5, 1.0)) <= TOL
+
+
+@pytest.mark.parametrize("sched", [dg.AG_ROTATING_A, dg.AG_ROTATING_B], ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_paced_transfers_same_bits(sched):
+    # copies of step s >= 2 held until the kernel reaches step s - 1, or all at once
+    m, n, k, l, tp = 2048, 2048, 512, 2, 8
+    a, b, c = host_inputs(m, n, k, l, seed=400 + sched)
+    A, B, C = to_dev(a), to_dev(b), to_dev(c)
+    D = {}
+    for pace in (0, 1):
+        r = Runner(m, n, k, l, tp, sched, 0.5, 1.0, options={dg.OPT_COPY_PACE: pace, dg.OPT_CHUNK_TILES: 1})
+        D[pace], _ = r.run(A, B, C)
+        D2, _ = r.run(A, B, C)                        # the progress words are reset per run
+        assert torch.equal(D[pace].view(torch.int16), D2.view(torch.int16))
+    assert torch.equal(D[0].view(torch.int16), D[1].view(torch.int16))
+    assert rel_err(D[1], oracle_full(a, b, c, 0.5, 1.0)) <= TOL
+
+
+def test_paced_transfers_with_held_copies():
+    # copies held back on the host and NaN-poisoned slots: pacing must still gate every load
+    m, n, k, l, tp = 1024, 1024, 256, 1, 4
+    a, b, c = host_inputs(m, n, k, l, seed=410)
+    A, B = to_dev(a), to_dev(b)
+    r = Runner(m, n, k, l, tp, dg.AG_ROTATING_A, options={dg.OPT_COPY_PACE: 1, dg.OPT_FAULT_DELAY_MS: 50})
+    info = r.plan.info()
+    r.ws[info["off_slots"]:info["off_slots"] + info["slot_bytes"] * tp * (tp - 1)].view(torch.int16).fill_(0x7FC0)
+    D, _ = r.run(A, B, None)
+    assert rel_err(D, oracle_full(a, b, c, 1.0, 0.0)) <= TOL
+
+
+@pytest.mark.parametrize("sched", [dg.AG_ROTATING_A, dg.AG_ROTATING_B], ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_copy_kinds_same_bits(sched):
+    # copy-engine (2D) and one-dimensional transfers move the same bytes
+    m, n, k, l, tp = 1024, 2048, 512, 2, 4
+    a, b, c = host_inputs(m, n, k, l, seed=420 + sched)
+    A, B, C = to_dev(a), to_dev(b), to_dev(c)
+    D = {}
+    for kind in (0, 1):
+        r = Runner(m, n, k, l, tp, sched, 0.5, 1.0, options={dg.OPT_COPY_KIND: kind})
+        D[kind], _ = r.run(A, B, C)
+    assert torch.equal(D[0].view(torch.int16), D[1].view(torch.int16))
