@@ -60,6 +60,13 @@ def parse_args(argv=None):
                     help="extra plan option, e.g. L2_HINT=9 (names of dg.OPT_*)")
     ap.add_argument("--cpu-sample-rows", type=int, default=1024)
     ap.add_argument("--cpu-sample-cols", type=int, default=4096)
+    ap.add_argument("--record-traffic", metavar="CSV", default=None,
+                    help="store the DRAM bytes of an ncu --csv capture (dram__bytes_read.sum, "
+                         "dram__bytes_write.sum, gpu__time_duration.sum of one dg_gemm launch) in "
+                         "profiles/dram_traffic.json for --workload, tagged with the kernel source hash, "
+                         "and exit")
+    ap.add_argument("--record-command", default="", help="the ncu command line the CSV came from")
+    ap.add_argument("--record-note", default="", help="a note stored with the record")
     return ap.parse_args(argv)
 
 
@@ -96,6 +103,47 @@ def recorded_traffic(workload: str):
     if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
         return None
     return ent.get("bytes_per_launch")
+
+
+_UNIT = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12,
+         "ns": 1.0, "nsecond": 1.0, "us": 1e3, "usecond": 1e3, "ms": 1e6, "msecond": 1e6}
+
+
+def record_traffic(workload: str, csv_path: str, command: str, note: str) -> dict:
+    """Parse one dg_gemm launch from an ncu --csv log and store it for the
+    bench's roofline.traffic (only trusted while the kernel source is unchanged)."""
+    import csv
+
+    metrics, kernel = {}, None
+    with open(csv_path, newline="") as f:
+        rows = [r for r in csv.reader(line for line in f if line.startswith('"'))]
+    head = rows[0]
+    col = {name: i for i, name in enumerate(head)}
+    for r in rows[1:]:
+        if "dg_gemm" not in r[col["Kernel Name"]]:
+            continue
+        if kernel is not None and r[col["ID"]] != kernel[0]:
+            break  # first captured launch only
+        kernel = (r[col["ID"]], r[col["Kernel Name"]])
+        val = float(r[col["Metric Value"]].replace(",", "")) * _UNIT.get(r[col["Metric Unit"]], float("nan"))
+        metrics[r[col["Metric Name"]]] = val
+    need = ("dram__bytes_read.sum", "dram__bytes_write.sum", "gpu__time_duration.sum")
+    if kernel is None or any(k not in metrics for k in need):
+        raise SystemExit(f"{csv_path}: no dg_gemm launch with {need}")
+    rd, wr = int(metrics[need[0]]), int(metrics[need[1]])
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        rec = {}
+    rec[workload] = {"bytes_per_launch": rd + wr, "dram_bytes_read": rd, "dram_bytes_write": wr,
+                     "kernel": kernel[1], "kernel_source_hash": kernel_source_hash(),
+                     "gpu__time_duration_ns": int(metrics[need[2]]), "command": command, "note": note}
+    with open(path, "w") as f:
+        json.dump(rec, f, indent=1)
+        f.write("\n")
+    return rec[workload]
 
 
 class ClockSampler:
@@ -491,6 +539,10 @@ def main(argv=None):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     w = configs.WORKLOADS[args.workload]
+
+    if args.record_traffic:
+        print(json.dumps(record_traffic(args.workload, args.record_traffic, args.record_command, args.record_note)))
+        return 0
 
     if args.impl == "reference":
         if rank != 0:

@@ -29,3 +29,32 @@ def test_reference_arm_line():
 def test_default_workload_is_the_tp8_run():
     args = bench.parse_args([])
     assert args.workload == "ag_a_tp8_pr" and args.gpus == 1 and args.warmup >= 3
+
+
+def test_record_traffic_parses_an_ncu_csv(tmp_path, monkeypatch):
+    import bench
+
+    csv = tmp_path / "dram.csv"
+    csv.write_text(
+        "==PROF== Connected to process 1\n"
+        '"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size","Grid Size",'
+        '"Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"\n'
+        '"0","1","p","h","void other_kernel()","1","7","(1,1,1)","(1,1,1)","0","10.3","s","dram__bytes_read.sum","byte","5"\n'
+        '"1","1","p","h","void dg_gemm_kernel<2, 1, 0>(KParams)","1","7","(192, 1, 1)","(152, 1, 1)","0","10.3","s",'
+        '"dram__bytes_read.sum","Gbyte","56.70"\n'
+        '"1","1","p","h","void dg_gemm_kernel<2, 1, 0>(KParams)","1","7","(192, 1, 1)","(152, 1, 1)","0","10.3","s",'
+        '"dram__bytes_write.sum","byte","3,491,002,624"\n'
+        '"1","1","p","h","void dg_gemm_kernel<2, 1, 0>(KParams)","1","7","(192, 1, 1)","(152, 1, 1)","0","10.3","s",'
+        '"gpu__time_duration.sum","ms","30.5"\n')
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "reduce_scatter_gb300" / "csrc").mkdir(parents=True)
+    for name in ("dg_kernel.cuh", "dg_geom.h"):
+        (tmp_path / "reduce_scatter_gb300" / "csrc" / name).write_text(name)
+    ent = bench.record_traffic("ag_a_tp8_pr", str(csv), "ncu ...", "note")
+    assert ent["dram_bytes_read"] == 56_700_000_000 and ent["dram_bytes_write"] == 3_491_002_624
+    assert ent["gpu__time_duration_ns"] == 30_500_000
+    assert bench.recorded_traffic("ag_a_tp8_pr") == ent["bytes_per_launch"]
+    (tmp_path / "reduce_scatter_gb300" / "csrc" / "dg_geom.h").write_text("changed")
+    assert bench.recorded_traffic("ag_a_tp8_pr") is None       # stale once the kernel changes
