@@ -408,6 +408,17 @@ def run_dg(args, rank, world, dist):
     plan.check(ws, main)
     clocks = clk.summary()
 
+    # latency-bound sizes: the same run replayed from a CUDA graph (one launch
+    # of the whole captured run instead of its host-side enqueue)
+    ms_graph = None
+    if not args.no_modes and mode == dg.MODE_FUSED and ms_fused < 1.0:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            plan.run(A, B, C, D, ws, torch.cuda.current_stream(), copy)
+        ms_graph = timed_loop(graph.replay, args.steps, args.warmup, main, flush)
+        plan.check(ws, main)
+        del graph
+
     ms_gemm = ms_serial = None
     if (not args.no_modes and mode == dg.MODE_FUSED and w.schedule in (dg.AG_ROTATING_A, dg.AG_ROTATING_B)
             and w.tp > 1):
@@ -521,6 +532,7 @@ def run_dg(args, rank, world, dist):
         "copy_hidden_fraction": None if hidden is None else round(hidden, 4),
         "fused_over_gemm_only": None if ms_gemm is None else round(ms_fused / ms_gemm, 4),
         "ms_unsharded_tp1": None if ms_tp1 is None else round(ms_tp1, 4),
+        "ms_graph_replay": None if ms_graph is None else round(ms_graph, 4),
         "ms_rs_nonfused_baseline": None if ms_nonfused is None else round(ms_nonfused, 4),
         "fused_speedup_vs_nonfused": None if ms_nonfused is None else round(ms_nonfused / ms_fused, 4),
         "roofline": {"bound": "tensor", "achieved": round(per_gpu, 2), "peak": peak, "unit": "TFLOP/s",

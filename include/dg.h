@@ -234,7 +234,13 @@ int dg_set_option(dg_plan_t plan, int option, int64_t value);
  * of the AG schedules).  Asynchronous: returns after enqueueing; the work is
  * ordered after prior work on main_stream and later work on main_stream is
  * ordered after all of it (copies included).  Device-side failures are
- * reported by dg_check. */
+ * reported by dg_check.  The call may be captured into a CUDA graph on
+ * main_stream (the copy streams join the capture through events); the graph
+ * then clears the workspace's status and flag words at the start of every
+ * replay, and replays must keep A, B, C, D and the workspace at the captured
+ * addresses.  dg_check reports a replay's device status only until the plan
+ * runs again outside the graph.  Make one run outside capture first (it sets
+ * up the kernels' attributes). */
 int dg_run(dg_plan_t plan, const void* A, const void* B, const dg_bf16_t* C,
            dg_bf16_t* D, void* workspace, void* main_stream, void* copy_stream);
 

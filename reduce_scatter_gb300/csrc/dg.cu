@@ -941,6 +941,12 @@ int dg_run_ex(dg_plan_t p, const void* A, const void* B, const dg_bf16_t* C, con
       clear = true;
     }
   }
+  // Under stream capture the run's epoch is frozen into the graph, so every
+  // replay must start from zeroed status and flag words: clear them in the
+  // graph itself (one memset node).
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  DG_CUDA(cudaStreamIsCapturing(ms, &cap));
+  if (cap == cudaStreamCaptureStatusActive) clear = true;
   if (clear) DG_CUDA(cudaMemsetAsync(ws, 0, p->off_flags + (size_t)p->n_flags * 4, ms));
   if (wrap) p->epoch = 0;
   p->epoch += 1;
