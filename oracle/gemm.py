@@ -164,3 +164,21 @@ def fused_gemm(A, B_nk, C, alpha: float, beta: float, *, P: int = 1, reduce_op=N
             raise ValueError("beta != 0 needs C")
         D = D + np.float64(beta) * np.asarray(C, dtype=np.float64)
     return D
+
+
+def fused_gemm_entries(A_rows, B_rows, C_block, alpha: float, beta: float, *, P: int = 1, reduce_op=None,
+                       bias_cols=None) -> np.ndarray:
+    """``fused_gemm`` on a sample: rows i of A against rows j of the stored
+    (N, K) B (any one batch), ``C_block`` (R, S) or None, ``bias_cols`` the
+    bias at those columns j (S,) or None.  Returns the (R, S) block of D."""
+    if reduce_op not in (None, "sum", "avg"):
+        raise ValueError(f"reduce_op must be None, 'sum' or 'avg', got {reduce_op!r}")
+    D = np.float64(alpha) * (np.asarray(A_rows, np.float64) @ np.asarray(B_rows, np.float64).T)
+    if bias_cols is not None:
+        copies = 1 if reduce_op is None else P
+        D = D + np.float64(copies) * np.asarray(bias_cols, dtype=np.float64)
+    if reduce_op == "avg":
+        D = D / np.float64(P)
+    if beta != 0.0:
+        D = D + np.float64(beta) * np.asarray(C_block, dtype=np.float64)
+    return D

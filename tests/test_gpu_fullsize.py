@@ -74,3 +74,41 @@ def test_full_size(name):
     else:
         err = (D.float() - ref.float()).abs().max().item() / ref.float().abs().max().item()
         assert err <= TOL, err
+
+
+@pytest.mark.parametrize("name,op", [("ag_b_tp4_batched", None), ("rs_b_tp4_batched", "avg"),
+                                     ("rs_a_tp8", "sum")])
+def test_full_size_bias_f32_out(name, op):
+    # the scaled ops' epilogue extras at full size: bias, fp32 D, the reduce op
+    w = configs.WORKLOADS[name]
+    A, B, C = _dev_inputs(w)
+    bias_bits = synth.tensor_bits_np(w.seed, synth.STREAM_BIAS, (w.n,), ("uniform", -4.0, 4.0))
+    bias = torch.from_numpy(bias_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    plan = dg.Plan(w.m, w.n, w.k, w.l, w.tp, w.schedule, w.alpha, w.beta, out_type="f32",
+                   reduce_op=op or "sum")
+    ws = torch.zeros(max(plan.workspace_bytes(), 256), dtype=torch.uint8, device="cuda")
+    D = torch.full((w.l, w.m, w.n), float("nan"), dtype=torch.float32, device="cuda")
+    main = torch.cuda.current_stream()
+    plan.run_ex(A, B, C, bias, D, ws, main, torch.cuda.Stream())
+    plan.check(ws, main)
+    assert not torch.isnan(D).any()
+    rng = np.random.default_rng(777)
+    LM = w.l * w.m
+    rows = np.unique(np.concatenate([rng.integers(0, LM, 40), [0, LM - 1]]))
+    cols = np.unique(np.concatenate([rng.integers(0, w.n, 40), [0, w.n - 1]]))
+    Dh = D.view(LM, w.n)[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()].cpu().numpy()
+    bcols = og.bf16_bits_to_f64(bias_bits)[cols]
+    for b in range(w.l):
+        rs = rows[(rows >= b * w.m) & (rows < (b + 1) * w.m)]
+        if len(rs) == 0:
+            continue
+        a = og.bf16_bits_to_f64(synth.rows_bits_np(w.seed, synth.STREAM_A, (LM, w.k), rs, w.dist_a))
+        bb = og.bf16_bits_to_f64(synth.rows_bits_np(w.seed, synth.STREAM_B, (w.l * w.n, w.k), cols + b * w.n, w.dist_b))
+        c = None
+        if w.beta != 0:
+            c = og.bf16_bits_to_f64(synth.rows_bits_np(w.seed, synth.STREAM_C, (LM, w.n), rs, w.dist_c)[:, cols])
+        want = og.fused_gemm_entries(a, bb, c, w.alpha, w.beta, P=w.tp, reduce_op=op, bias_cols=bcols)
+        got = Dh[np.isin(rows, rs)].astype(np.float64)
+        # fp32 D: fp32 accumulation over up to 28672 terms stays far inside 2e-3 of max|D|, and a
+        # result rounded to bf16 on the way (2^-9 relative) would not
+        assert np.abs(got - want).max() / np.abs(want).max() <= 2e-3

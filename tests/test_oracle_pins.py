@@ -108,3 +108,17 @@ def test_bias_and_reduce_op_closed_forms():
 
 def test_every_schedule_with_bias_and_reduce_op():
     pc.check_schedule_bias_reduce(osch.run_schedule, og.fused_gemm, osch.SCHEDULES)
+
+
+def test_fused_sampled_entries_match_full():
+    # the sampled form agrees with the pinned full form (integer inputs: exact)
+    A = pc._int_valued(4, 1, (1, 40, 24))[0]
+    B = pc._int_valued(4, 2, (1, 30, 24))[0]
+    C = pc._int_valued(4, 3, (1, 40, 30))[0]
+    bias = pc._int_valued(4, 4, (30,))
+    rows, cols = np.array([0, 7, 39]), np.array([1, 29, 5])
+    for op, P in ((None, 1), ("sum", 4), ("avg", 4)):
+        full = og.fused_gemm(A[None], B[None], C[None], 0.5, 1.0, P=P, reduce_op=op, bias=bias)[0]
+        blk = og.fused_gemm_entries(A[rows], B[cols], C[np.ix_(rows, cols)], 0.5, 1.0, P=P, reduce_op=op,
+                                    bias_cols=bias[cols])
+        assert np.array_equal(blk, full[np.ix_(rows, cols)]), op
