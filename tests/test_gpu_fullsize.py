@@ -109,6 +109,7 @@ def test_full_size_bias_f32_out(name, op):
             c = og.bf16_bits_to_f64(synth.rows_bits_np(w.seed, synth.STREAM_C, (LM, w.n), rs, w.dist_c)[:, cols])
         want = og.fused_gemm_entries(a, bb, c, w.alpha, w.beta, P=w.tp, reduce_op=op, bias_cols=bcols)
         got = Dh[np.isin(rows, rs)].astype(np.float64)
-        # fp32 D: fp32 accumulation over up to 28672 terms stays far inside 2e-3 of max|D|, and a
-        # result rounded to bf16 on the way (2^-9 relative) would not
-        assert np.abs(got - want).max() / np.abs(want).max() <= 2e-3
+        # fp32 D: the fp32 accumulation error (about sqrt(K) * 2^-24 relative for these random
+        # inputs) stays far inside 5e-4 of max|D|; a result rounded to bf16 on the way (up to
+        # 2^-9 of each entry) would exceed it at the largest entries
+        assert np.abs(got - want).max() / np.abs(want).max() <= 5e-4
