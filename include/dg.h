@@ -263,6 +263,21 @@ int dg_run(dg_plan_t plan, const void* A, const void* B, const dg_bf16_t* C,
 int dg_run_ex(dg_plan_t plan, const void* A, const void* B, const dg_bf16_t* C, const dg_bf16_t* bias,
               void* D, void* workspace, void* main_stream, void* copy_stream);
 
+/* dg_run_ex with host-resident operands, for callers whose data lives in
+ * host memory: on main_stream, copies A and B (and C when beta != 0) from
+ * host memory into the caller's device buffers, runs the plan on them, and
+ * copies D back into host memory.  Sizes follow the plan: A L*M*K elements,
+ * B L*N*K (both of the plan's input type), C L*M*N bf16, D L*M*N of the
+ * output type.  Host buffers should be page-locked (cudaHostAlloc or
+ * cudaHostRegister) for the copies to be asynchronous and to run on a copy
+ * engine; pageable memory works with host-synchronous copies.  bias, if not
+ * NULL, is a device pointer.  The device buffers follow dg_run's rules.
+ * Returns after enqueueing; D_host is valid once main_stream has reached
+ * that point (e.g. after dg_check). */
+int dg_run_host(dg_plan_t plan, const void* A_host, const void* B_host, const dg_bf16_t* C_host,
+                const dg_bf16_t* bias, void* D_host, void* A_dev, void* B_dev, dg_bf16_t* C_dev, void* D_dev,
+                void* workspace, void* main_stream, void* copy_stream);
+
 /* Synchronize `stream` and read the workspace status word of the plan's last
  * run: DG_OK, DG_ERR_TIMEOUT or DG_ERR_HANG (with the flag index in the
  * message), or DG_ERR_CUDA on a CUDA error. */

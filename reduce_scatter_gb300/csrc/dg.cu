@@ -1039,6 +1039,30 @@ int dg_run_ex(dg_plan_t p, const void* A, const void* B, const dg_bf16_t* C, con
   return DG_OK;
 }
 
+int dg_run_host(dg_plan_t p, const void* A_host, const void* B_host, const dg_bf16_t* C_host, const dg_bf16_t* bias,
+                void* D_host, void* A_dev, void* B_dev, dg_bf16_t* C_dev, void* D_dev, void* workspace,
+                void* main_stream, void* copy_stream) {
+  if (!p) return fail(DG_ERR_ARG, "plan is NULL");
+  if (p->g.total_tiles == 0) return DG_OK;  // empty output
+  if (!A_host || !B_host || !D_host) return fail(DG_ERR_ARG, "A_host, B_host and D_host must be non-NULL");
+  if (p->beta != 0.f && (!C_host || !C_dev)) return fail(DG_ERR_ARG, "C_host and C_dev are needed when beta != 0");
+  if (!A_dev || !B_dev || !D_dev) return fail(DG_ERR_ARG, "A_dev, B_dev and D_dev must be non-NULL");
+  auto ms = static_cast<cudaStream_t>(main_stream);
+  const size_t a_bytes = (size_t)(p->l * p->m * p->k) * (size_t)p->esz;
+  const size_t b_bytes = (size_t)(p->l * p->n * p->k) * (size_t)p->esz;
+  const size_t c_bytes = (size_t)(p->l * p->m * p->n) * 2;
+  const size_t d_bytes = (size_t)(p->l * p->m * p->n) * (p->out_type == DG_TYPE_F32 ? 4 : 2);
+  // host to device on the main stream (pinned host memory: copy engine, asynchronous)
+  DG_CUDA(cudaMemcpyAsync(A_dev, A_host, a_bytes, cudaMemcpyHostToDevice, ms));
+  DG_CUDA(cudaMemcpyAsync(B_dev, B_host, b_bytes, cudaMemcpyHostToDevice, ms));
+  if (p->beta != 0.f) DG_CUDA(cudaMemcpyAsync(C_dev, C_host, c_bytes, cudaMemcpyHostToDevice, ms));
+  int rc = dg_run_ex(p, A_dev, B_dev, p->beta != 0.f ? C_dev : nullptr, bias, D_dev, workspace, main_stream,
+                     copy_stream);
+  if (rc) return rc;
+  DG_CUDA(cudaMemcpyAsync(D_host, D_dev, d_bytes, cudaMemcpyDeviceToHost, ms));
+  return DG_OK;
+}
+
 int dg_check(dg_plan_t p, void* workspace, void* stream) {
   if (!p) return fail(DG_ERR_ARG, "plan is NULL");
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));

@@ -70,7 +70,7 @@ OPT_COPY_KIND = 14
 # Every symbol include/dg.h declares.
 EXPORTS = ("dg_plan", "dg_workspace_bytes", "dg_run_mode", "dg_set_option", "dg_run", "dg_check",
            "dg_plan_info_get", "dg_plan_tile", "dg_destroy", "dg_last_error", "dg_run_static",
-           "dg_plan_scaled", "dg_run_ex")
+           "dg_plan_scaled", "dg_run_ex", "dg_run_host")
 
 # Size of the library's built-in workspace used by dg_run_static.
 STATIC_WORKSPACE_BYTES = 32 << 20
@@ -147,6 +147,8 @@ def lib():
         L.dg_run.restype = i32
         L.dg_run_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.dg_run_ex.restype = i32
+        L.dg_run_host.argtypes = [vp] * 13
+        L.dg_run_host.restype = i32
         L.dg_run_static.argtypes = [vp, vp, vp, vp, vp, vp, vp]
         L.dg_run_static.restype = i32
         L.dg_check.argtypes = [vp, vp, vp]
@@ -265,6 +267,16 @@ class Plan:
         """``dg_run_ex``: an optional per-column bf16 bias; D of the plan's output type."""
         rc = lib().dg_run_ex(self._h, ptr(A), ptr(B), ptr(C), ptr(bias), ptr(D), ptr(workspace),
                              stream_handle(main_stream), stream_handle(copy_stream))
+        if raise_on_error:
+            _check(rc)
+        return rc
+
+    def run_host(self, A_host, B_host, C_host, bias, D_host, A_dev, B_dev, C_dev, D_dev, workspace, main_stream=None,
+                 copy_stream=None, raise_on_error=True) -> int:
+        """``dg_run_host``: inputs copied from host memory, D copied back (host tensors' data_ptr)."""
+        rc = lib().dg_run_host(self._h, ptr(A_host), ptr(B_host), ptr(C_host), ptr(bias), ptr(D_host), ptr(A_dev),
+                               ptr(B_dev), ptr(C_dev), ptr(D_dev), ptr(workspace), stream_handle(main_stream),
+                               stream_handle(copy_stream))
         if raise_on_error:
             _check(rc)
         return rc

@@ -305,3 +305,12 @@ def test_copy_kind_option_rules(L):
     p.set_option(dg.OPT_COPY_KIND, 0)
     with pytest.raises(dg.DGError):
         p.set_option(dg.OPT_COPY_KIND, 2)
+
+
+def test_run_host_argument_checks_without_gpu(L):
+    p = dg.Plan(256, 256, 256, 1, 2, dg.AG_ROTATING_A, 1.0, 0.5)
+    # missing host or device buffers, C missing with beta != 0: refused before any CUDA call
+    assert p.run_host(None, 16, None, None, 16, 16, 16, None, 16, 256, raise_on_error=False) == dg.ERR_ARG
+    assert p.run_host(16, 16, None, None, 16, 16, 16, None, 16, 256, raise_on_error=False) == dg.ERR_ARG
+    q = dg.Plan(256, 256, 256, 1, 2, dg.AG_ROTATING_A)
+    assert q.run_host(16, 16, None, None, 16, None, 16, None, 16, 256, raise_on_error=False) == dg.ERR_ARG

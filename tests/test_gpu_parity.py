@@ -252,3 +252,23 @@ def test_wave_sync_does_not_change_results(sched):
         D, rc = r.run(A, B, C)
         assert rc == dg.OK
         assert torch.equal(D.view(torch.int16), ref.view(torch.int16))
+
+
+@pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_run_host_matches_device_run(sched):
+    # dg_run_host: pinned host inputs uploaded, the run, D downloaded; same bits as dg_run
+    m, n, k, l, tp = 1024, 1024, 512, 2, 4
+    a, b, c = host_inputs(m, n, k, l, seed=90 + sched)
+    A_h = torch.from_numpy(a.view(np.int16)).pin_memory()
+    B_h = torch.from_numpy(b.view(np.int16)).pin_memory()
+    C_h = torch.from_numpy(c.view(np.int16)).pin_memory()
+    D_h = torch.empty((l, m, n), dtype=torch.int16).pin_memory()
+    r = Runner(m, n, k, l, tp, sched, 0.5, 1.0)
+    A = torch.empty((l, m, k), dtype=torch.bfloat16, device="cuda")
+    B = torch.empty((l, n, k), dtype=torch.bfloat16, device="cuda")
+    C = torch.empty((l, m, n), dtype=torch.bfloat16, device="cuda")
+    D = torch.empty((l, m, n), dtype=torch.bfloat16, device="cuda")
+    r.plan.run_host(A_h, B_h, C_h, None, D_h, A, B, C, D, r.ws, r.main, r.copy)
+    r.plan.check(r.ws, r.main)
+    want, _ = Runner(m, n, k, l, tp, sched, 0.5, 1.0).run(to_dev(a), to_dev(b), to_dev(c))
+    assert torch.equal(D_h, want.view(torch.int16).cpu())
