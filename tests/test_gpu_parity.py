@@ -272,3 +272,27 @@ def test_run_host_matches_device_run(sched):
     r.plan.check(r.ws, r.main)
     want, _ = Runner(m, n, k, l, tp, sched, 0.5, 1.0).run(to_dev(a), to_dev(b), to_dev(c))
     assert torch.equal(D_h, want.view(torch.int16).cpu())
+
+
+@pytest.mark.parametrize("tp", [1, 2, 4])
+@pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_tiny_shapes_against_brute_force(sched, tp):
+    # the device path against the triple loop itself (not only the oracle) on
+    # integer-valued inputs, where every summation order is exact
+    from tests.pin_checks import brute_gemm
+    for (m, n, k, l) in [(64, 64, 64, 1), (32, 48, 64, 2)]:
+        if not _shape_ok(sched, m, n, k, tp):
+            continue
+        rng = np.random.default_rng(1000 + 10 * sched + tp + m)
+        Ai = rng.integers(-4, 5, (l, m, k)).astype(np.float32)
+        Bi = rng.integers(-4, 5, (l, n, k)).astype(np.float32)
+        Ci = rng.integers(-4, 5, (l, m, n)).astype(np.float32)
+        A = torch.from_numpy(Ai).cuda().to(torch.bfloat16)
+        B = torch.from_numpy(Bi).cuda().to(torch.bfloat16)
+        C = torch.from_numpy(Ci).cuda().to(torch.bfloat16)
+        D, _ = Runner(m, n, k, l, tp, sched, 0.5, 2.0).run(A, B, C)
+        want = brute_gemm(Ai.astype(np.float64), Bi.astype(np.float64), Ci.astype(np.float64), 0.5, 2.0)
+        # every partial and the fp32 epilogue are exact here (|acc| <= 64 * 16), so D is the exact
+        # result rounded once to bf16 (nearest even): equal bits
+        want_bf16 = torch.from_numpy(want.astype(np.float32)).to(torch.bfloat16)
+        assert torch.equal(D.cpu().view(torch.int16), want_bf16.view(torch.int16)), (m, n, k, l)
