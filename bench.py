@@ -300,6 +300,7 @@ def timed_loop(run, steps, warmup, stream, flush=None):
         run()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.nvtx.range_push("timed loop")
     for s, e in ev:
         if flush is not None:
             flush()
@@ -307,6 +308,7 @@ def timed_loop(run, steps, warmup, stream, flush=None):
         run()
         e.record(stream)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     return sum(s.elapsed_time(e) for s, e in ev) / steps
 
 

@@ -19,6 +19,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <chrono>
@@ -108,6 +109,14 @@ std::unordered_map<const void*, uint64_t> g_ws_owner;
 uint64_t g_next_plan_id = 1;
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// NVTX range over a host-side call (a no-op unless a profiler is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Layout of the 256-byte status area: [0, 8) status word, [64, 68) wave
 // counter, [128, 128 + 4 * tp) copy-pacing progress words.
@@ -485,6 +494,7 @@ int ensure_extra_streams(dg_plan_s* p, int want) {
 // Chunks are dealt round-robin over `ns` streams.
 int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B, uint8_t* ws,
                    cudaStream_t* streams, int ns, bool pace) {
+  NvtxRange range("dg_enqueue_copies");
   auto* progress = reinterpret_cast<uint32_t*>(ws + p->off_status + kProgressOffset);
   const dg::Geom& g = p->g;
   const int64_t P = p->tp;
@@ -898,6 +908,7 @@ int dg_run(dg_plan_t p, const void* A, const void* B, const dg_bf16_t* C, dg_bf1
 
 int dg_run_ex(dg_plan_t p, const void* A, const void* B, const dg_bf16_t* C, const dg_bf16_t* bias, void* D,
               void* workspace, void* main_stream, void* copy_stream) {
+  NvtxRange range("dg_run");
   if (!p) return fail(DG_ERR_ARG, "plan is NULL");
   if (p->g.total_tiles == 0) return DG_OK;  // empty output
   if (!A || !B || !D) return fail(DG_ERR_ARG, "A, B and D must be non-NULL");
