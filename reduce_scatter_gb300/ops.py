@@ -156,7 +156,9 @@ def _gemm(schedule: int, A2: torch.Tensor, B: torch.Tensor, tp: int, *, alpha=1.
     D2 = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device=dev)
     key = (dev.index, schedule, M, N, K, tp, float(alpha), float(beta), ta, tb, float(scale_a), float(scale_b),
            to, op)
-    with _lock:
+    if Bnk.device != dev or (C2 is not None and C2.device != dev) or (bias is not None and bias.device != dev):
+        raise ValueError("A, B, C and bias must be on the same device")
+    with _lock, torch.cuda.device(dev):  # the library works on the current device
         plan = _plans.get(key)
         if plan is None:
             plan = dg.Plan(M, N, K, 1, tp, schedule, alpha, beta, ta, tb, scale_a, scale_b, out_type=to,
