@@ -29,9 +29,13 @@
  * (K / tp) % 8 == 0.  Shards need not be multiples of the tile.
  *
  * Ownership: the caller owns A, B, C, D, the workspace and both streams.  The
- * plan owns only host state (geometry, events, cached tensor maps).  A
- * workspace belongs to one plan at a time; the first run of a plan with a
- * given workspace clears the workspace's flag words on the main stream.
+ * plan owns only host state (geometry, events, cached tensor maps, the extra
+ * copy streams it creates).  A workspace belongs to one plan at a time; the
+ * first run of a plan with a given workspace clears the workspace's flag
+ * words on the main stream.  Calls on one plan must not overlap in time
+ * (different plans may be used from different threads); a plan's runs are
+ * ordered on its main stream, and two runs of one plan must not share a
+ * workspace while the first is still executing on another main stream.
  *
  * Errors: every int-returning call returns DG_OK (0) or a negative dg_status;
  * dg_last_error() gives a message for the calling thread.
