@@ -154,3 +154,33 @@ def test_scaled_ops_fp8_bias_f32(reduce_op):
     Db = ops.fused_scaled_matmul_reduce_scatter(A, W.t(), sa, sb, reduce_op, 1, tp, bias=bias)
     assert Db.dtype == torch.bfloat16
     assert torch.equal(Db.view(torch.int16), Dr.to(torch.bfloat16).view(torch.int16))
+
+
+@pytest.mark.gpu
+def test_four_dim_gather_and_restride():
+    # gather along a middle dimension of a 4-D A; a restrided A is read without a layout copy
+    tp = 4
+    A = _randn((2, 3, 256, 256), 12)
+    W = _randn((512, 256), 13, std=0.05)
+    _, (D,) = ops.fused_all_gather_matmul(A, [W.t()], 2, tp)
+    want = torch.matmul(A.double(), W.double().t())
+    assert D.shape == (2, 3, 256, 512) and _rel(D, want) <= TOL
+    Ar = ops.restride_A_shard_for_fused_all_gather_matmul(A, 2)
+    assert Ar.movedim(2, 0).is_contiguous()
+    _, (Dr,) = ops.fused_all_gather_matmul(Ar, [W.t()], 2, tp)
+    assert torch.equal(Dr.view(torch.int16), D.view(torch.int16))
+
+
+@pytest.mark.gpu
+def test_scaled_reduce_scatter_over_n_with_bias():
+    # scatter_dim = the output's last dimension: the N-slab schedule, with a bias and fp32 D
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("no float8 in this torch")
+    tp = 4
+    A = _randn((2, 256, 512), 14, dtype=torch.float32).to(torch.float8_e4m3fn)
+    W = _randn((1024, 512), 15, dtype=torch.float32).to(torch.float8_e4m3fn)
+    bias = _randn((1024,), 16)
+    D = ops.fused_scaled_matmul_reduce_scatter(A, W.t(), 0.5, 0.25, "sum", 2, tp, bias=bias,
+                                               out_dtype=torch.float32)
+    want = torch.matmul(A.double(), W.double().t()) * 0.125 + tp * bias.double()
+    assert D.shape == (2, 256, 1024) and _rel(D, want) <= 5e-4
