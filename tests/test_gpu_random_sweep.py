@@ -57,3 +57,39 @@ def test_random_configuration(i):
     D, _ = r.run(A, B, C if beta else None)
     err = rel_err(D, want)
     assert err <= TOL, (err, sched, tp, m, n, k, l, ta, tb, opts)
+
+
+@pytest.mark.parametrize("i", range(32))
+def test_random_configuration_with_epilogue_extras(i):
+    # the same space with a bias, fp32 or bf16 D and, for RS, sum or avg, against the oracle's
+    # fused_gemm (the definition of those extras); fp32 D is held to the fp32 tolerance
+    import torch
+
+    from oracle import gemm as og
+    from reduce_scatter_gb300 import synth
+    sched, tp, m, n, k, l, ta, tb, alpha, beta, sa, sb, opts = _case(500 + i)
+    rng = np.random.default_rng(7000 + i)
+    out_f32 = bool(rng.integers(0, 2))
+    op = "avg" if sched >= 2 and rng.integers(0, 2) else "sum"
+    bias_bits = synth.tensor_bits_np(3000 + i, synth.STREAM_BIAS, (n,), ("uniform", -4.0, 4.0))
+    if ta == "bf16":
+        a, b, c = host_inputs(m, n, k, l, seed=3000 + i)
+        A, B = to_dev(a), to_dev(b)
+        a64, b64 = og.bf16_bits_to_f64(a), og.bf16_bits_to_f64(b)
+    else:
+        a, b, c = host_inputs_fp8(m, n, k, l, seed=3000 + i, fmt_a=ta, fmt_b=tb)
+        A, B = to_dev_u8(a), to_dev_u8(b)
+        a64, b64 = og.fp8_bits_to_f64(a, ta), og.fp8_bits_to_f64(b, tb)
+    want = og.fused_gemm(a64, b64, og.bf16_bits_to_f64(c) if beta else None, alpha * sa * sb, beta, P=tp,
+                         reduce_op=None if sched <= 1 else op, bias=og.bf16_bits_to_f64(bias_bits))
+    plan = dg.Plan(m, n, k, l, tp, sched, alpha, beta, TCODE[ta], TCODE[tb], sa, sb,
+                   out_type="f32" if out_f32 else "bf16", reduce_op=op if sched >= 2 else "sum")
+    for o, v in opts.items():
+        plan.set_option(o, v)
+    ws = torch.zeros(max(plan.workspace_bytes(), 256), dtype=torch.uint8, device="cuda")
+    D = torch.full((l, m, n), float("nan"), dtype=torch.float32 if out_f32 else torch.bfloat16, device="cuda")
+    main = torch.cuda.current_stream()
+    plan.run_ex(A, B, to_dev(c) if beta else None, to_dev(bias_bits), D, ws, main, torch.cuda.Stream())
+    plan.check(ws, main)
+    err = rel_err(D, want)
+    assert err <= (5e-4 if out_f32 else TOL), (err, sched, tp, m, n, k, l, ta, tb, opts, out_f32, op)
