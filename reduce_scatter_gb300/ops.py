@@ -127,9 +127,19 @@ def _scale(s) -> float:
     return float(s)
 
 
+_SLOT_LAYOUT = ("off_slots", "slot_bytes", "chunk_tiles", "chunks_per_shard", "tile_m", "elem_bytes")
+
+
 def _gemm(schedule: int, A2: torch.Tensor, B: torch.Tensor, tp: int, *, alpha=1.0, beta=0.0, C2=None,
-          bias=None, out_dtype=None, reduce_op="sum", scale_a=1.0, scale_b=1.0) -> torch.Tensor:
-    """One run of the C ABI on an (M, K) A and a (K, N) B; returns (M, N) D."""
+          bias=None, out_dtype=None, reduce_op="sum", scale_a=1.0, scale_b=1.0, after=None):
+    """One run of the C ABI on an (M, K) A and a (K, N) B; returns (M, N) D and
+    a handle for ``after``.
+
+    ``after``: the handle of a run on the same A just before (AllGather
+    RotatingA).  When this plan lays out its receive slots like that run's,
+    this run reads the shards that run moved (GEMM_ONLY on its workspace), so
+    the A shards cross once for several Bs.
+    """
     if not (A2.is_cuda and B.is_cuda):
         raise ValueError("A and B must be CUDA tensors")
     M, K = A2.shape
@@ -164,10 +174,22 @@ def _gemm(schedule: int, A2: torch.Tensor, B: torch.Tensor, tp: int, *, alpha=1.
             plan = dg.Plan(M, N, K, 1, tp, schedule, alpha, beta, ta, tb, scale_a, scale_b, out_type=to,
                            reduce_op=op)
             _plans[key] = plan
-        ws = _workspace(dev, plan.workspace_bytes())
+        info = plan.info()
         main = torch.cuda.current_stream(dev)
-        plan.run_ex(A2, Bnk, C2, bias, D2, ws, main, _copy_stream(dev))
-    return D2
+        reuse = (after is not None and schedule == dg.AG_ROTATING_A and tp > 1 and after["A"] is A2
+                 and all(after["info"][f] == info[f] for f in _SLOT_LAYOUT)
+                 and after["ws"].numel() >= plan.workspace_bytes())
+        if reuse:
+            ws = after["ws"]
+            plan.set_mode(dg.MODE_GEMM_ONLY)
+            try:
+                plan.run_ex(A2, Bnk, C2, bias, D2, ws, main, _copy_stream(dev))
+            finally:
+                plan.set_mode(dg.MODE_FUSED)
+        else:
+            ws = _workspace(dev, plan.workspace_bytes())
+            plan.run_ex(A2, Bnk, C2, bias, D2, ws, main, _copy_stream(dev))
+    return D2, {"A": A2, "ws": ws, "info": info}
 
 
 def _ag_schedule(rotate: str) -> int:
@@ -182,23 +204,25 @@ def fused_all_gather_matmul(A: torch.Tensor, Bs, gather_dim: int, tp: int, *, ro
     """``all_gather(A shards, gather_dim) @ B`` for every B in ``Bs``, over
     ``tp`` virtual ranks; returns ``(A, [outputs])`` like the torch op.
 
-    Each B runs as one fused launch (its own shard transfers overlapped with
-    the GEMM).  ``Cs`` (one per B, shaped like its output) enters as
-    ``beta * C`` when ``beta != 0``.
+    The first B runs fused (its shard transfers overlapped with the GEMM);
+    with rotate="A" the later Bs read the A shards that run moved, so A
+    crosses once for all Bs as in the torch op.  ``Cs`` (one per B, shaped
+    like its output) enters as ``beta * C`` when ``beta != 0``.
     """
     sched = _ag_schedule(rotate)
     Bs = list(Bs)
     if Cs is not None and len(Cs) != len(Bs):
         raise ValueError("len(Cs) must be the same as len(Bs)")
     A2, lead = _rows(A, gather_dim, "gather_dim", tp)
-    outs = []
+    outs, prev = [], None
     for i, B in enumerate(Bs):
         C2 = None
         if beta != 0.0:
             if Cs is None:
                 raise ValueError("beta != 0 needs Cs")
             C2, _ = _rows(Cs[i], gather_dim, "gather_dim")
-        outs.append(_unflatten(_gemm(sched, A2, B, tp, alpha=alpha, beta=beta, C2=C2), lead, gather_dim))
+        D2, prev = _gemm(sched, A2, B, tp, alpha=alpha, beta=beta, C2=C2, after=prev)
+        outs.append(_unflatten(D2, lead, gather_dim))
     return A, outs
 
 
@@ -229,9 +253,9 @@ def fused_all_gather_scaled_matmul(A: torch.Tensor, Bs, A_scale, B_scales, gathe
         raise ValueError("result_scales apply to fp8 outputs, which are not built")
     sa = _scale(A_scale)
     A2, lead = _rows(A, gather_dim, "gather_dim", tp)
-    outs = []
+    outs, prev = [], None
     for B, sb, bias, dt in zip(Bs, B_scales, biases, out_dtypes):
-        D2 = _gemm(sched, A2, B, tp, bias=bias, out_dtype=dt, scale_a=sa, scale_b=_scale(sb))
+        D2, prev = _gemm(sched, A2, B, tp, bias=bias, out_dtype=dt, scale_a=sa, scale_b=_scale(sb), after=prev)
         outs.append(_unflatten(D2, lead, gather_dim))
     return A, outs
 
@@ -271,7 +295,7 @@ def fused_matmul_reduce_scatter(A: torch.Tensor, B: torch.Tensor, reduce_op: str
         if C is None:
             raise ValueError("beta != 0 needs C")
         C2 = C.reshape(-1, C.shape[-1]) if dim is None else _rows(C, dim, "scatter_dim")[0]
-    D2 = _gemm(sched, A2, B, tp, alpha=alpha, beta=beta, C2=C2, reduce_op=reduce_op)
+    D2, _ = _gemm(sched, A2, B, tp, alpha=alpha, beta=beta, C2=C2, reduce_op=reduce_op)
     return _rs_result(D2, lead, dim)
 
 
@@ -290,8 +314,8 @@ def fused_scaled_matmul_reduce_scatter(A: torch.Tensor, B: torch.Tensor, A_scale
     if result_scale is not None:
         raise ValueError("result_scale applies to fp8 outputs, which are not built")
     sched, A2, lead, dim = _rs_layout(A, scatter_dim, tp)
-    D2 = _gemm(sched, A2, B, tp, bias=bias, out_dtype=out_dtype, reduce_op=reduce_op,
-               scale_a=_scale(A_scale), scale_b=_scale(B_scale))
+    D2, _ = _gemm(sched, A2, B, tp, bias=bias, out_dtype=out_dtype, reduce_op=reduce_op,
+                  scale_a=_scale(A_scale), scale_b=_scale(B_scale))
     return _rs_result(D2, lead, dim)
 
 

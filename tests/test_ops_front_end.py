@@ -184,3 +184,17 @@ def test_scaled_reduce_scatter_over_n_with_bias():
                                                out_dtype=torch.float32)
     want = torch.matmul(A.double(), W.double().t()) * 0.125 + tp * bias.double()
     assert D.shape == (2, 256, 1024) and _rel(D, want) <= 5e-4
+
+
+@pytest.mark.gpu
+def test_multi_b_moves_a_once_and_stays_current():
+    # later Bs read the shards the first B's run moved: back-to-back calls with new A values
+    # must each see their own A
+    tp = 4
+    Ws = [_randn((512, 1024), 20 + i, std=0.05) for i in range(3)]
+    for seed in (30, 31):
+        A = _randn((1024, 1024), seed)
+        _, outs = ops.fused_all_gather_matmul(A, [W.t() for W in Ws], 0, tp)
+        for W, D in zip(Ws, outs):
+            ref, _ = Runner(1024, 512, 1024, 1, tp, dg.AG_ROTATING_A).run(A.unsqueeze(0), W.unsqueeze(0), None)
+            assert torch.equal(D.view(torch.int16), ref[0].view(torch.int16)), seed
