@@ -23,7 +23,8 @@ Parity status: pinned (tests/test_oracle_pins.py: brute-force triple loop,
 closed forms, the statistical mean printed on the all_gather+matmul blog
 page, schedule invariance; ``fused_gemm``: a loop-by-loop restatement of the
 torch module's per-rank composition, closed forms, schedule invariance with
-a bias and both reduce ops).
+a bias and both reduce ops; ``f64_to_fp8_bits``: every code round-trips,
+midpoints go to the even code, saturation, torch's own conversion).
 """
 
 from __future__ import annotations
@@ -182,3 +183,35 @@ def fused_gemm_entries(A_rows, B_rows, C_block, alpha: float, beta: float, *, P:
     if beta != 0.0:
         D = D + np.float64(beta) * np.asarray(C_block, dtype=np.float64)
     return D
+
+
+# ------------------------------------------------------- fp8 results
+#
+# fp8 outputs of the scaled ops (aten._scaled_mm with an fp8 out_dtype and a
+# result scale): the fp32 result times the result scale, rounded to the
+# nearest fp8 value -- ties to the even code -- and saturated at the largest
+# finite magnitude.  Written here as a nearest-neighbour search over the 256
+# codes of the format, decoded by fp8_bits_to_f64.
+
+
+def f64_to_fp8_bits(x, fmt: str) -> np.ndarray:
+    """The fp8 code nearest to each value (ties to the even code), saturating
+    at the largest finite magnitude; the sign of zero is kept."""
+    codes = np.arange(128, dtype=np.int64)
+    vals = fp8_bits_to_f64(codes, fmt)
+    ok = np.isfinite(vals)
+    pos_codes, pos_vals = codes[ok], vals[ok]           # ascending with the code
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    i = np.clip(np.searchsorted(pos_vals, a), 1, len(pos_vals) - 1)
+    lo, hi = pos_vals[i - 1], pos_vals[i]
+    take_hi = (a - lo > hi - a) | ((a - lo == hi - a) & (pos_codes[i] % 2 == 0))
+    code = np.where(take_hi, pos_codes[i], pos_codes[i - 1])
+    code = np.where(a >= pos_vals[-1], pos_codes[-1], code)
+    code = np.where(a <= pos_vals[0], pos_codes[0], code)
+    return (code | (np.signbit(x).astype(np.int64) << 7)).astype(np.uint8)
+
+
+def quantize_result(D, fmt: str, result_scale: float = 1.0) -> np.ndarray:
+    """fp8 codes of result_scale * D (the definition above)."""
+    return f64_to_fp8_bits(np.float64(result_scale) * np.asarray(D, dtype=np.float64), fmt)

@@ -177,3 +177,39 @@ def _sched_avg_weights_product_only(sched, A, B, C, alpha, beta, P, *, bias=None
                          ids=lambda f: f.__name__)
 def test_schedule_bias_mutants_caught(mutant):
     assert _fails(pc.check_schedule_bias_reduce, mutant, og.fused_gemm, osch.SCHEDULES)
+
+
+def test_fp8_result_encoding_mutants_caught():
+    def truncates(x, fmt):                      # rounds toward zero instead of to nearest
+        codes = np.arange(128)
+        vals = og.fp8_bits_to_f64(codes, fmt)
+        ok = np.isfinite(vals)
+        pv, pc = vals[ok], codes[ok]
+        a = np.abs(np.asarray(x, np.float64))
+        i = np.clip(np.searchsorted(pv, a, side="right") - 1, 0, len(pv) - 1)
+        return (pc[i] | (np.signbit(x).astype(np.int64) << 7)).astype(np.uint8)
+
+    orig = og.f64_to_fp8_bits
+
+    def ties_away(x, fmt):                      # ties away from zero instead of to even
+        out = orig(x, fmt).astype(np.int64)
+        codes = np.arange(128)
+        vals = og.fp8_bits_to_f64(codes, fmt)
+        pv = np.sort(vals[np.isfinite(vals)])
+        mids = (pv[:-1] + pv[1:]) / 2
+        a = np.abs(np.asarray(x, np.float64))
+        hit = np.isin(a, mids)
+        up = orig(np.nextafter(a, np.inf), fmt).astype(np.int64) | (np.signbit(x).astype(np.int64) << 7)
+        return np.where(hit, up, out).astype(np.uint8)
+
+    for mutant in (truncates, ties_away):
+        og.f64_to_fp8_bits = mutant
+        try:
+            assert _fails(_pins_fp8_result)
+        finally:
+            og.f64_to_fp8_bits = orig
+
+
+def _pins_fp8_result():
+    from tests import test_oracle_pins as tp
+    tp.test_fp8_result_encoding()

@@ -122,3 +122,36 @@ def test_fused_sampled_entries_match_full():
         blk = og.fused_gemm_entries(A[rows], B[cols], C[np.ix_(rows, cols)], 0.5, 1.0, P=P, reduce_op=op,
                                     bias_cols=bias[cols])
         assert np.array_equal(blk, full[np.ix_(rows, cols)]), op
+
+
+def test_fp8_result_encoding():
+    import torch
+    for fmt, tdt, top in (("e4m3", getattr(torch, "float8_e4m3fn", None), 448.0),
+                          ("e5m2", getattr(torch, "float8_e5m2", None), 57344.0)):
+        codes = np.arange(256)
+        vals = og.fp8_bits_to_f64(codes, fmt)
+        fin = np.isfinite(vals)
+        # every finite code round-trips (the sign of zero included)
+        assert np.array_equal(og.f64_to_fp8_bits(vals[fin], fmt), codes[fin].astype(np.uint8))
+        # midpoints between neighbouring positive codes go to the even code
+        pos = np.sort(vals[(codes < 128) & fin])
+        mids = (pos[:-1] + pos[1:]) / 2
+        got = og.f64_to_fp8_bits(mids, fmt)
+        lo_code = og.f64_to_fp8_bits(pos[:-1], fmt)
+        want = np.where(lo_code % 2 == 0, lo_code, lo_code + 1)
+        assert np.array_equal(got, want.astype(np.uint8))
+        # just off the midpoints: the nearer code
+        assert np.array_equal(og.f64_to_fp8_bits(mids * (1 - 1e-9), fmt), lo_code)
+        assert np.array_equal(og.f64_to_fp8_bits(mids * (1 + 1e-9), fmt), (lo_code + 1).astype(np.uint8))
+        # saturation at the largest finite magnitude, both signs
+        assert og.fp8_bits_to_f64(og.f64_to_fp8_bits(np.array([1e30, -1e30, top * 1.01]), fmt), fmt).tolist() == \
+            [top, -top, top]
+        # against torch's own float32 -> fp8 conversion on values inside the range
+        if tdt is not None:
+            x = (np.random.default_rng(5).standard_normal(20000) * top / 8).astype(np.float32)
+            x = x[np.abs(x) < top]
+            t = torch.from_numpy(x).to(tdt).view(torch.uint8).numpy()
+            assert np.array_equal(og.f64_to_fp8_bits(x.astype(np.float64), fmt), t)
+    # the result scale multiplies before rounding
+    assert og.quantize_result(np.array([1.0, 3.0]), "e4m3", 0.5).tolist() == \
+        og.f64_to_fp8_bits(np.array([0.5, 1.5]), "e4m3").tolist()
