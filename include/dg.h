@@ -17,7 +17,7 @@
  *   A  bf16 (or fp8, dg_plan_scaled), L x M x K, row-major (K innermost)
  *   B  bf16 (or fp8), stored transposed: L x N x K, row-major (K innermost)
  *   C  bf16, L x M x N, row-major (read only when beta != 0)
- *   D  bf16 (or fp32, DG_OPT_OUT_TYPE), L x M x N, row-major
+ *   D  bf16 (or fp32, e4m3, e5m2: DG_OPT_OUT_TYPE), L x M x N, row-major
  *   bias  bf16, N values (dg_run_ex only; optional)
  * Every batch is densely packed after the previous one.  bf16 values are
  * passed as raw 16-bit patterns (dg_bf16_t).
@@ -89,8 +89,10 @@ enum dg_schedule {
 enum dg_mode { DG_MODE_FUSED = 0, DG_MODE_GEMM_ONLY = 1, DG_MODE_SERIAL = 2 };
 
 /* Element types.  A and B: BF16, E4M3 or E5M2 (C and the bias are always
- * bf16).  D: BF16 (default) or F32 (DG_OPT_OUT_TYPE), after the out_dtype
- * argument of the scaled fused ops in torch/distributed/_symmetric_memory.
+ * bf16).  D: BF16 (default), F32, E4M3 or E5M2 (DG_OPT_OUT_TYPE), after the
+ * out_dtype argument of the scaled fused ops in torch/distributed/_symmetric_memory;
+ * an fp8 D holds result_scale * value (dg_set_result_scale) rounded to the
+ * nearest code, ties to even, saturating at the largest finite value.
  * fp8 follows the OCP 8-bit formats: E4M3 is the variant without infinities
  * (largest finite 448), E5M2 the IEEE-like one (largest finite 57344); both
  * are passed as raw bytes. */
@@ -149,8 +151,9 @@ enum dg_option {
                                  memset on the main stream per run), 0 = off, -1 (default) =
                                  on for AG plans whose per-wave operand strips exceed about
                                  96 MiB */
-  DG_OPT_OUT_TYPE = 11,       /* element type of D: DG_TYPE_BF16 (default) or DG_TYPE_F32
-                                 (fp32 D runs through dg_run_ex) */
+  DG_OPT_OUT_TYPE = 11,       /* element type of D: DG_TYPE_BF16 (default), DG_TYPE_F32,
+                                 DG_TYPE_E4M3 or DG_TYPE_E5M2 (all but bf16 run through
+                                 dg_run_ex; fp8 D is written by direct stores) */
   DG_OPT_REDUCE_OP = 12,      /* RS plans: dg_reduce_op, DG_REDUCE_SUM (default) or
                                  DG_REDUCE_AVG; AG plans accept only SUM */
   DG_OPT_COPY_PACE = 13,      /* AG FUSED runs with tp > 2: 1 = the shard transfers of step
@@ -281,6 +284,11 @@ int dg_run_ex(dg_plan_t plan, const void* A, const void* B, const dg_bf16_t* C, 
 int dg_run_host(dg_plan_t plan, const void* A_host, const void* B_host, const dg_bf16_t* C_host,
                 const dg_bf16_t* bias, void* D_host, void* A_dev, void* B_dev, dg_bf16_t* C_dev, void* D_dev,
                 void* workspace, void* main_stream, void* copy_stream);
+
+/* Multiplier applied to the result before it is rounded to an fp8 D (the
+ * result_scale of the scaled fused ops; default 1).  Ignored for bf16 and
+ * fp32 D.  DG_ERR_ARG for NaN. */
+int dg_set_result_scale(dg_plan_t plan, float scale);
 
 /* Synchronize `stream` and read the workspace status word of the plan's last
  * run: DG_OK, DG_ERR_TIMEOUT or DG_ERR_HANG (with the flag index in the

@@ -133,6 +133,7 @@ struct dg_plan_s {
   int esz = 2;                                       // bytes per A / B element
   float scale_a = 1.f, scale_b = 1.f;                // per-tensor scales (scaled GEMM)
   int out_type = DG_TYPE_BF16;                       // element type of D (DG_OPT_OUT_TYPE)
+  float result_scale = 1.f;                          // fp8 D: multiplier before rounding
   int reduce_op = DG_REDUCE_SUM;                     // RS: sum or mean over ranks (DG_OPT_REDUCE_OP)
   int mode = DG_MODE_FUSED;
   int64_t timeout_ms = 2000;
@@ -390,8 +391,11 @@ int build_epi_maps(dg_plan_s* p, const Driver& drv, const void* C, void* D, uint
   std::memset(&p->kp.tmD, 0, sizeof(CUtensorMap));
   if (p->epi != 1) return DG_OK;
   const int64_t rows = p->l * p->m;
-  int rc = encode_epi_map(drv, &p->kp.tmD, D, p->out_type == DG_TYPE_F32, p->n, rows);
-  if (rc) return rc;
+  int rc = DG_OK;
+  if (p->out_type == DG_TYPE_BF16 || p->out_type == DG_TYPE_F32) {  // fp8 D: direct stores only
+    rc = encode_epi_map(drv, &p->kp.tmD, D, p->out_type == DG_TYPE_F32, p->n, rows);
+    if (rc) return rc;
+  }
   if (C && p->beta != 0.f) {
     rc = encode_epi_map(drv, &p->kp.tmC, C, false, p->n, rows);
     if (rc) return rc;
@@ -700,7 +704,8 @@ int run_rs_serial(dg_plan_s* p, const Driver& drv, const void* C, void* D, uint8
   if (blocks < 1) blocks = 1;
   dg::dg_reduce_partials_kernel<<<(unsigned)blocks, 256, 0, st>>>(
       reinterpret_cast<const float*>(ws + p->off_serial), p->tp, n4,
-      reinterpret_cast<const __nv_bfloat16*>(C), p->beta, D, p->out_type == DG_TYPE_F32 ? 1 : 0);
+      reinterpret_cast<const __nv_bfloat16*>(C), p->beta, D, p->out_type == DG_TYPE_F32 ? 1 : 0,
+      p->out_type == DG_TYPE_E4M3 ? 1 : p->out_type == DG_TYPE_E5M2 ? 2 : 0, p->result_scale);
   DG_CUDA(cudaGetLastError());
   return DG_OK;
 }
@@ -840,8 +845,8 @@ int dg_set_option(dg_plan_t p, int option, int64_t value) {
       p->epi = (int)value;
       return DG_OK;
     case DG_OPT_OUT_TYPE:
-      if (value != DG_TYPE_BF16 && value != DG_TYPE_F32)
-        return fail(DG_ERR_ARG, "output type must be DG_TYPE_BF16 or DG_TYPE_F32");
+      if (value != DG_TYPE_BF16 && value != DG_TYPE_F32 && value != DG_TYPE_E4M3 && value != DG_TYPE_E5M2)
+        return fail(DG_ERR_ARG, "output type must be DG_TYPE_BF16, DG_TYPE_F32, DG_TYPE_E4M3 or DG_TYPE_E5M2");
       p->out_type = (int)value;
       return DG_OK;
     case DG_OPT_REDUCE_OP:
@@ -902,7 +907,7 @@ int dg_plan_tile(dg_plan_t p, int64_t t, dg_tile* o) {
 int dg_run(dg_plan_t p, const void* A, const void* B, const dg_bf16_t* C, dg_bf16_t* D,
            void* workspace, void* main_stream, void* copy_stream) {
   if (!p) return fail(DG_ERR_ARG, "plan is NULL");
-  if (p->out_type != DG_TYPE_BF16) return fail(DG_ERR_STATE, "the plan writes fp32 D: run it with dg_run_ex");
+  if (p->out_type != DG_TYPE_BF16) return fail(DG_ERR_STATE, "the plan writes fp32 or fp8 D: run it with dg_run_ex");
   return dg_run_ex(p, A, B, C, nullptr, D, workspace, main_stream, copy_stream);
 }
 
@@ -972,6 +977,8 @@ int dg_run_ex(dg_plan_t p, const void* A, const void* B, const dg_bf16_t* C, con
   kp.D = D;
   kp.bias = reinterpret_cast<const __nv_bfloat16*>(bias);
   kp.out_f32 = p->out_type == DG_TYPE_F32 ? 1u : 0u;
+  kp.out_fp8 = p->out_type == DG_TYPE_E4M3 ? 1u : p->out_type == DG_TYPE_E5M2 ? 2u : 0u;
+  kp.result_scale = p->result_scale;
   kp.X = reinterpret_cast<float*>(ws + p->off_partial);
   kp.flags = reinterpret_cast<uint32_t*>(ws + p->off_flags);
   kp.status = reinterpret_cast<unsigned long long*>(ws + p->off_status);
@@ -1062,7 +1069,8 @@ int dg_run_host(dg_plan_t p, const void* A_host, const void* B_host, const dg_bf
   const size_t a_bytes = (size_t)(p->l * p->m * p->k) * (size_t)p->esz;
   const size_t b_bytes = (size_t)(p->l * p->n * p->k) * (size_t)p->esz;
   const size_t c_bytes = (size_t)(p->l * p->m * p->n) * 2;
-  const size_t d_bytes = (size_t)(p->l * p->m * p->n) * (p->out_type == DG_TYPE_F32 ? 4 : 2);
+  const size_t d_elem = p->out_type == DG_TYPE_F32 ? 4 : (p->out_type == DG_TYPE_BF16 ? 2 : 1);
+  const size_t d_bytes = (size_t)(p->l * p->m * p->n) * d_elem;
   // host to device on the main stream (pinned host memory: copy engine, asynchronous)
   DG_CUDA(cudaMemcpyAsync(A_dev, A_host, a_bytes, cudaMemcpyHostToDevice, ms));
   DG_CUDA(cudaMemcpyAsync(B_dev, B_host, b_bytes, cudaMemcpyHostToDevice, ms));
@@ -1071,6 +1079,13 @@ int dg_run_host(dg_plan_t p, const void* A_host, const void* B_host, const dg_bf
                      copy_stream);
   if (rc) return rc;
   DG_CUDA(cudaMemcpyAsync(D_host, D_dev, d_bytes, cudaMemcpyDeviceToHost, ms));
+  return DG_OK;
+}
+
+int dg_set_result_scale(dg_plan_t p, float scale) {
+  if (!p) return fail(DG_ERR_ARG, "plan is NULL");
+  if (!(scale == scale)) return fail(DG_ERR_ARG, "result scale is NaN");
+  p->result_scale = scale;
   return DG_OK;
 }
 

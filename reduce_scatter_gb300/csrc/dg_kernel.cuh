@@ -34,6 +34,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include "dg_geom.h"
@@ -114,6 +115,8 @@ struct KParams {
   float alpha, beta;
   float bias_scale;  // weight of the bias in every epilogue pass (1, or 1/P for the mean)
   uint32_t out_f32;  // D is fp32
+  uint32_t out_fp8;  // D is fp8: 1 e4m3, 2 e5m2 (result_scale * value, nearest, saturating)
+  float result_scale;
   uint64_t timeout_ns;
   uint64_t hang_ns;
 };
@@ -512,6 +515,30 @@ __device__ __forceinline__ void add_bias(const KParams& p, int64_t gcol, int nco
   }
 }
 
+// 32 consecutive results as fp8 bytes (result_scale applied, round to nearest
+// even, saturating at the largest finite value), the ncols valid ones.
+__device__ __forceinline__ void store_fp8_row(const KParams& p, uint8_t* d, int ncols, const float (&out)[32],
+                                              bool vec) {
+  const __nv_fp8_interpretation_t fmt = p.out_fp8 == 1 ? __NV_E4M3 : __NV_E5M2;
+  uint32_t w[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+        make_float2(out[4 * q] * p.result_scale, out[4 * q + 1] * p.result_scale), __NV_SATFINITE, fmt);
+    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+        make_float2(out[4 * q + 2] * p.result_scale, out[4 * q + 3] * p.result_scale), __NV_SATFINITE, fmt);
+    w[q] = (uint32_t)lo | ((uint32_t)hi << 16);
+  }
+  if (vec) {
+    reinterpret_cast<uint4*>(d)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4*>(d)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < ncols) d[i] = (uint8_t)(w[i >> 2] >> (8 * (i & 3)));
+  }
+}
+
 // Plain stores of 32 consecutive fp32 values (the ncols valid ones).
 __device__ __forceinline__ void store_f32_row(float* x, int ncols, const float (&out)[32], bool vec) {
   if (vec) {
@@ -576,7 +603,9 @@ __device__ __forceinline__ void epilogue_row_chunk(const KParams& p, const Tile&
   for (int i = 0; i < 32; ++i) out[i] = fmaf(p.alpha, acc[i], src[i]);
   if (p.bias) add_bias(p, gcol, ncols, out);
 
-  if (tl.dst == DST_D && p.out_f32) {
+  if (tl.dst == DST_D && p.out_fp8) {
+    store_fp8_row(p, static_cast<uint8_t*>(p.D) + e0, ncols, out, ncols == 32 && (e0 & 15) == 0);
+  } else if (tl.dst == DST_D && p.out_f32) {
     store_f32_row(static_cast<float*>(p.D) + e0, ncols, out, ncols == 32 && (e0 & 3) == 0);
   } else if (tl.dst == DST_D) {
     __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.D) + e0;
@@ -605,7 +634,9 @@ __device__ __forceinline__ void epilogue_row_chunk(const KParams& p, const Tile&
 // (grow, gcol); the partial at `x`).
 __device__ __forceinline__ void store_row_chunk(const KParams& p, const Tile& tl, int64_t grow,
                                                 int64_t gcol, int ncols, const float (&out)[32], float* x) {
-  if (tl.dst == DST_D && p.out_f32) {
+  if (tl.dst == DST_D && p.out_fp8) {
+    store_fp8_row(p, static_cast<uint8_t*>(p.D) + grow * p.g.N + gcol, ncols, out, false);
+  } else if (tl.dst == DST_D && p.out_f32) {
     store_f32_row(static_cast<float*>(p.D) + grow * p.g.N + gcol, ncols, out, false);
   } else if (tl.dst == DST_D) {
     __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.D) + grow * p.g.N + gcol;
@@ -940,8 +971,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
       const int rows_here = tl.rows_valid - (int)crank * ROWS_PER_CTA;
       const int64_t row0 = tl.out_row + (int64_t)crank * ROWS_PER_CTA;
       const int nch = (tl.cols_valid + XCOLS - 1) / XCOLS;
-      // Staged tiles need 16-byte aligned TMA column coordinates (8 bf16).
-      const bool staged = EPI == 1 && (tl.out_col & 7) == 0;
+      // Staged tiles need 16-byte aligned TMA column coordinates (8 bf16); fp8
+      // results go out by direct stores.
+      const bool staged = EPI == 1 && (tl.out_col & 7) == 0 && !(p.out_fp8 && tl.dst == DST_D);
       const bool has_src = staged && tl.src != SRC_NONE;
       // Where the rotating partial is read and written: the shared partial X
       // (in-place hand-off), or, with copy-engine hand-off, this rank's receive
@@ -1138,7 +1170,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
 // its bias), four elements per thread and iteration, grid-stride.  HBM-bound.
 __global__ void __launch_bounds__(256) dg_reduce_partials_kernel(const float* __restrict__ X, int P,
                                                                  int64_t n4, const __nv_bfloat16* C,
-                                                                 float beta, void* D, int out_f32) {
+                                                                 float beta, void* D, int out_f32, int out_fp8,
+                                                                 float result_scale) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t plane = n4;  // float4 units per partial
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
@@ -1157,7 +1190,14 @@ __global__ void __launch_bounds__(256) dg_reduce_partials_kernel(const float* __
       acc.z += beta * bf16_bits_to_f32(cw.y & 0xFFFFu);
       acc.w += beta * bf16_bits_to_f32(cw.y >> 16);
     }
-    if (out_f32) {
+    if (out_fp8) {
+      const __nv_fp8_interpretation_t fmt = out_fp8 == 1 ? __NV_E4M3 : __NV_E5M2;
+      const __nv_fp8x2_storage_t lo =
+          __nv_cvt_float2_to_fp8x2(make_float2(acc.x * result_scale, acc.y * result_scale), __NV_SATFINITE, fmt);
+      const __nv_fp8x2_storage_t hi =
+          __nv_cvt_float2_to_fp8x2(make_float2(acc.z * result_scale, acc.w * result_scale), __NV_SATFINITE, fmt);
+      reinterpret_cast<uint32_t*>(D)[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+    } else if (out_f32) {
       reinterpret_cast<float4*>(D)[i] = acc;
     } else {
       uint2 o;

@@ -70,7 +70,7 @@ OPT_COPY_KIND = 14
 # Every symbol include/dg.h declares.
 EXPORTS = ("dg_plan", "dg_workspace_bytes", "dg_run_mode", "dg_set_option", "dg_run", "dg_check",
            "dg_plan_info_get", "dg_plan_tile", "dg_destroy", "dg_last_error", "dg_run_static",
-           "dg_plan_scaled", "dg_run_ex", "dg_run_host")
+           "dg_plan_scaled", "dg_run_ex", "dg_run_host", "dg_set_result_scale")
 
 # Size of the library's built-in workspace used by dg_run_static.
 STATIC_WORKSPACE_BYTES = 32 << 20
@@ -147,6 +147,8 @@ def lib():
         L.dg_run.restype = i32
         L.dg_run_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.dg_run_ex.restype = i32
+        L.dg_set_result_scale.argtypes = [vp, ctypes.c_float]
+        L.dg_set_result_scale.restype = i32
         L.dg_run_host.argtypes = [vp] * 13
         L.dg_run_host.restype = i32
         L.dg_run_static.argtypes = [vp, vp, vp, vp, vp, vp, vp]
@@ -200,7 +202,7 @@ class Plan:
     ``dg_set_option`` right after planning."""
 
     def __init__(self, m, n, k, l, tp, schedule, alpha=1.0, beta=0.0, a_type=TYPE_BF16, b_type=TYPE_BF16,
-                 scale_a=1.0, scale_b=1.0, out_type=TYPE_BF16, reduce_op=REDUCE_SUM):
+                 scale_a=1.0, scale_b=1.0, out_type=TYPE_BF16, reduce_op=REDUCE_SUM, result_scale=1.0):
         if isinstance(schedule, str):
             schedule = SCHEDULE_BY_NAME[schedule]
         a_type = TYPE_BY_NAME.get(a_type, a_type)
@@ -219,6 +221,8 @@ class Plan:
             self.set_option(OPT_OUT_TYPE, self.out_type)
         if self.reduce_op != REDUCE_SUM:
             self.set_option(OPT_REDUCE_OP, self.reduce_op)
+        if result_scale != 1.0:
+            self.set_result_scale(result_scale)
         self.m, self.n, self.k, self.l, self.tp, self.schedule = m, n, k, l, tp, schedule
         self.alpha, self.beta = alpha, beta
 
@@ -245,6 +249,10 @@ class Plan:
 
     def set_option(self, opt: int, value: int):
         _check(lib().dg_set_option(self._h, opt, value))
+
+    def set_result_scale(self, scale: float):
+        """``dg_set_result_scale``: multiplier before rounding to an fp8 D."""
+        _check(lib().dg_set_result_scale(self._h, float(scale)))
 
     def info(self) -> dict:
         inf = PlanInfo()

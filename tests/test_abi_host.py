@@ -272,7 +272,12 @@ def test_tile_order_simulator_random(L, i):
 def test_output_type_and_reduce_op_rules(L):
     p = dg.Plan(256, 256, 256, 1, 2, dg.AG_ROTATING_A)
     with pytest.raises(dg.DGError):
-        p.set_option(dg.OPT_OUT_TYPE, dg.TYPE_E4M3)        # fp8 D is not built
+        p.set_option(dg.OPT_OUT_TYPE, 7)                   # no such type
+    p.set_option(dg.OPT_OUT_TYPE, dg.TYPE_E4M3)            # fp8 D, with a result scale
+    p.set_result_scale(0.25)
+    with pytest.raises(dg.DGError):
+        p.set_result_scale(float("nan"))
+    assert p.run(16, 16, None, 16, 256, raise_on_error=False) == dg.ERR_STATE   # dg_run writes bf16 only
     with pytest.raises(dg.DGError):
         p.set_option(dg.OPT_REDUCE_OP, dg.REDUCE_AVG)      # AG plans have no reduction
     p.set_option(dg.OPT_REDUCE_OP, dg.REDUCE_SUM)

@@ -25,12 +25,13 @@ def _bias_bits(n, seed):
     return synth.tensor_bits_np(seed, synth.STREAM_BIAS, (n,), ("uniform", -4.0, 4.0))
 
 
-def _ok(sched, m, n, k, tp):
+def _ok(sched, m, n, k, tp, kq=8):
+    # kq: K elements per 16 bytes (8 bf16, 16 fp8), the granule of each rank's K-slab
     if sched in (0, 1, 2) and m % tp:
         return False
     if sched != 2 and n % tp:
         return False
-    if sched >= 2 and (k % tp or (k // tp) % 8):
+    if sched >= 2 and (k % tp or (k // tp) % kq):
         return False
     return True
 
@@ -149,3 +150,63 @@ def test_fp8_with_bias_and_f32_out(sched):
         want = og.fused_gemm(og.fp8_bits_to_f64(a, "e4m3"), og.fp8_bits_to_f64(b, "e5m2"), None, sa * sb, 0.0,
                              P=tp, reduce_op=None if sched <= 1 else op, bias=og.bf16_bits_to_f64(bias))
         assert _err(D, want) <= TOL_F32, op
+
+
+def _fp8_close(got_codes, want_codes, fmt):
+    """fp8 results against the oracle's codes: equal, or neighbours (the device
+    rounds an fp32 value, the oracle the fp64 one; a value within fp32 error of
+    a rounding midpoint may land on either side)."""
+    g = og.fp8_bits_to_f64(got_codes, fmt)
+    w = og.fp8_bits_to_f64(want_codes, fmt)
+    assert not np.any(np.isnan(g))
+    vals = np.sort(np.unique(og.fp8_bits_to_f64(np.arange(256), fmt)[np.isfinite(og.fp8_bits_to_f64(np.arange(256), fmt))]))
+    gi, wi = np.searchsorted(vals, g), np.searchsorted(vals, w)
+    assert np.abs(gi - wi).max() <= 1
+    return float(np.mean(got_codes == want_codes))
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("epi", [0, 1])
+@pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_fp8_out_with_result_scale_vs_oracle(sched, epi, fmt):
+    m, n, k, l = 392, 776, 320, 2
+    ops_ = ["sum"] if sched <= 1 else ["sum", "avg"]
+    for tp in (2, 8):
+        if not _ok(sched, m, n, k, tp, kq=16):
+            continue
+        a, b, c = host_inputs_fp8(m, n, k, l, seed=600 + tp + 10 * sched + epi, fmt_a="e4m3", fmt_b="e4m3")
+        bias = _bias_bits(n, 601)
+        A, B, Bias = to_dev_u8(a), to_dev_u8(b), to_dev(bias)
+        for op in ops_:
+            rs = 4.0 if fmt == "e4m3" else 0.5
+            plan = dg.Plan(m, n, k, l, tp, sched, 1.0, 0.0, "e4m3", "e4m3", 0.5, 0.25, out_type=fmt,
+                           reduce_op=op, result_scale=rs)
+            plan.set_option(dg.OPT_EPILOGUE, epi)
+            ws = torch.zeros(max(plan.workspace_bytes(), 256), dtype=torch.uint8, device="cuda")
+            D = torch.full((l, m, n), 0x7F, dtype=torch.uint8, device="cuda")   # NaN codes until written
+            main = torch.cuda.current_stream()
+            plan.run_ex(A, B, None, Bias, D, ws, main, torch.cuda.Stream())
+            plan.check(ws, main)
+            want = og.quantize_result(
+                og.fused_gemm(og.fp8_bits_to_f64(a, "e4m3"), og.fp8_bits_to_f64(b, "e4m3"), None, 0.125, 0.0,
+                              P=tp, reduce_op=None if sched <= 1 else op, bias=og.bf16_bits_to_f64(bias)),
+                fmt, rs)
+            same = _fp8_close(D.cpu().numpy(), want, fmt)
+            assert same >= 0.99, (tp, op, same)
+
+
+@pytest.mark.parametrize("sched", [dg.RS_TILING_A_ROTATING_C, dg.RS_TILING_B_ROTATING_C],
+                         ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_fp8_out_nonfused_baseline(sched):
+    m, n, k, l, tp = 1024, 1024, 1024, 1, 4
+    a, b, c = host_inputs(m, n, k, l, seed=620 + sched)
+    A, B = to_dev(a), to_dev(b)
+    plan = dg.Plan(m, n, k, l, tp, sched, 1.0, 0.0, out_type="e4m3", result_scale=2.0)
+    plan.set_mode(dg.MODE_SERIAL)
+    ws = torch.zeros(plan.workspace_bytes(), dtype=torch.uint8, device="cuda")
+    D = torch.full((l, m, n), 0x7F, dtype=torch.uint8, device="cuda")
+    main = torch.cuda.current_stream()
+    plan.run_ex(A, B, None, None, D, ws, main, main)
+    plan.check(ws, main)
+    want = og.quantize_result(og.gemm(og.bf16_bits_to_f64(a), og.bf16_bits_to_f64(b), None, 1.0, 0.0), "e4m3", 2.0)
+    assert _fp8_close(D.cpu().numpy(), want, "e4m3") >= 0.99
