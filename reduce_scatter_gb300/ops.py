@@ -53,6 +53,7 @@ for _name, _t in (("float8_e4m3fn", dg.TYPE_E4M3), ("float8_e5m2", dg.TYPE_E5M2)
         _FP8[getattr(torch, _name)] = _t
 
 _OUT_TYPES = {torch.bfloat16: dg.TYPE_BF16, torch.float32: dg.TYPE_F32}
+_OUT_TYPES.update(_FP8)
 
 
 def _in_type(t: torch.Tensor) -> int:
@@ -64,10 +65,8 @@ def _in_type(t: torch.Tensor) -> int:
 
 
 def _out_type(dtype) -> int:
-    if dtype is None:
-        return dg.TYPE_BF16
     if dtype not in _OUT_TYPES:
-        raise ValueError(f"out_dtype must be None, torch.bfloat16 or torch.float32, got {dtype}")
+        raise ValueError(f"out_dtype must be bfloat16, float32 or a float8 type, got {dtype}")
     return _OUT_TYPES[dtype]
 
 
@@ -131,7 +130,8 @@ _SLOT_LAYOUT = ("off_slots", "slot_bytes", "chunk_tiles", "chunks_per_shard", "t
 
 
 def _gemm(schedule: int, A2: torch.Tensor, B: torch.Tensor, tp: int, *, alpha=1.0, beta=0.0, C2=None,
-          bias=None, out_dtype=None, reduce_op="sum", scale_a=1.0, scale_b=1.0, after=None):
+          bias=None, out_dtype=torch.bfloat16, reduce_op="sum", scale_a=1.0, scale_b=1.0, result_scale=1.0,
+          after=None):
     """One run of the C ABI on an (M, K) A and a (K, N) B; returns (M, N) D and
     a handle for ``after``.
 
@@ -163,16 +163,17 @@ def _gemm(schedule: int, A2: torch.Tensor, B: torch.Tensor, tp: int, *, alpha=1.
         bias = bias.to(device=dev, dtype=torch.bfloat16).contiguous()
         if bias.dim() != 1 or bias.shape[0] != N:
             raise ValueError(f"bias must be a vector of {N} values")
-    D2 = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device=dev)
+    D2 = torch.empty((M, N), dtype=out_dtype, device=dev)
+    rs = float(result_scale) if to in (dg.TYPE_E4M3, dg.TYPE_E5M2) else 1.0
     key = (dev.index, schedule, M, N, K, tp, float(alpha), float(beta), ta, tb, float(scale_a), float(scale_b),
-           to, op)
+           to, op, rs)
     if Bnk.device != dev or (C2 is not None and C2.device != dev) or (bias is not None and bias.device != dev):
         raise ValueError("A, B, C and bias must be on the same device")
     with _lock, torch.cuda.device(dev):  # the library works on the current device
         plan = _plans.get(key)
         if plan is None:
             plan = dg.Plan(M, N, K, 1, tp, schedule, alpha, beta, ta, tb, scale_a, scale_b, out_type=to,
-                           reduce_op=op)
+                           reduce_op=op, result_scale=rs)
             _plans[key] = plan
         info = plan.info()
         main = torch.cuda.current_stream(dev)
@@ -232,8 +233,9 @@ def fused_all_gather_scaled_matmul(A: torch.Tensor, Bs, A_scale, B_scales, gathe
     """fp8 (or bf16) all-gather matmuls with per-tensor scales:
     ``A_scale * B_scales[i] * (A @ Bs[i]) + biases[i]``; returns ``(A, [outputs])``.
 
-    ``out_dtypes[i]`` is None (bf16), torch.bfloat16 or torch.float32;
-    fp8 outputs, and therefore ``result_scales``, are not built.
+    ``out_dtypes[i]``: None (the dtype of ``Bs[i]``, as in the torch op),
+    bfloat16, float32 or a float8 type; an fp8 output holds
+    ``result_scales[i] * value`` rounded to the format (nearest, saturating).
     ``use_fast_accum`` is accepted and has no effect: the tensor cores always
     accumulate in fp32.
     """
@@ -249,13 +251,12 @@ def fused_all_gather_scaled_matmul(A: torch.Tensor, Bs, A_scale, B_scales, gathe
                       ("out_dtypes", out_dtypes), ("use_fast_accum", use_fast_accum)):
         if len(lst) != n:
             raise ValueError(f"len({name}) must be the same as len(Bs)")
-    if any(r is not None for r in result_scales):
-        raise ValueError("result_scales apply to fp8 outputs, which are not built")
     sa = _scale(A_scale)
     A2, lead = _rows(A, gather_dim, "gather_dim", tp)
     outs, prev = [], None
-    for B, sb, bias, dt in zip(Bs, B_scales, biases, out_dtypes):
-        D2, prev = _gemm(sched, A2, B, tp, bias=bias, out_dtype=dt, scale_a=sa, scale_b=_scale(sb), after=prev)
+    for B, sb, bias, rsc, dt in zip(Bs, B_scales, biases, result_scales, out_dtypes):
+        D2, prev = _gemm(sched, A2, B, tp, bias=bias, out_dtype=dt if dt is not None else B.dtype, scale_a=sa,
+                         scale_b=_scale(sb), result_scale=_scale(rsc), after=prev)
         outs.append(_unflatten(D2, lead, gather_dim))
     return A, outs
 
@@ -305,17 +306,17 @@ def fused_scaled_matmul_reduce_scatter(A: torch.Tensor, B: torch.Tensor, A_scale
     """fp8 (or bf16) matmul-reduce-scatter with per-tensor scales: each rank's
     ``A_scale * B_scale * (A_r @ B_r) + bias``, reduced over the ranks (so a
     "sum" carries tp copies of the bias, an "avg" one, as in the torch module's
-    reference composition).  ``out_dtype`` None (bf16), torch.bfloat16 or
-    torch.float32; ``result_scale`` must be None (fp8 outputs are not built);
+    reference composition).  ``out_dtype``: None (A's dtype, as in the torch
+    op), bfloat16, float32 or a float8 type (then ``result_scale * value``
+    rounded to the format; the partials stay fp32 until the last step);
     ``use_fast_accum`` has no effect.
     """
     if reduce_op not in ("sum", "avg"):
         raise ValueError("reduce_op must be sum or avg")
-    if result_scale is not None:
-        raise ValueError("result_scale applies to fp8 outputs, which are not built")
     sched, A2, lead, dim = _rs_layout(A, scatter_dim, tp)
-    D2, _ = _gemm(sched, A2, B, tp, bias=bias, out_dtype=out_dtype, reduce_op=reduce_op,
-                  scale_a=_scale(A_scale), scale_b=_scale(B_scale))
+    D2, _ = _gemm(sched, A2, B, tp, bias=bias, out_dtype=out_dtype if out_dtype is not None else A.dtype,
+                  reduce_op=reduce_op, scale_a=_scale(A_scale), scale_b=_scale(B_scale),
+                  result_scale=_scale(result_scale))
     return _rs_result(D2, lead, dim)
 
 

@@ -29,11 +29,12 @@ def test_argument_checks_on_cpu():
     with pytest.raises(ValueError):
         ops.fused_all_gather_scaled_matmul(a, [w.t()], 1.0, [1.0, 1.0], 0, 2)   # list lengths
     with pytest.raises(ValueError):
-        ops.fused_all_gather_scaled_matmul(a, [w.t()], 1.0, [1.0], 0, 2, result_scales=[torch.ones(())])
-    with pytest.raises(ValueError):
-        ops.fused_scaled_matmul_reduce_scatter(a, w.t(), 1.0, 1.0, "sum", 0, 2, result_scale=1.0)
+        ops.fused_all_gather_scaled_matmul(a, [w.t()], 1.0, [1.0], 0, 2, result_scales=[1.0, 2.0])
     with pytest.raises(ValueError):
         ops._out_type(torch.float16)
+    assert ops._out_type(torch.float32) == dg.TYPE_F32
+    if hasattr(torch, "float8_e5m2"):
+        assert ops._out_type(torch.float8_e5m2) == dg.TYPE_E5M2
     with pytest.raises(TypeError):
         ops._in_type(torch.zeros(2, dtype=torch.float32))
     with pytest.raises(ValueError):
@@ -151,7 +152,8 @@ def test_scaled_ops_fp8_bias_f32(reduce_op):
         want = want / tp
     assert _rel(Dr, want) <= 5e-4
     # bf16 output is the fp32 result rounded
-    Db = ops.fused_scaled_matmul_reduce_scatter(A, W.t(), sa, sb, reduce_op, 1, tp, bias=bias)
+    Db = ops.fused_scaled_matmul_reduce_scatter(A, W.t(), sa, sb, reduce_op, 1, tp, bias=bias,
+                                                out_dtype=torch.bfloat16)
     assert Db.dtype == torch.bfloat16
     assert torch.equal(Db.view(torch.int16), Dr.to(torch.bfloat16).view(torch.int16))
 
@@ -198,3 +200,24 @@ def test_multi_b_moves_a_once_and_stays_current():
         for W, D in zip(Ws, outs):
             ref, _ = Runner(1024, 512, 1024, 1, tp, dg.AG_ROTATING_A).run(A.unsqueeze(0), W.unsqueeze(0), None)
             assert torch.equal(D.view(torch.int16), ref[0].view(torch.int16)), seed
+
+
+@pytest.mark.gpu
+def test_scaled_ops_default_to_the_input_dtype():
+    # out_dtype None: the torch op's default, the dtype of B (all-gather) or A (reduce-scatter);
+    # for fp8 inputs an fp8 result, result_scale * value rounded to the format
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("no float8 in this torch")
+    from oracle import gemm as og
+    tp = 4
+    A = _randn((512, 512), 17, dtype=torch.float32).to(torch.float8_e4m3fn)
+    W = _randn((1024, 512), 18, dtype=torch.float32).to(torch.float8_e4m3fn)
+    prod = (torch.matmul(A.double(), W.double().t()) * 0.125).cpu().numpy()
+    _, (D,) = ops.fused_all_gather_scaled_matmul(A, [W.t()], 0.5, [0.25], 0, tp, result_scales=[2.0])
+    assert D.dtype == torch.float8_e4m3fn
+    want = og.quantize_result(prod, "e4m3", 2.0)
+    got = D.view(torch.uint8).cpu().numpy()
+    assert np.mean(got == want) >= 0.99
+    Dr = ops.fused_scaled_matmul_reduce_scatter(A, W.t(), 0.5, 0.25, "sum", 0, tp, result_scale=2.0)
+    assert Dr.dtype == torch.float8_e4m3fn
+    assert np.mean(Dr.view(torch.uint8).cpu().numpy() == want) >= 0.99
