@@ -1000,6 +1000,7 @@ int dg_run_ex(dg_plan_t p, const void* A, const void* B, const dg_bf16_t* C, con
   kp.l2_hint = p->l2_hint;
   kp.done = reinterpret_cast<uint32_t*>(ws + p->off_done);
   kp.S = reinterpret_cast<float*>(ws + p->off_send);
+  kp.R = reinterpret_cast<const float*>(ws + p->off_recv);
   kp.wave_sync = wave_sync_on(p) ? 1u : 0u;
   kp.wave_ctr = reinterpret_cast<uint32_t*>(ws + p->off_status + 64);
   if (kp.wave_sync) DG_CUDA(cudaMemsetAsync(ws + p->off_status + 64, 0, 4, ms));

@@ -96,6 +96,7 @@ struct KParams {
   CUtensorMap tmS, tmR;
   uint32_t* done;       // per (rank, step, batch, band): half-tiles written to the send buffer
   float* S;             // send buffers (plain-store address of tmS)
+  const float* R;       // receive buffers (plain-load address of tmR)
   Geom g;
   const __nv_bfloat16* C;
   void* D;                    // bf16, or fp32 when out_f32
@@ -555,8 +556,12 @@ __device__ __forceinline__ void store_f32_row(float* x, int ncols, const float (
 // Source term (beta*C, the fp32 partial, or 0) for 32 consecutive columns of
 // one output row, then d = alpha*acc + src (+ the bias), stored as D (bf16 or
 // fp32) or as the fp32 partial.
+// xsrc / xdst: where this row's 32 partial values are read / written (the
+// shared partial X, or with the copy-engine hand-off the rank's receive and
+// send buffers).
 __device__ __forceinline__ void epilogue_row_chunk(const KParams& p, const Tile& tl, int64_t grow,
-                                                   int64_t gcol, int ncols, float (&acc)[32]) {
+                                                   int64_t gcol, int ncols, float (&acc)[32], const float* xsrc,
+                                                   float* xdst) {
   const int64_t N = p.g.N;
   const int64_t e0 = grow * N + gcol;  // element offset in C / D / X
   float src[32];
@@ -580,8 +585,8 @@ __device__ __forceinline__ void epilogue_row_chunk(const KParams& p, const Tile&
       for (int i = 0; i < 32; ++i) src[i] = i < ncols ? p.beta * bf16_bits_to_f32(cs[i]) : 0.f;
     }
   } else if (tl.src == SRC_X) {
-    const float* x = p.X + e0;
-    if (ncols == 32 && (e0 & 3) == 0) {
+    const float* x = xsrc;
+    if (ncols == 32 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) {
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         float4 v = __ldcg(reinterpret_cast<const float4*>(x) + q);
@@ -626,7 +631,7 @@ __device__ __forceinline__ void epilogue_row_chunk(const KParams& p, const Tile&
         if (i < ncols) d[i] = __float2bfloat16_rn(out[i]);
     }
   } else {
-    store_f32_row(p.X + e0, ncols, out, ncols == 32 && (e0 & 3) == 0);
+    store_f32_row(xdst, ncols, out, ncols == 32 && (reinterpret_cast<uintptr_t>(xdst) & 15) == 0);
   }
 }
 
@@ -1060,7 +1065,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
         }
         const int ncols = tl.cols_valid - c * XCOLS < XCOLS ? tl.cols_valid - c * XCOLS : XCOLS;
         if (!staged) {
-          if (row_ok) epilogue_row_chunk(p, tl, grow, tl.out_col + c * XCOLS, ncols, acc);
+          if (row_ok) {
+            const float* xs = cep ? p.R + (src_row0 + row) * p.g.blk_n + src_col0 + c * XCOLS
+                                  : p.X + grow * p.g.N + tl.out_col + c * XCOLS;
+            float* xd = (cep ? p.S : p.X) + (xd_row0 + row) * xd_pitch + xd_col0 + c * XCOLS;
+            epilogue_row_chunk(p, tl, grow, tl.out_col + c * XCOLS, ncols, acc, xs, xd);
+          }
           continue;
         }
         float src[32];

@@ -69,7 +69,8 @@ def test_random_configuration_with_epilogue_extras(i):
     from reduce_scatter_gb300 import synth
     sched, tp, m, n, k, l, ta, tb, alpha, beta, sa, sb, opts = _case(500 + i)
     rng = np.random.default_rng(7000 + i)
-    out_f32 = bool(rng.integers(0, 2))
+    out_kind = ["bf16", "f32", "e4m3", "e5m2"][int(rng.integers(0, 4))]
+    out_f32 = out_kind == "f32"
     op = "avg" if sched >= 2 and rng.integers(0, 2) else "sum"
     bias_bits = synth.tensor_bits_np(3000 + i, synth.STREAM_BIAS, (n,), ("uniform", -4.0, 4.0))
     if ta == "bf16":
@@ -82,14 +83,29 @@ def test_random_configuration_with_epilogue_extras(i):
         a64, b64 = og.fp8_bits_to_f64(a, ta), og.fp8_bits_to_f64(b, tb)
     want = og.fused_gemm(a64, b64, og.bf16_bits_to_f64(c) if beta else None, alpha * sa * sb, beta, P=tp,
                          reduce_op=None if sched <= 1 else op, bias=og.bf16_bits_to_f64(bias_bits))
-    plan = dg.Plan(m, n, k, l, tp, sched, alpha, beta, TCODE[ta], TCODE[tb], sa, sb,
-                   out_type="f32" if out_f32 else "bf16", reduce_op=op if sched >= 2 else "sum")
+    fp8_out = out_kind in ("e4m3", "e5m2")
+    rscale = 1.0 / max(float(np.abs(want).max()), 1e-30) * 64.0 if fp8_out else 1.0   # results well inside the format
+    plan = dg.Plan(m, n, k, l, tp, sched, alpha, beta, TCODE[ta], TCODE[tb], sa, sb, out_type=out_kind,
+                   reduce_op=op if sched >= 2 else "sum", result_scale=rscale)
     for o, v in opts.items():
         plan.set_option(o, v)
     ws = torch.zeros(max(plan.workspace_bytes(), 256), dtype=torch.uint8, device="cuda")
-    D = torch.full((l, m, n), float("nan"), dtype=torch.float32 if out_f32 else torch.bfloat16, device="cuda")
+    if fp8_out:
+        D = torch.full((l, m, n), 0x7F, dtype=torch.uint8, device="cuda")
+    else:
+        D = torch.full((l, m, n), float("nan"), dtype=torch.float32 if out_f32 else torch.bfloat16, device="cuda")
     main = torch.cuda.current_stream()
     plan.run_ex(A, B, to_dev(c) if beta else None, to_dev(bias_bits), D, ws, main, torch.cuda.Stream())
     plan.check(ws, main)
+    if fp8_out:
+        # codes equal to the oracle's, or neighbours (fp32 against fp64 rounding of a midpoint)
+        got = D.cpu().numpy()
+        wc = og.quantize_result(want, out_kind, rscale)
+        table = og.fp8_bits_to_f64(np.arange(256), out_kind)
+        vals = np.sort(np.unique(table[np.isfinite(table)]))
+        gv, wv = og.fp8_bits_to_f64(got, out_kind), og.fp8_bits_to_f64(wc, out_kind)
+        assert not np.any(np.isnan(gv))
+        assert np.abs(np.searchsorted(vals, gv) - np.searchsorted(vals, wv)).max() <= 1, (sched, tp, out_kind)
+        return
     err = rel_err(D, want)
     assert err <= (5e-4 if out_f32 else TOL), (err, sched, tp, m, n, k, l, ta, tb, opts, out_f32, op)

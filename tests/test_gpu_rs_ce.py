@@ -4,6 +4,7 @@ to the in-place hand-off (same order of the K-slab sums), gated by its ready
 flags (poisoned receive buffers, late copies), and bounded when a ready flag
 never comes."""
 
+import numpy as np
 import pytest
 import torch
 
@@ -95,3 +96,29 @@ def test_serial_baseline_unaffected_by_ce_option(sched):
     plan.run(A, B, C, D, ws, main, main)
     plan.check(ws, main)
     assert rel_err(D, oracle_full(a, b, c, 0.5, 1.0)) <= TOL
+
+
+@pytest.mark.parametrize("sched", RS, ids=lambda s: dg.SCHEDULE_NAMES[s])
+@pytest.mark.parametrize("epi", [0, 1])
+def test_ce_handoff_direct_paths_and_fp8_out(sched, epi):
+    # tiles that leave the staged path (fp8 D at the last step; every tile with EPILOGUE=0 set
+    # after the hand-off option) read the partial from the receive buffer and write the send buffer
+    from oracle import gemm as og
+    m, n, k, l, tp = 1024, 2048, 1024, 2, 4
+    a, b, c = host_inputs(m, n, k, l, seed=140 + sched + epi)
+    A, B, C = to_dev(a), to_dev(b), to_dev(c)
+    ref, _ = Runner(m, n, k, l, tp, sched, 0.5, 1.0).run(A, B, C)
+    r = Runner(m, n, k, l, tp, sched, 0.5, 1.0, options={dg.OPT_RS_CE_PARTIALS: 1, dg.OPT_EPILOGUE: epi})
+    D, _ = r.run(A, B, C)
+    assert torch.equal(D.view(torch.int16), ref.view(torch.int16))
+    plan = dg.Plan(m, n, k, l, tp, sched, 0.5, 1.0, out_type="e4m3", result_scale=2.0)
+    plan.set_option(dg.OPT_RS_CE_PARTIALS, 1)
+    plan.set_option(dg.OPT_EPILOGUE, epi)
+    ws = torch.zeros(plan.workspace_bytes(), dtype=torch.uint8, device="cuda")
+    D8 = torch.full((l, m, n), 0x7F, dtype=torch.uint8, device="cuda")
+    main = torch.cuda.current_stream()
+    plan.run_ex(A, B, C, None, D8, ws, main, torch.cuda.Stream())
+    plan.check(ws, main)
+    want = og.quantize_result(og.gemm(og.bf16_bits_to_f64(a), og.bf16_bits_to_f64(b), og.bf16_bits_to_f64(c),
+                                      0.5, 1.0), "e4m3", 2.0)
+    assert np.mean(D8.cpu().numpy() == want) >= 0.98
