@@ -163,12 +163,17 @@ enum dg_option {
                                  instead of all running at the start; 0 = all transfers are
                                  issued at once; -1 (default) = on */
   DG_OPT_COPY_KIND = 14       /* how shard and partial transfers are issued: 0 (default) =
-                                 two-dimensional device-to-device copies, which run on a copy
-                                 engine beside a kernel that fills every SM; 1 = one-dimensional
+                                 two-dimensional device-to-device copies in the operand's own
+                                 rows, which run on a copy engine beside a kernel that fills
+                                 every SM (~1.0 TB/s on GB300); 1 = one-dimensional
                                  cudaMemcpyAsync, which on GB300 runs as a copy kernel on SMs
                                  and so only progresses where the GEMM kernel leaves an SM
-                                 registers to spare (faster, ~3.2 TB/s against ~1-1.8 TB/s,
-                                 but it competes with the GEMM for SMs) */
+                                 registers to spare (~3.2 TB/s when it gets SMs, but it
+                                 competes with the GEMM for them); 2 = two-dimensional copies
+                                 reshaped to at least 65,536 rows (the bytes are contiguous,
+                                 so the row width is free), which a copy engine moves at
+                                 ~1.8-2.1 TB/s alone on GB300, at the price of more HBM
+                                 bandwidth taken from a GEMM running beside them */
 };
 
 /* Plan geometry and workspace layout, for callers and tests. */

@@ -148,7 +148,8 @@ struct dg_plan_s {
   uint32_t l2_hint = 0;  // L2 policy of operand loads (DG_OPT_L2_HINT)
   int wave_sync = -1;  // DG_OPT_WAVE_SYNC: -1 auto, 0 off, 1 on
   int copy_pace = -1;  // DG_OPT_COPY_PACE: -1 auto, 0 off, 1 on
-  int copy_kind = 0;   // DG_OPT_COPY_KIND: 0 copy engine (2D copies), 1 one-dimensional cudaMemcpyAsync
+  int copy_kind = 0;   // DG_OPT_COPY_KIND: 0 copy engine (2D copies in the operand's rows), 1
+                       // one-dimensional cudaMemcpyAsync, 2 copy engine (tall 2D copies)
   uint64_t id = 0;
   uint32_t epoch = 0;
   bool serial_ws = false;
@@ -464,17 +465,40 @@ int build_maps(dg_plan_s* p, const Driver& drv, const void* A, const void* B, ui
   return DG_OK;
 }
 
-// Device-to-device transfer of `rows` contiguous rows of `row_bytes` bytes on
-// a copy engine.  Issued as a two-dimensional copy: a one-dimensional
-// device-to-device cudaMemcpyAsync runs as a copy kernel on the SMs, which can
-// only start where the persistent GEMM kernel leaves registers free (measured
-// on GB300: such copies stall until the kernel exits when it holds 47 K of an
-// SM's 64 K registers, and move 3.2 TB/s when they get SMs), while the
-// two-dimensional form runs on a copy engine beside a kernel that fills every
-// SM (1.8 TB/s per copy).
-// DG_OPT_COPY_KIND = 1 selects the one-dimensional form instead.
+// Device-to-device transfer of `rows` contiguous rows of `row_bytes` bytes.
+//
+// kind 0 (default): a two-dimensional copy in the operand's own rows (pitch =
+// row bytes).  Two-dimensional copies run on a copy engine beside a kernel
+// that fills every SM, ~1.0 TB/s on GB300 (several such copies on separate
+// streams share that rate).
+// kind 1: one-dimensional cudaMemcpyAsync, which runs as a copy kernel on the
+// SMs and so only starts where the persistent GEMM kernel leaves registers
+// free (such copies stall until the kernel exits when it holds 47 K of an
+// SM's 64 K registers, and move 3.2 TB/s when they get SMs).
+// kind 2: a two-dimensional copy reshaped to at least kTallRows rows.  On
+// GB300 a copy of 65,536 rows or more moves 1.8-2.1 TB/s where the same bytes
+// in fewer, wider rows move ~1.0 TB/s.  The bytes are contiguous on both
+// sides, so any row width that divides them gives the same result; the widest
+// power of two that keeps kTallRows rows is taken and a remainder shorter than
+// one row goes as a one-row copy.  Faster alone, but beside the GEMM kernel it
+// takes more of the HBM bandwidth and power, and the fused runs measured no
+// faster (AG-RotatingB a few percent slower).
+constexpr size_t kTallRows = 65536;
+constexpr size_t kMinTallWidth = 128;
+
 cudaError_t ce_copy(void* dst, const void* src, size_t row_bytes, size_t rows, cudaStream_t st, int kind) {
-  if (kind == 1) return cudaMemcpyAsync(dst, src, row_bytes * rows, cudaMemcpyDeviceToDevice, st);
+  const size_t bytes = row_bytes * rows;
+  if (kind == 1) return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st);
+  if (kind == 2 && rows < kTallRows && bytes >= kTallRows * kMinTallWidth) {
+    size_t w = kMinTallWidth;
+    while (w * 2 * kTallRows <= bytes) w *= 2;
+    const size_t h = bytes / w, body = h * w;
+    cudaError_t e = cudaMemcpy2DAsync(dst, w, src, w, w, h, cudaMemcpyDeviceToDevice, st);
+    if (e != cudaSuccess || body == bytes) return e;
+    const size_t rest = bytes - body;
+    return cudaMemcpy2DAsync(static_cast<uint8_t*>(dst) + body, rest, static_cast<const uint8_t*>(src) + body, rest,
+                             rest, 1, cudaMemcpyDeviceToDevice, st);
+  }
   return cudaMemcpy2DAsync(dst, row_bytes, src, row_bytes, row_bytes, rows, cudaMemcpyDeviceToDevice, st);
 }
 
@@ -823,7 +847,8 @@ int dg_set_option(dg_plan_t p, int option, int64_t value) {
       layout(p);
       return DG_OK;
     case DG_OPT_COPY_KIND:
-      if (value != 0 && value != 1) return fail(DG_ERR_ARG, "copy kind must be 0 (copy engine) or 1 (1D memcpy)");
+      if (value < 0 || value > 2)
+        return fail(DG_ERR_ARG, "copy kind must be 0 (copy engine), 1 (1D memcpy) or 2 (copy engine, tall copies)");
       p->copy_kind = (int)value;
       return DG_OK;
     case DG_OPT_COPY_PACE:

@@ -306,10 +306,11 @@ def test_copy_pace_option_rules(L):
 
 def test_copy_kind_option_rules(L):
     p = dg.Plan(512, 512, 512, 1, 4, dg.AG_ROTATING_A)
-    p.set_option(dg.OPT_COPY_KIND, 1)
-    p.set_option(dg.OPT_COPY_KIND, 0)
-    with pytest.raises(dg.DGError):
-        p.set_option(dg.OPT_COPY_KIND, 2)
+    for v in (1, 2, 0):
+        p.set_option(dg.OPT_COPY_KIND, v)
+    for v in (-1, 3):
+        with pytest.raises(dg.DGError):
+            p.set_option(dg.OPT_COPY_KIND, v)
 
 
 def test_run_host_argument_checks_without_gpu(L):

@@ -170,12 +170,33 @@ def test_paced_transfers_with_held_copies():
 
 @pytest.mark.parametrize("sched", [dg.AG_ROTATING_A, dg.AG_ROTATING_B], ids=lambda s: dg.SCHEDULE_NAMES[s])
 def test_copy_kinds_same_bits(sched):
-    # copy-engine (2D) and one-dimensional transfers move the same bytes
+    # row-shaped 2D, one-dimensional and tall 2D transfers move the same bytes
     m, n, k, l, tp = 1024, 2048, 512, 2, 4
     a, b, c = host_inputs(m, n, k, l, seed=420 + sched)
     A, B, C = to_dev(a), to_dev(b), to_dev(c)
     D = {}
-    for kind in (0, 1):
+    for kind in (0, 1, 2):
         r = Runner(m, n, k, l, tp, sched, 0.5, 1.0, options={dg.OPT_COPY_KIND: kind})
         D[kind], _ = r.run(A, B, C)
     assert torch.equal(D[0].view(torch.int16), D[1].view(torch.int16))
+    assert torch.equal(D[0].view(torch.int16), D[2].view(torch.int16))
+
+
+@pytest.mark.parametrize("sched,m,n,tp", [(dg.AG_ROTATING_A, 8198, 512, 2), (dg.AG_ROTATING_B, 256, 32792, 8)],
+                         ids=["AG-RotatingA", "AG-RotatingB"])
+def test_tall_copies_with_a_remainder(sched, m, n, tp):
+    # one chunk per shard of 4099 rows x 2064 bytes = 8,460,336 bytes: the tall
+    # copy (kind 2) takes 66,096 rows of 128 bytes and a 48-byte remainder
+    k, l = 1032, 1
+    a, b, c = host_inputs(m, n, k, l, seed=431 + sched)
+    A, B, C = to_dev(a), to_dev(b), to_dev(c)
+    D = {}
+    for kind in (0, 1, 2):
+        r = Runner(m, n, k, l, tp, sched, 0.5, 1.0, options={dg.OPT_COPY_KIND: kind, dg.OPT_CHUNK_TILES: 64})
+        assert r.plan.info()["chunks_per_shard"] == 1
+        D[kind], _ = r.run(A, B, C)
+    assert torch.equal(D[0].view(torch.int16), D[1].view(torch.int16))
+    assert torch.equal(D[0].view(torch.int16), D[2].view(torch.int16))
+    rows = np.r_[0:3, m // 2 - 1:m // 2 + 2, m - 3:m]
+    ref = oracle_full(a[:, rows], b, c[:, rows], 0.5, 1.0)
+    assert rel_err(D[0][:, torch.as_tensor(rows, device="cuda")], ref) <= TOL

@@ -122,3 +122,18 @@ def test_ce_handoff_direct_paths_and_fp8_out(sched, epi):
     want = og.quantize_result(og.gemm(og.bf16_bits_to_f64(a), og.bf16_bits_to_f64(b), og.bf16_bits_to_f64(c),
                                       0.5, 1.0), "e4m3", 2.0)
     assert np.mean(D8.cpu().numpy() == want) >= 0.98
+
+
+@pytest.mark.parametrize("sched,n", [(dg.RS_TILING_A_ROTATING_C, 8200), (dg.RS_TILING_B_ROTATING_C, 16400)],
+                         ids=["RS-TilingA", "RS-TilingB"])
+def test_ce_handoff_with_tall_copies(sched, n):
+    # 256-row bands of 8200 fp32 columns = 8,396,800 bytes: the tall copy
+    # (DG_OPT_COPY_KIND=2) moves each as 65,600 rows of 128 bytes
+    m, k, l, tp = 1024, 256, 1, 2
+    a, b, c = host_inputs(m, n, k, l, seed=130 + sched)
+    A, B, C = to_dev(a), to_dev(b), to_dev(c)
+    ref, _ = Runner(m, n, k, l, tp, sched, 0.5, 1.0).run(A, B, C)
+    r = Runner(m, n, k, l, tp, sched, 0.5, 1.0, options={dg.OPT_RS_CE_PARTIALS: 1, dg.OPT_COPY_KIND: 2})
+    D, _ = r.run(A, B, C)
+    assert rel_err(D, oracle_full(a, b, c, 0.5, 1.0)) <= TOL
+    assert torch.equal(D.view(torch.int16), ref.view(torch.int16))
