@@ -468,7 +468,8 @@ def run_dg(args, rank, world, dist):
         plan.check(ws, main)
         e2e = {"value": None, "unit": "TFLOP/s", "ms_per_step": ms_e2e, "steps": e2e_steps,
                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": D.numel() * 2,
-               "mode": "sequential: dg_run_host (upload inputs, run, download D) every step"}
+               "mode": "one dg_run_host call per step: inputs uploaded and D downloaded inside the call "
+                       "(per-rank uploads gate the kernel's tiles, finished D blocks download during the run)"}
         if not args.no_e2e_pipelined:
             e2e["pipelined"] = e2e_pipelined(plan, ws, main, copy, A_h, B_h, C_h, A, B, C, D, e2e_steps + 2)
             plan.check(ws, main)

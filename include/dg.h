@@ -162,7 +162,7 @@ enum dg_option {
                                  so each step's transfers overlap the previous step's GEMM
                                  instead of all running at the start; 0 = all transfers are
                                  issued at once; -1 (default) = on */
-  DG_OPT_COPY_KIND = 14       /* how shard and partial transfers are issued: 0 (default) =
+  DG_OPT_COPY_KIND = 14,      /* how shard and partial transfers are issued: 0 (default) =
                                  two-dimensional device-to-device copies in the operand's own
                                  rows, which run on a copy engine beside a kernel that fills
                                  every SM (~1.0 TB/s on GB300); 1 = one-dimensional
@@ -174,6 +174,11 @@ enum dg_option {
                                  so the row width is free), which a copy engine moves at
                                  ~1.8-2.1 TB/s alone on GB300, at the price of more HBM
                                  bandwidth taken from a GEMM running beside them */
+  DG_OPT_HOST_OVERLAP = 15    /* dg_run_host in FUSED mode with pinned host buffers: 1 (default) =
+                                 launch the kernel at once and overlap the transfers with it
+                                 (rank r's tiles wait for rank r's uploaded inputs; each
+                                 finished (step, rank) block of D is downloaded while later
+                                 steps run); 0 = upload everything, run, then download */
 };
 
 /* Plan geometry and workspace layout, for callers and tests. */
@@ -276,16 +281,26 @@ int dg_run_ex(dg_plan_t plan, const void* A, const void* B, const dg_bf16_t* C, 
               void* D, void* workspace, void* main_stream, void* copy_stream);
 
 /* dg_run_ex with host-resident operands, for callers whose data lives in
- * host memory: on main_stream, copies A and B (and C when beta != 0) from
- * host memory into the caller's device buffers, runs the plan on them, and
- * copies D back into host memory.  Sizes follow the plan: A L*M*K elements,
- * B L*N*K (both of the plan's input type), C L*M*N bf16, D L*M*N of the
- * output type.  Host buffers should be page-locked (cudaHostAlloc or
- * cudaHostRegister) for the copies to be asynchronous and to run on a copy
- * engine; pageable memory works with host-synchronous copies.  bias, if not
+ * host memory: copies A and B (and C when beta != 0) from host memory into
+ * the caller's device buffers, runs the plan on them, and copies D back into
+ * host memory.  Sizes follow the plan: A L*M*K elements, B L*N*K (both of the
+ * plan's input type), C L*M*N bf16, D L*M*N of the output type.  bias, if not
  * NULL, is a device pointer.  The device buffers follow dg_run's rules.
- * Returns after enqueueing; D_host is valid once main_stream has reached
- * that point (e.g. after dg_check). */
+ *
+ * In FUSED mode with every host buffer page-locked (cudaHostAlloc or
+ * cudaHostRegister) and DG_OPT_HOST_OVERLAP on (the default), the transfers
+ * overlap the kernel: it is launched at once; plan-owned streams upload each
+ * rank's inputs in the kernel's order (rank r: its home shards of A and B and
+ * the part of C its tiles read), and the tiles of rank r wait (bounded, like
+ * the shard flags) for rank r's upload; each (step, rank) block of D is copied
+ * back as soon as the kernel has finished it.  Otherwise (another mode,
+ * pageable memory, or the option off) the call uploads everything on
+ * main_stream, runs, then downloads: pageable memory works with
+ * host-synchronous copies.  Either way the call is one operation on
+ * main_stream: it starts after the work already enqueued there, and returns
+ * after enqueueing; D_host is valid once main_stream has reached that point
+ * (e.g. after dg_check).  D_host and the device buffers must not be touched
+ * by other work until then. */
 int dg_run_host(dg_plan_t plan, const void* A_host, const void* B_host, const dg_bf16_t* C_host,
                 const dg_bf16_t* bias, void* D_host, void* A_dev, void* B_dev, dg_bf16_t* C_dev, void* D_dev,
                 void* workspace, void* main_stream, void* copy_stream);

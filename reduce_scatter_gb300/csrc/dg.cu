@@ -119,8 +119,10 @@ struct NvtxRange {
 };
 
 // Layout of the 256-byte status area: [0, 8) status word, [64, 68) wave
-// counter, [128, 128 + 4 * tp) copy-pacing progress words.
+// counter, [128, 128 + 4 * tp) copy-pacing progress words, [192, 192 + 4 * tp)
+// per-rank upload flags of runs that take host buffers.
 constexpr size_t kProgressOffset = 128;
+constexpr size_t kUpOffset = 192;
 
 }  // namespace
 
@@ -150,12 +152,14 @@ struct dg_plan_s {
   int copy_pace = -1;  // DG_OPT_COPY_PACE: -1 auto, 0 off, 1 on
   int copy_kind = 0;   // DG_OPT_COPY_KIND: 0 copy engine (2D copies in the operand's rows), 1
                        // one-dimensional cudaMemcpyAsync, 2 copy engine (tall 2D copies)
+  int host_overlap = 1;  // DG_OPT_HOST_OVERLAP: dg_run_host overlaps its transfers with the kernel
   uint64_t id = 0;
   uint32_t epoch = 0;
   bool serial_ws = false;
   // layout
   int64_t n_flags = 0;
   size_t off_status = 0, off_flags = 0, off_slots = 0, off_partial = 0, off_serial = 0;
+  size_t off_ddone = 0;  // per (step, rank) counters of finished D half tiles (dg_run_host)
   size_t slot_bytes = 0, ws_bytes_base = 0, ws_bytes_serial = 0;
   int64_t copies = 0;
   // runtime state
@@ -170,6 +174,11 @@ struct dg_plan_s {
   int n_extra = 0;
   cudaStream_t extra[7] = {};
   cudaEvent_t extra_done[7] = {};
+  // dg_run_host with overlapped transfers: host-to-device and device-to-host
+  // streams, the fork point on the main stream, one event per rank's upload
+  bool io_rt = false;
+  cudaStream_t up_st = nullptr, down_st = nullptr;
+  cudaEvent_t ev_io = nullptr, ev_up[8] = {}, ev_up_done = nullptr, ev_down_done = nullptr;
   dg::KParams kp;
   dg::Geom gser{};   // RS SERIAL baseline: per-rank partial GEMMs (SCHED_PARTIAL)
   dg::KParams kser;  // its kernel parameters
@@ -253,7 +262,8 @@ int layout(dg_plan_s* p) {
   p->gser.total_tiles = P * p->gser.tiles_block;
   p->off_status = 0;
   p->off_flags = 256;
-  size_t off = round_up(p->off_flags + (size_t)p->n_flags * 4, 1024);
+  p->off_ddone = round_up(p->off_flags + (size_t)p->n_flags * 4, 256);
+  size_t off = round_up(p->off_ddone + (size_t)(P * P) * 4, 1024);
   p->off_slots = off;
   p->slot_bytes = is_ag(p->schedule) ? (size_t)g.shard * (size_t)p->k * (size_t)p->esz : 0;
   if (is_ag(p->schedule) && P > 1) off = round_up(off + (size_t)(P * (P - 1) * g.L) * p->slot_bytes, 1024);
@@ -519,9 +529,11 @@ int ensure_extra_streams(dg_plan_s* p, int want) {
 
 // Shard transfers of every rank and step >= 1, each chunk followed by its
 // ready-flag write on the same stream, in the order the kernel consumes them.
-// Chunks are dealt round-robin over `ns` streams.
+// Chunks are dealt round-robin over `ns` streams.  With `wait_up` (inputs
+// uploaded by the same call) a stream first waits for the upload of the rank
+// whose home shard it copies.
 int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B, uint8_t* ws,
-                   cudaStream_t* streams, int ns, bool pace) {
+                   cudaStream_t* streams, int ns, bool pace, bool wait_up = false) {
   NvtxRange range("dg_enqueue_copies");
   auto* progress = reinterpret_cast<uint32_t*>(ws + p->off_status + kProgressOffset);
   const dg::Geom& g = p->g;
@@ -537,6 +549,7 @@ int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B
   const int64_t chunk_rows = g.chunk_tiles * tile_rows;
   auto* slots = ws + p->off_slots;
   auto* flags = reinterpret_cast<uint32_t*>(ws + p->off_flags);
+  uint32_t up_waited[8] = {};  // per stream: ranks whose upload it already waits for
   int64_t idx = 0;
   for (int64_t s = 1; s < P; ++s) {
     if (pace && s >= 2)
@@ -554,6 +567,10 @@ int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B
         const int64_t slot = (r * (P - 1) + (s - 1)) * g.L + l;
         for (int64_t c = 0; c < g.nchunks; ++c, ++idx) {
           cudaStream_t st = streams[idx % ns];
+          if (wait_up && !((up_waited[idx % ns] >> j) & 1u)) {
+            DG_CUDA(cudaStreamWaitEvent(st, p->ev_up[j], 0));
+            up_waited[idx % ns] |= 1u << j;
+          }
           const int64_t row0 = c * chunk_rows;
           const int64_t rows = std::min(chunk_rows, g.shard - row0);
           if (rows > 0) {
@@ -734,6 +751,355 @@ int run_rs_serial(dg_plan_s* p, const Driver& drv, const void* C, void* D, uint8
   return DG_OK;
 }
 
+// --------------------------------------------------- runs with host buffers
+//
+// dg_run_host with DG_OPT_HOST_OVERLAP (default) in FUSED mode, with pinned
+// host buffers: the kernel is launched at once and its tiles wait for their
+// rank's inputs instead of for the whole upload, and D leaves the device one
+// (step, rank) block at a time while later steps still run.
+//   upload stream:   for r = 0..P-1 in the kernel's order: rank r's home
+//                    operand shards and the part of C its tiles read, then
+//                    up_flags[r] = epoch (the producers and C-reading
+//                    epilogues of rank r's tiles wait on it) and an event (the
+//                    shard transfers of rank r's home shard wait on it)
+//   download stream: for every (step, rank) block that writes D, wait until
+//                    the kernel has counted all its half tiles, then copy the
+//                    block to the host
+// The main stream joins both at the end, so the call stays one stream-ordered
+// operation like the sequential form.
+
+struct HostIO {
+  const void* A;
+  const void* B;
+  const void* C;
+  void* D;
+};
+
+int ensure_io(dg_plan_s* p) {
+  if (p->io_rt) return DG_OK;
+  DG_CUDA(cudaStreamCreateWithFlags(&p->up_st, cudaStreamNonBlocking));
+  DG_CUDA(cudaStreamCreateWithFlags(&p->down_st, cudaStreamNonBlocking));
+  DG_CUDA(cudaEventCreateWithFlags(&p->ev_io, cudaEventDisableTiming));
+  DG_CUDA(cudaEventCreateWithFlags(&p->ev_up_done, cudaEventDisableTiming));
+  DG_CUDA(cudaEventCreateWithFlags(&p->ev_down_done, cudaEventDisableTiming));
+  for (int i = 0; i < 8; ++i) DG_CUDA(cudaEventCreateWithFlags(&p->ev_up[i], cudaEventDisableTiming));
+  p->io_rt = true;
+  return DG_OK;
+}
+
+// `rows` rows of `width` bytes at row pitch `pitch` (the same on both sides).
+int copy_rows(void* dst, const void* src, size_t pitch, size_t width, size_t rows, cudaMemcpyKind kind,
+              cudaStream_t st) {
+  if (width == 0 || rows == 0) return DG_OK;
+  DG_CUDA(cudaMemcpy2DAsync(dst, pitch, src, pitch, width, rows, kind, st));
+  return DG_OK;
+}
+
+// Host-to-device copies of rank r's inputs:
+//   AG-RotatingA   A rows M_r, B rows N_r, C[:, N_r]
+//   AG-RotatingB   A rows M_r, B rows N_r, C[M_r, :]
+//   RS-TilingA     A[:, K_r], B[:, K_r], C[M_j, :] with j = (r + 1) mod P
+//   RS-TilingB     A[:, K_r], B[:, K_r], C[:, N_j] with j = (r + 1) mod P
+// (every batch l; C only when beta != 0).  In the RS schedules rank r reads
+// user C only at step 0, for slab (r + 1) mod P.
+int upload_rank(dg_plan_s* p, const HostIO& io, const void* A, const void* B, void* C, int64_t r,
+                cudaStream_t st) {
+  const dg::Geom& g = p->g;
+  const int64_t L = g.L, M = p->m, N = p->n, K = p->k, P = p->tp;
+  const size_t es = (size_t)p->esz, rowA = (size_t)K * es, rowC = (size_t)N * 2;
+  auto* a_d = static_cast<uint8_t*>(const_cast<void*>(A));
+  auto* b_d = static_cast<uint8_t*>(const_cast<void*>(B));
+  auto* c_d = static_cast<uint8_t*>(C);
+  const auto* a_h = static_cast<const uint8_t*>(io.A);
+  const auto* b_h = static_cast<const uint8_t*>(io.B);
+  const auto* c_h = static_cast<const uint8_t*>(io.C);
+  const bool with_c = p->beta != 0.f;
+  const auto H2D = cudaMemcpyHostToDevice;
+  int rc = DG_OK;
+  if (is_ag(p->schedule)) {
+    for (int64_t l = 0; l < L && !rc; ++l) {
+      const size_t a0 = (size_t)(l * M + r * g.blk_m) * rowA, b0 = (size_t)(l * N + r * g.blk_n) * rowA;
+      rc = copy_rows(a_d + a0, a_h + a0, rowA, rowA, (size_t)g.blk_m, H2D, st);
+      if (!rc) rc = copy_rows(b_d + b0, b_h + b0, rowA, rowA, (size_t)g.blk_n, H2D, st);
+    }
+    if (rc || !with_c) return rc;
+    if (p->schedule == DG_AG_ROTATING_A) {
+      const size_t c0 = (size_t)(r * g.blk_n) * 2;
+      return copy_rows(c_d + c0, c_h + c0, rowC, (size_t)g.blk_n * 2, (size_t)(L * M), H2D, st);
+    }
+    for (int64_t l = 0; l < L && !rc; ++l) {
+      const size_t c0 = (size_t)(l * M + r * g.blk_m) * rowC;
+      rc = copy_rows(c_d + c0, c_h + c0, rowC, rowC, (size_t)g.blk_m, H2D, st);
+    }
+    return rc;
+  }
+  const size_t k0 = (size_t)(r * g.Ks) * es, kw = (size_t)g.Ks * es;
+  rc = copy_rows(a_d + k0, a_h + k0, rowA, kw, (size_t)(L * M), H2D, st);
+  if (!rc) rc = copy_rows(b_d + k0, b_h + k0, rowA, kw, (size_t)(L * N), H2D, st);
+  if (rc || !with_c) return rc;
+  const int64_t j = (r + 1) % P;
+  if (p->schedule == DG_RS_TILING_A_ROTATING_C) {
+    for (int64_t l = 0; l < L && !rc; ++l) {
+      const size_t c0 = (size_t)(l * M + j * g.blk_m) * rowC;
+      rc = copy_rows(c_d + c0, c_h + c0, rowC, rowC, (size_t)g.blk_m, H2D, st);
+    }
+    return rc;
+  }
+  const size_t c0 = (size_t)(j * g.blk_n) * 2;
+  return copy_rows(c_d + c0, c_h + c0, rowC, (size_t)g.blk_n * 2, (size_t)(L * M), H2D, st);
+}
+
+// Uploads of every rank on the upload stream, after everything already on the
+// main stream (which may still read the device inputs).
+int enqueue_uploads(dg_plan_s* p, const Driver& drv, const HostIO& io, const void* A, const void* B, void* C,
+                    uint8_t* ws) {
+  auto* up = reinterpret_cast<uint32_t*>(ws + p->off_status + kUpOffset);
+  if (p->fault_delay_ms > 0)
+    DG_CUDA(cudaLaunchHostFunc(p->up_st, sleep_cb, (void*)(intptr_t)p->fault_delay_ms));
+  for (int64_t r = 0; r < p->tp; ++r) {
+    int rc = upload_rank(p, io, A, B, C, r, p->up_st);
+    if (rc) return rc;
+    CUresult cr = drv.write32((CUstream)p->up_st, (CUdeviceptr)(up + r), p->epoch, 0);
+    if (cr != CUDA_SUCCESS)
+      return fail(cr == CUDA_ERROR_NOT_SUPPORTED ? DG_ERR_UNSUPPORTED : DG_ERR_CUDA, "cuStreamWriteValue32 failed (%d)",
+                  (int)cr);
+    DG_CUDA(cudaEventRecord(p->ev_up[r], p->up_st));
+  }
+  DG_CUDA(cudaEventRecord(p->ev_up_done, p->up_st));
+  return DG_OK;
+}
+
+// Downloads of D, block by block as the kernel finishes them.
+int enqueue_downloads(dg_plan_s* p, const Driver& drv, const HostIO& io, const void* D, uint8_t* ws) {
+  const dg::Geom& g = p->g;
+  const int64_t P = p->tp, L = g.L, M = p->m;
+  const size_t de = p->out_type == DG_TYPE_F32 ? 4 : (p->out_type == DG_TYPE_BF16 ? 2 : 1);
+  const size_t pitch = (size_t)p->n * de;
+  auto* done = reinterpret_cast<uint32_t*>(ws + p->off_ddone);
+  const uint32_t target = (uint32_t)(g.tiles_block * p->cg);  // half tiles of one (step, rank) block
+  const auto* d_d = static_cast<const uint8_t*>(D);
+  auto* d_h = static_cast<uint8_t*>(io.D);
+  const auto D2H = cudaMemcpyDeviceToHost;
+  const bool ag = is_ag(p->schedule);
+  for (int64_t s = ag ? 0 : P - 1; s < P; ++s)
+    for (int64_t r = 0; r < P; ++r) {
+      CUresult cr = drv.wait32((CUstream)p->down_st, (CUdeviceptr)(done + s * P + r), target,
+                               CU_STREAM_WAIT_VALUE_GEQ);
+      if (cr != CUDA_SUCCESS)
+        return fail(cr == CUDA_ERROR_NOT_SUPPORTED ? DG_ERR_UNSUPPORTED : DG_ERR_CUDA,
+                    "cuStreamWaitValue32 failed (%d)", (int)cr);
+      const int64_t j = ag ? (r + s) % P : r;  // the RS block of the last step is the rank's own slab
+      int rc = DG_OK;
+      if (p->schedule == DG_RS_TILING_B_ROTATING_C) {
+        const size_t o = (size_t)(j * g.blk_n) * de;
+        rc = copy_rows(d_h + o, d_d + o, pitch, (size_t)g.blk_n * de, (size_t)(L * M), D2H, p->down_st);
+      } else {
+        for (int64_t l = 0; l < L && !rc; ++l) {
+          int64_t row0, col0, cols;
+          if (p->schedule == DG_AG_ROTATING_A) row0 = j * g.blk_m, col0 = r * g.blk_n, cols = g.blk_n;
+          else if (p->schedule == DG_AG_ROTATING_B) row0 = r * g.blk_m, col0 = j * g.blk_n, cols = g.blk_n;
+          else row0 = j * g.blk_m, col0 = 0, cols = p->n;
+          const size_t o = (size_t)(l * M + row0) * pitch + (size_t)col0 * de;
+          rc = copy_rows(d_h + o, d_d + o, pitch, (size_t)cols * de, (size_t)g.blk_m, D2H, p->down_st);
+        }
+      }
+      if (rc) return rc;
+    }
+  return DG_OK;
+}
+
+bool pinned_host(const void* q) {
+  if (!q) return false;
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, q) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
+
+int dispatch_run(dg_plan_s* p, const Driver& drv, const void* A, const void* B, const dg_bf16_t* C, void* D,
+                 uint8_t* ws, cudaStream_t ms, cudaStream_t cs, bool rs_serial, bool pace, bool wait_up);
+
+int run_impl(dg_plan_s* p, const void* A, const void* B, const dg_bf16_t* C, const dg_bf16_t* bias, void* D,
+             void* workspace, void* main_stream, void* copy_stream, const HostIO* io) {
+  NvtxRange range("dg_run");
+  if (!p) return fail(DG_ERR_ARG, "plan is NULL");
+  if (p->g.total_tiles == 0) return DG_OK;  // empty output
+  if (!A || !B || !D) return fail(DG_ERR_ARG, "A, B and D must be non-NULL");
+  if (p->beta != 0.f && !C) return fail(DG_ERR_ARG, "C is NULL but beta != 0");
+  auto misaligned = [](const void* q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) & (a - 1)) != 0; };
+  if (misaligned(A, 16) || misaligned(B, 16) || misaligned(D, 16) || (C && misaligned(C, 16)) ||
+      (bias && misaligned(bias, 16)))
+    return fail(DG_ERR_ARG, "A, B, C, D and bias must be 16-byte aligned");
+  // bytes this run uses (no side effect on the plan's SERIAL sizing record)
+  const size_t need =
+      (!is_ag(p->schedule) && p->mode == DG_MODE_SERIAL) ? p->ws_bytes_serial : p->ws_bytes_base;
+  if (need > 0 && (!workspace || misaligned(workspace, 256)))
+    return fail(DG_ERR_ARG, "workspace must be non-NULL and 256-byte aligned");
+  const bool rs_serial = !is_ag(p->schedule) && p->mode == DG_MODE_SERIAL;
+  if (rs_serial && !p->serial_ws)
+    return fail(DG_ERR_STATE, "RS SERIAL needs the larger workspace: size it with dg_workspace_bytes in SERIAL mode");
+  int rc = rt_init(p);
+  if (rc) return rc;
+  Driver drv;
+  rc = get_driver(&drv);
+  if (rc) return rc;
+  auto ms = static_cast<cudaStream_t>(main_stream);
+  auto cs = static_cast<cudaStream_t>(copy_stream);
+  auto* ws = static_cast<uint8_t*>(workspace);
+
+  // Epochs grow per plan across all of its workspaces, so flag words left in
+  // any workspace by this plan's earlier runs stay below the current epoch.
+  // A workspace new to this plan starts from zeroed flags.  Only when the
+  // epoch would overflow is it restarted, and then every other workspace of
+  // this plan is forgotten so that it is cleared again on its next use.
+  bool clear = false;
+  const bool wrap = (uint64_t)(p->epoch + 2) * (uint64_t)p->tp >= 0x7FFFFFFFull;
+  {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    if (wrap)
+      for (auto it = g_ws_owner.begin(); it != g_ws_owner.end();)
+        it = it->second == p->id ? g_ws_owner.erase(it) : std::next(it);
+    auto it = g_ws_owner.find(workspace);
+    if (it == g_ws_owner.end() || it->second != p->id) {
+      g_ws_owner[workspace] = p->id;
+      clear = true;
+    }
+  }
+  // Under stream capture the run's epoch is frozen into the graph, so every
+  // replay must start from zeroed status and flag words: clear them in the
+  // graph itself (one memset node).
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  DG_CUDA(cudaStreamIsCapturing(ms, &cap));
+  if (cap == cudaStreamCaptureStatusActive) clear = true;
+  if (clear) DG_CUDA(cudaMemsetAsync(ws, 0, p->off_flags + (size_t)p->n_flags * 4, ms));
+  if (wrap) p->epoch = 0;
+  p->epoch += 1;
+
+  rc = build_maps(p, drv, A, B, ws);
+  if (rc) return rc;
+  rc = build_epi_maps(p, drv, C, D, ws);
+  if (rc) return rc;
+  dg::KParams& kp = p->kp;
+  kp.g = p->g;
+  kp.C = reinterpret_cast<const __nv_bfloat16*>(C);
+  kp.D = D;
+  kp.bias = reinterpret_cast<const __nv_bfloat16*>(bias);
+  kp.out_f32 = p->out_type == DG_TYPE_F32 ? 1u : 0u;
+  kp.out_fp8 = p->out_type == DG_TYPE_E4M3 ? 1u : p->out_type == DG_TYPE_E5M2 ? 2u : 0u;
+  kp.result_scale = p->result_scale;
+  kp.X = reinterpret_cast<float*>(ws + p->off_partial);
+  kp.flags = reinterpret_cast<uint32_t*>(ws + p->off_flags);
+  kp.status = reinterpret_cast<unsigned long long*>(ws + p->off_status);
+  kp.epoch = p->epoch;
+  // scaled GEMM: alpha * scale_a * scale_b folded into one fp32 factor; the
+  // mean over ranks weighs every rank's product and bias by 1/P (exact: P is a
+  // power of two)
+  const float w = p->reduce_op == DG_REDUCE_AVG ? 1.f / (float)p->tp : 1.f;
+  kp.alpha = p->alpha * p->scale_a * p->scale_b * w;
+  kp.bias_scale = w;
+  kp.beta = p->beta;
+  {
+    const int tm = p->cg == 2 ? dg::Cfg<2>::TILE_M : dg::Cfg<1>::TILE_M;
+    const uint32_t fa = p->esz == 1 ? (p->a_type == DG_TYPE_E5M2 ? 1u : 0u) : 1u;
+    const uint32_t fb = p->esz == 1 ? (p->b_type == DG_TYPE_E5M2 ? 1u : 0u) : 1u;
+    kp.idesc = dg::idesc_f32acc(tm, dg::TILE_N, fa, fb);
+  }
+  kp.n_maps = p->n_maps;
+  kp.l2_hint = p->l2_hint;
+  kp.done = reinterpret_cast<uint32_t*>(ws + p->off_done);
+  kp.S = reinterpret_cast<float*>(ws + p->off_send);
+  kp.R = reinterpret_cast<const float*>(ws + p->off_recv);
+  kp.wave_sync = wave_sync_on(p) ? 1u : 0u;
+  kp.wave_ctr = reinterpret_cast<uint32_t*>(ws + p->off_status + 64);
+  if (kp.wave_sync) DG_CUDA(cudaMemsetAsync(ws + p->off_status + 64, 0, 4, ms));
+  const bool pace = copy_pace_on(p) && is_ag(p->schedule) && p->tp > 2 && p->mode == DG_MODE_FUSED && cs != ms &&
+                    cs != nullptr;
+  kp.progress = pace ? reinterpret_cast<uint32_t*>(ws + p->off_status + kProgressOffset) : nullptr;
+  if (pace) DG_CUDA(cudaMemsetAsync(ws + p->off_status + kProgressOffset, 0, (size_t)p->tp * 4, ms));
+  kp.timeout_ns = (uint64_t)p->timeout_ms * 1000000ull;
+  kp.hang_ns = kp.timeout_ns * 4 + 1000000000ull;
+  kp.up_flags = nullptr;
+  kp.d_done = nullptr;
+  if (io) {
+    rc = ensure_io(p);
+    if (rc) return rc;
+    kp.up_flags = reinterpret_cast<const uint32_t*>(ws + p->off_status + kUpOffset);
+    kp.d_done = reinterpret_cast<uint32_t*>(ws + p->off_ddone);
+    DG_CUDA(cudaMemsetAsync(ws + p->off_ddone, 0, (size_t)(p->tp * p->tp) * 4, ms));
+    DG_CUDA(cudaEventRecord(p->ev_io, ms));
+    DG_CUDA(cudaStreamWaitEvent(p->up_st, p->ev_io, 0));
+    DG_CUDA(cudaStreamWaitEvent(p->down_st, p->ev_io, 0));
+    rc = enqueue_uploads(p, drv, *io, A, B, const_cast<dg_bf16_t*>(C), ws);
+    if (rc) return rc;
+  }
+  rc = dispatch_run(p, drv, A, B, C, D, ws, ms, cs, rs_serial, pace, io != nullptr);
+  if (io) {
+    const int rc_down = rc ? rc : enqueue_downloads(p, drv, *io, D, ws);
+    // Raise every count once the kernel is done (one that stopped early leaves
+    // blocks unfinished): no download wait outlives the kernel.  Then join.
+    DG_CUDA(cudaMemsetAsync(ws + p->off_ddone, 0x7F, (size_t)(p->tp * p->tp) * 4, ms));
+    DG_CUDA(cudaEventRecord(p->ev_down_done, p->down_st));
+    DG_CUDA(cudaStreamWaitEvent(ms, p->ev_up_done, 0));
+    DG_CUDA(cudaStreamWaitEvent(ms, p->ev_down_done, 0));
+    if (!rc) rc = rc_down;
+  }
+  return rc;
+}
+
+// The launch (and, for AG FUSED, the shard transfers around it) of one run
+// whose parameters are set.
+int dispatch_run(dg_plan_s* p, const Driver& drv, const void* A, const void* B, const dg_bf16_t* C, void* D,
+                 uint8_t* ws, cudaStream_t ms, cudaStream_t cs, bool rs_serial, bool pace, bool wait_up) {
+  int rc = DG_OK;
+  if (rs_serial) return run_rs_serial(p, drv, C, D, ws, ms);
+  if (!is_ag(p->schedule) && p->tp > 1 && p->cep) {
+    if (cs == ms || cs == nullptr)
+      return fail(DG_ERR_ARG, "copy-engine hand-off needs a copy stream distinct from the main stream");
+    return run_rs_ce(p, drv, ws, ms, cs);
+  }
+  if (is_ag(p->schedule) && p->tp > 1) {
+    int mode = p->mode;
+    if (mode == DG_MODE_FUSED && (cs == ms || cs == nullptr)) mode = DG_MODE_SERIAL;
+    if (mode == DG_MODE_FUSED) {
+      const int ns = p->copy_streams;
+      rc = ensure_extra_streams(p, ns - 1);
+      if (rc) return rc;
+      cudaStream_t streams[8];
+      streams[0] = cs;
+      for (int i = 1; i < ns; ++i) streams[i] = p->extra[i - 1];
+      DG_CUDA(cudaEventRecord(p->ev_fork, ms));
+      rc = launch(p, ms, 1);
+      if (rc) return rc;
+      for (int i = 0; i < ns; ++i) DG_CUDA(cudaStreamWaitEvent(streams[i], p->ev_fork, 0));
+      rc = enqueue_copies(p, drv, A, B, ws, streams, ns, pace, wait_up);
+      if (rc) return rc;
+      // Release every pacing wait still pending (a kernel that stopped early
+      // never reaches the later steps): no copy-stream wait outlives the kernel.
+      if (pace) DG_CUDA(cudaMemsetAsync(ws + p->off_status + kProgressOffset, 0x01, (size_t)p->tp * 4, ms));
+      for (int i = 1; i < ns; ++i) {
+        DG_CUDA(cudaEventRecord(p->extra_done[i - 1], streams[i]));
+        DG_CUDA(cudaStreamWaitEvent(cs, p->extra_done[i - 1], 0));
+      }
+      DG_CUDA(cudaEventRecord(p->ev_join, cs));
+      DG_CUDA(cudaStreamWaitEvent(ms, p->ev_join, 0));
+    } else if (mode == DG_MODE_SERIAL) {
+      rc = enqueue_copies(p, drv, A, B, ws, &ms, 1, false, wait_up);
+      if (rc) return rc;
+      rc = launch(p, ms, 1);
+      if (rc) return rc;
+    } else {
+      rc = launch(p, ms, 0);
+      if (rc) return rc;
+    }
+  } else {
+    rc = launch(p, ms, 0);
+    if (rc) return rc;
+  }
+  return DG_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -851,6 +1217,10 @@ int dg_set_option(dg_plan_t p, int option, int64_t value) {
         return fail(DG_ERR_ARG, "copy kind must be 0 (copy engine), 1 (1D memcpy) or 2 (copy engine, tall copies)");
       p->copy_kind = (int)value;
       return DG_OK;
+    case DG_OPT_HOST_OVERLAP:
+      if (value != 0 && value != 1) return fail(DG_ERR_ARG, "host overlap must be 0 or 1");
+      p->host_overlap = (int)value;
+      return DG_OK;
     case DG_OPT_COPY_PACE:
       if (value < -1 || value > 1) return fail(DG_ERR_ARG, "copy pacing must be -1 (auto), 0 or 1");
       p->copy_pace = (int)value;
@@ -938,149 +1308,7 @@ int dg_run(dg_plan_t p, const void* A, const void* B, const dg_bf16_t* C, dg_bf1
 
 int dg_run_ex(dg_plan_t p, const void* A, const void* B, const dg_bf16_t* C, const dg_bf16_t* bias, void* D,
               void* workspace, void* main_stream, void* copy_stream) {
-  NvtxRange range("dg_run");
-  if (!p) return fail(DG_ERR_ARG, "plan is NULL");
-  if (p->g.total_tiles == 0) return DG_OK;  // empty output
-  if (!A || !B || !D) return fail(DG_ERR_ARG, "A, B and D must be non-NULL");
-  if (p->beta != 0.f && !C) return fail(DG_ERR_ARG, "C is NULL but beta != 0");
-  auto misaligned = [](const void* q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) & (a - 1)) != 0; };
-  if (misaligned(A, 16) || misaligned(B, 16) || misaligned(D, 16) || (C && misaligned(C, 16)) ||
-      (bias && misaligned(bias, 16)))
-    return fail(DG_ERR_ARG, "A, B, C, D and bias must be 16-byte aligned");
-  // bytes this run uses (no side effect on the plan's SERIAL sizing record)
-  const size_t need =
-      (!is_ag(p->schedule) && p->mode == DG_MODE_SERIAL) ? p->ws_bytes_serial : p->ws_bytes_base;
-  if (need > 0 && (!workspace || misaligned(workspace, 256)))
-    return fail(DG_ERR_ARG, "workspace must be non-NULL and 256-byte aligned");
-  const bool rs_serial = !is_ag(p->schedule) && p->mode == DG_MODE_SERIAL;
-  if (rs_serial && !p->serial_ws)
-    return fail(DG_ERR_STATE, "RS SERIAL needs the larger workspace: size it with dg_workspace_bytes in SERIAL mode");
-  int rc = rt_init(p);
-  if (rc) return rc;
-  Driver drv;
-  rc = get_driver(&drv);
-  if (rc) return rc;
-  auto ms = static_cast<cudaStream_t>(main_stream);
-  auto cs = static_cast<cudaStream_t>(copy_stream);
-  auto* ws = static_cast<uint8_t*>(workspace);
-
-  // Epochs grow per plan across all of its workspaces, so flag words left in
-  // any workspace by this plan's earlier runs stay below the current epoch.
-  // A workspace new to this plan starts from zeroed flags.  Only when the
-  // epoch would overflow is it restarted, and then every other workspace of
-  // this plan is forgotten so that it is cleared again on its next use.
-  bool clear = false;
-  const bool wrap = (uint64_t)(p->epoch + 2) * (uint64_t)p->tp >= 0x7FFFFFFFull;
-  {
-    std::lock_guard<std::mutex> lk(g_ws_mu);
-    if (wrap)
-      for (auto it = g_ws_owner.begin(); it != g_ws_owner.end();)
-        it = it->second == p->id ? g_ws_owner.erase(it) : std::next(it);
-    auto it = g_ws_owner.find(workspace);
-    if (it == g_ws_owner.end() || it->second != p->id) {
-      g_ws_owner[workspace] = p->id;
-      clear = true;
-    }
-  }
-  // Under stream capture the run's epoch is frozen into the graph, so every
-  // replay must start from zeroed status and flag words: clear them in the
-  // graph itself (one memset node).
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  DG_CUDA(cudaStreamIsCapturing(ms, &cap));
-  if (cap == cudaStreamCaptureStatusActive) clear = true;
-  if (clear) DG_CUDA(cudaMemsetAsync(ws, 0, p->off_flags + (size_t)p->n_flags * 4, ms));
-  if (wrap) p->epoch = 0;
-  p->epoch += 1;
-
-  rc = build_maps(p, drv, A, B, ws);
-  if (rc) return rc;
-  rc = build_epi_maps(p, drv, C, D, ws);
-  if (rc) return rc;
-  dg::KParams& kp = p->kp;
-  kp.g = p->g;
-  kp.C = reinterpret_cast<const __nv_bfloat16*>(C);
-  kp.D = D;
-  kp.bias = reinterpret_cast<const __nv_bfloat16*>(bias);
-  kp.out_f32 = p->out_type == DG_TYPE_F32 ? 1u : 0u;
-  kp.out_fp8 = p->out_type == DG_TYPE_E4M3 ? 1u : p->out_type == DG_TYPE_E5M2 ? 2u : 0u;
-  kp.result_scale = p->result_scale;
-  kp.X = reinterpret_cast<float*>(ws + p->off_partial);
-  kp.flags = reinterpret_cast<uint32_t*>(ws + p->off_flags);
-  kp.status = reinterpret_cast<unsigned long long*>(ws + p->off_status);
-  kp.epoch = p->epoch;
-  // scaled GEMM: alpha * scale_a * scale_b folded into one fp32 factor; the
-  // mean over ranks weighs every rank's product and bias by 1/P (exact: P is a
-  // power of two)
-  const float w = p->reduce_op == DG_REDUCE_AVG ? 1.f / (float)p->tp : 1.f;
-  kp.alpha = p->alpha * p->scale_a * p->scale_b * w;
-  kp.bias_scale = w;
-  kp.beta = p->beta;
-  {
-    const int tm = p->cg == 2 ? dg::Cfg<2>::TILE_M : dg::Cfg<1>::TILE_M;
-    const uint32_t fa = p->esz == 1 ? (p->a_type == DG_TYPE_E5M2 ? 1u : 0u) : 1u;
-    const uint32_t fb = p->esz == 1 ? (p->b_type == DG_TYPE_E5M2 ? 1u : 0u) : 1u;
-    kp.idesc = dg::idesc_f32acc(tm, dg::TILE_N, fa, fb);
-  }
-  kp.n_maps = p->n_maps;
-  kp.l2_hint = p->l2_hint;
-  kp.done = reinterpret_cast<uint32_t*>(ws + p->off_done);
-  kp.S = reinterpret_cast<float*>(ws + p->off_send);
-  kp.R = reinterpret_cast<const float*>(ws + p->off_recv);
-  kp.wave_sync = wave_sync_on(p) ? 1u : 0u;
-  kp.wave_ctr = reinterpret_cast<uint32_t*>(ws + p->off_status + 64);
-  if (kp.wave_sync) DG_CUDA(cudaMemsetAsync(ws + p->off_status + 64, 0, 4, ms));
-  const bool pace = copy_pace_on(p) && is_ag(p->schedule) && p->tp > 2 && p->mode == DG_MODE_FUSED && cs != ms &&
-                    cs != nullptr;
-  kp.progress = pace ? reinterpret_cast<uint32_t*>(ws + p->off_status + kProgressOffset) : nullptr;
-  if (pace) DG_CUDA(cudaMemsetAsync(ws + p->off_status + kProgressOffset, 0, (size_t)p->tp * 4, ms));
-  kp.timeout_ns = (uint64_t)p->timeout_ms * 1000000ull;
-  kp.hang_ns = kp.timeout_ns * 4 + 1000000000ull;
-
-  if (rs_serial) return run_rs_serial(p, drv, C, D, ws, ms);
-  if (!is_ag(p->schedule) && p->tp > 1 && p->cep) {
-    if (cs == ms || cs == nullptr)
-      return fail(DG_ERR_ARG, "copy-engine hand-off needs a copy stream distinct from the main stream");
-    return run_rs_ce(p, drv, ws, ms, cs);
-  }
-  if (is_ag(p->schedule) && p->tp > 1) {
-    int mode = p->mode;
-    if (mode == DG_MODE_FUSED && (cs == ms || cs == nullptr)) mode = DG_MODE_SERIAL;
-    if (mode == DG_MODE_FUSED) {
-      const int ns = p->copy_streams;
-      rc = ensure_extra_streams(p, ns - 1);
-      if (rc) return rc;
-      cudaStream_t streams[8];
-      streams[0] = cs;
-      for (int i = 1; i < ns; ++i) streams[i] = p->extra[i - 1];
-      DG_CUDA(cudaEventRecord(p->ev_fork, ms));
-      rc = launch(p, ms, 1);
-      if (rc) return rc;
-      for (int i = 0; i < ns; ++i) DG_CUDA(cudaStreamWaitEvent(streams[i], p->ev_fork, 0));
-      rc = enqueue_copies(p, drv, A, B, ws, streams, ns, pace);
-      if (rc) return rc;
-      // Release every pacing wait still pending (a kernel that stopped early
-      // never reaches the later steps): no copy-stream wait outlives the kernel.
-      if (pace) DG_CUDA(cudaMemsetAsync(ws + p->off_status + kProgressOffset, 0x01, (size_t)p->tp * 4, ms));
-      for (int i = 1; i < ns; ++i) {
-        DG_CUDA(cudaEventRecord(p->extra_done[i - 1], streams[i]));
-        DG_CUDA(cudaStreamWaitEvent(cs, p->extra_done[i - 1], 0));
-      }
-      DG_CUDA(cudaEventRecord(p->ev_join, cs));
-      DG_CUDA(cudaStreamWaitEvent(ms, p->ev_join, 0));
-    } else if (mode == DG_MODE_SERIAL) {
-      rc = enqueue_copies(p, drv, A, B, ws, &ms, 1, false);
-      if (rc) return rc;
-      rc = launch(p, ms, 1);
-      if (rc) return rc;
-    } else {
-      rc = launch(p, ms, 0);
-      if (rc) return rc;
-    }
-  } else {
-    rc = launch(p, ms, 0);
-    if (rc) return rc;
-  }
-  return DG_OK;
+  return run_impl(p, A, B, C, bias, D, workspace, main_stream, copy_stream, nullptr);
 }
 
 int dg_run_host(dg_plan_t p, const void* A_host, const void* B_host, const dg_bf16_t* C_host, const dg_bf16_t* bias,
@@ -1097,7 +1325,14 @@ int dg_run_host(dg_plan_t p, const void* A_host, const void* B_host, const dg_bf
   const size_t c_bytes = (size_t)(p->l * p->m * p->n) * 2;
   const size_t d_elem = p->out_type == DG_TYPE_F32 ? 4 : (p->out_type == DG_TYPE_BF16 ? 2 : 1);
   const size_t d_bytes = (size_t)(p->l * p->m * p->n) * d_elem;
-  // host to device on the main stream (pinned host memory: copy engine, asynchronous)
+  const bool overlap = p->host_overlap && p->mode == DG_MODE_FUSED && pinned_host(A_host) && pinned_host(B_host) &&
+                       pinned_host(D_host) && (p->beta == 0.f || pinned_host(C_host));
+  if (overlap) {
+    const HostIO io{A_host, B_host, C_host, D_host};
+    return run_impl(p, A_dev, B_dev, p->beta != 0.f ? C_dev : nullptr, bias, D_dev, workspace, main_stream,
+                    copy_stream, &io);
+  }
+  // sequential: host to device on the main stream, the run, device to host
   DG_CUDA(cudaMemcpyAsync(A_dev, A_host, a_bytes, cudaMemcpyHostToDevice, ms));
   DG_CUDA(cudaMemcpyAsync(B_dev, B_host, b_bytes, cudaMemcpyHostToDevice, ms));
   if (p->beta != 0.f) DG_CUDA(cudaMemcpyAsync(C_dev, C_host, c_bytes, cudaMemcpyHostToDevice, ms));
@@ -1126,6 +1361,8 @@ int dg_check(dg_plan_t p, void* workspace, void* stream) {
   if ((uint32_t)(st >> 32) != p->epoch) return DG_OK;
   const uint32_t code = (uint32_t)(st >> 24) & 0xFF;
   const uint32_t info = (uint32_t)st & 0xFFFFFF;
+  if (code == dg::DEV_TIMEOUT && (info & 0xF00000u) == dg::UP_FLAG_INFO)
+    return fail(DG_ERR_TIMEOUT, "upload wait ran out (inputs of rank %u, run %u)", info & 0xFFu, p->epoch);
   if (code == dg::DEV_TIMEOUT)
     return fail(DG_ERR_TIMEOUT, "ready-flag wait ran out (flag %u, run %u)", info, p->epoch);
   if (code == dg::DEV_HANG)
@@ -1145,6 +1382,14 @@ void dg_destroy(dg_plan_t p) {
   for (int i = 0; i < p->n_extra; ++i) {
     cudaStreamDestroy(p->extra[i]);
     cudaEventDestroy(p->extra_done[i]);
+  }
+  if (p->io_rt) {
+    cudaStreamDestroy(p->up_st);
+    cudaStreamDestroy(p->down_st);
+    cudaEventDestroy(p->ev_io);
+    cudaEventDestroy(p->ev_up_done);
+    cudaEventDestroy(p->ev_down_done);
+    for (int i = 0; i < 8; ++i) cudaEventDestroy(p->ev_up[i]);
   }
   delete p;
 }

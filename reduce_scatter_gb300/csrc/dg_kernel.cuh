@@ -82,6 +82,7 @@ struct Cfg {
 
 // Device status word: (epoch << 32) | (code << 24) | (info & 0xffffff).
 constexpr uint32_t DEV_TIMEOUT = 1;  // a ready-flag wait ran out
+constexpr uint32_t UP_FLAG_INFO = 0x600000u;  // status info of an upload-flag wait: | rank
 constexpr uint32_t DEV_HANG = 2;     // a pipeline wait ran out
 
 struct KParams {
@@ -113,6 +114,12 @@ struct KParams {
   uint32_t wave_sync;   // producers start tile i only after every CTA issued tile i-1
   uint32_t* wave_ctr;   // per-run counter of tiles whose loads are issued (zeroed per run)
   uint32_t* progress;   // AG copy pacing: progress[s] set to 1 once a producer reaches step s, or null
+  // Runs that upload their inputs and download D themselves (host buffers):
+  // rank r's operands and C are on the device once up_flags[r] >= epoch, and
+  // d_done[s * P + r] counts the half tiles of D finished for step s, rank r.
+  // Both null otherwise.
+  const uint32_t* up_flags;
+  uint32_t* d_done;
   float alpha, beta;
   float bias_scale;  // weight of the bias in every epilogue pass (1, or 1/P for the mean)
   uint32_t out_f32;  // D is fp32
@@ -810,6 +817,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
       bool ok = true;
       uint32_t wave = 0;
       int32_t step_seen = -1;
+      uint32_t up_ok = 0;  // ranks whose uploaded inputs this producer has seen
       for (int64_t t = unit; t < T && ok; t += nunits, ++wave) {
         const Tile tl = decode_tile(p.g, t);
         if (p.progress && tl.s != step_seen) {
@@ -827,6 +835,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
             if (globaltimer() - t0 > p.timeout_ns) break;
             __nanosleep(64);
           }
+        }
+        if (p.up_flags && !((up_ok >> tl.r) & 1u)) {
+          // this rank's operands have been uploaded from the host
+          wait_flag_geq(p, p.up_flags + tl.r, p.epoch, UP_FLAG_INFO | (uint32_t)tl.r);
+          fence_proxy_async_global();
+          up_ok |= 1u << tl.r;
         }
         if (tl.flag >= 0 && p.wait_flags) {
           wait_flag_geq(p, p.flags + tl.flag, p.epoch, (uint32_t)tl.flag);
@@ -968,6 +982,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
     uint32_t pend_val = 0;
     uint32_t nload = 0;   // staged source chunks loaded so far (buffer idx & 1)
     uint32_t nstore = 0;  // staged destination chunks stored so far (buffer idx & 1)
+    uint32_t up_ok = 0;   // ranks whose uploaded C this thread has seen (thread 0)
     uint32_t it = 0;
     for (int64_t t = unit; t < T; t += nunits, ++it) {
       const Tile tl = decode_tile(p.g, t);
@@ -1016,6 +1031,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
         if (need_flag) {
           // partial of this half tile from the previous step
           wait_flag_geq(p, p.flags + tflag, want, (uint32_t)tflag);
+        }
+        if (p.up_flags && tl.src == SRC_C && !((up_ok >> tl.r) & 1u)) {
+          // C of this rank's tiles has been uploaded from the host (the other
+          // threads read it after the barrier below)
+          wait_flag_geq(p, p.up_flags + tl.r, p.epoch, UP_FLAG_INFO | (uint32_t)tl.r);
+          fence_proxy_async_global();
+          up_ok |= 1u << tl.r;
         }
         if (has_src) {
           // the source needs only the previous step: load it while the MMAs run
@@ -1114,6 +1136,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           staged_load_src(p, tl, row0, c + 2, nload + c + 2, xsrc_addr, bar_xfull, src_map, src_col0, src_row0);
       }
       if (has_src) nload += (uint32_t)nch;
+      if (p.d_done && tl.dst == DST_D) {
+        // count this half tile of D as finished: its bulk and plain stores
+        // complete and fenced first (the device-to-host stream waits on it)
+        if (EPI == 1 && et == 0) bulk_wait<0>();
+        __threadfence();
+        named_bar_sync(1, EPI_THREADS);
+        if (et == 0) {
+          if (EPI == 1) fence_proxy_async_global();
+          __threadfence();
+          atomicAdd(p.d_done + (int64_t)tl.s * p.g.P + tl.r, 1u);
+        }
+      }
       if (cep && tl.dst == DST_X) {
         // count this half tile as written to the send buffer: its bulk and
         // plain stores complete and fenced first (the copy stream waits on it)

@@ -66,6 +66,7 @@ OPT_OUT_TYPE = 11
 OPT_REDUCE_OP = 12
 OPT_COPY_PACE = 13
 OPT_COPY_KIND = 14
+OPT_HOST_OVERLAP = 15
 
 # Every symbol include/dg.h declares.
 EXPORTS = ("dg_plan", "dg_workspace_bytes", "dg_run_mode", "dg_set_option", "dg_run", "dg_check",

@@ -313,6 +313,15 @@ def test_copy_kind_option_rules(L):
             p.set_option(dg.OPT_COPY_KIND, v)
 
 
+def test_host_overlap_option_rules(L):
+    p = dg.Plan(512, 512, 512, 1, 4, dg.AG_ROTATING_A)
+    for v in (0, 1):
+        p.set_option(dg.OPT_HOST_OVERLAP, v)
+    for v in (-1, 2):
+        with pytest.raises(dg.DGError):
+            p.set_option(dg.OPT_HOST_OVERLAP, v)
+
+
 def test_run_host_argument_checks_without_gpu(L):
     p = dg.Plan(256, 256, 256, 1, 2, dg.AG_ROTATING_A, 1.0, 0.5)
     # missing host or device buffers, C missing with beta != 0: refused before any CUDA call
