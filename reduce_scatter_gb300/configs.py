@@ -84,6 +84,9 @@ WORKLOADS = {
         Workload("ag_a_tp8_pr_e4m3", 0, 8, 16384, 106496, 16384, dist_a=N1, dist_b=N1, in_type="e4m3",
                  scale_b=0.02),
         Workload("rs_a_tp8_e4m3", 2, 8, 16384, 8192, 28672, dist_a=N1, dist_b=N1, in_type="e4m3", scale_b=0.02),
+        # ag_a_tp8_pr_small in e4m3 (about 1.3 GB on the device), for full profiler captures
+        Workload("ag_a_tp8_pr_small_e4m3", 0, 8, 8192, 13312, 16384, dist_a=N1, dist_b=N1, in_type="e4m3",
+                 scale_b=0.02),
         # a quarter of rs_b_tp4_batched's N and one batch: small enough (about 1 GB on the
         # device) for a full profiler capture, same per-tile work
         Workload("rs_b_tp4_quarter", 3, 4, 8192, 13312, 8192, l=1, alpha=0.5, beta=1.0, dist_a=N1,
