@@ -174,11 +174,17 @@ enum dg_option {
                                  so the row width is free), which a copy engine moves at
                                  ~1.8-2.1 TB/s alone on GB300, at the price of more HBM
                                  bandwidth taken from a GEMM running beside them */
-  DG_OPT_HOST_OVERLAP = 15    /* dg_run_host in FUSED mode with pinned host buffers: 1 (default) =
+  DG_OPT_HOST_OVERLAP = 15,   /* dg_run_host in FUSED mode with pinned host buffers: 1 (default) =
                                  launch the kernel at once and overlap the transfers with it
                                  (rank r's tiles wait for rank r's uploaded inputs; each
                                  finished (step, rank) block of D is downloaded while later
                                  steps run); 0 = upload everything, run, then download */
+  DG_OPT_TILE_ORDER = 16      /* order of the (rank, step) blocks of tiles: 0 = step-major (every
+                                 rank's step s before any step s + 1); 1 = upload frontier, AG
+                                 plans only: blocks (rank r, shard j) in groups g = max(r, j),
+                                 so group g needs the inputs of ranks 0..g alone (copy pacing
+                                 off); -1 (default) = 1 for AG runs of dg_run_host that overlap
+                                 their uploads, else 0.  Results are bit-identical either way */
 };
 
 /* Plan geometry and workspace layout, for callers and tests. */

@@ -28,6 +28,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 #include <thread>
 #include <unordered_map>
 
@@ -153,6 +154,7 @@ struct dg_plan_s {
   int copy_kind = 0;   // DG_OPT_COPY_KIND: 0 copy engine (2D copies in the operand's rows), 1
                        // one-dimensional cudaMemcpyAsync, 2 copy engine (tall 2D copies)
   int host_overlap = 1;  // DG_OPT_HOST_OVERLAP: dg_run_host overlaps its transfers with the kernel
+  int tile_order = -1;   // DG_OPT_TILE_ORDER: -1 auto, 0 step-major, 1 upload frontier (AG)
   uint64_t id = 0;
   uint32_t epoch = 0;
   bool serial_ws = false;
@@ -204,6 +206,7 @@ int layout(dg_plan_s* p) {
   g.BK = dg::KROW_BYTES / p->esz;  // 64 bf16 or 128 fp8 elements: 128 bytes per row
   g.group_m = 16;
   g.beta_nonzero = p->beta != 0.f;
+  g.order = p->tile_order == 1 ? 1 : 0;
   switch (p->schedule) {
     case DG_AG_ROTATING_A:
       g.blk_m = p->m / P, g.blk_n = p->n / P, g.shard = p->m / P, g.Ks = p->k;
@@ -527,6 +530,29 @@ int ensure_extra_streams(dg_plan_s* p, int want) {
   return DG_OK;
 }
 
+// The (step, rank) blocks of steps >= first_step in the order the kernel's
+// tiles visit them: step-major, or for the upload-frontier order by groups of
+// max(rank, shard).
+struct Block {
+  int64_t s, r;
+};
+std::vector<Block> consumption_order(const dg::Geom& g, int64_t first_step) {
+  std::vector<Block> out;
+  const int64_t P = g.P;
+  if (g.order == 1) {
+    for (int64_t b = 0; b < P * P; ++b) {
+      int64_t r = 0, j = 0;
+      dg::frontier_block(b, &r, &j);
+      const int64_t s = (j - r + P) % P;
+      if (s >= first_step) out.push_back({s, r});
+    }
+  } else {
+    for (int64_t s = first_step; s < P; ++s)
+      for (int64_t r = 0; r < P; ++r) out.push_back({s, r});
+  }
+  return out;
+}
+
 // Shard transfers of every rank and step >= 1, each chunk followed by its
 // ready-flag write on the same stream, in the order the kernel consumes them.
 // Chunks are dealt round-robin over `ns` streams.  With `wait_up` (inputs
@@ -551,8 +577,10 @@ int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B
   auto* flags = reinterpret_cast<uint32_t*>(ws + p->off_flags);
   uint32_t up_waited[8] = {};  // per stream: ranks whose upload it already waits for
   int64_t idx = 0;
-  for (int64_t s = 1; s < P; ++s) {
-    if (pace && s >= 2)
+  int64_t last_s = 0;
+  for (const Block& bk : consumption_order(p->kp.g, 1)) {
+    const int64_t s = bk.s, r = bk.r;
+    if (pace && s >= 2 && s != last_s)
       // step s's shards move while the kernel computes step s - 1
       for (int i = 0; i < ns; ++i) {
         CUresult rc = drv.wait32((CUstream)streams[i], (CUdeviceptr)(progress + (s - 1)), 1u,
@@ -561,30 +589,29 @@ int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B
           return fail(rc == CUDA_ERROR_NOT_SUPPORTED ? DG_ERR_UNSUPPORTED : DG_ERR_CUDA,
                       "cuStreamWaitValue32 failed (%d)", (int)rc);
       }
-    for (int64_t r = 0; r < P; ++r) {
-      const int64_t j = (r + s) % P;
-      for (int64_t l = 0; l < g.L; ++l) {
-        const int64_t slot = (r * (P - 1) + (s - 1)) * g.L + l;
-        for (int64_t c = 0; c < g.nchunks; ++c, ++idx) {
-          cudaStream_t st = streams[idx % ns];
-          if (wait_up && !((up_waited[idx % ns] >> j) & 1u)) {
-            DG_CUDA(cudaStreamWaitEvent(st, p->ev_up[j], 0));
-            up_waited[idx % ns] |= 1u << j;
-          }
-          const int64_t row0 = c * chunk_rows;
-          const int64_t rows = std::min(chunk_rows, g.shard - row0);
-          if (rows > 0) {
-            const uint8_t* src = home + (l * outer + j * g.shard + row0) * row_bytes;
-            uint8_t* dst = slots + (slot * g.shard + row0) * row_bytes;
-            DG_CUDA(ce_copy(dst, src, (size_t)row_bytes, (size_t)rows, st, p->copy_kind));
-          }
-          if (idx != p->fault_skip) {
-            CUresult rc = drv.write32((CUstream)st, (CUdeviceptr)(flags + slot * g.nchunks + c),
-                                      p->epoch, 0);
-            if (rc != CUDA_SUCCESS)
-              return fail(rc == CUDA_ERROR_NOT_SUPPORTED ? DG_ERR_UNSUPPORTED : DG_ERR_CUDA,
-                          "cuStreamWriteValue32 failed (%d)", (int)rc);
-          }
+    last_s = s;
+    const int64_t j = (r + s) % P;
+    for (int64_t l = 0; l < g.L; ++l) {
+      const int64_t slot = (r * (P - 1) + (s - 1)) * g.L + l;
+      for (int64_t c = 0; c < g.nchunks; ++c, ++idx) {
+        cudaStream_t st = streams[idx % ns];
+        if (wait_up && !((up_waited[idx % ns] >> j) & 1u)) {
+          DG_CUDA(cudaStreamWaitEvent(st, p->ev_up[j], 0));
+          up_waited[idx % ns] |= 1u << j;
+        }
+        const int64_t row0 = c * chunk_rows;
+        const int64_t rows = std::min(chunk_rows, g.shard - row0);
+        if (rows > 0) {
+          const uint8_t* src = home + (l * outer + j * g.shard + row0) * row_bytes;
+          uint8_t* dst = slots + (slot * g.shard + row0) * row_bytes;
+          DG_CUDA(ce_copy(dst, src, (size_t)row_bytes, (size_t)rows, st, p->copy_kind));
+        }
+        if (idx != p->fault_skip) {
+          CUresult rc = drv.write32((CUstream)st, (CUdeviceptr)(flags + slot * g.nchunks + c),
+                                    p->epoch, 0);
+          if (rc != CUDA_SUCCESS)
+            return fail(rc == CUDA_ERROR_NOT_SUPPORTED ? DG_ERR_UNSUPPORTED : DG_ERR_CUDA,
+                        "cuStreamWriteValue32 failed (%d)", (int)rc);
         }
       }
     }
@@ -881,8 +908,8 @@ int enqueue_downloads(dg_plan_s* p, const Driver& drv, const HostIO& io, const v
   auto* d_h = static_cast<uint8_t*>(io.D);
   const auto D2H = cudaMemcpyDeviceToHost;
   const bool ag = is_ag(p->schedule);
-  for (int64_t s = ag ? 0 : P - 1; s < P; ++s)
-    for (int64_t r = 0; r < P; ++r) {
+  for (const Block& bk : consumption_order(p->kp.g, ag ? 0 : P - 1)) {
+      const int64_t s = bk.s, r = bk.r;
       CUresult cr = drv.wait32((CUstream)p->down_st, (CUdeviceptr)(done + s * P + r), target,
                                CU_STREAM_WAIT_VALUE_GEQ);
       if (cr != CUDA_SUCCESS)
@@ -983,6 +1010,9 @@ int run_impl(dg_plan_s* p, const void* A, const void* B, const dg_bf16_t* C, con
   if (rc) return rc;
   dg::KParams& kp = p->kp;
   kp.g = p->g;
+  // Upload-frontier block order (AG): asked for, or automatic when this run
+  // uploads its inputs rank by rank.
+  kp.g.order = is_ag(p->schedule) && (p->tile_order == 1 || (p->tile_order < 0 && io)) ? 1 : 0;
   kp.C = reinterpret_cast<const __nv_bfloat16*>(C);
   kp.D = D;
   kp.bias = reinterpret_cast<const __nv_bfloat16*>(bias);
@@ -1014,7 +1044,7 @@ int run_impl(dg_plan_s* p, const void* A, const void* B, const dg_bf16_t* C, con
   kp.wave_sync = wave_sync_on(p) ? 1u : 0u;
   kp.wave_ctr = reinterpret_cast<uint32_t*>(ws + p->off_status + 64);
   if (kp.wave_sync) DG_CUDA(cudaMemsetAsync(ws + p->off_status + 64, 0, 4, ms));
-  const bool pace = copy_pace_on(p) && is_ag(p->schedule) && p->tp > 2 && p->mode == DG_MODE_FUSED && cs != ms &&
+  const bool pace = copy_pace_on(p) && kp.g.order == 0 && is_ag(p->schedule) && p->tp > 2 && p->mode == DG_MODE_FUSED && cs != ms &&
                     cs != nullptr;
   kp.progress = pace ? reinterpret_cast<uint32_t*>(ws + p->off_status + kProgressOffset) : nullptr;
   if (pace) DG_CUDA(cudaMemsetAsync(ws + p->off_status + kProgressOffset, 0, (size_t)p->tp * 4, ms));
@@ -1216,6 +1246,13 @@ int dg_set_option(dg_plan_t p, int option, int64_t value) {
       if (value < 0 || value > 2)
         return fail(DG_ERR_ARG, "copy kind must be 0 (copy engine), 1 (1D memcpy) or 2 (copy engine, tall copies)");
       p->copy_kind = (int)value;
+      return DG_OK;
+    case DG_OPT_TILE_ORDER:
+      if (value < -1 || value > 1) return fail(DG_ERR_ARG, "tile order must be -1 (auto), 0 or 1");
+      if (value == 1 && !is_ag(p->schedule))
+        return fail(DG_ERR_UNSUPPORTED, "the upload-frontier order is for the AllGather schedules");
+      p->tile_order = (int)value;
+      layout(p);
       return DG_OK;
     case DG_OPT_HOST_OVERLAP:
       if (value != 0 && value != 1) return fail(DG_ERR_ARG, "host overlap must be 0 or 1");

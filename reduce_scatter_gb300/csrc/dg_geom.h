@@ -12,6 +12,13 @@
 // then in groups of GROUP_M tile rows swept column by column, so that the
 // CTAs in flight share A rows and B columns in L2.
 //
+// A second order for the AllGather schedules (Geom::order = 1, "upload
+// frontier"), used when the inputs are still arriving from the host rank by
+// rank: the (rank r, shard j) blocks go in groups g = max(r, j) = 0..P-1, so a
+// group needs nothing beyond the first g + 1 ranks' inputs.  Inside group g:
+// (g, g) (step 0, no transfer), then (g, j < g), then (r < g, g).  The step of
+// a block is s = (j - r) mod P.
+//
 // Which shard/slab a rank handles at a step (the rotation) follows
 // _pipelined_all_gather_and_consume (AG: j = (r + s) mod P, local shard first)
 // and _pipelined_produce_and_all2all (RS: j = (r + s + 1) mod P, own slab last)
@@ -52,6 +59,7 @@ struct Geom {
   int64_t nchunks;          // AG: chunks per shard
   int32_t beta_nonzero;
   int32_t ce_partials;  // RS: partials handed on by copy-engine transfers between rank buffers
+  int32_t order;        // AG block order: 0 step-major, 1 upload frontier
 };
 
 struct Tile {
@@ -74,14 +82,37 @@ struct Tile {
 DG_HD int64_t dg_min64(int64_t a, int64_t b) { return a < b ? a : b; }
 DG_HD int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Block b (0 <= b < P * P) of the upload-frontier order: its rank r and shard j.
+DG_HD void frontier_block(int64_t b, int64_t* r, int64_t* j) {
+  int64_t g = 0;
+  while ((g + 1) * (g + 1) <= b) ++g;  // groups 0..g-1 hold g * g blocks
+  const int64_t i = b - g * g;          // 0 .. 2g
+  if (i == 0) {
+    *r = g, *j = g;
+  } else if (i <= g) {
+    *r = g, *j = i - 1;
+  } else {
+    *r = i - g - 1, *j = g;
+  }
+}
+
 DG_HD Tile decode_tile(const Geom& g, int64_t t) {
   Tile o;
   const int64_t P = g.P;
-  const int64_t per_step = P * g.tiles_block;
-  const int64_t s = t / per_step;
-  const int64_t rem = t - s * per_step;
-  const int64_t r = rem / g.tiles_block;
-  const int64_t u = rem - r * g.tiles_block;
+  int64_t s, r, u;
+  if (g.order == 1) {
+    const int64_t b = t / g.tiles_block;
+    u = t - b * g.tiles_block;
+    int64_t jb;
+    frontier_block(b, &r, &jb);
+    s = (jb - r + P) % P;
+  } else {
+    const int64_t per_step = P * g.tiles_block;
+    s = t / per_step;
+    const int64_t rem = t - s * per_step;
+    r = rem / g.tiles_block;
+    u = rem - r * g.tiles_block;
+  }
   const int64_t per_batch = g.tiles_m * g.tiles_n;
   const int64_t l = u / per_batch;
   const int64_t v = u - l * per_batch;

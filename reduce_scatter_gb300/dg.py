@@ -67,6 +67,7 @@ OPT_REDUCE_OP = 12
 OPT_COPY_PACE = 13
 OPT_COPY_KIND = 14
 OPT_HOST_OVERLAP = 15
+OPT_TILE_ORDER = 16
 
 # Every symbol include/dg.h declares.
 EXPORTS = ("dg_plan", "dg_workspace_bytes", "dg_run_mode", "dg_set_option", "dg_run", "dg_check",

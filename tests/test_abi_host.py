@@ -313,6 +313,47 @@ def test_copy_kind_option_rules(L):
             p.set_option(dg.OPT_COPY_KIND, v)
 
 
+@pytest.mark.parametrize("tp", [1, 2, 4, 8])
+@pytest.mark.parametrize("sched", [dg.AG_ROTATING_A, dg.AG_ROTATING_B], ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_upload_frontier_order_is_a_permutation_by_groups(L, sched, tp):
+    # the same tiles as the step-major order, visited by (rank, shard) blocks in
+    # groups g = max(r, j) that never go back, each group touching ranks 0..g only
+    m, n, k, l = 1024, 1536, 256, 2
+    ref = dg.Plan(m, n, k, l, tp, sched)
+    fr = dg.Plan(m, n, k, l, tp, sched)
+    fr.set_option(dg.OPT_TILE_ORDER, 1)
+    T = ref.info()["total_tiles"]
+    assert fr.info()["total_tiles"] == T
+    key = lambda d: (d["step"], d["rank"], d["batch"], d["out_row"], d["out_col"], d["a_map"], d["a_row"],
+                     d["b_map"], d["b_row"], d["flag"])  # noqa: E731
+    a = sorted(key(ref.tile(t)) for t in range(T))
+    tiles = [fr.tile(t) for t in range(T)]
+    assert sorted(key(d) for d in tiles) == a
+    groups = [max(d["rank"], d["slab"]) for d in tiles]
+    assert groups == sorted(groups)
+    per_block = T // (tp * tp)
+    for t in range(0, T, per_block):
+        blk = {(d["step"], d["rank"]) for d in tiles[t:t + per_block]}
+        assert len(blk) == 1  # a block's tiles stay together
+    for d in tiles:
+        assert d["slab"] == (d["rank"] + d["step"]) % tp
+    # group 0 is rank 0's step 0, its own inputs only
+    assert (tiles[0]["rank"], tiles[0]["step"]) == (0, 0)
+
+
+def test_tile_order_option_rules(L):
+    p = dg.Plan(512, 512, 512, 1, 4, dg.AG_ROTATING_B)
+    for v in (-1, 0, 1):
+        p.set_option(dg.OPT_TILE_ORDER, v)
+    for v in (-2, 2):
+        with pytest.raises(dg.DGError):
+            p.set_option(dg.OPT_TILE_ORDER, v)
+    q = dg.Plan(512, 512, 512, 1, 4, dg.RS_TILING_A_ROTATING_C)
+    q.set_option(dg.OPT_TILE_ORDER, 0)
+    with pytest.raises(dg.DGError):
+        q.set_option(dg.OPT_TILE_ORDER, 1)
+
+
 def test_host_overlap_option_rules(L):
     p = dg.Plan(512, 512, 512, 1, 4, dg.AG_ROTATING_A)
     for v in (0, 1):

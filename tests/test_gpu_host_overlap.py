@@ -167,3 +167,24 @@ def test_back_to_back_calls_reuse_buffers():
     for (a, b), D_h in zip(ins, outs):
         want, _ = Runner(m, n, k, l, tp, dg.AG_ROTATING_A, 1.0, 0.0).run(to_dev(a), to_dev(b), None)
         assert torch.equal(D_h, want.view(torch.int16).cpu())
+
+
+@pytest.mark.parametrize("cg", [1, 2])
+@pytest.mark.parametrize("tp", [2, 4, 8])
+@pytest.mark.parametrize("sched", [dg.AG_ROTATING_A, dg.AG_ROTATING_B], ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_upload_frontier_order_on_device_runs(sched, tp, cg):
+    # the block order of the upload frontier, asked for on a device-buffer run,
+    # with late transfers over NaN-filled receive slots: the same bits
+    m, n, k, l = 1024, 1536, 512, 2
+    a, b, c = host_inputs(m, n, k, l, seed=380 + 10 * sched + tp)
+    A, B, C = to_dev(a), to_dev(b), to_dev(c)
+    ref, _ = Runner(m, n, k, l, tp, sched, 0.5, 1.0, options={dg.OPT_CTA_GROUP: cg}).run(A, B, C)
+    r = Runner(m, n, k, l, tp, sched, 0.5, 1.0,
+               options={dg.OPT_CTA_GROUP: cg, dg.OPT_TILE_ORDER: 1, dg.OPT_FAULT_DELAY_MS: 20,
+                        dg.OPT_TIMEOUT_MS: 5000})
+    info = r.plan.info()
+    r.ws[info["off_slots"]:info["off_slots"] + info["slot_bytes"] * tp * (tp - 1) * l].view(torch.int16).fill_(0x7FC0)
+    for _ in range(2):
+        D, rc = r.run(A, B, C)
+        assert rc == dg.OK
+        assert torch.equal(D.view(torch.int16), ref.view(torch.int16))
