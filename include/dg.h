@@ -295,11 +295,14 @@ int dg_run_ex(dg_plan_t plan, const void* A, const void* B, const dg_bf16_t* C, 
  *
  * In FUSED mode with every host buffer page-locked (cudaHostAlloc or
  * cudaHostRegister) and DG_OPT_HOST_OVERLAP on (the default), the transfers
- * overlap the kernel: it is launched at once; plan-owned streams upload each
- * rank's inputs in the kernel's order (rank r: its home shards of A and B and
- * the part of C its tiles read), and the tiles of rank r wait (bounded, like
- * the shard flags) for rank r's upload; each (step, rank) block of D is copied
- * back as soon as the kernel has finished it.  Otherwise (another mode,
+ * overlap the kernel: it is launched at once; plan-owned streams upload the
+ * inputs in P units in the kernel's order (AG: rank r's home shards of A and
+ * B and the part of C its tiles read; RS: the operand every tile reads whole,
+ * then row slabs of the other operand and of C in the order the steps need
+ * them), and each tile waits (bounded, like the shard flags) for the unit
+ * holding its inputs; AG runs also take their blocks in the upload-frontier
+ * order (DG_OPT_TILE_ORDER); each (step, rank) block of D is copied back as
+ * soon as the kernel has finished it.  Otherwise (another mode,
  * pageable memory, or the option off) the call uploads everything on
  * main_stream, runs, then downloads: pageable memory works with
  * host-synchronous copies.  Either way the call is one operation on

@@ -782,13 +782,14 @@ int run_rs_serial(dg_plan_s* p, const Driver& drv, const void* C, void* D, uint8
 //
 // dg_run_host with DG_OPT_HOST_OVERLAP (default) in FUSED mode, with pinned
 // host buffers: the kernel is launched at once and its tiles wait for their
-// rank's inputs instead of for the whole upload, and D leaves the device one
+// own inputs instead of for the whole upload, and D leaves the device one
 // (step, rank) block at a time while later steps still run.
-//   upload stream:   for r = 0..P-1 in the kernel's order: rank r's home
-//                    operand shards and the part of C its tiles read, then
-//                    up_flags[r] = epoch (the producers and C-reading
-//                    epilogues of rank r's tiles wait on it) and an event (the
-//                    shard transfers of rank r's home shard wait on it)
+//   upload stream:   for f = 0..P-1: upload unit f (AG: rank f's home operand
+//                    shards and the part of C its tiles read; RS: row slabs,
+//                    see upload_unit), then up_flags[f] = epoch (the
+//                    producers and C-reading epilogues of the tiles that need
+//                    unit f wait on it) and an event (AG shard transfers of
+//                    rank f's home shard wait on it)
 //   download stream: for every (step, rank) block that writes D, wait until
 //                    the kernel has counted all its half tiles, then copy the
 //                    block to the host
@@ -822,14 +823,18 @@ int copy_rows(void* dst, const void* src, size_t pitch, size_t width, size_t row
   return DG_OK;
 }
 
-// Host-to-device copies of rank r's inputs:
-//   AG-RotatingA   A rows M_r, B rows N_r, C[:, N_r]
-//   AG-RotatingB   A rows M_r, B rows N_r, C[M_r, :]
-//   RS-TilingA     A[:, K_r], B[:, K_r], C[M_j, :] with j = (r + 1) mod P
-//   RS-TilingB     A[:, K_r], B[:, K_r], C[:, N_j] with j = (r + 1) mod P
-// (every batch l; C only when beta != 0).  In the RS schedules rank r reads
-// user C only at step 0, for slab (r + 1) mod P.
-int upload_rank(dg_plan_s* p, const HostIO& io, const void* A, const void* B, void* C, int64_t r,
+// Host-to-device copies of upload unit f, the inputs the tiles waiting on
+// flag f need:
+//   AG-RotatingA   rank f: A rows M_f, B rows N_f, C[:, N_f]
+//   AG-RotatingB   rank f: A rows M_f, B rows N_f, C[M_f, :]
+//   RS-TilingA     B whole (unit 0 only), then A rows M_j and C rows M_j
+//   RS-TilingB     A and C whole (unit 0 only), then B rows N_j
+// with j = (f + 1) mod P, every batch l, C only when beta != 0.  An RS tile
+// (s, r) works on slab (r + s + 1) mod P for every step, so it waits on unit
+// (r + s) mod P.  Every RS copy is contiguous in host memory: row slabs
+// rather than each rank's K columns, and TilingB's C (whose slabs are column
+// blocks) whole; strided host copies ran at a fraction of the link's rate.
+int upload_unit(dg_plan_s* p, const HostIO& io, const void* A, const void* B, void* C, int64_t f,
                 cudaStream_t st) {
   const dg::Geom& g = p->g;
   const int64_t L = g.L, M = p->m, N = p->n, K = p->k, P = p->tp;
@@ -845,38 +850,43 @@ int upload_rank(dg_plan_s* p, const HostIO& io, const void* A, const void* B, vo
   int rc = DG_OK;
   if (is_ag(p->schedule)) {
     for (int64_t l = 0; l < L && !rc; ++l) {
-      const size_t a0 = (size_t)(l * M + r * g.blk_m) * rowA, b0 = (size_t)(l * N + r * g.blk_n) * rowA;
+      const size_t a0 = (size_t)(l * M + f * g.blk_m) * rowA, b0 = (size_t)(l * N + f * g.blk_n) * rowA;
       rc = copy_rows(a_d + a0, a_h + a0, rowA, rowA, (size_t)g.blk_m, H2D, st);
       if (!rc) rc = copy_rows(b_d + b0, b_h + b0, rowA, rowA, (size_t)g.blk_n, H2D, st);
     }
     if (rc || !with_c) return rc;
     if (p->schedule == DG_AG_ROTATING_A) {
-      const size_t c0 = (size_t)(r * g.blk_n) * 2;
+      const size_t c0 = (size_t)(f * g.blk_n) * 2;
       return copy_rows(c_d + c0, c_h + c0, rowC, (size_t)g.blk_n * 2, (size_t)(L * M), H2D, st);
     }
     for (int64_t l = 0; l < L && !rc; ++l) {
-      const size_t c0 = (size_t)(l * M + r * g.blk_m) * rowC;
+      const size_t c0 = (size_t)(l * M + f * g.blk_m) * rowC;
       rc = copy_rows(c_d + c0, c_h + c0, rowC, rowC, (size_t)g.blk_m, H2D, st);
     }
     return rc;
   }
-  const size_t k0 = (size_t)(r * g.Ks) * es, kw = (size_t)g.Ks * es;
-  rc = copy_rows(a_d + k0, a_h + k0, rowA, kw, (size_t)(L * M), H2D, st);
-  if (!rc) rc = copy_rows(b_d + k0, b_h + k0, rowA, kw, (size_t)(L * N), H2D, st);
-  if (rc || !with_c) return rc;
-  const int64_t j = (r + 1) % P;
-  if (p->schedule == DG_RS_TILING_A_ROTATING_C) {
-    for (int64_t l = 0; l < L && !rc; ++l) {
-      const size_t c0 = (size_t)(l * M + j * g.blk_m) * rowC;
-      rc = copy_rows(c_d + c0, c_h + c0, rowC, rowC, (size_t)g.blk_m, H2D, st);
-    }
-    return rc;
+  const bool rs_a = p->schedule == DG_RS_TILING_A_ROTATING_C;
+  const int64_t j = (f + 1) % P;
+  if (f == 0) {  // the operand every tile reads whole (and TilingB's C)
+    rc = rs_a ? copy_rows(b_d, b_h, rowA, rowA, (size_t)(L * N), H2D, st)
+              : copy_rows(a_d, a_h, rowA, rowA, (size_t)(L * M), H2D, st);
+    if (!rc && !rs_a && with_c) rc = copy_rows(c_d, c_h, rowC, rowC, (size_t)(L * M), H2D, st);
+    if (rc) return rc;
   }
-  const size_t c0 = (size_t)(j * g.blk_n) * 2;
-  return copy_rows(c_d + c0, c_h + c0, rowC, (size_t)g.blk_n * 2, (size_t)(L * M), H2D, st);
+  for (int64_t l = 0; l < L && !rc; ++l) {
+    const size_t o = rs_a ? (size_t)(l * M + j * g.blk_m) * rowA : (size_t)(l * N + j * g.blk_n) * rowA;
+    rc = rs_a ? copy_rows(a_d + o, a_h + o, rowA, rowA, (size_t)g.blk_m, H2D, st)
+              : copy_rows(b_d + o, b_h + o, rowA, rowA, (size_t)g.blk_n, H2D, st);
+  }
+  if (rc || !with_c || !rs_a) return rc;
+  for (int64_t l = 0; l < L && !rc; ++l) {
+    const size_t c0 = (size_t)(l * M + j * g.blk_m) * rowC;
+    rc = copy_rows(c_d + c0, c_h + c0, rowC, rowC, (size_t)g.blk_m, H2D, st);
+  }
+  return rc;
 }
 
-// Uploads of every rank on the upload stream, after everything already on the
+// Uploads of every unit on the upload stream, after everything already on the
 // main stream (which may still read the device inputs).
 int enqueue_uploads(dg_plan_s* p, const Driver& drv, const HostIO& io, const void* A, const void* B, void* C,
                     uint8_t* ws) {
@@ -884,7 +894,7 @@ int enqueue_uploads(dg_plan_s* p, const Driver& drv, const HostIO& io, const voi
   if (p->fault_delay_ms > 0)
     DG_CUDA(cudaLaunchHostFunc(p->up_st, sleep_cb, (void*)(intptr_t)p->fault_delay_ms));
   for (int64_t r = 0; r < p->tp; ++r) {
-    int rc = upload_rank(p, io, A, B, C, r, p->up_st);
+    int rc = upload_unit(p, io, A, B, C, r, p->up_st);
     if (rc) return rc;
     CUresult cr = drv.write32((CUstream)p->up_st, (CUdeviceptr)(up + r), p->epoch, 0);
     if (cr != CUDA_SUCCESS)
@@ -896,7 +906,9 @@ int enqueue_uploads(dg_plan_s* p, const Driver& drv, const HostIO& io, const voi
   return DG_OK;
 }
 
-// Downloads of D, block by block as the kernel finishes them.
+// Downloads of D, block by block as the kernel finishes them.  RS-TilingB
+// writes all of D in its last step and its blocks are column blocks, so it
+// waits for every block of that step and copies D whole (contiguous).
 int enqueue_downloads(dg_plan_s* p, const Driver& drv, const HostIO& io, const void* D, uint8_t* ws) {
   const dg::Geom& g = p->g;
   const int64_t P = p->tp, L = g.L, M = p->m;
@@ -909,29 +921,28 @@ int enqueue_downloads(dg_plan_s* p, const Driver& drv, const HostIO& io, const v
   const auto D2H = cudaMemcpyDeviceToHost;
   const bool ag = is_ag(p->schedule);
   for (const Block& bk : consumption_order(p->kp.g, ag ? 0 : P - 1)) {
-      const int64_t s = bk.s, r = bk.r;
-      CUresult cr = drv.wait32((CUstream)p->down_st, (CUdeviceptr)(done + s * P + r), target,
-                               CU_STREAM_WAIT_VALUE_GEQ);
-      if (cr != CUDA_SUCCESS)
-        return fail(cr == CUDA_ERROR_NOT_SUPPORTED ? DG_ERR_UNSUPPORTED : DG_ERR_CUDA,
-                    "cuStreamWaitValue32 failed (%d)", (int)cr);
-      const int64_t j = ag ? (r + s) % P : r;  // the RS block of the last step is the rank's own slab
-      int rc = DG_OK;
-      if (p->schedule == DG_RS_TILING_B_ROTATING_C) {
-        const size_t o = (size_t)(j * g.blk_n) * de;
-        rc = copy_rows(d_h + o, d_d + o, pitch, (size_t)g.blk_n * de, (size_t)(L * M), D2H, p->down_st);
-      } else {
-        for (int64_t l = 0; l < L && !rc; ++l) {
-          int64_t row0, col0, cols;
-          if (p->schedule == DG_AG_ROTATING_A) row0 = j * g.blk_m, col0 = r * g.blk_n, cols = g.blk_n;
-          else if (p->schedule == DG_AG_ROTATING_B) row0 = r * g.blk_m, col0 = j * g.blk_n, cols = g.blk_n;
-          else row0 = j * g.blk_m, col0 = 0, cols = p->n;
-          const size_t o = (size_t)(l * M + row0) * pitch + (size_t)col0 * de;
-          rc = copy_rows(d_h + o, d_d + o, pitch, (size_t)cols * de, (size_t)g.blk_m, D2H, p->down_st);
-        }
+    const int64_t s = bk.s, r = bk.r;
+    CUresult cr = drv.wait32((CUstream)p->down_st, (CUdeviceptr)(done + s * P + r), target,
+                             CU_STREAM_WAIT_VALUE_GEQ);
+    if (cr != CUDA_SUCCESS)
+      return fail(cr == CUDA_ERROR_NOT_SUPPORTED ? DG_ERR_UNSUPPORTED : DG_ERR_CUDA,
+                  "cuStreamWaitValue32 failed (%d)", (int)cr);
+    const int64_t j = ag ? (r + s) % P : r;  // the RS block of the last step is the rank's own slab
+    int rc = DG_OK;
+    if (p->schedule == DG_RS_TILING_B_ROTATING_C) {
+      if (r == P - 1) rc = copy_rows(d_h, d_d, pitch, pitch, (size_t)(L * M), D2H, p->down_st);
+    } else {
+      for (int64_t l = 0; l < L && !rc; ++l) {
+        int64_t row0, col0, cols;
+        if (p->schedule == DG_AG_ROTATING_A) row0 = j * g.blk_m, col0 = r * g.blk_n, cols = g.blk_n;
+        else if (p->schedule == DG_AG_ROTATING_B) row0 = r * g.blk_m, col0 = j * g.blk_n, cols = g.blk_n;
+        else row0 = j * g.blk_m, col0 = 0, cols = p->n;
+        const size_t o = (size_t)(l * M + row0) * pitch + (size_t)col0 * de;
+        rc = copy_rows(d_h + o, d_d + o, pitch, (size_t)cols * de, (size_t)g.blk_m, D2H, p->down_st);
       }
-      if (rc) return rc;
     }
+    if (rc) return rc;
+  }
   return DG_OK;
 }
 
@@ -1399,7 +1410,7 @@ int dg_check(dg_plan_t p, void* workspace, void* stream) {
   const uint32_t code = (uint32_t)(st >> 24) & 0xFF;
   const uint32_t info = (uint32_t)st & 0xFFFFFF;
   if (code == dg::DEV_TIMEOUT && (info & 0xF00000u) == dg::UP_FLAG_INFO)
-    return fail(DG_ERR_TIMEOUT, "upload wait ran out (inputs of rank %u, run %u)", info & 0xFFu, p->epoch);
+    return fail(DG_ERR_TIMEOUT, "upload wait ran out (upload unit %u, run %u)", info & 0xFFu, p->epoch);
   if (code == dg::DEV_TIMEOUT)
     return fail(DG_ERR_TIMEOUT, "ready-flag wait ran out (flag %u, run %u)", info, p->epoch);
   if (code == dg::DEV_HANG)

@@ -115,9 +115,9 @@ struct KParams {
   uint32_t* wave_ctr;   // per-run counter of tiles whose loads are issued (zeroed per run)
   uint32_t* progress;   // AG copy pacing: progress[s] set to 1 once a producer reaches step s, or null
   // Runs that upload their inputs and download D themselves (host buffers):
-  // rank r's operands and C are on the device once up_flags[r] >= epoch, and
-  // d_done[s * P + r] counts the half tiles of D finished for step s, rank r.
-  // Both null otherwise.
+  // the inputs of a tile are on the device once up_flags[upload_unit(tile)]
+  // >= epoch, and d_done[s * P + r] counts the half tiles of D finished for
+  // step s, rank r.  Both null otherwise.
   const uint32_t* up_flags;
   uint32_t* d_done;
   float alpha, beta;
@@ -734,6 +734,15 @@ __device__ __forceinline__ void staged_load_src(const KParams& p, const Tile& tl
     tma_load_2d(sbase + sb * XBUF, &p.tmC, bar_xfull + 8 * sb, (int32_t)(tl.out_col + c * XCOLS), (int32_t)row0);
 }
 
+// Upload unit whose flag a tile's inputs wait on (runs with host buffers).
+// AG: rank r's unit holds its home shards and the C its tiles read.  RS: unit
+// f holds the row slab (f + 1) mod P of the sliced operand and of C (unit 0
+// also the operand every tile reads whole); tile (s, r) works on slab
+// (r + s + 1) mod P.
+__device__ __forceinline__ int32_t upload_unit(const Geom& g, const Tile& tl) {
+  return (g.sched == SCHED_AG_A || g.sched == SCHED_AG_B) ? tl.r : (tl.r + tl.s) % g.P;
+}
+
 // ------------------------------------------------------------------ kernel
 
 template <int CG, int EPI, int F8>
@@ -836,11 +845,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
             __nanosleep(64);
           }
         }
-        if (p.up_flags && !((up_ok >> tl.r) & 1u)) {
-          // this rank's operands have been uploaded from the host
-          wait_flag_geq(p, p.up_flags + tl.r, p.epoch, UP_FLAG_INFO | (uint32_t)tl.r);
-          fence_proxy_async_global();
-          up_ok |= 1u << tl.r;
+        if (p.up_flags) {
+          const int32_t uu = upload_unit(p.g, tl);
+          if (!((up_ok >> uu) & 1u)) {
+            // this tile's operands have been uploaded from the host
+            wait_flag_geq(p, p.up_flags + uu, p.epoch, UP_FLAG_INFO | (uint32_t)uu);
+            fence_proxy_async_global();
+            up_ok |= 1u << uu;
+          }
         }
         if (tl.flag >= 0 && p.wait_flags) {
           wait_flag_geq(p, p.flags + tl.flag, p.epoch, (uint32_t)tl.flag);
@@ -1032,12 +1044,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           // partial of this half tile from the previous step
           wait_flag_geq(p, p.flags + tflag, want, (uint32_t)tflag);
         }
-        if (p.up_flags && tl.src == SRC_C && !((up_ok >> tl.r) & 1u)) {
-          // C of this rank's tiles has been uploaded from the host (the other
-          // threads read it after the barrier below)
-          wait_flag_geq(p, p.up_flags + tl.r, p.epoch, UP_FLAG_INFO | (uint32_t)tl.r);
+        if (p.up_flags && tl.src == SRC_C && !((up_ok >> upload_unit(p.g, tl)) & 1u)) {
+          // C of this tile has been uploaded from the host (the other threads
+          // read it after the barrier below)
+          const int32_t uu = upload_unit(p.g, tl);
+          wait_flag_geq(p, p.up_flags + uu, p.epoch, UP_FLAG_INFO | (uint32_t)uu);
           fence_proxy_async_global();
-          up_ok |= 1u << tl.r;
+          up_ok |= 1u << uu;
         }
         if (has_src) {
           // the source needs only the previous step: load it while the MMAs run

@@ -1,6 +1,7 @@
 """dg_run_host with its transfers overlapping the kernel (DG_OPT_HOST_OVERLAP):
-per-rank uploads gate the tiles of that rank, finished (step, rank) blocks of
-D are downloaded while later steps run.  The result must be bit-equal to the
+uploads in P units gate the tiles that need them (AG also in the
+upload-frontier block order), finished (step, rank) blocks of D are downloaded
+while later steps run.  The result must be bit-equal to the
 sequential form (upload all, run, download) and to a run on device buffers,
 whatever the schedule, tp, tile config, beta or input type; uploads that
 arrive late must still be waited for; a missing upload must end in a bounded
