@@ -825,15 +825,17 @@ int copy_rows(void* dst, const void* src, size_t pitch, size_t width, size_t row
 
 // Host-to-device copies of upload unit f, the inputs the tiles waiting on
 // flag f need:
-//   AG-RotatingA   rank f: A rows M_f, B rows N_f, C[:, N_f]
-//   AG-RotatingB   rank f: A rows M_f, B rows N_f, C[M_f, :]
+//   AG-RotatingA   rank f: A rows M_f, B rows N_f, C rows M_f (read by the
+//                  tiles of shard f, which wait on unit f for their C)
+//   AG-RotatingB   rank f: A rows M_f, B rows N_f, C rows M_f
 //   RS-TilingA     B whole (unit 0 only), then A rows M_j and C rows M_j
 //   RS-TilingB     A and C whole (unit 0 only), then B rows N_j
 // with j = (f + 1) mod P, every batch l, C only when beta != 0.  An RS tile
 // (s, r) works on slab (r + s + 1) mod P for every step, so it waits on unit
-// (r + s) mod P.  Every RS copy is contiguous in host memory: row slabs
-// rather than each rank's K columns, and TilingB's C (whose slabs are column
-// blocks) whole; strided host copies ran at a fraction of the link's rate.
+// (r + s) mod P.  Every copy is contiguous in host memory: row slabs rather
+// than each rank's K columns or C's column blocks, and TilingB's C (whose
+// slabs are column blocks) whole; strided host copies ran at a fraction of
+// the link's rate.
 int upload_unit(dg_plan_s* p, const HostIO& io, const void* A, const void* B, void* C, int64_t f,
                 cudaStream_t st) {
   const dg::Geom& g = p->g;
@@ -855,10 +857,6 @@ int upload_unit(dg_plan_s* p, const HostIO& io, const void* A, const void* B, vo
       if (!rc) rc = copy_rows(b_d + b0, b_h + b0, rowA, rowA, (size_t)g.blk_n, H2D, st);
     }
     if (rc || !with_c) return rc;
-    if (p->schedule == DG_AG_ROTATING_A) {
-      const size_t c0 = (size_t)(f * g.blk_n) * 2;
-      return copy_rows(c_d + c0, c_h + c0, rowC, (size_t)g.blk_n * 2, (size_t)(L * M), H2D, st);
-    }
     for (int64_t l = 0; l < L && !rc; ++l) {
       const size_t c0 = (size_t)(l * M + f * g.blk_m) * rowC;
       rc = copy_rows(c_d + c0, c_h + c0, rowC, rowC, (size_t)g.blk_m, H2D, st);

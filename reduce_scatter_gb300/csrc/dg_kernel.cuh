@@ -734,13 +734,17 @@ __device__ __forceinline__ void staged_load_src(const KParams& p, const Tile& tl
     tma_load_2d(sbase + sb * XBUF, &p.tmC, bar_xfull + 8 * sb, (int32_t)(tl.out_col + c * XCOLS), (int32_t)row0);
 }
 
-// Upload unit whose flag a tile's inputs wait on (runs with host buffers).
-// AG: rank r's unit holds its home shards and the C its tiles read.  RS: unit
-// f holds the row slab (f + 1) mod P of the sliced operand and of C (unit 0
-// also the operand every tile reads whole); tile (s, r) works on slab
+// Upload units whose flags a tile's inputs wait on (runs with host buffers).
+// AG: unit f holds rank f's home shards and C's row band M_f (the C of
+// AG-RotatingB's rank f; AG-RotatingA's tile (r, j) reads C[M_j, N_r]).  RS:
+// unit f holds the row slab (f + 1) mod P of the sliced operand and of C
+// (unit 0 also what every tile reads whole); tile (s, r) works on slab
 // (r + s + 1) mod P.
 __device__ __forceinline__ int32_t upload_unit(const Geom& g, const Tile& tl) {
   return (g.sched == SCHED_AG_A || g.sched == SCHED_AG_B) ? tl.r : (tl.r + tl.s) % g.P;
+}
+__device__ __forceinline__ int32_t upload_unit_c(const Geom& g, const Tile& tl) {
+  return g.sched == SCHED_AG_A ? tl.j : upload_unit(g, tl);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -1044,10 +1048,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           // partial of this half tile from the previous step
           wait_flag_geq(p, p.flags + tflag, want, (uint32_t)tflag);
         }
-        if (p.up_flags && tl.src == SRC_C && !((up_ok >> upload_unit(p.g, tl)) & 1u)) {
+        if (p.up_flags && tl.src == SRC_C && !((up_ok >> upload_unit_c(p.g, tl)) & 1u)) {
           // C of this tile has been uploaded from the host (the other threads
           // read it after the barrier below)
-          const int32_t uu = upload_unit(p.g, tl);
+          const int32_t uu = upload_unit_c(p.g, tl);
           wait_flag_geq(p, p.up_flags + uu, p.epoch, UP_FLAG_INFO | (uint32_t)uu);
           fence_proxy_async_global();
           up_ok |= 1u << uu;
