@@ -466,8 +466,13 @@ def run_dg(args, rank, world, dist):
         e2e_steps = max(2, min(args.steps, 5))
         ms_e2e = timed_loop(run_e2e, e2e_steps, 3, main)
         plan.check(ws, main)
+        # the machine's host link on these buffers (it differs between boxes and sets the e2e floor)
+        link = {}
+        for name, dst, src in (("h2d_gbs", B, B_h), ("d2h_gbs", D_h, D)):
+            t = timed_loop(lambda: dst.copy_(src, non_blocking=True), 3, 1, main)
+            link[name] = round(src.numel() * src.element_size() / t / 1e6, 1)
         e2e = {"value": None, "unit": "TFLOP/s", "ms_per_step": ms_e2e, "steps": e2e_steps,
-               "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": D.numel() * 2,
+               "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": D.numel() * D.element_size(), "link": link,
                "mode": "one dg_run_host call per step: inputs uploaded and D downloaded inside the call "
                        "(per-rank uploads gate the kernel's tiles, finished D blocks download during the run)"}
         if not args.no_e2e_pipelined:
