@@ -785,8 +785,8 @@ int run_rs_serial(dg_plan_s* p, const Driver& drv, const void* C, void* D, uint8
 // own inputs instead of for the whole upload, and D leaves the device one
 // (step, rank) block at a time while later steps still run.
 //   upload stream:   for f = 0..P-1: upload unit f (AG: rank f's home operand
-//                    shards and the part of C its tiles read; RS: row slabs,
-//                    see upload_unit), then up_flags[f] = epoch (the
+//                    shards and C's row band M_f; RS: row slabs, see
+//                    enqueue_upload_unit), then up_flags[f] = epoch (the
 //                    producers and C-reading epilogues of the tiles that need
 //                    unit f wait on it) and an event (AG shard transfers of
 //                    rank f's home shard wait on it)
@@ -832,12 +832,12 @@ int copy_rows(void* dst, const void* src, size_t pitch, size_t width, size_t row
 //   RS-TilingB     A and C whole (unit 0 only), then B rows N_j
 // with j = (f + 1) mod P, every batch l, C only when beta != 0.  An RS tile
 // (s, r) works on slab (r + s + 1) mod P for every step, so it waits on unit
-// (r + s) mod P.  Every copy is contiguous in host memory: row slabs rather
+// (r + s) mod P (dg::upload_unit in the kernel).  Every copy is contiguous in host memory: row slabs rather
 // than each rank's K columns or C's column blocks, and TilingB's C (whose
 // slabs are column blocks) whole; strided host copies ran at a fraction of
 // the link's rate.
-int upload_unit(dg_plan_s* p, const HostIO& io, const void* A, const void* B, void* C, int64_t f,
-                cudaStream_t st) {
+int enqueue_upload_unit(dg_plan_s* p, const HostIO& io, const void* A, const void* B, void* C, int64_t f,
+                        cudaStream_t st) {
   const dg::Geom& g = p->g;
   const int64_t L = g.L, M = p->m, N = p->n, K = p->k, P = p->tp;
   const size_t es = (size_t)p->esz, rowA = (size_t)K * es, rowC = (size_t)N * 2;
@@ -892,7 +892,7 @@ int enqueue_uploads(dg_plan_s* p, const Driver& drv, const HostIO& io, const voi
   if (p->fault_delay_ms > 0)
     DG_CUDA(cudaLaunchHostFunc(p->up_st, sleep_cb, (void*)(intptr_t)p->fault_delay_ms));
   for (int64_t r = 0; r < p->tp; ++r) {
-    int rc = upload_unit(p, io, A, B, C, r, p->up_st);
+    int rc = enqueue_upload_unit(p, io, A, B, C, r, p->up_st);
     if (rc) return rc;
     CUresult cr = drv.write32((CUstream)p->up_st, (CUdeviceptr)(up + r), p->epoch, 0);
     if (cr != CUDA_SUCCESS)
@@ -1053,8 +1053,8 @@ int run_impl(dg_plan_s* p, const void* A, const void* B, const dg_bf16_t* C, con
   kp.wave_sync = wave_sync_on(p) ? 1u : 0u;
   kp.wave_ctr = reinterpret_cast<uint32_t*>(ws + p->off_status + 64);
   if (kp.wave_sync) DG_CUDA(cudaMemsetAsync(ws + p->off_status + 64, 0, 4, ms));
-  const bool pace = copy_pace_on(p) && kp.g.order == 0 && is_ag(p->schedule) && p->tp > 2 && p->mode == DG_MODE_FUSED && cs != ms &&
-                    cs != nullptr;
+  const bool pace = copy_pace_on(p) && kp.g.order == 0 && is_ag(p->schedule) && p->tp > 2 &&
+                    p->mode == DG_MODE_FUSED && cs != ms && cs != nullptr;
   kp.progress = pace ? reinterpret_cast<uint32_t*>(ws + p->off_status + kProgressOffset) : nullptr;
   if (pace) DG_CUDA(cudaMemsetAsync(ws + p->off_status + kProgressOffset, 0, (size_t)p->tp * 4, ms));
   kp.timeout_ns = (uint64_t)p->timeout_ms * 1000000ull;
