@@ -832,10 +832,10 @@ int copy_rows(void* dst, const void* src, size_t pitch, size_t width, size_t row
 //   RS-TilingB     A and C whole (unit 0 only), then B rows N_j
 // with j = (f + 1) mod P, every batch l, C only when beta != 0.  An RS tile
 // (s, r) works on slab (r + s + 1) mod P for every step, so it waits on unit
-// (r + s) mod P (dg::upload_unit in the kernel).  Every copy is contiguous in host memory: row slabs rather
-// than each rank's K columns or C's column blocks, and TilingB's C (whose
-// slabs are column blocks) whole; strided host copies ran at a fraction of
-// the link's rate.
+// (r + s) mod P (dg::upload_unit in the kernel).  Every copy is contiguous in
+// host memory: row slabs rather than each rank's K columns or C's column
+// blocks, and TilingB's C (whose slabs are column blocks) whole; strided host
+// copies ran at a fraction of the link's rate.
 int enqueue_upload_unit(dg_plan_s* p, const HostIO& io, const void* A, const void* B, void* C, int64_t f,
                         cudaStream_t st) {
   const dg::Geom& g = p->g;
