@@ -7,7 +7,8 @@ against a single-device GEMM, and prints the disposition, the average runtime
 and the throughput.  The flags follow the example's (Distributed GEMM README,
 "Getting started": --m --n --k --l --alpha --beta --iterations
 --warmup-iterations --eps), plus --tp and --schedule, which the example fixes
-at build time.
+at build time, --mode (fused, or the GEMM-only and serial copy-then-GEMM
+timings), --seed and --dist.
 
 The single-device reference is the same kernel run unsharded (tp = 1): the
 AllGather schedules keep every output's K order, so they match it bit for bit
@@ -16,8 +17,8 @@ match within a tolerance.  The check is
 
     max |D - D_ref| <= eps * max |D_ref|
 
-(eps = 0: bit-identical).  Inputs: A and B uniform in [-1, 1), C likewise
-when beta != 0, from the package's seeded generator.
+(eps = 0: bit-identical).  Inputs from the package's seeded generator: A, B
+and (when beta != 0) C drawn from --dist, uniform in [-1, 1) by default.
 """
 
 from __future__ import annotations
@@ -43,7 +44,12 @@ def parse(argv=None):
     ap.add_argument("--tp", type=int, default=8, choices=[1, 2, 4, 8], help="tensor-parallel ranks")
     ap.add_argument("--schedule", default="AllGather1D_TilingCD_RotatingA", choices=sorted(dg.SCHEDULE_BY_NAME),
                     help="distributed GEMM schedule")
+    ap.add_argument("--mode", default="fused", choices=["fused", "gemm_only", "serial"],
+                    help="fused (transfers overlapping the kernel), gemm_only (transfers skipped, "
+                         "slots pre-filled) or serial (transfers, then the kernel)")
     ap.add_argument("--seed", type=int, default=1, help="seed of the synthetic inputs")
+    ap.add_argument("--dist", default="uniform:-1:1",
+                    help="input distribution: uniform:LO:HI or normal:MEAN:STD (default uniform:-1:1)")
     a = ap.parse_args(argv)
     for name in ("m", "n", "k", "l"):
         if getattr(a, name) < 1:
@@ -52,6 +58,14 @@ def parse(argv=None):
         ap.error("--iterations must be >= 1 and --warmup-iterations >= 0")
     if a.eps < 0:
         ap.error("--eps must be >= 0")
+    try:
+        kind, x, y = a.dist.split(":")
+        a.dist = (kind, float(x), float(y))
+        if kind not in ("uniform", "normal") or (kind == "uniform" and not a.dist[1] < a.dist[2]) or \
+                (kind == "normal" and not a.dist[2] > 0):
+            raise ValueError
+    except ValueError:
+        ap.error("--dist must be uniform:LO:HI (LO < HI) or normal:MEAN:STD (STD > 0)")
     return a
 
 
@@ -66,10 +80,9 @@ def main(argv=None) -> int:
         return 2
     sched = dg.SCHEDULE_BY_NAME[a.schedule]
     dev = torch.device("cuda", torch.cuda.current_device())
-    u = ("uniform", -1.0, 1.0)
 
     def draw(stream, shape):
-        return synth.tensor_bits_torch(a.seed, stream, shape, u, device=dev).view(torch.bfloat16)
+        return synth.tensor_bits_torch(a.seed, stream, shape, a.dist, device=dev).view(torch.bfloat16)
 
     A = draw(synth.STREAM_A, (a.l, a.m, a.k))
     B = draw(synth.STREAM_B, (a.l, a.n, a.k))  # stored N x K (its transpose), K innermost
@@ -77,11 +90,18 @@ def main(argv=None) -> int:
     D = torch.empty((a.l, a.m, a.n), dtype=torch.bfloat16, device=dev)
 
     plan = dg.Plan(a.m, a.n, a.k, a.l, a.tp, sched, a.alpha, a.beta)
+    modes = {"fused": dg.MODE_FUSED, "gemm_only": dg.MODE_GEMM_ONLY, "serial": dg.MODE_SERIAL}
     info = plan.info()
     ws = torch.zeros(max(plan.workspace_bytes(), 256), dtype=torch.uint8, device=dev)
     main_s = torch.cuda.current_stream(dev)
     copy_s = torch.cuda.Stream(dev)
 
+    # one fused run first: it fills the receive slots GEMM_ONLY reads
+    plan.run(A, B, C, D, ws, main_s, copy_s)
+    plan.check(ws, main_s)
+    plan.set_mode(modes[a.mode])
+    if a.mode == "serial":  # an RS plan's serial baseline needs the larger workspace, sized in that mode
+        ws = torch.zeros(max(plan.workspace_bytes(), 256), dtype=torch.uint8, device=dev)
     for _ in range(a.warmup_iterations):
         plan.run(A, B, C, D, ws, main_s, copy_s)
     plan.check(ws, main_s)
@@ -108,7 +128,7 @@ def main(argv=None) -> int:
         passed = err <= a.eps * scale
     flops = 2.0 * a.m * a.n * a.k * a.l
     tflops = flops / (ms * 1e-3) / 1e12
-    print(f"  Schedule: {a.schedule}, TP={a.tp} (all ranks on one GPU)")
+    print(f"  Schedule: {a.schedule}, TP={a.tp} (all ranks on one GPU), mode {a.mode}")
     print(f"  Problem size: {a.m} x {a.n} x {a.k} x {a.l}")
     print(f"  Local GEMM problem size: {info['local_m']} x {info['local_n']} x {info['local_k']} x {a.l}")
     print(f"  Disposition (eps: {a.eps:g}): {'Passed' if passed else 'Failed'}"
