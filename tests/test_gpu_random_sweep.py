@@ -109,3 +109,46 @@ def test_random_configuration_with_epilogue_extras(i):
         return
     err = rel_err(D, want)
     assert err <= (5e-4 if out_f32 else TOL), (err, sched, tp, m, n, k, l, ta, tb, opts, out_f32, op)
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_configuration_from_host_buffers(i):
+    # the same space through dg_run_host: pinned or pageable host buffers, transfers
+    # overlapping the kernel or not, either block order (AG); bit-equal to the run on
+    # device buffers
+    import torch
+    sched, tp, m, n, k, l, ta, tb, alpha, beta, sa, sb, opts = _case(900 + i)
+    rng = np.random.default_rng(9000 + i)
+    if ta == "bf16":
+        a, b, c = host_inputs(m, n, k, l, seed=4000 + i)
+        A, B = to_dev(a), to_dev(b)
+        in_dt, view = torch.bfloat16, np.int16
+    else:
+        a, b, c = host_inputs_fp8(m, n, k, l, seed=4000 + i, fmt_a=ta, fmt_b=tb)
+        A, B = to_dev_u8(a), to_dev_u8(b)
+        in_dt, view = torch.uint8, np.uint8
+    C = to_dev(c) if beta else None
+    mk = lambda: Runner(m, n, k, l, tp, sched, alpha, beta, options=opts, a_type=TCODE[ta],  # noqa: E731
+                        b_type=TCODE[tb], scale_a=sa, scale_b=sb)
+    want, _ = mk().run(A, B, C)
+    r = mk()
+    r.plan.set_option(dg.OPT_HOST_OVERLAP, int(rng.integers(0, 2)))
+    if sched <= 1:
+        r.plan.set_option(dg.OPT_TILE_ORDER, int(rng.integers(-1, 2)))
+    pinned = bool(rng.integers(0, 4))  # mostly pinned
+    host = lambda x: (torch.from_numpy(np.ascontiguousarray(x).view(view)).pin_memory() if pinned  # noqa: E731
+                      else torch.from_numpy(np.ascontiguousarray(x).view(view)).clone())
+    A_h, B_h = host(a), host(b)
+    C_h = (torch.from_numpy(c.view(np.int16)).pin_memory() if pinned else torch.from_numpy(c.view(np.int16)).clone()) \
+        if beta else None
+    D_h = torch.zeros((l, m, n), dtype=torch.int16)
+    if pinned:
+        D_h = D_h.pin_memory()
+    poison = 0xFF if in_dt == torch.uint8 else float("nan")  # NaN in bf16, e4m3 and e5m2
+    A2 = torch.full((l, m, k), poison, dtype=in_dt, device="cuda")
+    B2 = torch.full((l, n, k), poison, dtype=in_dt, device="cuda")
+    C2 = torch.full((l, m, n), float("nan"), dtype=torch.bfloat16, device="cuda") if beta else None
+    D2 = torch.full((l, m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+    r.plan.run_host(A_h, B_h, C_h, None, D_h, A2, B2, C2, D2, r.ws, r.main, r.copy)
+    r.plan.check(r.ws, r.main)
+    assert torch.equal(D_h, want.view(torch.int16).cpu()), (sched, tp, m, n, k, l, ta, tb, opts, pinned)
