@@ -162,8 +162,9 @@ enum dg_option {
                                  so each step's transfers overlap the previous step's GEMM
                                  instead of all running at the start; 0 = all transfers are
                                  issued at once; -1 (default) = on */
-  DG_OPT_COPY_KIND = 14,      /* how shard and partial transfers are issued: 0 (default) =
-                                 two-dimensional device-to-device copies in the operand's own
+  DG_OPT_COPY_KIND = 14,      /* how shard and partial transfers are issued: -1 (default) = auto,
+                                 0 for the AG shard transfers and 2 for the RS hand-off copies;
+                                 0 = two-dimensional device-to-device copies in the operand's own
                                  rows, which run on a copy engine beside a kernel that fills
                                  every SM (~1.0 TB/s on GB300); 1 = one-dimensional
                                  cudaMemcpyAsync, which on GB300 runs as a copy kernel on SMs
@@ -171,20 +172,25 @@ enum dg_option {
                                  registers to spare (~3.2 TB/s when it gets SMs, but it
                                  competes with the GEMM for them); 2 = two-dimensional copies
                                  reshaped to at least 65,536 rows (the bytes are contiguous,
-                                 so the row width is free), which a copy engine moves at
-                                 ~1.8-2.1 TB/s alone on GB300, at the price of more HBM
-                                 bandwidth taken from a GEMM running beside them */
+                                 so the row width is free), which the copy engines move at
+                                 ~1.8 TB/s on GB300 for copies of 32 MiB or more (slower than 0
+                                 below ~16 MiB), at the price of more HBM bandwidth taken from
+                                 a GEMM running beside them */
   DG_OPT_HOST_OVERLAP = 15,   /* dg_run_host in FUSED mode with pinned host buffers: 1 (default) =
                                  launch the kernel at once and overlap the transfers with it
                                  (rank r's tiles wait for rank r's uploaded inputs; each
                                  finished (step, rank) block of D is downloaded while later
                                  steps run); 0 = upload everything, run, then download */
-  DG_OPT_TILE_ORDER = 16      /* order of the (rank, step) blocks of tiles: 0 = step-major (every
+  DG_OPT_TILE_ORDER = 16,     /* order of the (rank, step) blocks of tiles: 0 = step-major (every
                                  rank's step s before any step s + 1); 1 = upload frontier, AG
                                  plans only: blocks (rank r, shard j) in groups g = max(r, j),
                                  so group g needs the inputs of ranks 0..g alone (copy pacing
                                  off); -1 (default) = 1 for AG runs of dg_run_host that overlap
                                  their uploads, else 0.  Results are bit-identical either way */
+  DG_OPT_RS_CE_BANDS = 17     /* RS with DG_OPT_RS_CE_PARTIALS: 256-row bands per hand-off copy
+                                 (consecutive bands of one rank, step and batch go as one copy
+                                 once all are complete, then each band's ready flag); 0
+                                 (default) = auto, enough bands for >= 32 MiB per copy */
 };
 
 /* Plan geometry and workspace layout, for callers and tests. */

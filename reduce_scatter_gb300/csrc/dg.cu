@@ -151,10 +151,12 @@ struct dg_plan_s {
   uint32_t l2_hint = 0;  // L2 policy of operand loads (DG_OPT_L2_HINT)
   int wave_sync = -1;  // DG_OPT_WAVE_SYNC: -1 auto, 0 off, 1 on
   int copy_pace = -1;  // DG_OPT_COPY_PACE: -1 auto, 0 off, 1 on
-  int copy_kind = 0;   // DG_OPT_COPY_KIND: 0 copy engine (2D copies in the operand's rows), 1
-                       // one-dimensional cudaMemcpyAsync, 2 copy engine (tall 2D copies)
+  int copy_kind = -1;  // DG_OPT_COPY_KIND: -1 auto (AG shards 0, RS hand-off 2), 0 copy engine (2D
+                       // copies in the operand's rows), 1 one-dimensional cudaMemcpyAsync, 2 copy
+                       // engine (tall 2D copies)
   int host_overlap = 1;  // DG_OPT_HOST_OVERLAP: dg_run_host overlaps its transfers with the kernel
   int tile_order = -1;   // DG_OPT_TILE_ORDER: -1 auto, 0 step-major, 1 upload frontier (AG)
+  int64_t ce_bands = 0;  // DG_OPT_RS_CE_BANDS: 256-row bands per hand-off copy, 0 auto
   uint64_t id = 0;
   uint32_t epoch = 0;
   bool serial_ws = false;
@@ -480,8 +482,8 @@ int build_maps(dg_plan_s* p, const Driver& drv, const void* A, const void* B, ui
 
 // Device-to-device transfer of `rows` contiguous rows of `row_bytes` bytes.
 //
-// kind 0 (default): a two-dimensional copy in the operand's own rows (pitch =
-// row bytes).  Two-dimensional copies run on a copy engine beside a kernel
+// kind 0 (the AG shard transfers' default): a two-dimensional copy in the
+// operand's own rows (pitch = row bytes).  Two-dimensional copies run on a copy engine beside a kernel
 // that fills every SM, ~1.0 TB/s on GB300 (several such copies on separate
 // streams share that rate).
 // kind 1: one-dimensional cudaMemcpyAsync, which runs as a copy kernel on the
@@ -493,9 +495,12 @@ int build_maps(dg_plan_s* p, const Driver& drv, const void* A, const void* B, ui
 // in fewer, wider rows move ~1.0 TB/s.  The bytes are contiguous on both
 // sides, so any row width that divides them gives the same result; the widest
 // power of two that keeps kTallRows rows is taken and a remainder shorter than
-// one row goes as a one-row copy.  Faster alone, but beside the GEMM kernel it
-// takes more of the HBM bandwidth and power, and the fused runs measured no
-// faster (AG-RotatingB a few percent slower).
+// one row goes as a one-row copy.  The default for the RS hand-off, whose
+// merged band copies (>= 32 MiB) it moves ~1.8 TB/s (RS-TilingB 12% faster
+// than in rows); for the AG shard transfers it takes more of the HBM
+// bandwidth and power beside the GEMM kernel, and those fused runs measured no
+// faster (AG-RotatingB a few percent slower).  Below ~16 MiB the rows it needs
+// get narrow (128 B at 8 MiB) and it is slower than kind 0.
 constexpr size_t kTallRows = 65536;
 constexpr size_t kMinTallWidth = 128;
 
@@ -604,7 +609,7 @@ int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B
         if (rows > 0) {
           const uint8_t* src = home + (l * outer + j * g.shard + row0) * row_bytes;
           uint8_t* dst = slots + (slot * g.shard + row0) * row_bytes;
-          DG_CUDA(ce_copy(dst, src, (size_t)row_bytes, (size_t)rows, st, p->copy_kind));
+          DG_CUDA(ce_copy(dst, src, (size_t)row_bytes, (size_t)rows, st, p->copy_kind < 0 ? 0 : p->copy_kind));
         }
         if (idx != p->fault_skip) {
           CUresult rc = drv.write32((CUstream)st, (CUdeviceptr)(flags + slot * g.nchunks + c),
@@ -712,28 +717,40 @@ int run_rs_ce(dg_plan_s* p, const Driver& drv, uint8_t* ws, cudaStream_t ms, cud
                              : fail(r == CUDA_ERROR_NOT_SUPPORTED ? DG_ERR_UNSUPPORTED : DG_ERR_CUDA, "%s failed (%d)",
                                     what, (int)r);
   };
+  // Bands per copy: consecutive bands of one (rank, step, batch) are contiguous
+  // in the send and receive buffers, so G of them go as one copy once all G
+  // are counted complete (then G ready flags).  Auto: enough bands for >= 32
+  // MiB, the size from which a copy reshaped to >= 65,536 rows reaches the
+  // copy engines' full rate on GB300.
+  const size_t band_bytes = row_bytes * (size_t)g.BM;
+  int64_t G = p->ce_bands > 0 ? p->ce_bands : (int64_t)((size_t(32) << 20) + band_bytes - 1) / (int64_t)band_bytes;
+  G = std::max<int64_t>(1, std::min<int64_t>(G, TM));
   int64_t n = 0;
   for (int64_t s = 0; s + 1 < P; ++s)
     for (int64_t r = 0; r < P; ++r) {
       const int64_t q = (r + P - 1) % P;  // the ring neighbour that adds the next K-slab
       for (int64_t l = 0; l < L; ++l)
-        for (int64_t b = 0; b < TM; ++b, ++n) {
+        for (int64_t b0 = 0; b0 < TM; b0 += G, ++n) {
+          const int64_t nb = std::min<int64_t>(G, TM - b0);
           cudaStream_t st = streams[n % ns];
-          rc = check(drv.wait32((CUstream)st, (CUdeviceptr)(done + idx(r, s, l, b)), target,
-                                CU_STREAM_WAIT_VALUE_GEQ),
-                     "cuStreamWaitValue32");
-          if (rc) return rc;
-          if (s >= 1) {
-            rc = check(drv.wait32((CUstream)st, (CUdeviceptr)(done + idx(q, s - 1, l, b)), target,
+          for (int64_t b = b0; b < b0 + nb; ++b) {
+            rc = check(drv.wait32((CUstream)st, (CUdeviceptr)(done + idx(r, s, l, b)), target,
                                   CU_STREAM_WAIT_VALUE_GEQ),
                        "cuStreamWaitValue32");
             if (rc) return rc;
+            if (s >= 1) {
+              rc = check(drv.wait32((CUstream)st, (CUdeviceptr)(done + idx(q, s - 1, l, b)), target,
+                                    CU_STREAM_WAIT_VALUE_GEQ),
+                         "cuStreamWaitValue32");
+              if (rc) return rc;
+            }
           }
-          const int64_t rows = std::min<int64_t>(g.BM, g.blk_m - b * g.BM);
-          const uint8_t* src = ws + p->off_send + (size_t)((r * L + l) * g.blk_m + b * g.BM) * row_bytes;
-          uint8_t* dst = ws + p->off_recv + (size_t)(((2 * q + ((s + 1) & 1)) * L + l) * g.blk_m + b * g.BM) * row_bytes;
-          DG_CUDA(ce_copy(dst, src, row_bytes, (size_t)rows, st, p->copy_kind));
-          if (n != p->fault_skip) {
+          const int64_t rows = std::min<int64_t>(nb * g.BM, g.blk_m - b0 * g.BM);
+          const uint8_t* src = ws + p->off_send + (size_t)((r * L + l) * g.blk_m + b0 * g.BM) * row_bytes;
+          uint8_t* dst = ws + p->off_recv + (size_t)(((2 * q + ((s + 1) & 1)) * L + l) * g.blk_m + b0 * g.BM) * row_bytes;
+          DG_CUDA(ce_copy(dst, src, row_bytes, (size_t)rows, st, p->copy_kind < 0 ? 2 : p->copy_kind));
+          for (int64_t b = b0; b < b0 + nb; ++b) {
+            if (n == p->fault_skip && b == b0) continue;
             rc = check(drv.write32((CUstream)st, (CUdeviceptr)(flags + idx(q, s + 1, l, b)), p->epoch, 0),
                        "cuStreamWriteValue32");
             if (rc) return rc;
@@ -1252,9 +1269,14 @@ int dg_set_option(dg_plan_t p, int option, int64_t value) {
       layout(p);
       return DG_OK;
     case DG_OPT_COPY_KIND:
-      if (value < 0 || value > 2)
-        return fail(DG_ERR_ARG, "copy kind must be 0 (copy engine), 1 (1D memcpy) or 2 (copy engine, tall copies)");
+      if (value < -1 || value > 2)
+        return fail(DG_ERR_ARG,
+                    "copy kind must be -1 (auto), 0 (copy engine), 1 (1D memcpy) or 2 (copy engine, tall copies)");
       p->copy_kind = (int)value;
+      return DG_OK;
+    case DG_OPT_RS_CE_BANDS:
+      if (value < 0 || value > (1 << 20)) return fail(DG_ERR_ARG, "bands per hand-off copy must be 0 (auto) or positive");
+      p->ce_bands = value;
       return DG_OK;
     case DG_OPT_TILE_ORDER:
       if (value < -1 || value > 1) return fail(DG_ERR_ARG, "tile order must be -1 (auto), 0 or 1");

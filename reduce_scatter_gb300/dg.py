@@ -68,6 +68,7 @@ OPT_COPY_PACE = 13
 OPT_COPY_KIND = 14
 OPT_HOST_OVERLAP = 15
 OPT_TILE_ORDER = 16
+OPT_RS_CE_BANDS = 17
 
 # Every symbol include/dg.h declares.
 EXPORTS = ("dg_plan", "dg_workspace_bytes", "dg_run_mode", "dg_set_option", "dg_run", "dg_check",

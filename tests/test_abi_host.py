@@ -306,11 +306,16 @@ def test_copy_pace_option_rules(L):
 
 def test_copy_kind_option_rules(L):
     p = dg.Plan(512, 512, 512, 1, 4, dg.AG_ROTATING_A)
-    for v in (1, 2, 0):
+    for v in (1, 2, 0, -1):
         p.set_option(dg.OPT_COPY_KIND, v)
-    for v in (-1, 3):
+    for v in (-2, 3):
         with pytest.raises(dg.DGError):
             p.set_option(dg.OPT_COPY_KIND, v)
+    q = dg.Plan(512, 512, 512, 1, 4, dg.RS_TILING_A_ROTATING_C)
+    for v in (0, 3, 1):
+        q.set_option(dg.OPT_RS_CE_BANDS, v)
+    with pytest.raises(dg.DGError):
+        q.set_option(dg.OPT_RS_CE_BANDS, -1)
 
 
 @pytest.mark.parametrize("tp", [1, 2, 4, 8])

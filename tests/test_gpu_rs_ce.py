@@ -137,3 +137,20 @@ def test_ce_handoff_with_tall_copies(sched, n):
     D, _ = r.run(A, B, C)
     assert rel_err(D, oracle_full(a, b, c, 0.5, 1.0)) <= TOL
     assert torch.equal(D.view(torch.int16), ref.view(torch.int16))
+
+
+@pytest.mark.parametrize("sched", RS, ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_ce_handoff_band_merging_and_copy_shapes(sched):
+    # hand-off copies of 1, 3 (a shorter last group) or all bands at once, in the
+    # operand's rows or reshaped tall: the same bits as the in-place hand-off
+    # (4096 rows: RS-TilingA slabs of 4 bands, RS-TilingB of 16)
+    m, n, k, l, tp = 4096, 2048, 1024, 2, 4
+    a, b, c = host_inputs(m, n, k, l, seed=140 + sched)
+    A, B, C = to_dev(a), to_dev(b), to_dev(c)
+    ref, _ = Runner(m, n, k, l, tp, sched, 0.5, 1.0).run(A, B, C)
+    for bands in (1, 3, 0, 64):
+        for kind in (-1, 0, 2):
+            r = Runner(m, n, k, l, tp, sched, 0.5, 1.0,
+                       options={dg.OPT_RS_CE_PARTIALS: 1, dg.OPT_RS_CE_BANDS: bands, dg.OPT_COPY_KIND: kind})
+            D, _ = r.run(A, B, C)
+            assert torch.equal(D.view(torch.int16), ref.view(torch.int16)), (bands, kind)
