@@ -524,8 +524,8 @@ void CUDART_CB sleep_cb(void* ms) {
   std::this_thread::sleep_for(std::chrono::milliseconds((int64_t)(intptr_t)ms));
 }
 
-// Shard transfers of every rank and step >= 1, each chunk followed by its
-// ready-flag write, in the order the kernel consumes them.
+// Plan-owned copy streams beyond the caller's (created on first use, each with
+// an event the main stream joins on).
 int ensure_extra_streams(dg_plan_s* p, int want) {
   while (p->n_extra < want) {
     DG_CUDA(cudaStreamCreateWithFlags(&p->extra[p->n_extra], cudaStreamNonBlocking));
