@@ -13,9 +13,12 @@
 //     involved);
 //   * one persistent kernel runs every rank's steps in rotation order and its
 //     producer waits on a chunk's flag before loading from the slot.
-// The RS schedules move no shards on one GPU: the rotating partial X_j lives
+// The RS schedules move no shards: by default the rotating partial X_j lives
 // in the workspace and each tile's hand-off from step s to s + 1 is a release
-// / acquire on a per-tile flag.
+// / acquire on a per-tile flag; with DG_OPT_RS_CE_PARTIALS the partial moves
+// between rank send and receive buffers by copy-engine copies (run_rs_ce).
+// dg_run_host adds plan-owned upload and download streams around a run
+// (enqueue_uploads / enqueue_downloads).
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -28,9 +31,9 @@
 #include <cstring>
 #include <mutex>
 #include <string>
-#include <vector>
 #include <thread>
 #include <unordered_map>
+#include <vector>
 
 #include "dg.h"
 #include "dg_kernel.cuh"
