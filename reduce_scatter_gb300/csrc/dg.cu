@@ -609,7 +609,7 @@ int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B
         }
         const int64_t row0 = c * chunk_rows;
         const int64_t rows = std::min(chunk_rows, g.shard - row0);
-        if (rows > 0) {
+        if (rows > 0 && row_bytes > 0) {  // K = 0: nothing to move, the flag still goes
           const uint8_t* src = home + (l * outer + j * g.shard + row0) * row_bytes;
           uint8_t* dst = slots + (slot * g.shard + row0) * row_bytes;
           DG_CUDA(ce_copy(dst, src, (size_t)row_bytes, (size_t)rows, st, p->copy_kind < 0 ? 0 : p->copy_kind));

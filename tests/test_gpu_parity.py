@@ -296,3 +296,22 @@ def test_tiny_shapes_against_brute_force(sched, tp):
         # result rounded once to bf16 (nearest even): equal bits
         want_bf16 = torch.from_numpy(want.astype(np.float32)).to(torch.bfloat16)
         assert torch.equal(D.cpu().view(torch.int16), want_bf16.view(torch.int16)), (m, n, k, l)
+
+
+@pytest.mark.parametrize("tp", [1, 2, 4])
+@pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_zero_k(sched, tp):
+    # K = 0: no MMA, the accumulator is zero, D = beta * C exactly (beta = 1 gives C's
+    # bits, beta = 0 gives +0), through every hand-off and transfer path
+    m, n, k, l = 512, 768, 0, 2
+    if not _shape_ok(sched, m, n, 8 * tp, tp):
+        pytest.skip("shape not divisible")
+    a, b, c = host_inputs(m, n, 8, l, seed=150 + sched)
+    C = to_dev(c)
+    A = torch.zeros(64, dtype=torch.bfloat16, device="cuda")  # never read (no K blocks), but not NULL
+    B = torch.zeros(64, dtype=torch.bfloat16, device="cuda")
+    for opts in ({}, {dg.OPT_CTA_GROUP: 1}, {dg.OPT_RS_CE_PARTIALS: 1} if sched >= 2 and tp > 1 else {}):
+        D, _ = Runner(m, n, k, l, tp, sched, 0.75, 1.0, options=opts).run(A, B, C)
+        assert torch.equal(D.view(torch.int16), C.view(torch.int16)), opts
+        D0, _ = Runner(m, n, k, l, tp, sched, 0.75, 0.0, options=opts).run(A, B, None)
+        assert torch.equal(D0.view(torch.int16), torch.zeros_like(D0.view(torch.int16))), opts
