@@ -315,3 +315,19 @@ def test_zero_k(sched, tp):
         assert torch.equal(D.view(torch.int16), C.view(torch.int16)), opts
         D0, _ = Runner(m, n, k, l, tp, sched, 0.75, 0.0, options=opts).run(A, B, None)
         assert torch.equal(D0.view(torch.int16), torch.zeros_like(D0.view(torch.int16))), opts
+
+
+@pytest.mark.parametrize("cg", [1, 2])
+@pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_one_row_and_eight_column_shards(sched, cg):
+    # tp = 8 with one row per M-shard (M = 8) or eight columns per N-shard (N = 64):
+    # tiles almost all outside the shard, transfers of one row, K of one block
+    tp, l = 8, 2
+    m, n, k = (8, 200, 64) if sched in (dg.AG_ROTATING_A, dg.RS_TILING_A_ROTATING_C) else (40, 64, 64)
+    a, b, c = host_inputs(m, n, k, l, seed=160 + sched)
+    A, B, C = to_dev(a), to_dev(b), to_dev(c)
+    D, _ = Runner(m, n, k, l, tp, sched, 0.5, 1.0, options={dg.OPT_CTA_GROUP: cg}).run(A, B, C)
+    assert rel_err(D, oracle_full(a, b, c, 0.5, 1.0)) <= TOL
+    if sched in (dg.AG_ROTATING_A, dg.AG_ROTATING_B):
+        ref, _ = Runner(m, n, k, l, 1, sched, 0.5, 1.0, options={dg.OPT_CTA_GROUP: cg}).run(A, B, C)
+        assert torch.equal(D.view(torch.int16), ref.view(torch.int16))
