@@ -135,3 +135,16 @@ def test_full_size_from_host_buffers(name):
     r.plan.check(r.ws, r.main)
     assert torch.equal(D_h.view(torch.int16), ref.view(torch.int16).cpu())
     _sample_check(w, D_h.cuda())
+
+
+def test_operands_beyond_32_bit_element_counts():
+    # B of 131072 x 32768 (4.3e9 elements, 8.6 GB) and D of 16384 x 131072 (2.1e9):
+    # element offsets past 2^31 and 2^32 in every addressing path (TMA rows, the
+    # epilogue's plain accesses, the shard transfers)
+    from reduce_scatter_gb300.configs import Workload, N1, N002
+    w = Workload("ag_a_tp8_wide", 0, 8, 16384, 131072, 32768, dist_a=N1, dist_b=N002)
+    A, B, C = _dev_inputs(w)
+    r = Runner(w.m, w.n, w.k, w.l, w.tp, w.schedule, w.alpha, w.beta)
+    D, _ = r.run(A, B, C)
+    assert not torch.isnan(D).any()
+    _sample_check(w, D, nrows=24, ncols=24)
