@@ -148,3 +148,16 @@ def test_operands_beyond_32_bit_element_counts():
     D, _ = r.run(A, B, C)
     assert not torch.isnan(D).any()
     _sample_check(w, D, nrows=24, ncols=24)
+
+
+@pytest.mark.parametrize("cep", [0, 1])
+def test_rs_partials_beyond_32_bit_element_counts(cep):
+    # RS-TilingB with D of 16384 x 131072 (2.1e9 elements): the fp32 partial (8.6 GB), and
+    # with the copy-engine hand-off the send and receive buffers, addressed past 2^31
+    from reduce_scatter_gb300.configs import Workload, N1, N002
+    w = Workload("rs_b_tp4_wide", 3, 4, 16384, 131072, 4096, dist_a=N1, dist_b=N002)
+    A, B, C = _dev_inputs(w)
+    r = Runner(w.m, w.n, w.k, w.l, w.tp, w.schedule, w.alpha, w.beta, options={dg.OPT_RS_CE_PARTIALS: cep})
+    D, _ = r.run(A, B, C)
+    assert not torch.isnan(D).any()
+    _sample_check(w, D, nrows=24, ncols=24)
