@@ -7,7 +7,7 @@ import pytest
 import torch
 
 from reduce_scatter_gb300 import dg
-from tests.gpu_common import TOL, Runner, dev_bits, host_inputs, oracle_full, rel_err, to_dev
+from tests.gpu_common import TOL, Runner, host_inputs, oracle_full, rel_err, to_dev
 
 pytestmark = pytest.mark.gpu
 
