@@ -25,10 +25,6 @@ def to_dev(bits: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
 
 
-def dev_bits(t: torch.Tensor) -> np.ndarray:
-    return t.view(torch.int16).cpu().numpy().view(np.uint16)
-
-
 def host_inputs_fp8(m, n, k, l, seed=1, fmt_a="e4m3", fmt_b="e4m3", da=("normal", 0.0, 1.0),
                     db=("normal", 0.0, 1.0), dc=UNIFORM):
     a = synth.tensor_fp8_bits_np(seed, synth.STREAM_A, (l, m, k), da, fmt_a)
