@@ -4,18 +4,24 @@
 // One CTA per SM, 192 threads; with CG = 2 the CTAs of a cluster pair share
 // each 256 x 256 tile (the even CTA issues the MMAs for both SMs):
 //   warp 0      TMA producer: for each tile, waits (acquire, bounded) on the
-//               ready flag of the shard chunk the tile reads, then streams
-//               64-wide K blocks of its 128 rows of A and its rows of B into a
-//               ring of shared-memory stages (128-byte swizzle).
+//               ready flag of the shard chunk the tile reads (and, in runs that
+//               upload their inputs, on the flag of the upload unit holding
+//               them), then streams 128-byte K blocks (64 bf16 or 128 fp8
+//               elements) of its 128 rows of A and its rows of B into a ring of
+//               shared-memory stages (128-byte swizzle).
 //   warp 1      MMA issuer (even CTA): 2 x 256 TMEM columns per CTA (two fp32
 //               accumulators of 128 lanes x 256 columns), issues
-//               tcgen05.mma.cta_group::{1,2}.kind::f16 (bf16 x bf16 -> fp32),
-//               four K=16 instructions per K block, and commits stage-release
-//               and accumulator-full barriers (to both CTAs of a pair).
+//               tcgen05.mma.cta_group::{1,2}.kind::f16 (bf16) or kind::f8f6f4
+//               (e4m3 / e5m2), four instructions per K block, and commits
+//               stage-release and accumulator-full barriers (to both CTAs of a
+//               pair).
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (each warp owns the 32
-//               TMEM lanes of its warp id mod 4), d = alpha*acc + source, where
-//               the source is beta*C (AG, RS step 0), the rotating fp32 partial
-//               (RS later steps) or nothing; writes bf16 D or the fp32 partial.
+//               TMEM lanes of its warp id mod 4), d = alpha*acc + source (+ the
+//               bias), where the source is beta*C (AG, RS step 0), the rotating
+//               fp32 partial (RS later steps) or nothing; writes D (bf16, fp32
+//               or fp8) or the fp32 partial (in place, or into the rank's send
+//               buffer for the copy-engine hand-off); counts finished D tiles
+//               when the host downloads D block by block.
 //
 // Ordering across proxies:
 //   copy engine -> shard data, then stream write of the ready flag;
@@ -82,7 +88,7 @@ struct Cfg {
 
 // Device status word: (epoch << 32) | (code << 24) | (info & 0xffffff).
 constexpr uint32_t DEV_TIMEOUT = 1;  // a ready-flag wait ran out
-constexpr uint32_t UP_FLAG_INFO = 0x600000u;  // status info of an upload-flag wait: | rank
+constexpr uint32_t UP_FLAG_INFO = 0x600000u;  // status info of an upload-flag wait: | upload unit
 constexpr uint32_t DEV_HANG = 2;     // a pipeline wait ran out
 
 struct KParams {
@@ -100,7 +106,7 @@ struct KParams {
   const float* R;       // receive buffers (plain-load address of tmR)
   Geom g;
   const __nv_bfloat16* C;
-  void* D;                    // bf16, or fp32 when out_f32
+  void* D;                    // bf16, fp32 when out_f32, fp8 when out_fp8
   const __nv_bfloat16* bias;  // per-column bias (N values), or null
   float* X;
   uint32_t* flags;  // AG chunk flags or RS tile flags
