@@ -315,7 +315,9 @@ int dg_run_ex(dg_plan_t plan, const void* A, const void* B, const dg_bf16_t* C, 
  * main_stream: it starts after the work already enqueued there, and returns
  * after enqueueing; D_host is valid once main_stream has reached that point
  * (e.g. after dg_check).  D_host and the device buffers must not be touched
- * by other work until then. */
+ * by other work until then.  The call can be captured into a CUDA graph on
+ * main_stream like dg_run (the plan's own streams join the capture); a replay
+ * reads the host buffers' contents at replay time. */
 int dg_run_host(dg_plan_t plan, const void* A_host, const void* B_host, const dg_bf16_t* C_host,
                 const dg_bf16_t* bias, void* D_host, void* A_dev, void* B_dev, dg_bf16_t* C_dev, void* D_dev,
                 void* workspace, void* main_stream, void* copy_stream);

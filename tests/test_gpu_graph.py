@@ -42,3 +42,42 @@ def test_graph_replays_match_eager_runs(sched):
         want, _ = ref.run(A, B, C)
         assert not torch.isnan(D.float()).any()
         assert torch.equal(D.view(torch.int16), want.view(torch.int16)), i
+
+
+@pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_graph_of_a_host_buffer_run(sched):
+    # dg_run_host captured whole (uploads gating the tiles, the kernel, block-wise
+    # downloads on the plan's own streams): replays with new host inputs in the same
+    # pinned buffers give the eager results in the pinned D, over NaN-filled device buffers
+    m, n, k, l, tp = 1024, 1024, 512, 2, 4
+    alpha, beta = 0.5, 1.0
+    cap = Runner(m, n, k, l, tp, sched, alpha, beta)
+    ref = Runner(m, n, k, l, tp, sched, alpha, beta)
+    a, b, c = host_inputs(m, n, k, l, seed=520 + sched)
+    A_h = torch.from_numpy(a.view(np.int16)).pin_memory()
+    B_h = torch.from_numpy(b.view(np.int16)).pin_memory()
+    C_h = torch.from_numpy(c.view(np.int16)).pin_memory()
+    D_h = torch.zeros((l, m, n), dtype=torch.int16).pin_memory()
+    A = torch.empty((l, m, k), dtype=torch.bfloat16, device="cuda")
+    B = torch.empty((l, n, k), dtype=torch.bfloat16, device="cuda")
+    C = torch.empty((l, m, n), dtype=torch.bfloat16, device="cuda")
+    D = torch.empty((l, m, n), dtype=torch.bfloat16, device="cuda")
+    cap.plan.run_host(A_h, B_h, C_h, None, D_h, A, B, C, D, cap.ws, torch.cuda.current_stream(), cap.copy)
+    cap.plan.check(cap.ws, torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cap.plan.run_host(A_h, B_h, C_h, None, D_h, A, B, C, D, cap.ws, torch.cuda.current_stream(), cap.copy)
+    for i in range(3):
+        a2, b2, c2 = host_inputs(m, n, k, l, seed=530 + 7 * i + sched)
+        A_h.copy_(torch.from_numpy(a2.view(np.int16)))
+        B_h.copy_(torch.from_numpy(b2.view(np.int16)))
+        C_h.copy_(torch.from_numpy(c2.view(np.int16)))
+        for t in (A, B, C, D):
+            t.fill_(float("nan"))
+        D_h.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert cap.plan.check(cap.ws, torch.cuda.current_stream(), raise_on_error=False) == dg.OK
+        want, _ = ref.run(to_dev(a2), to_dev(b2), to_dev(c2))
+        assert torch.equal(D_h, want.view(torch.int16).cpu()), i
