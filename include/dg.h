@@ -37,6 +37,16 @@
  * ordered on its main stream, and two runs of one plan must not share a
  * workspace while the first is still executing on another main stream.
  *
+ * Concurrency on the GPU: the kernel is persistent, one CTA (pair) per SM,
+ * and its transfers sit on copy streams behind stream waits.  Run dg runs one
+ * after another (on one main stream, or with the next waiting for the
+ * previous).  Two runs in flight on different streams can block each other:
+ * CUDA multiplexes streams onto a limited number of hardware queues, so one
+ * run's transfers may queue behind the other run's stream waits while the
+ * other run's kernel holds every SM; the bounded waits then end the run with
+ * DG_ERR_TIMEOUT (no hang).  An RS run's tiles also wait on tiles of other
+ * CTAs of the same launch, so all of its CTAs must be resident together.
+ *
  * Errors: every int-returning call returns DG_OK (0) or a negative dg_status;
  * dg_last_error() gives a message for the calling thread.
  */
