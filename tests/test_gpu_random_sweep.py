@@ -152,3 +152,50 @@ def test_random_configuration_from_host_buffers(i):
     r.plan.run_host(A_h, B_h, C_h, None, D_h, A2, B2, C2, D2, r.ws, r.main, r.copy)
     r.plan.check(r.ws, r.main)
     assert torch.equal(D_h, want.view(torch.int16).cpu()), (sched, tp, m, n, k, l, ta, tb, opts, pinned)
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_medium_configuration(i):
+    # shapes of 2048-8192 rows and columns: many waves of the persistent grid, the
+    # wave gate in any setting, the copy-engine hand-off; sampled entries against the
+    # oracle and, for AG, the same bits as tp = 1
+    import torch
+
+    from oracle import gemm as og
+    from reduce_scatter_gb300 import synth
+    rng = np.random.default_rng(6000 + i)
+    sched = int(rng.integers(0, 4))
+    tp = int(rng.choice([2, 4, 8]))
+    m = int(rng.integers(2048 // (8 * tp), 8192 // (8 * tp) + 1)) * 8 * tp
+    n = int(rng.integers(2048 // (8 * tp), 8192 // (8 * tp) + 1)) * 8 * tp
+    k = int(rng.integers(512 // (16 * tp), 4096 // (16 * tp) + 1)) * 16 * tp
+    l = int(rng.integers(1, 3))
+    alpha, beta = float(rng.choice([1.0, 0.5])), float(rng.choice([0.0, 1.0]))
+    opts = {dg.OPT_CTA_GROUP: int(rng.integers(1, 3)), dg.OPT_WAVE_SYNC: int(rng.integers(-1, 2))}
+    if sched >= 2 and rng.integers(0, 2):
+        opts[dg.OPT_RS_CE_PARTIALS] = 1
+    seed, dist = 100 + i, ("normal", 0.0, 1.0)
+    A = synth.tensor_bits_torch(seed, synth.STREAM_A, (l, m, k), dist, device="cuda").view(torch.bfloat16)
+    B = synth.tensor_bits_torch(seed, synth.STREAM_B, (l, n, k), dist, device="cuda").view(torch.bfloat16)
+    C = synth.tensor_bits_torch(seed, synth.STREAM_C, (l, m, n), dist, device="cuda").view(torch.bfloat16) \
+        if beta else None
+    D, _ = Runner(m, n, k, l, tp, sched, alpha, beta, options=opts).run(A, B, C)
+    assert not torch.isnan(D).any()
+    rows = np.unique(rng.integers(0, l * m, 24))
+    cols = np.unique(rng.integers(0, n, 24))
+    Dh = D.view(l * m, n)[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()].float().cpu().numpy()
+    for b in range(l):
+        rs = rows[(rows >= b * m) & (rows < (b + 1) * m)]
+        if len(rs) == 0:
+            continue
+        a = og.bf16_bits_to_f64(synth.rows_bits_np(seed, synth.STREAM_A, (l * m, k), rs, dist))
+        bb = og.bf16_bits_to_f64(synth.rows_bits_np(seed, synth.STREAM_B, (l * n, k), cols + b * n, dist))
+        c = og.bf16_bits_to_f64(synth.rows_bits_np(seed, synth.STREAM_C, (l * m, n), rs, dist)[:, cols]) \
+            if beta else None
+        want = og.gemm_entries(a, bb, c, alpha, beta)
+        got = Dh[np.isin(rows, rs)].astype(np.float64)
+        assert np.abs(got - want).max() / np.abs(want).max() <= TOL, (sched, tp, m, n, k, l, opts)
+    if sched <= 1:
+        ref, _ = Runner(m, n, k, l, 1, sched, alpha, beta, options={dg.OPT_CTA_GROUP: opts[dg.OPT_CTA_GROUP]}).run(
+            A, B, C)
+        assert torch.equal(D.view(torch.int16), ref.view(torch.int16))
