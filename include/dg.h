@@ -324,8 +324,9 @@ int dg_run_ex(dg_plan_t plan, const void* A, const void* B, const dg_bf16_t* C, 
  * host-synchronous copies.  Either way the call is one operation on
  * main_stream: it starts after the work already enqueued there, and returns
  * after enqueueing; D_host is valid once main_stream has reached that point
- * (e.g. after dg_check).  D_host and the device buffers must not be touched
- * by other work until then.  The call can be captured into a CUDA graph on
+ * (e.g. after dg_check).  Until then the host inputs must stay allocated and
+ * unchanged (the uploads read them asynchronously, as cudaMemcpyAsync does),
+ * and D_host and the device buffers must not be touched by other work.  The call can be captured into a CUDA graph on
  * main_stream like dg_run (the plan's own streams join the capture); a replay
  * reads the host buffers' contents at replay time. */
 int dg_run_host(dg_plan_t plan, const void* A_host, const void* B_host, const dg_bf16_t* C_host,

@@ -159,10 +159,15 @@ def test_back_to_back_calls_reuse_buffers():
     A = torch.empty((l, m, k), dtype=torch.bfloat16, device="cuda")
     B = torch.empty((l, n, k), dtype=torch.bfloat16, device="cuda")
     D = torch.empty((l, m, n), dtype=torch.bfloat16, device="cuda")
-    outs = []
+    outs, keep = [], []
     for a, b in ins:
         D_h = torch.zeros((l, m, n), dtype=torch.int16).pin_memory()
-        r.plan.run_host(_host(a), _host(b), None, None, D_h, A, B, None, D, r.ws, r.main, r.copy)
+        # the host inputs must outlive the asynchronous call: the library holds raw
+        # pointers, so torch's pinned-memory cache would otherwise hand a freed block
+        # to the next iteration while this call's upload still reads it
+        A_h, B_h = _host(a), _host(b)
+        keep += [A_h, B_h]
+        r.plan.run_host(A_h, B_h, None, None, D_h, A, B, None, D, r.ws, r.main, r.copy)
         outs.append(D_h)
     r.plan.check(r.ws, r.main)
     for (a, b), D_h in zip(ins, outs):
