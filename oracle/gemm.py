@@ -19,7 +19,9 @@ one library matrix product (numpy ``matmul`` on float64), then scaled and
 offset elementwise.  When ``beta == 0`` C is not read at all (BLAS
 convention; the pages are silent), so NaNs in C do not reach D.
 
-Parity status: pinned (tests/test_oracle_pins.py: brute-force triple loop,
+Parity status: pinned (tests/test_oracle_pins.py: ``bf16_bits_to_f64`` against
+the format's definition on hand-decoded patterns and torch's own widening of
+all 65,536 codes; ``gemm``: brute-force triple loop,
 closed forms, the statistical mean printed on the all_gather+matmul blog
 page, schedule invariance; ``fused_gemm``: a loop-by-loop restatement of the
 torch module's per-rank composition, closed forms, schedule invariance with

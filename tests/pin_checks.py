@@ -307,3 +307,41 @@ def check_schedule_bias_reduce(run_schedule, fused_gemm, schedules):
                 got = run_schedule(sched, A, B, C, 0.5, 1.0, P, bias=bias, reduce_op=op)
                 want = fused_gemm(A, B, C, 0.5, 1.0, P=P, reduce_op=op, bias=bias)
                 assert np.array_equal(got, want), (sched, P, op)
+
+
+# ------------------------------------------------------- bf16 input decoding
+
+# bfloat16 is the upper half of an IEEE-754 binary32: 1 sign bit, 8 exponent
+# bits (bias 127) and 7 stored mantissa bits.  Hand-decoded patterns with the
+# value each must widen to (NaN marked by None).
+BF16_PATTERNS = [
+    (0x0000, 0.0), (0x8000, -0.0), (0x3F80, 1.0), (0xBF80, -1.0), (0x4000, 2.0), (0xC040, -3.0),
+    (0x3F00, 0.5), (0x4049, 3.140625), (0x0080, 2.0 ** -126),           # smallest normal
+    (0x0001, 2.0 ** -133), (0x807F, -127 * 2.0 ** -133),               # subnormals
+    (0x7F7F, (2.0 - 2.0 ** -7) * 2.0 ** 127),                            # largest finite
+    (0x7F80, math.inf), (0xFF80, -math.inf), (0x7FC0, None), (0xFFC1, None),
+]
+
+
+def check_bf16_decode(decode, torch_decode):
+    """``decode`` (bit patterns -> float64) against the format's definition on
+    hand-written patterns (both as uint16 and as int16 input, so that a
+    sign-extension slip shows), and against ``torch_decode`` (a library
+    widening) on all 65,536 codes."""
+    for bits, want in BF16_PATTERNS:
+        for dtype in (np.uint16, np.int16):
+            arr = np.array([bits], dtype=np.uint16).astype(dtype)
+            got = float(np.asarray(decode(arr), dtype=np.float64).reshape(-1)[0])
+            if want is None:
+                assert math.isnan(got), (hex(bits), got)
+            else:
+                assert got == want and math.copysign(1.0, got) == math.copysign(1.0, want), (hex(bits), got, want)
+    codes = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):  # signalling-NaN codes widen to quiet NaNs
+        got = np.asarray(decode(codes), dtype=np.float64)
+    want = np.asarray(torch_decode(codes), dtype=np.float64)
+    assert got.shape == want.shape
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))

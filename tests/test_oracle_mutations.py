@@ -213,3 +213,34 @@ def test_fp8_result_encoding_mutants_caught():
 def _pins_fp8_result():
     from tests import test_oracle_pins as tp
     tp.test_fp8_result_encoding()
+
+
+# ------------------------------------------------------- bf16 input decoding
+
+def _bf16_shift_15(bits):
+    u = np.asarray(bits).astype(np.uint16).astype(np.uint32) << np.uint32(15)
+    return u.view(np.float32).astype(np.float64)
+
+
+def _bf16_as_fp16(bits):
+    # reads the 16-bit patterns as IEEE half precision
+    return np.asarray(bits).astype(np.uint16).view(np.float16).astype(np.float64)
+
+
+def _bf16_sign_extended(bits):
+    # widens int16 patterns through a signed 32-bit integer, then drops the sign
+    v = np.asarray(bits).astype(np.int16).astype(np.int32)
+    return (np.abs(v).astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def _bf16_truncates_mantissa(bits):
+    # keeps only 6 of the 7 stored mantissa bits
+    u = (np.asarray(bits).astype(np.uint16).astype(np.uint32) & np.uint32(0xFFFE)) << np.uint32(16)
+    return u.view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("mutant", [_bf16_shift_15, _bf16_as_fp16, _bf16_sign_extended, _bf16_truncates_mantissa],
+                         ids=lambda f: f.__name__)
+def test_bf16_decode_mutants_caught(mutant):
+    from tests.test_oracle_pins import _torch_bf16_to_f64
+    assert _fails(pc.check_bf16_decode, mutant, _torch_bf16_to_f64)

@@ -155,3 +155,15 @@ def test_fp8_result_encoding():
     # the result scale multiplies before rounding
     assert og.quantize_result(np.array([1.0, 3.0]), "e4m3", 0.5).tolist() == \
         og.f64_to_fp8_bits(np.array([0.5, 1.5]), "e4m3").tolist()
+
+
+def _torch_bf16_to_f64(codes):
+    import torch
+
+    t = torch.from_numpy(np.asarray(codes, dtype=np.uint16).view(np.int16).copy()).view(torch.bfloat16)
+    return t.to(torch.float64).numpy()
+
+
+def test_bf16_decode_matches_the_format_and_torch():
+    # every oracle input passes through this widening
+    pc.check_bf16_decode(og.bf16_bits_to_f64, _torch_bf16_to_f64)
