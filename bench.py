@@ -60,6 +60,10 @@ def parse_args(argv=None):
                     help="extra plan option, e.g. L2_HINT=9 (names of dg.OPT_*)")
     ap.add_argument("--cpu-sample-rows", type=int, default=1024)
     ap.add_argument("--cpu-sample-cols", type=int, default=4096)
+    ap.add_argument("--parity-rows", type=int, default=128,
+                    help="rows of the sampled parity check on ranks other than 0 (rank 0 at N=1 checks the "
+                         "CPU baseline's sample)")
+    ap.add_argument("--parity-cols", type=int, default=1024)
     ap.add_argument("--record-traffic", metavar="CSV", default=None,
                     help="store the DRAM bytes of an ncu --csv capture (dram__bytes_read.sum, "
                          "dram__bytes_write.sum, gpu__time_duration.sum of one dg_gemm launch) in "
@@ -202,20 +206,30 @@ class ClockSampler:
                 "power_w_max": max(r[2] for r in rows), "samples": len(loaded), "reasons": reasons}
 
 
-def cpu_oracle_sample(w, rows: int, cols: int):
-    """Time the CPU oracle on rows x cols entries of D (all of K)."""
+def sample_indices(w, rows: int, cols: int):
+    """Rows and columns of batch 0 of D that the oracle evaluates: spread
+    evenly over every shard (and so over every rank's output)."""
+    import numpy as np
+
+    rows = min(rows, w.m)
+    cols = min(cols, w.n)
+    ridx = np.linspace(0, w.m - 1, rows).astype(np.int64)
+    cidx = np.linspace(0, w.n - 1, cols).astype(np.int64)
+    return ridx, cidx
+
+
+def cpu_oracle_sample(w, rows: int, cols: int, keep_entries: bool = False):
+    """Time the CPU oracle on rows x cols entries of D (all of K); with
+    ``keep_entries`` also return the entries (for the parity check)."""
     import numpy as np
 
     from oracle import gemm as og
     from reduce_scatter_gb300 import synth
 
     LM, LN = w.l * w.m, w.l * w.n
-    rows = min(rows, LM)
-    cols = min(cols, w.n)
-    rows = min(rows, w.m)
-    ridx = np.linspace(0, w.m - 1, rows).astype(np.int64)   # spread over every shard of batch 0
+    ridx, cidx = sample_indices(w, rows, cols)
+    rows, cols = len(ridx), len(cidx)
     batch = 0
-    cidx = np.linspace(0, w.n - 1, cols).astype(np.int64)
     if w.in_type == "bf16":
         a = og.bf16_bits_to_f64(synth.rows_bits_np(w.seed, synth.STREAM_A, (LM, w.k), ridx, w.dist_a))
         b = og.bf16_bits_to_f64(synth.rows_bits_np(w.seed, synth.STREAM_B, (LN, w.k), cidx, w.dist_b))
@@ -229,7 +243,7 @@ def cpu_oracle_sample(w, rows: int, cols: int):
         crow = synth.rows_bits_np(w.seed, synth.STREAM_C, (LM, w.n), ridx, w.dist_c)[:, cidx - batch * w.n]
         c = og.bf16_bits_to_f64(crow)
     t0 = time.perf_counter()
-    og.gemm_entries(a, b, c, w.alpha * w.scale_a * w.scale_b, w.beta)
+    entries = og.gemm_entries(a, b, c, w.alpha * w.scale_a * w.scale_b, w.beta)
     dt = time.perf_counter() - t0
     flops = 2.0 * rows * cols * w.k
     try:
@@ -239,10 +253,28 @@ def cpu_oracle_sample(w, rows: int, cols: int):
                     default=os.cpu_count())
     except Exception:
         cores = os.cpu_count()
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "seconds": dt,
-            "sample": f"{rows} rows x {cols} columns of D (all K={w.k}) of {w.name}, fp64 numpy matmul; "
-                      f"{flops:.3e} flop"}
+    out = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+           "seconds": dt,
+           "sample": f"{rows} rows x {cols} columns of D (all K={w.k}) of {w.name}, fp64 numpy matmul; "
+                     f"{flops:.3e} flop"}
+    if keep_entries:
+        out["entries"] = entries
+    return out
+
+
+PARITY_TOL = 2e-2  # max|D - D_oracle| <= PARITY_TOL * max|D_oracle| (bf16 inputs, fp32 accumulation)
+
+
+def parity_check(d_sample, entries, rows, cols):
+    """The timed run's D on the sampled entries against the oracle's."""
+    import numpy as np
+
+    got = np.asarray(d_sample, dtype=np.float64)
+    finite = bool(np.isfinite(got).all())
+    scale = float(max(np.abs(entries).max(), 1e-30))
+    err = float(np.abs(got - entries).max() / scale) if finite else float("inf")
+    return {"max_rel_err": err, "tol": PARITY_TOL, "rows": rows, "cols": cols, "ok": finite and err <= PARITY_TOL,
+            "against": "oracle (fp64) on sampled entries of the timed run's D"}
 
 
 # ------------------------------------------------------------ multi-rank
@@ -409,6 +441,15 @@ def run_dg(args, rank, world, dist):
         barrier()
     plan.check(ws, main)
     clocks = clk.summary()
+    # the timed runs' D: the sampled entries for the oracle check, and (AG) all of it for the bit
+    # comparison with the same kernel unsharded
+    rows, cols = (args.cpu_sample_rows, args.cpu_sample_cols) if world == 1 else (args.parity_rows,
+                                                                                  args.parity_cols)
+    ridx, cidx = sample_indices(w, rows, cols)
+    ri, ci = torch.from_numpy(ridx).to(dev), torch.from_numpy(cidx).to(dev)
+    d_sample = D[0].index_select(0, ri).index_select(1, ci).float().cpu().numpy()
+    ag = w.schedule in (dg.AG_ROTATING_A, dg.AG_ROTATING_B)
+    D_fused = D.clone() if ag and w.tp > 1 and not args.no_modes and mode == dg.MODE_FUSED else None
 
     # latency-bound sizes: the same run replayed from a CUDA graph (one launch
     # of the whole captured run instead of its host-side enqueue)
@@ -435,6 +476,7 @@ def run_dg(args, rank, world, dist):
     # schedules the non-fused baseline (per-rank partial GEMMs, then a
     # separate reduction kernel)
     ms_tp1 = ms_nonfused = None
+    bit_exact = None
     if not args.no_modes and mode == dg.MODE_FUSED and w.tp > 1:
         p1 = dg.Plan(w.m, w.n, w.k, w.l, 1, w.schedule, w.alpha, w.beta, w.in_type, w.in_type, w.scale_a,
                      w.scale_b)
@@ -442,6 +484,11 @@ def run_dg(args, rank, world, dist):
         ms_tp1 = timed_loop(lambda: p1.run(A, B, C, D, ws1, main, copy), max(3, args.steps // 2), 2, main, flush)
         p1.check(ws1, main)
         del ws1, p1
+        if D_fused is not None:
+            # AG keeps every output element's K order: the fused run equals tp = 1 bit for bit
+            bit_exact = bool(torch.equal(D_fused.view(torch.int16), D.view(torch.int16)))
+            del D_fused
+            D_fused = None
         if w.schedule in (dg.RS_TILING_A_ROTATING_C, dg.RS_TILING_B_ROTATING_C):
             ps = dg.Plan(w.m, w.n, w.k, w.l, w.tp, w.schedule, w.alpha, w.beta, w.in_type, w.in_type,
                          w.scale_a, w.scale_b)
@@ -480,6 +527,17 @@ def run_dg(args, rank, world, dist):
             plan.check(ws, main)
         del A_h, B_h, C_h, D_h
 
+    # parity of the timed D on sampled entries: at N = 1 against the CPU baseline's own sample (main),
+    # with N > 1 every rank checks a smaller sample of its replica
+    parity = None
+    if world > 1:
+        ent = cpu_oracle_sample(w, rows, cols, keep_entries=True)["entries"]
+        parity = parity_check(d_sample, ent, len(ridx), len(cidx))
+        err_max, bad = max_over_ranks([parity["max_rel_err"], 0.0 if parity["ok"] else 1.0], dist, dev)
+        parity.update(max_rel_err=err_max, ok=bad == 0.0, ranks=world)
+    if parity is not None:
+        parity["bit_exact_vs_tp1"] = bit_exact
+
     # max over ranks
     ms_fused, ms_gemm_m, ms_serial_m, ms_e2e, ms_tp1_m, ms_nonfused_m, ms_pipe = max_over_ranks(
         [ms_fused, ms_gemm or 0.0, ms_serial or 0.0, (e2e or {}).get("ms_per_step", 0.0), ms_tp1 or 0.0,
@@ -489,7 +547,7 @@ def run_dg(args, rank, world, dist):
     ms_tp1 = ms_tp1_m if ms_tp1 is not None else None
     ms_nonfused = ms_nonfused_m if ms_nonfused is not None else None
     if rank != 0:
-        return None
+        return None, None
     ms_gemm = ms_gemm_m if ms_gemm is not None else None
     ms_serial = ms_serial_m if ms_serial is not None else None
 
@@ -554,8 +612,9 @@ def run_dg(args, rank, world, dist):
         "clocks": clocks,
         "gpu_launches": args.steps,  # one dg_gemm_kernel launch per fused step
         "e2e": e2e,
+        "parity": parity,
     }
-    return line
+    return line, (d_sample, bit_exact, len(ridx), len(cidx))
 
 
 def main(argv=None):
@@ -596,16 +655,26 @@ def main(argv=None):
         backend = "nccl"
         tdist.init_process_group(backend=backend)
         dist = tdist
-    line = run_dg(args, rank, world, dist)
+    line, sample = run_dg(args, rank, world, dist)
+    ok = True
     if line is not None:
-        if not args.no_cpu_baseline and world == 1:
-            line["cpu_baseline"] = cpu_oracle_sample(w, args.cpu_sample_rows, args.cpu_sample_cols)
-            line["cpu_baseline"].pop("seconds", None)
+        if world == 1:
+            # the CPU baseline's timed oracle entries double as the parity check of the timed D
+            d_sample, bit_exact, rows, cols = sample
+            base = cpu_oracle_sample(w, args.cpu_sample_rows, args.cpu_sample_cols, keep_entries=True)
+            line["parity"] = parity_check(d_sample, base.pop("entries"), rows, cols)
+            line["parity"]["bit_exact_vs_tp1"] = bit_exact
+            base.pop("seconds", None)
+            if not args.no_cpu_baseline:
+                line["cpu_baseline"] = base
+        ok = line["parity"]["ok"] and line["parity"].get("bit_exact_vs_tp1") is not False
         print(json.dumps(line), flush=True)
+        if not ok:
+            print("bench: the timed run's D fails the parity check", file=sys.stderr)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
-    return 0
+    return 0 if ok else 1
 
 
 if __name__ == "__main__":

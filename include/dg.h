@@ -170,8 +170,11 @@ enum dg_option {
                                  s >= 2 start only once the kernel has reached step s - 1
                                  (progress words the producers set; copy streams wait on them),
                                  so each step's transfers overlap the previous step's GEMM
-                                 instead of all running at the start; 0 = all transfers are
-                                 issued at once; -1 (default) = on */
+                                 instead of all running at the start; paced transfers are
+                                 enqueued after the kernel, so a layer that serializes launches
+                                 (a profiler, CUDA_LAUNCH_BLOCKING) ends such a run with
+                                 DG_ERR_TIMEOUT; 0 or -1 (default) = all transfers are issued
+                                 at once, before the kernel */
   DG_OPT_COPY_KIND = 14,      /* how shard and partial transfers are issued: -1 (default) = auto,
                                  0 for the AG shard transfers and 2 for the RS hand-off copies;
                                  0 = two-dimensional device-to-device copies in the operand's own
@@ -340,7 +343,9 @@ int dg_set_result_scale(dg_plan_t plan, float scale);
 
 /* Synchronize `stream` and read the workspace status word of the plan's last
  * run: DG_OK, DG_ERR_TIMEOUT or DG_ERR_HANG (with the flag index in the
- * message), or DG_ERR_CUDA on a CUDA error. */
+ * message), or DG_ERR_CUDA on a CUDA error.  workspace NULL: the built-in
+ * array if the plan's last run was dg_run_static, else only the
+ * synchronization is checked. */
 int dg_check(dg_plan_t plan, void* workspace, void* stream);
 
 /* Geometry and workspace layout. */
@@ -373,13 +378,14 @@ int dg_plan_tile(dg_plan_t plan, int64_t t, dg_tile* out);
  *     cleared on the main stream whenever a different plan used the array
  *     last.  Calls whose GPU work overlaps (on different streams, or from
  *     several threads) race on the array: serialize them.
+ *   - main_stream must belong to the current device (DG_ERR_ARG otherwise):
+ *     the array's address differs from device to device.
  *   - It makes no device-memory allocation or free (no cudaMalloc/cudaFree,
  *     no allocating library call).
- * dg_check(plan, NULL, stream) reports CUDA errors of such a run.  The
- * device status word (ready-flag wait timeouts) lives in the shared array,
- * which dg_check cannot read, so this variant does not report timeouts; a
- * run that timed out leaves D undefined.  Use dg_run with a workspace when
- * that report is needed. */
+ * dg_check(plan, NULL, stream) reports the plan's last dg_run_static call
+ * like any run: it reads the device status word from the shared array
+ * (DG_ERR_TIMEOUT when a ready-flag wait ran out; D is then undefined), as
+ * long as no other call has used the array since. */
 #define DG_STATIC_WORKSPACE_BYTES ((size_t)32 << 20)
 int dg_run_static(dg_plan_t plan, const dg_bf16_t* A, const dg_bf16_t* B, const dg_bf16_t* C,
                   dg_bf16_t* D, void* main_stream, void* copy_stream);

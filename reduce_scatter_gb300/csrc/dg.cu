@@ -162,6 +162,7 @@ struct dg_plan_s {
   int64_t ce_bands = 0;  // DG_OPT_RS_CE_BANDS: 256-row bands per hand-off copy, 0 auto
   uint64_t id = 0;
   uint32_t epoch = 0;
+  int static_dev = -1;  // device whose built-in workspace the plan's last run used (dg_run_static), or -1
   bool serial_ws = false;
   // layout
   int64_t n_flags = 0;
@@ -561,18 +562,21 @@ std::vector<Block> consumption_order(const dg::Geom& g, int64_t first_step) {
   return out;
 }
 
-// Shard transfers of every rank and step >= 1, each chunk followed by its
-// ready-flag write on the same stream, in the order the kernel consumes them.
-// Chunks are dealt round-robin over `ns` streams.  With `wait_up` (inputs
-// uploaded by the same call) a stream first waits for the upload of the rank
-// whose home shard it copies.
+// Shard transfers of every rank and step s in [s_lo, s_hi] (s >= 1), each
+// chunk followed by its ready-flag write on the same stream, in the order the
+// kernel consumes them.  Chunks are dealt round-robin over `ns` streams;
+// `*idx` is the enqueue index of the first chunk (and on return of the next),
+// so that a run enqueued in two parts deals and numbers its chunks as one.
+// With `wait_up` (inputs uploaded by the same call) a stream first waits for
+// the upload of the rank whose home shard it copies.
 int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B, uint8_t* ws,
-                   cudaStream_t* streams, int ns, bool pace, bool wait_up = false) {
+                   cudaStream_t* streams, int ns, bool pace, bool wait_up, int64_t s_lo, int64_t s_hi,
+                   int64_t* idx_io) {
   NvtxRange range("dg_enqueue_copies");
   auto* progress = reinterpret_cast<uint32_t*>(ws + p->off_status + kProgressOffset);
   const dg::Geom& g = p->g;
   const int64_t P = p->tp;
-  if (p->fault_delay_ms > 0)
+  if (p->fault_delay_ms > 0 && *idx_io == 0)
     for (int i = 0; i < ns; ++i)
       DG_CUDA(cudaLaunchHostFunc(streams[i], sleep_cb, (void*)(intptr_t)p->fault_delay_ms));
   const bool rot_a = p->schedule == DG_AG_ROTATING_A;
@@ -584,10 +588,11 @@ int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B
   auto* slots = ws + p->off_slots;
   auto* flags = reinterpret_cast<uint32_t*>(ws + p->off_flags);
   uint32_t up_waited[8] = {};  // per stream: ranks whose upload it already waits for
-  int64_t idx = 0;
+  int64_t idx = *idx_io;
   int64_t last_s = 0;
   for (const Block& bk : consumption_order(p->kp.g, 1)) {
     const int64_t s = bk.s, r = bk.r;
+    if (s < s_lo || s > s_hi) continue;
     if (pace && s >= 2 && s != last_s)
       // step s's shards move while the kernel computes step s - 1
       for (int i = 0; i < ns; ++i) {
@@ -624,6 +629,7 @@ int enqueue_copies(dg_plan_s* p, const Driver& drv, const void* A, const void* B
       }
     }
   }
+  *idx_io = idx;
   return DG_OK;
 }
 
@@ -674,8 +680,11 @@ int launch_kp(dg_plan_s* p, const dg::KParams& kp, cudaStream_t st) {
 }
 
 // Pacing of the AG shard transfers: the copies of step s >= 2 wait until the
-// kernel has reached step s - 1 (progress words in the status area).
-bool copy_pace_on(const dg_plan_s* p) { return p->copy_pace != 0; }
+// kernel has reached step s - 1 (progress words in the status area).  Off
+// unless asked for: it measured neutral, and paced copies can only be
+// enqueued after the kernel, so under a layer that serializes launches
+// (a profiler, CUDA_LAUNCH_BLOCKING) they could not run before it.
+bool copy_pace_on(const dg_plan_s* p) { return p->copy_pace == 1; }
 
 int launch(dg_plan_s* p, cudaStream_t st, uint32_t wait_flags) {
   p->kp.wait_flags = wait_flags;
@@ -981,6 +990,7 @@ int run_impl(dg_plan_s* p, const void* A, const void* B, const dg_bf16_t* C, con
              void* workspace, void* main_stream, void* copy_stream, const HostIO* io) {
   NvtxRange range("dg_run");
   if (!p) return fail(DG_ERR_ARG, "plan is NULL");
+  p->static_dev = -1;
   if (p->g.total_tiles == 0) return DG_OK;  // empty output
   if (!A || !B || !D) return fail(DG_ERR_ARG, "A, B and D must be non-NULL");
   if (p->beta != 0.f && !C) return fail(DG_ERR_ARG, "C is NULL but beta != 0");
@@ -1129,11 +1139,23 @@ int dispatch_run(dg_plan_s* p, const Driver& drv, const void* A, const void* B, 
       streams[0] = cs;
       for (int i = 1; i < ns; ++i) streams[i] = p->extra[i - 1];
       DG_CUDA(cudaEventRecord(p->ev_fork, ms));
+      for (int i = 0; i < ns; ++i) DG_CUDA(cudaStreamWaitEvent(streams[i], p->ev_fork, 0));
+      // Transfers that wait on nothing the kernel does are enqueued before
+      // it: every one without pacing, the first step's with it.  A layer
+      // that serializes work in issue order (a profiler, CUDA_LAUNCH_BLOCKING)
+      // then completes them before the kernel starts, instead of leaving the
+      // kernel to wait for copies queued behind it.  Paced transfers wait on
+      // the kernel's progress words, so they follow the launch.
+      const int64_t P = p->tp;
+      int64_t idx = 0;
+      rc = enqueue_copies(p, drv, A, B, ws, streams, ns, pace, wait_up, 1, pace ? 1 : P - 1, &idx);
+      if (rc) return rc;
       rc = launch(p, ms, 1);
       if (rc) return rc;
-      for (int i = 0; i < ns; ++i) DG_CUDA(cudaStreamWaitEvent(streams[i], p->ev_fork, 0));
-      rc = enqueue_copies(p, drv, A, B, ws, streams, ns, pace, wait_up);
-      if (rc) return rc;
+      if (pace) {
+        rc = enqueue_copies(p, drv, A, B, ws, streams, ns, pace, wait_up, 2, P - 1, &idx);
+        if (rc) return rc;
+      }
       // Release every pacing wait still pending (a kernel that stopped early
       // never reaches the later steps): no copy-stream wait outlives the kernel.
       if (pace) DG_CUDA(cudaMemsetAsync(ws + p->off_status + kProgressOffset, 0x01, (size_t)p->tp * 4, ms));
@@ -1144,7 +1166,8 @@ int dispatch_run(dg_plan_s* p, const Driver& drv, const void* A, const void* B, 
       DG_CUDA(cudaEventRecord(p->ev_join, cs));
       DG_CUDA(cudaStreamWaitEvent(ms, p->ev_join, 0));
     } else if (mode == DG_MODE_SERIAL) {
-      rc = enqueue_copies(p, drv, A, B, ws, &ms, 1, false, wait_up);
+      int64_t idx = 0;
+      rc = enqueue_copies(p, drv, A, B, ws, &ms, 1, false, wait_up, 1, p->tp - 1, &idx);
       if (rc) return rc;
       rc = launch(p, ms, 1);
       if (rc) return rc;
@@ -1160,6 +1183,29 @@ int dispatch_run(dg_plan_s* p, const Driver& drv, const void* A, const void* B, 
 }
 
 }  // namespace
+
+// ---------------------------------------------------------------------------
+// No-allocation entry point.
+//
+// Some callers cannot allocate device memory where they run the GEMM (their
+// host framework owns and budgets all of it, or they are a plug-in that must
+// not grow the process's device footprint).  For them the workspace can live
+// in this one file-scope device array instead.  Its size is fixed at build
+// time, every GPU that loads this library holds it until the process exits,
+// and all calls share it.
+//
+// In host code `dg_static_workspace` only names a host-side stand-in for the
+// array, not a device address: its device address is looked up once per
+// device with cudaGetSymbolAddress (with that device current) and then
+// passed to the kernel like any caller workspace.
+static __device__ __align__(256) unsigned char dg_static_workspace[DG_STATIC_WORKSPACE_BYTES];
+
+namespace {
+constexpr int kMaxStaticDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxStaticDevices] = {};
+}  // namespace
+
 
 extern "C" {
 
@@ -1425,6 +1471,11 @@ int dg_check(dg_plan_t p, void* workspace, void* stream) {
   if (!p) return fail(DG_ERR_ARG, "plan is NULL");
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  if (!workspace && p->static_dev >= 0) {
+    // the last run used the built-in array (dg_run_static): its status word is there
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    workspace = g_static_ptr[p->static_dev];
+  }
   if (!workspace || p->epoch == 0) return DG_OK;
   unsigned long long st = 0;
   e = cudaMemcpy(&st, static_cast<uint8_t*>(workspace) + p->off_status, sizeof(st), cudaMemcpyDeviceToHost);
@@ -1467,28 +1518,6 @@ void dg_destroy(dg_plan_t p) {
 
 }  // extern "C"
 
-// ---------------------------------------------------------------------------
-// No-allocation entry point.
-//
-// Some callers cannot allocate device memory where they run the GEMM (their
-// host framework owns and budgets all of it, or they are a plug-in that must
-// not grow the process's device footprint).  For them the workspace can live
-// in this one file-scope device array instead.  Its size is fixed at build
-// time, every GPU that loads this library holds it until the process exits,
-// and all calls share it.
-//
-// In host code `dg_static_workspace` only names a host-side stand-in for the
-// array, not a device address: its device address is looked up once per
-// device with cudaGetSymbolAddress (with that device current) and then
-// passed to the kernel like any caller workspace.
-static __device__ __align__(256) unsigned char dg_static_workspace[DG_STATIC_WORKSPACE_BYTES];
-
-namespace {
-constexpr int kMaxStaticDevices = 64;
-std::mutex g_static_mu;
-void* g_static_ptr[kMaxStaticDevices] = {};
-}  // namespace
-
 extern "C" int dg_run_static(dg_plan_t p, const dg_bf16_t* A, const dg_bf16_t* B, const dg_bf16_t* C,
                              dg_bf16_t* D, void* main_stream, void* copy_stream) {
   if (!p) return fail(DG_ERR_ARG, "plan is NULL");
@@ -1499,8 +1528,15 @@ extern "C" int dg_run_static(dg_plan_t p, const dg_bf16_t* A, const dg_bf16_t* B
                 "use dg_run with a caller workspace",
                 need, (size_t)DG_STATIC_WORKSPACE_BYTES);
   if (p->g.total_tiles == 0) return DG_OK;
+  // The array's address is per device: take the device the main stream runs
+  // on, which must be the current one (the kernel launches there).
   int dev = 0;
   DG_CUDA(cudaGetDevice(&dev));
+  int sdev = dev;
+  DG_CUDA(cudaStreamGetDevice(static_cast<cudaStream_t>(main_stream), &sdev));
+  if (sdev != dev)
+    return fail(DG_ERR_ARG, "dg_run_static: the main stream belongs to device %d but device %d is current", sdev,
+                dev);
   if (dev < 0 || dev >= kMaxStaticDevices) return fail(DG_ERR_UNSUPPORTED, "device index %d too large", dev);
   void* ws = nullptr;
   {
@@ -1515,5 +1551,8 @@ extern "C" int dg_run_static(dg_plan_t p, const dg_bf16_t* A, const dg_bf16_t* B
   }
   // The flag and status words that must start at zero are cleared by dg_run
   // on the main stream whenever another plan used this array last.
-  return dg_run(p, A, B, C, D, ws, main_stream, copy_stream);
+  const int rc = dg_run(p, A, B, C, D, ws, main_stream, copy_stream);
+  // dg_check(plan, NULL, stream) reads this run's status word from the array
+  if (rc == DG_OK) p->static_dev = dev;
+  return rc;
 }

@@ -173,6 +173,20 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+// Count `bytes` of the barrier's current phase as arrived without a transfer
+// (for a load that will never be issued).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Bounded wait for the phase of parity `parity` of a barrier, with no status
+// report (exit paths: wait for transfers in flight to land).
+__device__ __forceinline__ void mbar_settle(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity) && globaltimer() - t0 < 200000000ull) {
+  }
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int32_t x, int32_t y) {
   asm volatile(
@@ -313,6 +327,9 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
+}
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
@@ -775,6 +792,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
   const uint32_t bar_xfull = smem_u32(bars + 2 * STAGES + 5);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 7);
   volatile uint32_t* s_go = s_tmem + 1;  // [2] epilogue go/abort, by tile parity
+  // [2] K-block loads each CTA of a pair issued (kept in the even CTA's
+  // shared memory, for the exit: every load must land before its CTA exits)
+  volatile uint32_t* s_kcnt = s_tmem + 3;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -831,8 +851,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
       const uint32_t hint_a = p.l2_hint & 3u, hint_b = (p.l2_hint >> 2) & 3u;
       const uint64_t pol_a = hint_a ? l2_policy(hint_a) : 0, pol_b = hint_b ? l2_policy(hint_b) : 0;
       uint32_t stage = 0, phase = 0;
-      int32_t issued[STAGES];  // parity of the last load issued per stage, -1 none
-      for (int i = 0; i < STAGES; ++i) issued[i] = -1;
+      uint32_t nloads = 0;  // K-block loads issued: load n goes to stage n % STAGES, phase n / STAGES
       bool ok = true;
       uint32_t wave = 0;
       int32_t step_seen = -1;
@@ -901,7 +920,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
             else
               tma_load_2d(sa + C::A_BYTES, mb, fb, kb * kblk, b_row);
           }
-          issued[stage] = (int32_t)phase;
+          ++nloads;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -909,20 +928,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
         }
         if (p.wave_sync) atomicAdd(p.wave_ctr, 1u);
       }
-      if (!ok) {
-        aborted = true;
-        if (CG == 1) {
-          // every load issued must land before the CTA exits
-          for (int i = 0; i < STAGES; ++i)
-            if (issued[i] >= 0) {
-              const uint64_t t0 = globaltimer();
-              while (!mbar_try_wait(bar_full + 8 * i, (uint32_t)issued[i]) &&
-                     globaltimer() - t0 < 200000000ull) {
-              }
-            }
-        }
-        // CG = 2: completions are counted on the even CTA's barriers; the
-        // bounded settle below covers loads still in flight.
+      if (!ok) aborted = true;
+      if (CG == 1) {
+        // every load issued must land before the CTA exits: the last phase of
+        // each stage (phases of a stage complete in order)
+        if (!ok)
+          for (uint32_t n = nloads > (uint32_t)STAGES ? nloads - STAGES : 0u; n < nloads; ++n)
+            mbar_settle(bar_full + 8 * (n % STAGES), (n / STAGES) & 1u);
+      } else {
+        // the loads of both CTAs are counted on the even CTA's barriers: hand
+        // it this CTA's count (it waits for them before either CTA exits)
+        st_shared_cluster_u32(mapa_shared(smem_u32((const void*)(s_kcnt + crank)), 0), nloads);
       }
     }
   } else if (warp == 1) {
@@ -1003,6 +1019,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
     int64_t pend_flag = -1;  // half-tile flag whose release waits for this CTA's bulk stores
     uint32_t pend_val = 0;
     uint32_t nload = 0;   // staged source chunks loaded so far (buffer idx & 1)
+    uint32_t nsrc = 0;    // staged source loads issued (thread 0), for the exit
     uint32_t nstore = 0;  // staged destination chunks stored so far (buffer idx & 1)
     uint32_t up_ok = 0;   // ranks whose uploaded C this thread has seen (thread 0)
     uint32_t it = 0;
@@ -1067,6 +1084,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           fence_proxy_async_global();
           for (int c = 0; c < nch && c < 2; ++c)
             staged_load_src(p, tl, row0, c, nload + c, xsrc_addr, bar_xfull, src_map, src_col0, src_row0);
+          nsrc = nload + (uint32_t)(nch < 2 ? nch : 2);
         }
         bool go = mbar_wait(p, bar_tfull + 8 * buf, use & 1, 0x400000u | buf);
         if (pend_flag >= 0) {  // the previous tile's bulk stores have long completed
@@ -1155,8 +1173,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           if (tl.dst == DST_X) xp = (cep ? p.S : p.X) + (xd_row0 + row) * xd_pitch + xd_col0 + c * XCOLS;
           store_row_chunk(p, tl, grow, tl.out_col + c * XCOLS, ncols, out, xp);
         }
-        if (et == 0 && has_src && c + 2 < nch)
+        if (et == 0 && has_src && c + 2 < nch) {
           staged_load_src(p, tl, row0, c + 2, nload + c + 2, xsrc_addr, bar_xfull, src_map, src_col0, src_row0);
+          nsrc = nload + (uint32_t)c + 3;
+        }
       }
       if (has_src) nload += (uint32_t)nch;
       if (p.d_done && tl.dst == DST_D) {
@@ -1205,14 +1225,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
       }
     }
     if (et == 0 && pend_flag >= 0) release_partial(p, pend_flag, pend_val);
-    if (EPI == 1 && et == 0) bulk_wait<0>();  // no bulk store may outlive the CTA
+    if (EPI == 1 && et == 0) {
+      bulk_wait<0>();  // no bulk store may outlive the CTA
+      if (aborted)     // nor a source load that was issued but never consumed
+        for (uint32_t idx = nsrc > 2u ? nsrc - 2u : 0u; idx < nsrc; ++idx)
+          mbar_settle(bar_xfull + 8 * (idx & 1u), (idx >> 1) & 1u);
+    }
   }
 
-  if (aborted) {
-    // let loads (operand stages, staged epilogue sources) and MMAs still in
-    // flight for this CTA or pair land before exit
-    const uint64_t t0 = globaltimer();
-    while (globaltimer() - t0 < 20000000ull) {
+  if (CG == 2) {
+    // Both CTAs' operand loads complete on the even CTA's barriers, so the
+    // even CTA waits for all of them before either CTA may exit.  After an
+    // abort the two producers may have stopped at different loads (they
+    // differ by at most one ring of stages: a load is issued only once the
+    // MMA consumed the stage's previous load, which needed both CTAs' bytes),
+    // so first the phases only one CTA loaded are balanced: a load of the odd
+    // CTA alone is armed for its bytes, a missing load of the odd CTA is
+    // counted as arrived.  Without an abort both counts are equal and every
+    // phase has already completed.
+    tc_fence_before();
+    __syncwarp();
+    cluster_sync_all();  // both producers' counts are in the even CTA's shared memory
+    tc_fence_after();
+    if (leader && warp == 0 && lane == 0) {
+      const uint32_t kl = s_kcnt[0], ko = s_kcnt[1];
+      const uint32_t kmin = kl < ko ? kl : ko, kmax = kl < ko ? ko : kl;
+      for (uint32_t n = kmin; n < kmax; ++n) {
+        const uint32_t fb = bar_full + 8 * (n % STAGES);
+        if (n >= kl)
+          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+        else
+          mbar_complete_tx(fb, C::STAGE_BYTES);
+      }
+      for (uint32_t n = kmax > (uint32_t)STAGES ? kmax - STAGES : 0u; n < kmax; ++n)
+        mbar_settle(bar_full + 8 * (n % STAGES), (n / STAGES) & 1u);
     }
   }
   tc_fence_before();

@@ -58,3 +58,26 @@ def test_record_traffic_parses_an_ncu_csv(tmp_path, monkeypatch):
     assert bench.recorded_traffic("ag_a_tp8_pr") == ent["bytes_per_launch"]
     (tmp_path / "reduce_scatter_gb300" / "csrc" / "dg_geom.h").write_text("changed")
     assert bench.recorded_traffic("ag_a_tp8_pr") is None       # stale once the kernel changes
+
+
+def test_parity_check_of_the_timed_sample():
+    import numpy as np
+
+    ent = np.arange(12.0).reshape(3, 4) - 5.0
+    assert bench.parity_check(ent + 1e-3, ent, 3, 4)["ok"]
+    bad = ent.copy()
+    bad[1, 2] += 1.0                                  # one wrong entry
+    assert not bench.parity_check(bad, ent, 3, 4)["ok"]
+    nan = ent.copy()
+    nan[0, 0] = np.nan                                # an unwritten (NaN) entry
+    assert not bench.parity_check(nan, ent, 3, 4)["ok"]
+
+
+def test_parity_sample_spans_every_rank():
+    from reduce_scatter_gb300 import configs
+
+    for name, w in configs.WORKLOADS.items():
+        ridx, cidx = bench.sample_indices(w, 128, 1024)
+        assert ridx.min() == 0 and ridx.max() == w.m - 1 and cidx.min() == 0 and cidx.max() == w.n - 1
+        assert len(set((ridx * w.tp) // w.m)) == w.tp, name   # rows from every M-shard
+        assert len(set((cidx * w.tp) // w.n)) == w.tp, name   # columns from every N-shard

@@ -1,12 +1,14 @@
 """The torch-op front end (the fused-op signatures of the torch symmetric-memory
-module over the C ABI): argument rules and layouts on CPU; on the GPU the same
-bits as the C ABI on the flattened problem, and torch's matmul within
-tolerance."""
+module over the C ABI): argument rules and layouts on CPU; on the GPU every
+result element by element against the CPU oracle (``oracle.gemm.fused_gemm``
+on the exactly decoded inputs), and the same bits as the C ABI on the
+flattened problem."""
 
 import numpy as np
 import pytest
 import torch
 
+from oracle import gemm as og
 from reduce_scatter_gb300 import dg, ops
 from tests.gpu_common import TOL, Runner
 
@@ -67,8 +69,36 @@ def _randn(shape, seed, dtype=torch.bfloat16, std=1.0):
     return (torch.randn(shape, device="cuda", generator=g) * std).to(dtype)
 
 
+def _f64(t):
+    """Exact fp64 values of a bf16 or fp8 tensor, decoded by the oracle."""
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.bfloat16:
+        return og.bf16_bits_to_f64(t.view(torch.int16).numpy())
+    if hasattr(torch, "float8_e4m3fn") and t.dtype == torch.float8_e4m3fn:
+        return og.fp8_bits_to_f64(t.view(torch.uint8).numpy(), "e4m3")
+    if hasattr(torch, "float8_e5m2") and t.dtype == torch.float8_e5m2:
+        return og.fp8_bits_to_f64(t.view(torch.uint8).numpy(), "e5m2")
+    raise TypeError(t.dtype)
+
+
+def _oracle(A, W, *, alpha=1.0, beta=0.0, C=None, P=1, reduce_op=None, bias=None, k_slice=None):
+    """The oracle's D for A (..., K) times the (N, K) weight W: every leading
+    dimension of A flattened into rows, the result reshaped back.  ``k_slice``
+    restricts the product to those K columns (one rank's K-slab)."""
+    a = _f64(A).reshape(1, -1, A.shape[-1])
+    w = _f64(W)[None]
+    if k_slice is not None:
+        a, w = a[:, :, k_slice], w[:, :, k_slice]
+    c = None if C is None else _f64(C).reshape(1, -1, W.shape[0])
+    D = og.fused_gemm(a, w, c, alpha, beta, P=P, reduce_op=reduce_op, bias=None if bias is None else _f64(bias))
+    return D.reshape(*A.shape[:-1], W.shape[0])
+
+
 def _rel(got, want):
-    return ((got.double() - want).abs().max() / want.abs().max()).item()
+    g = got.detach().double().cpu().numpy()
+    assert g.shape == want.shape, (g.shape, want.shape)
+    assert not np.isnan(g).any()
+    return float(np.abs(g - want).max() / max(np.abs(want).max(), 1e-30))
 
 
 @pytest.mark.gpu
@@ -86,8 +116,7 @@ def test_all_gather_matmul_multi_b(rotate, gather_dim):
     A2 = A.movedim(gather_dim, 0).reshape(-1, 512).contiguous()
     for W, B, D in zip(Ws, Bs, outs):
         assert D.shape == (4, 256, W.shape[0])
-        want = torch.matmul(A.double(), B.double())
-        assert _rel(D, want) <= TOL
+        assert _rel(D, _oracle(A, W)) <= TOL
         # the same bits as the C ABI on the flattened problem
         ref, _ = Runner(A2.shape[0], W.shape[0], 512, 1, tp, sched).run(A2.unsqueeze(0), W.unsqueeze(0), None)
         flat = D.movedim(gather_dim, 0).reshape(-1, W.shape[0])
@@ -101,8 +130,7 @@ def test_all_gather_matmul_alpha_beta_c():
     W = _randn((384, 256), 5, std=0.05)
     C = _randn((512, 384), 6)
     _, (D,) = ops.fused_all_gather_matmul(A, [W.t()], 0, tp, alpha=0.5, beta=1.0, Cs=[C])
-    want = 0.5 * torch.matmul(A.double(), W.double().t()) + C.double()
-    assert _rel(D, want) <= TOL
+    assert _rel(D, _oracle(A, W, alpha=0.5, beta=1.0, C=C)) <= TOL
     # a B that is not a K-major view is copied once: same bits
     _, (D2,) = ops.fused_all_gather_matmul(A, [W.t().contiguous()], 0, tp, alpha=0.5, beta=1.0, Cs=[C])
     assert torch.equal(D.view(torch.int16), D2.view(torch.int16))
@@ -117,14 +145,12 @@ def test_matmul_reduce_scatter(scatter_dim, reduce_op):
     W = _randn((512, 1024), 8, std=0.05)
     D = ops.fused_matmul_reduce_scatter(A, W.t(), reduce_op, scatter_dim, tp)
     assert D.shape == (4, 256, 512)
-    want = torch.matmul(A.double(), W.double().t()) / (tp if reduce_op == "avg" else 1)
-    assert _rel(D, want) <= TOL
+    assert _rel(D, _oracle(A, W, P=tp, reduce_op=reduce_op)) <= TOL
     # rank r's slab of scatter_dim is the r-th block: per-rank K-slab products reduce to it
     r = 1
     sl = [slice(None)] * 3
     sl[scatter_dim] = slice(r * D.shape[scatter_dim] // tp, (r + 1) * D.shape[scatter_dim] // tp)
-    parts = sum(torch.matmul(A[..., q * 256:(q + 1) * 256].double(), W[:, q * 256:(q + 1) * 256].double().t())
-                for q in range(tp))
+    parts = sum(_oracle(A, W, k_slice=slice(q * 256, (q + 1) * 256)) for q in range(tp))
     if reduce_op == "avg":
         parts = parts / tp
     assert _rel(D[tuple(sl)], parts[tuple(sl)]) <= TOL
@@ -140,17 +166,13 @@ def test_scaled_ops_fp8_bias_f32(reduce_op):
     W = _randn((1024, 512), 10, dtype=torch.float32).to(torch.float8_e4m3fn)
     bias = _randn((1024,), 11)
     sa, sb = torch.tensor(0.5, device="cuda"), 0.25
-    prod = torch.matmul(A.double(), W.double().t()) * 0.125
     _, (D,) = ops.fused_all_gather_scaled_matmul(A, [W.t()], sa, [sb], 1, tp, biases=[bias],
                                                  out_dtypes=[torch.float32])
     assert D.dtype == torch.float32 and D.shape == (2, 512, 1024)
-    assert _rel(D, prod + bias.double()) <= 5e-4
+    assert _rel(D, _oracle(A, W, alpha=0.125, bias=bias)) <= 5e-4
     Dr = ops.fused_scaled_matmul_reduce_scatter(A, W.t(), sa, sb, reduce_op, 1, tp, bias=bias,
                                                 out_dtype=torch.float32)
-    want = prod + tp * bias.double()
-    if reduce_op == "avg":
-        want = want / tp
-    assert _rel(Dr, want) <= 5e-4
+    assert _rel(Dr, _oracle(A, W, alpha=0.125, P=tp, reduce_op=reduce_op, bias=bias)) <= 5e-4
     # bf16 output is the fp32 result rounded
     Db = ops.fused_scaled_matmul_reduce_scatter(A, W.t(), sa, sb, reduce_op, 1, tp, bias=bias,
                                                 out_dtype=torch.bfloat16)
@@ -165,8 +187,7 @@ def test_four_dim_gather_and_restride():
     A = _randn((2, 3, 256, 256), 12)
     W = _randn((512, 256), 13, std=0.05)
     _, (D,) = ops.fused_all_gather_matmul(A, [W.t()], 2, tp)
-    want = torch.matmul(A.double(), W.double().t())
-    assert D.shape == (2, 3, 256, 512) and _rel(D, want) <= TOL
+    assert D.shape == (2, 3, 256, 512) and _rel(D, _oracle(A, W)) <= TOL
     Ar = ops.restride_A_shard_for_fused_all_gather_matmul(A, 2)
     assert Ar.movedim(2, 0).is_contiguous()
     _, (Dr,) = ops.fused_all_gather_matmul(Ar, [W.t()], 2, tp)
@@ -184,7 +205,7 @@ def test_scaled_reduce_scatter_over_n_with_bias():
     bias = _randn((1024,), 16)
     D = ops.fused_scaled_matmul_reduce_scatter(A, W.t(), 0.5, 0.25, "sum", 2, tp, bias=bias,
                                                out_dtype=torch.float32)
-    want = torch.matmul(A.double(), W.double().t()) * 0.125 + tp * bias.double()
+    want = _oracle(A, W, alpha=0.125, P=tp, reduce_op="sum", bias=bias)
     assert D.shape == (2, 256, 1024) and _rel(D, want) <= 5e-4
 
 
@@ -208,11 +229,10 @@ def test_scaled_ops_default_to_the_input_dtype():
     # for fp8 inputs an fp8 result, result_scale * value rounded to the format
     if not hasattr(torch, "float8_e4m3fn"):
         pytest.skip("no float8 in this torch")
-    from oracle import gemm as og
     tp = 4
     A = _randn((512, 512), 17, dtype=torch.float32).to(torch.float8_e4m3fn)
     W = _randn((1024, 512), 18, dtype=torch.float32).to(torch.float8_e4m3fn)
-    prod = (torch.matmul(A.double(), W.double().t()) * 0.125).cpu().numpy()
+    prod = _oracle(A, W, alpha=0.125)
     _, (D,) = ops.fused_all_gather_scaled_matmul(A, [W.t()], 0.5, [0.25], 0, tp, result_scales=[2.0])
     assert D.dtype == torch.float8_e4m3fn
     want = og.quantize_result(prod, "e4m3", 2.0)
