@@ -324,6 +324,24 @@ def make_inputs(w, device):
     return A, B, C
 
 
+def input_bytes(w) -> int:
+    """Bytes of A, B (and C when beta != 0) of a workload."""
+    esz = 2 if w.in_type == "bf16" else 1
+    return (w.l * w.m * w.k + w.l * w.n * w.k) * esz + (w.l * w.m * w.n * 2 if w.beta != 0 else 0)
+
+
+def flushes_l2(w) -> bool:
+    """Inputs smaller than twice the L2: the bench flushes L2 between steps."""
+    return input_bytes(w) < 2 * L2_BYTES
+
+
+def workload_config(w, world: int) -> dict:
+    """The line's ``config``, the same for both arms."""
+    return dict(w.describe(), parallelism=f"tp{w.tp} virtual ranks on 1 GPU" + (
+        f", {world} replicas" if world > 1 else ""),
+        l2="flushed between steps" if flushes_l2(w) else "inputs larger than L2 (no flush)")
+
+
 def timed_loop(run, steps, warmup, stream, flush=None):
     """Per-step CUDA events on ``stream``; returns mean ms per step."""
     import torch
@@ -414,8 +432,9 @@ def run_dg(args, rank, world, dist):
     copy = torch.cuda.Stream(dev)
     in_bytes = (A.numel() * A.element_size() + B.numel() * B.element_size()
                 + (C.numel() * 2 if C is not None else 0))
+    assert in_bytes == input_bytes(w)
     flush_buf = None
-    if in_bytes < 2 * L2_BYTES:
+    if flushes_l2(w):
         flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     flush = (lambda: flush_buf.fill_(1.0)) if flush_buf is not None else None
 
@@ -592,9 +611,7 @@ def run_dg(args, rank, world, dist):
         "data": "synthetic (seeded SplitMix64 inputs with the workload's distributions)",
         "mode": args.mode,
         "options": args.option,
-        "config": dict(w.describe(), parallelism=f"tp{w.tp} virtual ranks on 1 GPU" + (
-            f", {world} replicas" if world > 1 else ""),
-            l2="flushed between steps" if flush is not None else "inputs larger than L2 (no flush)"),
+        "config": workload_config(w, world),
         "pct_of_peak": round(100.0 * per_gpu / peak, 2),
         "ms_gemm_only": None if ms_gemm is None else round(ms_gemm, 4),
         "ms_serial": None if ms_serial is None else round(ms_serial, 4),
@@ -640,7 +657,7 @@ def main(argv=None):
         line = {"impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": "TFLOP/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3, 3),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": w.describe(),
+                "data": "synthetic", "config": workload_config(w, world),
                 "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": steps[0]["cores"],
                                  "kind": "oracle", "sample": steps[0]["sample"]},
                 "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,

@@ -81,3 +81,16 @@ def test_parity_sample_spans_every_rank():
         assert ridx.min() == 0 and ridx.max() == w.m - 1 and cidx.min() == 0 and cidx.max() == w.n - 1
         assert len(set((ridx * w.tp) // w.m)) == w.tp, name   # rows from every M-shard
         assert len(set((cidx * w.tp) // w.n)) == w.tp, name   # columns from every N-shard
+
+
+def test_both_arms_report_the_same_config():
+    from reduce_scatter_gb300 import configs
+
+    for name, w in configs.WORKLOADS.items():
+        c1 = bench.workload_config(w, 1)
+        assert c1["workload"] == name and "parallelism" in c1 and "l2" in c1
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.main(["--impl", "reference", "--steps", "1", "--warmup", "1", "--workload", "ag_a_tp2_256"])
+    d = json.loads(buf.getvalue().strip().splitlines()[-1])
+    assert d["config"] == bench.workload_config(configs.WORKLOADS["ag_a_tp2_256"], 1)
