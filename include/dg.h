@@ -145,7 +145,11 @@ enum dg_option {
                                  chunks staged in shared memory and moved by TMA (default for
                                  the RS schedules, fp8 inputs and K >= 16384), 0 = direct
                                  per-row global accesses (one more operand stage; default for
-                                 bf16 AG plans with K < 16384) */
+                                 bf16 AG plans with K < 16384), 2 = staged per warp (each
+                                 epilogue warp moves its own 32-row boxes, three source loads
+                                 ahead, with no barrier between the warps; results bit-equal
+                                 to 1; default for RS plans where at least half the steps load
+                                 a source: tp <= 2, or tp <= 4 with beta != 0) */
   DG_OPT_L2_HINT = 8,         /* L2 eviction policy of the operand loads: bits 0-1 for A,
                                  bits 2-3 for B; 0 = none, 1 = evict first, 2 = evict last */
   DG_OPT_RS_CE_PARTIALS = 10, /* RS plans with tp > 1, before the first run: 1 = hand the
@@ -200,10 +204,24 @@ enum dg_option {
                                  so group g needs the inputs of ranks 0..g alone (copy pacing
                                  off); -1 (default) = 1 for AG runs of dg_run_host that overlap
                                  their uploads, else 0.  Results are bit-identical either way */
-  DG_OPT_RS_CE_BANDS = 17     /* RS with DG_OPT_RS_CE_PARTIALS: 256-row bands per hand-off copy
+  DG_OPT_RS_CE_BANDS = 17,    /* RS with DG_OPT_RS_CE_PARTIALS: 256-row bands per hand-off copy
                                  (consecutive bands of one rank, step and batch go as one copy
                                  once all are complete, then each band's ready flag); 0
                                  (default) = auto, enough bands for >= 32 MiB per copy */
+  DG_OPT_GROUP_M = 18,        /* raster of the tiles inside one (step, rank, batch) block: groups
+                                 of this many tile rows, each swept column by column (so the
+                                 tiles in flight share operand strips in L2); 0 (default) = auto */
+  DG_OPT_RS_REDUCE = 19       /* RS plans, before the first run: how the tiles of the middle steps
+                                 (0 < s < tp - 1) update the rotating partial.  1 = add
+                                 alpha' * product into it by TMA reductions (fp32 adds performed
+                                 at the L2; alpha' = alpha * scale_a * scale_b, / tp for the
+                                 mean) instead of loading it and storing fmaf(alpha', product,
+                                 partial); needs a staged epilogue (selects it if the direct one
+                                 is set); no effect with DG_OPT_RS_CE_PARTIALS.  The product is
+                                 then rounded before the add, so with a bias or with alpha' not
+                                 a power of two the partial takes two roundings per step.
+                                 0 = load, fmaf, store.  -1 (default) = 1 where it gives the
+                                 same bits as 0 (alpha' a power of two or zero, no bias), else 0 */
 };
 
 /* Plan geometry and workspace layout, for callers and tests. */
@@ -224,6 +242,8 @@ typedef struct dg_plan_info {
   int32_t elem_bytes;                /* bytes per A / B element (2 bf16, 1 fp8) */
   int32_t out_type;                  /* dg_type of D */
   int32_t reduce_op;                 /* dg_reduce_op */
+  int32_t epilogue;                  /* DG_OPT_EPILOGUE in effect: 0 direct, 1 staged, 2 staged per warp */
+  int32_t flag_parts;                /* RS hand-off flags per CTA half tile (4 with the per-warp epilogue) */
 } dg_plan_info;
 
 /* One tile of the step-major rotation order (host decoder, for tests). */

@@ -25,6 +25,7 @@
 #include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
+#include <cmath>
 #include <chrono>
 #include <cstdarg>
 #include <cstdio>
@@ -160,6 +161,9 @@ struct dg_plan_s {
   int host_overlap = 1;  // DG_OPT_HOST_OVERLAP: dg_run_host overlaps its transfers with the kernel
   int tile_order = -1;   // DG_OPT_TILE_ORDER: -1 auto, 0 step-major, 1 upload frontier (AG)
   int64_t ce_bands = 0;  // DG_OPT_RS_CE_BANDS: 256-row bands per hand-off copy, 0 auto
+  int64_t group_m_req = 0;  // DG_OPT_GROUP_M: tile rows per raster group, 0 auto
+  int rs_reduce = -1;       // DG_OPT_RS_REDUCE: middle RS steps add into the partial by TMA reduction
+                            // (-1 auto: where that gives the same bits as load, fmaf, store)
   uint64_t id = 0;
   uint32_t epoch = 0;
   int static_dev = -1;  // device whose built-in workspace the plan's last run used (dg_run_static), or -1
@@ -198,6 +202,12 @@ namespace {
 
 bool is_ag(int s) { return s == DG_AG_ROTATING_A || s == DG_AG_ROTATING_B; }
 
+// Epilogue variant: 0 direct, 1 staged per CTA, 2 staged per warp.  The
+// per-warp epilogue hands partials on, and counts finished tiles, per warp
+// quarter of a CTA's half tile.
+int epi_parts(const dg_plan_s* p) { return p->epi == 2 ? dg::EPI_WARPS : 1; }
+int epi_box_rows(const dg_plan_s* p) { return p->epi == 2 ? dg::WROWS : dg::ROWS_PER_CTA; }
+
 int layout(dg_plan_s* p) {
   dg::Geom& g = p->g;
   const int64_t P = p->tp;
@@ -210,7 +220,7 @@ int layout(dg_plan_s* p) {
   g.BM = p->cg == 2 ? dg::Cfg<2>::TILE_M : dg::Cfg<1>::TILE_M;
   g.BN = dg::TILE_N;
   g.BK = dg::KROW_BYTES / p->esz;  // 64 bf16 or 128 fp8 elements: 128 bytes per row
-  g.group_m = 16;
+  g.group_m = (int32_t)(p->group_m_req > 0 ? p->group_m_req : 16);
   g.beta_nonzero = p->beta != 0.f;
   g.order = p->tile_order == 1 ? 1 : 0;
   switch (p->schedule) {
@@ -255,8 +265,9 @@ int layout(dg_plan_s* p) {
     // copy-engine hand-off: one ready flag per (receiving rank, step, batch, band)
     p->n_flags = P * P * g.L * g.tiles_m;
   } else if (P > 1) {
-    // one flag per tile and CTA of the group (each CTA hands on its own half)
-    p->n_flags = g.L * P * g.tiles_m * g.tiles_n * p->cg;
+    // one flag per tile and CTA of the group (each CTA hands on its own half),
+    // or per warp quarter of it (per-warp epilogue)
+    p->n_flags = g.L * P * g.tiles_m * g.tiles_n * p->cg * epi_parts(p);
   }
   g.ce_partials = p->cep ? 1 : 0;
   // RS SERIAL baseline geometry: every rank's full M x N partial over its K-slab
@@ -338,6 +349,10 @@ int rt_init(dg_plan_s* p) {
   DG_SMEM_ATTR(1, 1, 1);
   DG_SMEM_ATTR(2, 0, 1);
   DG_SMEM_ATTR(2, 1, 1);
+  DG_SMEM_ATTR(1, 2, 0);
+  DG_SMEM_ATTR(2, 2, 0);
+  DG_SMEM_ATTR(1, 2, 1);
+  DG_SMEM_ATTR(2, 2, 1);
 #undef DG_SMEM_ATTR
   {
     cudaLaunchConfig_t cfg = {};
@@ -355,7 +370,10 @@ int rt_init(dg_plan_s* p) {
     DG_CUDA(cudaOccupancyMaxActiveClusters(&ncl0, dg::dg_gemm_kernel<2, 0, 0>, &cfg));
     cfg.dynamicSmemBytes = dg::Cfg<2, 1>::SMEM_BYTES;
     DG_CUDA(cudaOccupancyMaxActiveClusters(&ncl1, dg::dg_gemm_kernel<2, 1, 0>, &cfg));
-    p->max_pairs = std::min(ncl0, ncl1);
+    int ncl2 = 0;
+    cfg.dynamicSmemBytes = dg::Cfg<2, 2>::SMEM_BYTES;
+    DG_CUDA(cudaOccupancyMaxActiveClusters(&ncl2, dg::dg_gemm_kernel<2, 2, 0>, &cfg));
+    p->max_pairs = std::min(std::min(ncl0, ncl1), ncl2);
   }
   DG_CUDA(cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming));
   DG_CUDA(cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming));
@@ -385,14 +403,15 @@ int encode_map(const Driver& drv, CUtensorMap* map, const void* base, int64_t in
 }
 
 // Epilogue chunk map: `rows` x `cols` elements (fp32 or bf16) with a row pitch
-// of `cols`, box of 32 columns x 128 rows, swizzle matching the 32-column
+// of `cols`, box of 32 columns x `box_rows` rows (128: a CTA's chunk, staged
+// epilogue; 32: a warp's, per-warp epilogue), swizzle matching the 32-column
 // chunk's row bytes (128 B for fp32, 64 B for bf16).
 int encode_epi_map(const Driver& drv, CUtensorMap* map, const void* base, bool f32, int64_t cols,
-                   int64_t rows) {
+                   int64_t rows, int box_rows) {
   const int64_t esz = f32 ? 4 : 2;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)(cols * esz)};
-  cuuint32_t box[2] = {(cuuint32_t)dg::XCOLS, (cuuint32_t)dg::ROWS_PER_CTA};
+  cuuint32_t box[2] = {(cuuint32_t)dg::XCOLS, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = drv.encode(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -409,27 +428,28 @@ int build_epi_maps(dg_plan_s* p, const Driver& drv, const void* C, void* D, uint
   std::memset(&p->kp.tmX, 0, sizeof(CUtensorMap));
   std::memset(&p->kp.tmC, 0, sizeof(CUtensorMap));
   std::memset(&p->kp.tmD, 0, sizeof(CUtensorMap));
-  if (p->epi != 1) return DG_OK;
+  if (p->epi == 0) return DG_OK;
   const int64_t rows = p->l * p->m;
+  const int br = epi_box_rows(p);
   int rc = DG_OK;
   if (p->out_type == DG_TYPE_BF16 || p->out_type == DG_TYPE_F32) {  // fp8 D: direct stores only
-    rc = encode_epi_map(drv, &p->kp.tmD, D, p->out_type == DG_TYPE_F32, p->n, rows);
+    rc = encode_epi_map(drv, &p->kp.tmD, D, p->out_type == DG_TYPE_F32, p->n, rows, br);
     if (rc) return rc;
   }
   if (C && p->beta != 0.f) {
-    rc = encode_epi_map(drv, &p->kp.tmC, C, false, p->n, rows);
+    rc = encode_epi_map(drv, &p->kp.tmC, C, false, p->n, rows, br);
     if (rc) return rc;
   }
   std::memset(&p->kp.tmS, 0, sizeof(CUtensorMap));
   std::memset(&p->kp.tmR, 0, sizeof(CUtensorMap));
   if (!is_ag(p->schedule) && p->tp > 1 && p->cep) {
     const dg::Geom& g = p->g;
-    rc = encode_epi_map(drv, &p->kp.tmS, ws + p->off_send, true, g.blk_n, p->tp * g.L * g.blk_m);
+    rc = encode_epi_map(drv, &p->kp.tmS, ws + p->off_send, true, g.blk_n, p->tp * g.L * g.blk_m, br);
     if (rc) return rc;
-    rc = encode_epi_map(drv, &p->kp.tmR, ws + p->off_recv, true, g.blk_n, 2 * p->tp * g.L * g.blk_m);
+    rc = encode_epi_map(drv, &p->kp.tmR, ws + p->off_recv, true, g.blk_n, 2 * p->tp * g.L * g.blk_m, br);
     if (rc) return rc;
   } else if (!is_ag(p->schedule) && p->tp > 1) {
-    rc = encode_epi_map(drv, &p->kp.tmX, ws + p->off_partial, true, p->n, rows);
+    rc = encode_epi_map(drv, &p->kp.tmX, ws + p->off_partial, true, p->n, rows, br);
     if (rc) return rc;
   }
   return DG_OK;
@@ -640,7 +660,11 @@ int launch_kp(dg_plan_s* p, const dg::KParams& kp, cudaStream_t st) {
     grid = std::min<int64_t>(grid, tiles);
     if (grid <= 0) return DG_OK;
     const bool f8 = p->esz == 1;
-    if (p->epi == 1 && f8)
+    if (p->epi == 2 && f8)
+      dg::dg_gemm_kernel<1, 2, 1><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 2>::SMEM_BYTES, st>>>(kp);
+    else if (p->epi == 2)
+      dg::dg_gemm_kernel<1, 2, 0><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 2>::SMEM_BYTES, st>>>(kp);
+    else if (p->epi == 1 && f8)
       dg::dg_gemm_kernel<1, 1, 1><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 1>::SMEM_BYTES, st>>>(kp);
     else if (p->epi == 1)
       dg::dg_gemm_kernel<1, 1, 0><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 1>::SMEM_BYTES, st>>>(kp);
@@ -663,12 +687,18 @@ int launch_kp(dg_plan_s* p, const dg::KParams& kp, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
   cfg.blockDim = dim3(dg::NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = p->epi == 1 ? dg::Cfg<2, 1>::SMEM_BYTES : dg::Cfg<2, 0>::SMEM_BYTES;
+  cfg.dynamicSmemBytes = p->epi == 2   ? dg::Cfg<2, 2>::SMEM_BYTES
+                         : p->epi == 1 ? dg::Cfg<2, 1>::SMEM_BYTES
+                                       : dg::Cfg<2, 0>::SMEM_BYTES;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const bool f8 = p->esz == 1;
-  if (p->epi == 1 && f8)
+  if (p->epi == 2 && f8)
+    DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 2, 1>, kp));
+  else if (p->epi == 2)
+    DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 2, 0>, kp));
+  else if (p->epi == 1 && f8)
     DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 1, 1>, kp));
   else if (p->epi == 1)
     DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 1, 0>, kp));
@@ -721,7 +751,7 @@ int run_rs_ce(dg_plan_s* p, const Driver& drv, uint8_t* ws, cudaStream_t ms, cud
       DG_CUDA(cudaLaunchHostFunc(streams[i], sleep_cb, (void*)(intptr_t)p->fault_delay_ms));
   auto* done = reinterpret_cast<uint32_t*>(ws + p->off_done);
   auto* flags = reinterpret_cast<uint32_t*>(ws + p->off_flags);
-  const uint32_t target = (uint32_t)(g.tiles_n * p->cg);  // half tiles per band
+  const uint32_t target = (uint32_t)(g.tiles_n * p->cg * epi_parts(p));  // half (quarter) tiles per band
   const size_t row_bytes = (size_t)g.blk_n * 4;
   auto idx = [&](int64_t q, int64_t s, int64_t l, int64_t b) { return ((q * P + s) * L + l) * TM + b; };
   auto check = [&](CUresult r, const char* what) {
@@ -790,8 +820,9 @@ int run_rs_serial(dg_plan_s* p, const Driver& drv, const void* C, void* D, uint8
   p->kser.X = reinterpret_cast<float*>(ws + p->off_serial);
   p->kser.wait_flags = 0;
   std::memset(&p->kser.tmX, 0, sizeof(CUtensorMap));
-  if (p->epi == 1) {
-    int rc = encode_epi_map(drv, &p->kser.tmX, ws + p->off_serial, true, p->n, p->tp * p->l * p->m);
+  if (p->epi != 0) {
+    int rc = encode_epi_map(drv, &p->kser.tmX, ws + p->off_serial, true, p->n, p->tp * p->l * p->m,
+                            epi_box_rows(p));
     if (rc) return rc;
   }
   int rc = launch_kp(p, p->kser, st);
@@ -942,7 +973,7 @@ int enqueue_downloads(dg_plan_s* p, const Driver& drv, const HostIO& io, const v
   const size_t de = p->out_type == DG_TYPE_F32 ? 4 : (p->out_type == DG_TYPE_BF16 ? 2 : 1);
   const size_t pitch = (size_t)p->n * de;
   auto* done = reinterpret_cast<uint32_t*>(ws + p->off_ddone);
-  const uint32_t target = (uint32_t)(g.tiles_block * p->cg);  // half tiles of one (step, rank) block
+  const uint32_t target = (uint32_t)(g.tiles_block * p->cg * epi_parts(p));  // half (quarter) tiles of a block
   const auto* d_d = static_cast<const uint8_t*>(D);
   auto* d_h = static_cast<uint8_t*>(io.D);
   const auto D2H = cudaMemcpyDeviceToHost;
@@ -1081,6 +1112,18 @@ int run_impl(dg_plan_s* p, const void* A, const void* B, const dg_bf16_t* C, con
   kp.S = reinterpret_cast<float*>(ws + p->off_send);
   kp.R = reinterpret_cast<const float*>(ws + p->off_recv);
   kp.wave_sync = wave_sync_on(p) ? 1u : 0u;
+  {
+    // Middle RS steps may add alpha' * acc into the partial by TMA reduction
+    // (a round-to-nearest fp32 add at the L2) instead of loading the partial
+    // and storing fmaf(alpha', acc, partial).  With alpha' a power of two (or
+    // zero) and no bias, alpha' * acc is exact, so both round the same exact
+    // sum once: the same bits.  Automatic only then.
+    int e = 0;
+    const float fr = std::frexp(kp.alpha, &e);
+    const bool exact = kp.alpha == 0.f || fr == 0.5f || fr == -0.5f;
+    const bool want = p->rs_reduce == 1 || (p->rs_reduce < 0 && exact && bias == nullptr);
+    kp.rs_reduce = want && p->epi != 0 && !is_ag(p->schedule) && !p->cep ? 1u : 0u;
+  }
   kp.wave_ctr = reinterpret_cast<uint32_t*>(ws + p->off_status + 64);
   if (kp.wave_sync) DG_CUDA(cudaMemsetAsync(ws + p->off_status + 64, 0, 4, ms));
   const bool pace = copy_pace_on(p) && kp.g.order == 0 && is_ag(p->schedule) && p->tp > 2 &&
@@ -1244,9 +1287,16 @@ int dg_plan_scaled(dg_plan_t* out, int64_t m, int64_t n, int64_t k, int64_t l, i
   p->alpha = alpha, p->beta = beta;
   p->a_type = a_type, p->b_type = b_type, p->esz = esz;
   p->scale_a = scale_a, p->scale_b = scale_b;
-  // staged epilogue by default for RS, for fp8 and for long K (where a tile's
-  // mainloop is long and one fewer operand stage costs least); direct otherwise
-  p->epi = (!is_ag(schedule) || esz == 1 || k >= 16384) ? 1 : 0;
+  // Staged epilogue by default for RS, for fp8 and for long K (where a tile's
+  // mainloop is long and one fewer operand stage costs least); direct otherwise.
+  // RS plans in which at least half the steps load a source chunk per tile
+  // (the last step the partial, the first beta * C) take the per-warp staged
+  // epilogue, whose loads run further ahead; with fewer such steps the
+  // per-CTA one, whose larger boxes store the others' results faster.
+  if (is_ag(schedule))
+    p->epi = (esz == 1 || k >= 16384) ? 1 : 0;
+  else
+    p->epi = (1 + (beta != 0.f ? 1 : 0)) * 2 >= tp ? 2 : 1;
   {
     std::lock_guard<std::mutex> lk(g_ws_mu);
     p->id = g_next_plan_id++;
@@ -1312,7 +1362,7 @@ int dg_set_option(dg_plan_t p, int option, int64_t value) {
           return fail(DG_ERR_UNSUPPORTED, "copy-engine hand-off is for RS plans with tp > 1");
         if (p->schedule == DG_RS_TILING_B_ROTATING_C && (p->n / p->tp) % 8)
           return fail(DG_ERR_UNSUPPORTED, "copy-engine hand-off needs N/tp %% 8 == 0");
-        p->epi = 1;  // the hand-off runs through the staged epilogue
+        if (p->epi == 0) p->epi = 1;  // the hand-off runs through a staged epilogue
       }
       p->cep = value == 1;
       layout(p);
@@ -1322,6 +1372,20 @@ int dg_set_option(dg_plan_t p, int option, int64_t value) {
         return fail(DG_ERR_ARG,
                     "copy kind must be -1 (auto), 0 (copy engine), 1 (1D memcpy) or 2 (copy engine, tall copies)");
       p->copy_kind = (int)value;
+      return DG_OK;
+    case DG_OPT_RS_REDUCE:
+      if (value < -1 || value > 1) return fail(DG_ERR_ARG, "RS reduction must be -1 (auto), 0 or 1");
+      if (p->epoch != 0) return fail(DG_ERR_STATE, "the RS reduction is fixed after the first run");
+      if (value == 1) {
+        if (is_ag(p->schedule)) return fail(DG_ERR_UNSUPPORTED, "the reduction is for the RS schedules");
+        if (p->epi == 0) p->epi = 1;  // it runs in a staged epilogue
+      }
+      p->rs_reduce = (int)value;
+      return DG_OK;
+    case DG_OPT_GROUP_M:
+      if (value < 0 || value > (1 << 20)) return fail(DG_ERR_ARG, "raster group must be 0 (auto) or positive");
+      p->group_m_req = value;
+      layout(p);
       return DG_OK;
     case DG_OPT_RS_CE_BANDS:
       if (value < 0 || value > (1 << 20)) return fail(DG_ERR_ARG, "bands per hand-off copy must be 0 (auto) or positive");
@@ -1352,9 +1416,11 @@ int dg_set_option(dg_plan_t p, int option, int64_t value) {
       p->l2_hint = (uint32_t)value;
       return DG_OK;
     case DG_OPT_EPILOGUE:
-      if (value != 0 && value != 1) return fail(DG_ERR_ARG, "epilogue must be 0 (direct) or 1 (staged)");
+      if (value < 0 || value > 2)
+        return fail(DG_ERR_ARG, "epilogue must be 0 (direct), 1 (staged) or 2 (staged per warp)");
       if (p->epoch != 0) return fail(DG_ERR_STATE, "the epilogue is fixed after the first run");
       p->epi = (int)value;
+      layout(p);
       return DG_OK;
     case DG_OPT_OUT_TYPE:
       if (value != DG_TYPE_BF16 && value != DG_TYPE_F32 && value != DG_TYPE_E4M3 && value != DG_TYPE_E5M2)
@@ -1398,6 +1464,7 @@ int dg_plan_info_get(dg_plan_t p, dg_plan_info* o) {
   o->copies_per_run = p->copies;
   o->a_type = p->a_type, o->b_type = p->b_type, o->elem_bytes = p->esz;
   o->out_type = p->out_type, o->reduce_op = p->reduce_op;
+  o->epilogue = p->epi, o->flag_parts = epi_parts(p);
   return DG_OK;
 }
 

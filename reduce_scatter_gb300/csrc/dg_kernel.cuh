@@ -66,6 +66,17 @@ constexpr uint32_t TMEM_COLS = 2 * TILE_N;  // two accumulators
 //           Costs one operand stage of the ring (64 KB of staging).
 constexpr int XCOLS = 32;                            // columns per epilogue chunk
 constexpr uint32_t XBUF = ROWS_PER_CTA * XCOLS * 4;  // 16 KB: one fp32 chunk
+//   EPI = 2 (per-warp staged): each epilogue warp moves its own 32 rows of a
+//           chunk (32 x 32 boxes, 4 KB in fp32) through WSLOTS slots of its
+//           own in shared memory: the source is TMA-loaded WPRE chunks ahead
+//           into a slot, the result is written back into the same slot and
+//           TMA-stored from it.  No barrier couples the four warps; the
+//           rotating-partial hand-off is flagged per warp quarter of a tile.
+constexpr int EPI_WARPS = 4;
+constexpr int WROWS = ROWS_PER_CTA / EPI_WARPS;   // 32 rows per warp
+constexpr uint32_t WBUF = WROWS * XCOLS * 4;      // 4 KB: one fp32 box
+constexpr int WSLOTS = 4;                         // slots per warp (64 KB in all)
+constexpr int WPRE = 3;                           // source loads issued ahead
 
 // Tile configuration per CTA group.
 //   CG = 1: one SM, tile 128 x 256, tcgen05.mma.cta_group::1 (M=128, N=256).
@@ -83,7 +94,7 @@ struct Cfg {
   static constexpr int STAGES = CG == 1 ? (EPI ? 3 : 4) : (EPI ? 5 : 6);
   static constexpr uint32_t STAGING_BYTES = EPI ? 4 * XBUF : 0;  // 2 source + 2 destination chunks
   static constexpr uint32_t SMEM_BYTES =
-      STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+      STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 512 /*barriers*/;
 };
 
 // Device status word: (epoch << 32) | (code << 24) | (info & 0xffffff).
@@ -120,6 +131,7 @@ struct KParams {
   uint32_t wave_sync;   // producers start tile i only after every CTA issued tile i-1
   uint32_t* wave_ctr;   // per-run counter of tiles whose loads are issued (zeroed per run)
   uint32_t* progress;   // AG copy pacing: progress[s] set to 1 once a producer reaches step s, or null
+  uint32_t rs_reduce;   // staged epilogues, in-place RS: middle steps add into the partial by TMA reduction
   // Runs that upload their inputs and download D themselves (host buffers):
   // the inputs of a tile are on the device once up_flags[upload_unit(tile)]
   // >= epoch, and d_done[s * P + r] counts the half tiles of D finished for
@@ -254,6 +266,14 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+// Element-wise add of a shared-memory box into global memory (the reduction
+// is performed at the L2; the map's element type, fp32 here, sets the add).
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
                "r"(src), "r"(x), "r"(y)
                : "memory");
@@ -783,14 +803,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
   uint8_t* xsrc = smem + STAGES * C::STAGE_BYTES;
   uint8_t* xdst = xsrc + 2 * XBUF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES + C::STAGING_BYTES);
-  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, xfull[2]
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, xfull[2], wfull[16]
   const uint32_t bar_full = smem_u32(bars);
   const uint32_t bar_empty = smem_u32(bars + STAGES);
   const uint32_t bar_tfull = smem_u32(bars + 2 * STAGES);
   const uint32_t bar_tempty = smem_u32(bars + 2 * STAGES + 2);
   const uint32_t bar_drain = smem_u32(bars + 2 * STAGES + 4);
   const uint32_t bar_xfull = smem_u32(bars + 2 * STAGES + 5);
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 7);
+  const uint32_t bar_wfull = smem_u32(bars + 2 * STAGES + 7);  // [EPI_WARPS * WSLOTS] (EPI = 2)
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 7 + EPI_WARPS * WSLOTS);
   volatile uint32_t* s_go = s_tmem + 1;  // [2] epilogue go/abort, by tile parity
   // [2] K-block loads each CTA of a pair issued (kept in the even CTA's
   // shared memory, for the exit: every load must land before its CTA exits)
@@ -816,6 +837,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
     mbar_init(bar_drain, 1);
     mbar_init(bar_xfull, 1);
     mbar_init(bar_xfull + 8, 1);
+    for (int i = 0; i < EPI_WARPS * WSLOTS; ++i) mbar_init(bar_wfull + 8 * i, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -1009,6 +1031,263 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
         }
       }
     }
+  } else if constexpr (EPI == 2) {
+    // ------------------------------------------------- epilogue, per warp
+    // Warp q owns TMEM lanes 32q..32q+31 (rows of the CTA's half tile).  Lane
+    // 0 issues this warp's TMA loads and stores and its flag operations; the
+    // chunk slots, their load barriers and the bulk groups are the warp's own.
+    const int q = warp & 3;
+    uint8_t* wb = xsrc + (uint32_t)q * (WSLOTS * WBUF);
+    const uint32_t wb_addr = smem_u32(wb);
+    const uint32_t wbar = bar_wfull + 8u * (uint32_t)(WSLOTS * q);
+    uint32_t seq = 0;       // chunks of staged tiles so far: chunk g uses slot g % WSLOTS and
+                            // commits bulk group g (lane 0), so a slot's last store is a group index
+    uint32_t ph = 0;        // per slot: parity of its next load completion
+    uint32_t inflight = 0;  // slots whose load is issued and not yet consumed
+    int64_t pend_flag = -1;  // quarter-tile flag whose release waits for this warp's bulk stores
+    uint32_t pend_val = 0;
+    uint32_t up_ok = 0;
+    uint32_t it = 0;
+    for (int64_t t = unit; t < T; t += nunits, ++it) {
+      __syncwarp();  // every lane is done with the previous tile's slots before lane 0 reloads them
+      const Tile tl = decode_tile(p.g, t);
+      const uint32_t buf = it & 1, use = it >> 1;
+      const int64_t tflag = tl.tile_flag >= 0 ? (tl.tile_flag * CG + crank) * EPI_WARPS + q : -1;
+      const int64_t wrow = (int64_t)crank * ROWS_PER_CTA + q * WROWS;  // this warp's first row in the tile
+      int rows_here = tl.rows_valid - (int)wrow;
+      rows_here = rows_here < 0 ? 0 : (rows_here > WROWS ? WROWS : rows_here);
+      const int64_t row0 = tl.out_row + wrow;
+      const int nch = (tl.cols_valid + XCOLS - 1) / XCOLS;
+      // TMA needs 16-byte aligned column coordinates (8 bf16); fp8 D goes out by direct stores
+      const bool staged = (tl.out_col & 7) == 0 && !(p.out_fp8 && tl.dst == DST_D);
+      const bool cep = p.g.ce_partials != 0;
+      // a middle step of an in-place RS run may add its product into the
+      // partial by TMA reduction instead of loading, adding and storing it
+      const bool red = p.rs_reduce != 0 && staged && !cep && tl.src == SRC_X && tl.dst == DST_X;
+      const bool has_src = staged && tl.src != SRC_NONE && rows_here > 0 && !red;
+      const bool src_f32 = tl.src == SRC_X;
+      const bool dst_f32 = tl.dst == DST_X || p.out_f32 != 0;
+      const CUtensorMap* src_map = src_f32 ? (cep ? &p.tmR : &p.tmX) : &p.tmC;
+      const CUtensorMap* dst_map = tl.dst == DST_X ? (cep ? &p.tmS : &p.tmX) : &p.tmD;
+      const int64_t src_col0 = src_f32 && cep ? tl.x_col : tl.out_col;
+      const int64_t src_row0 = src_f32 && cep ? tl.xr_row + wrow : row0;
+      const int64_t dst_col0 = tl.dst == DST_X && cep ? tl.x_col : tl.out_col;
+      const int64_t dst_row0 = tl.dst == DST_X && cep ? tl.xs_row + wrow : row0;
+      const int64_t xd_pitch = cep ? p.g.blk_n : p.g.N;
+      const int npre = has_src ? (nch < WPRE ? nch : WPRE) : 0;
+      uint32_t go = 1;
+      if (lane == 0) {
+        if (cep && tl.s > 0) {
+          const int64_t P = p.g.P;
+          // the partial this step adds to has arrived in this rank's receive buffer
+          const int64_t fsrc = ((tl.r * P + tl.s) * p.g.L + tl.l) * p.g.tiles_m + tl.band;
+          wait_flag_geq(p, p.flags + fsrc, p.epoch, (uint32_t)fsrc);
+          if (tl.dst == DST_X) {
+            // the send buffer's previous contents have been copied out
+            const int64_t fsnd = ((((tl.r + P - 1) % P) * P + tl.s) * p.g.L + tl.l) * p.g.tiles_m + tl.band;
+            wait_flag_geq(p, p.flags + fsnd, p.epoch, (uint32_t)fsnd);
+          }
+        }
+        const bool need_flag = tflag >= 0 && tl.s > 0;
+        const uint32_t want = p.epoch * (uint32_t)p.g.P + (uint32_t)tl.s - 1;
+        // never hold a deferred hand-off while waiting for one (a ring of
+        // warps could each wait on the next one's)
+        if (pend_flag >= 0 && need_flag && ld_acquire_u32(p.flags + tflag) < want) {
+          release_partial(p, pend_flag, pend_val);
+          pend_flag = -1;
+        }
+        if (need_flag) wait_flag_geq(p, p.flags + tflag, want, (uint32_t)tflag);
+        if (p.up_flags && tl.src == SRC_C && !((up_ok >> upload_unit_c(p.g, tl)) & 1u)) {
+          // C of this tile has been uploaded from the host
+          const int32_t uu = upload_unit_c(p.g, tl);
+          wait_flag_geq(p, p.up_flags + uu, p.epoch, UP_FLAG_INFO | (uint32_t)uu);
+          fence_proxy_async_global();
+          up_ok |= 1u << uu;
+        }
+        if (npre > 0) {
+          // the source needs only the previous step: load it while the MMAs run.
+          // Chunk seq + c reuses the slot of chunk seq + c - WSLOTS, whose store
+          // is bulk group seq + c - WSLOTS of seq committed ones.
+          fence_proxy_async_global();
+          for (int c = 0; c < npre; ++c) {
+            if (c == 0)
+              bulk_wait_read<WSLOTS - 1>();
+            else if (c == 1)
+              bulk_wait_read<WSLOTS - 2>();
+            else
+              bulk_wait_read<WSLOTS - 3>();
+            const uint32_t sl = (seq + (uint32_t)c) % WSLOTS;
+            mbar_arrive_expect_tx(wbar + 8 * sl, src_f32 ? WBUF : WBUF / 2);
+            tma_load_2d(wb_addr + sl * WBUF, src_map, wbar + 8 * sl, (int32_t)(src_col0 + c * XCOLS),
+                        (int32_t)src_row0);
+          }
+        }
+        // No warp blocks while it holds a deferred hand-off: the accumulator
+        // depends on every warp of the pair having read the one before, and
+        // one of those may wait for this very hand-off.  So the release is
+        // deferred past this wait only when the accumulator is already full.
+        if (pend_flag >= 0 && !mbar_try_wait(bar_tfull + 8 * buf, use & 1)) {
+          release_partial(p, pend_flag, pend_val);
+          pend_flag = -1;
+        }
+        go = mbar_wait(p, bar_tfull + 8 * buf, use & 1, 0x400000u | buf) ? 1u : 0u;
+        if (pend_flag >= 0) {  // the previous tile's bulk stores have had a tile's time to complete
+          release_partial(p, pend_flag, pend_val);
+          pend_flag = -1;
+        }
+      }
+      for (int c = 0; c < npre; ++c) inflight |= 1u << ((seq + (uint32_t)c) % WSLOTS);
+      go = __shfl_sync(0xffffffffu, go, 0);
+      __syncwarp();  // lane 0's acquires are seen by the lanes that read C or the partial directly
+      if (go == 0) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      const bool row_ok = lane < rows_here;
+      const int64_t grow = row0 + lane;
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + buf * TILE_N;
+#pragma unroll 1
+      for (int c = 0; c < nch; ++c) {
+        float acc[32];
+        if (tl.k_blocks > 0) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tbase + c * XCOLS, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(v[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+        }
+        if (c == nch - 1) {
+          // the accumulator has been read: hand the TMEM buffer back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (CG == 2)
+              mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * buf, 0));  // the even CTA's barrier
+            else
+              mbar_arrive(bar_tempty + 8 * buf);
+          }
+        }
+        const int ncols = tl.cols_valid - c * XCOLS < XCOLS ? tl.cols_valid - c * XCOLS : XCOLS;
+        if (!staged) {
+          if (row_ok) {
+            const float* xs = cep ? p.R + (src_row0 + lane) * p.g.blk_n + src_col0 + c * XCOLS
+                                  : p.X + grow * p.g.N + tl.out_col + c * XCOLS;
+            float* xd = (cep ? p.S : p.X) + (dst_row0 + lane) * xd_pitch + dst_col0 + c * XCOLS;
+            epilogue_row_chunk(p, tl, grow, tl.out_col + c * XCOLS, ncols, acc, xs, xd);
+          }
+          continue;
+        }
+        const uint32_t g = seq + (uint32_t)c, sl = g % WSLOTS;
+        // a box whose rows and columns are all inside the tile (and its shard) goes out by TMA
+        const bool tma_ok = rows_here == WROWS && ncols == XCOLS;
+        float src[32];
+        if (has_src) {
+          mbar_wait(p, wbar + 8 * sl, (ph >> sl) & 1u, 0x500000u | (uint32_t)(q * WSLOTS) | sl);
+          ph ^= 1u << sl;
+          inflight &= ~(1u << sl);
+          staged_read_row(wb + sl * WBUF, lane, src_f32, p.beta, src);
+        } else if (red && !tma_ok && row_ok) {
+          // a ragged box of a reducing tile: load, add and store it directly
+          const float* x = p.X + grow * p.g.N + tl.out_col + c * XCOLS;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) src[i] = i < ncols ? __ldcg(x + i) : 0.f;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) src[i] = 0.f;
+        }
+        float out[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) out[i] = fmaf(p.alpha, acc[i], src[i]);
+        if (p.bias) add_bias(p, tl.out_col + c * XCOLS, ncols, out);
+        if (tma_ok) {
+          // the slot is free: every lane has read its source row, or (no source)
+          // the store of chunk g - WSLOTS, bulk group g - WSLOTS, has read it
+          if (!has_src && lane == 0) bulk_wait_read<WSLOTS - 1>();
+          __syncwarp();
+          staged_write_row(wb + sl * WBUF, lane, dst_f32, out);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (red)
+              tma_reduce_add_2d(dst_map, wb_addr + sl * WBUF, (int32_t)(dst_col0 + c * XCOLS), (int32_t)dst_row0);
+            else
+              tma_store_2d(dst_map, wb_addr + sl * WBUF, (int32_t)(dst_col0 + c * XCOLS), (int32_t)dst_row0);
+          }
+        } else if (row_ok) {
+          float* xp = nullptr;  // the partial's plain-store address (send buffer or X)
+          if (tl.dst == DST_X) xp = (cep ? p.S : p.X) + (dst_row0 + lane) * xd_pitch + dst_col0 + c * XCOLS;
+          store_row_chunk(p, tl, grow, tl.out_col + c * XCOLS, ncols, out, xp);
+        }
+        if (lane == 0) bulk_commit();  // bulk group g (empty when the chunk went out by plain stores)
+        if (has_src && c + WPRE < nch) {
+          // chunk c + WPRE goes to the slot of chunk c - 1, whose store is the
+          // group before the one just committed
+          const uint32_t sn = (g + WPRE) % WSLOTS;
+          __syncwarp();  // every lane has read chunk c - 1's source from that slot
+          if (lane == 0) {
+            bulk_wait_read<1>();
+            mbar_arrive_expect_tx(wbar + 8 * sn, src_f32 ? WBUF : WBUF / 2);
+            tma_load_2d(wb_addr + sn * WBUF, src_map, wbar + 8 * sn, (int32_t)(src_col0 + (c + WPRE) * XCOLS),
+                        (int32_t)src_row0);
+          }
+          inflight |= 1u << sn;
+        }
+      }
+      if (staged) seq += (uint32_t)nch;
+      if (p.d_done && tl.dst == DST_D) {
+        // count this quarter tile of D as finished: its bulk and plain stores
+        // complete and fenced first (the device-to-host stream waits on it)
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+          bulk_wait<0>();
+          fence_proxy_async_global();
+          __threadfence();
+          atomicAdd(p.d_done + (int64_t)tl.s * p.g.P + tl.r, 1u);
+        }
+      }
+      if (cep && tl.dst == DST_X) {
+        // count this quarter tile as written to the send buffer (the copy stream waits on it)
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+          bulk_wait<0>();
+          fence_proxy_async_global();
+          __threadfence();
+          const int64_t fd = ((tl.r * p.g.P + tl.s) * p.g.L + tl.l) * p.g.tiles_m + tl.band;
+          atomicAdd(p.done + fd, 1u);
+        }
+      }
+      if (tflag >= 0 && tl.dst == DST_X) {
+        const uint32_t val = p.epoch * (uint32_t)p.g.P + (uint32_t)tl.s;
+        const bool all_bulk = staged && rows_here == WROWS && (tl.cols_valid % XCOLS) == 0;
+        if (all_bulk) {
+          // hand the partial on later, once the bulk stores are surely done
+          pend_flag = tflag;
+          pend_val = val;
+        } else {
+          // plain stores from the lanes: fence, gather, release now
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) {
+            bulk_wait<0>();
+            fence_proxy_async_global();
+            st_release_u32(p.flags + tflag, val);
+          }
+        }
+      }
+    }
+    if (lane == 0) {
+      if (pend_flag >= 0) release_partial(p, pend_flag, pend_val);
+      bulk_wait<0>();  // no bulk store may outlive the CTA
+      if (aborted)     // nor a source load that was issued but never consumed
+        for (uint32_t sl = 0; sl < (uint32_t)WSLOTS; ++sl)
+          if ((inflight >> sl) & 1u) mbar_settle(wbar + 8 * sl, (ph >> sl) & 1u);
+    }
   } else {
     // ---------------------------------------------------------- epilogue
     const int et = threadIdx.x - 64;  // 0..127
@@ -1033,7 +1312,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
       // Staged tiles need 16-byte aligned TMA column coordinates (8 bf16); fp8
       // results go out by direct stores.
       const bool staged = EPI == 1 && (tl.out_col & 7) == 0 && !(p.out_fp8 && tl.dst == DST_D);
-      const bool has_src = staged && tl.src != SRC_NONE;
+      // a middle step of an in-place RS run may add its product into the
+      // partial by TMA reduction instead of loading, adding and storing it
+      const bool red = p.rs_reduce != 0 && staged && p.g.ce_partials == 0 && tl.src == SRC_X && tl.dst == DST_X;
+      const bool has_src = staged && tl.src != SRC_NONE && !red;
       // Where the rotating partial is read and written: the shared partial X
       // (in-place hand-off), or, with copy-engine hand-off, this rank's receive
       // and send buffers.
@@ -1136,11 +1418,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           }
           continue;
         }
+        // A whole chunk inside the tile (and inside its shard) goes out by TMA.
+        const bool tma_ok = rows_here >= ROWS_PER_CTA && ncols == XCOLS;
         float src[32];
         if (has_src) {
           const uint32_t idx = nload + c, sb = idx & 1;
           mbar_wait(p, bar_xfull + 8 * sb, (idx >> 1) & 1, 0x500000u | sb);
           staged_read_row(xsrc + sb * XBUF, row, tl.src == SRC_X, p.beta, src);
+        } else if (red && !tma_ok && row_ok) {
+          // a ragged chunk of a reducing tile: load, add and store it directly
+          const float* x = p.X + grow * p.g.N + tl.out_col + c * XCOLS;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) src[i] = i < ncols ? __ldcg(x + i) : 0.f;
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) src[i] = 0.f;
@@ -1149,8 +1438,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
 #pragma unroll
         for (int i = 0; i < 32; ++i) out[i] = fmaf(p.alpha, acc[i], src[i]);
         if (p.bias) add_bias(p, tl.out_col + c * XCOLS, ncols, out);
-        // A whole chunk inside the tile (and inside its shard) goes out by TMA.
-        const bool tma_ok = rows_here >= ROWS_PER_CTA && ncols == XCOLS;
         // barrier A: every thread is done with the source buffer, and the
         // store that used this destination buffer two chunks ago has read it
         if (et == 0 && tma_ok) bulk_wait_read<1>();
@@ -1161,7 +1448,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           fence_proxy_async_smem();
           named_bar_sync(1, EPI_THREADS);  // barrier B: the chunk is complete in shared memory
           if (et == 0) {
-            if (tl.dst == DST_X)
+            if (red)
+              tma_reduce_add_2d(xdst_map, xdst_addr + db * XBUF, (int32_t)(xd_col0 + c * XCOLS), (int32_t)xd_row0);
+            else if (tl.dst == DST_X)
               tma_store_2d(xdst_map, xdst_addr + db * XBUF, (int32_t)(xd_col0 + c * XCOLS), (int32_t)xd_row0);
             else
               tma_store_2d(&p.tmD, xdst_addr + db * XBUF, (int32_t)(tl.out_col + c * XCOLS), (int32_t)row0);

@@ -178,7 +178,8 @@ def test_tile_order_simulator(L, sched, tp, shape, cg):
     _simulate(plan, m, n, k, l, tp, sched)
     if sched >= 2 and tp > 1:
         info = plan.info()
-        assert info["n_flags"] == l * tp * info["tiles_m"] * info["tiles_n"] * cg
+        assert info["flag_parts"] == (4 if info["epilogue"] == 2 else 1)
+        assert info["n_flags"] == l * tp * info["tiles_m"] * info["tiles_n"] * cg * info["flag_parts"]
 
 
 def test_ag_flag_indices_follow_copy_order(L):
@@ -375,3 +376,43 @@ def test_run_host_argument_checks_without_gpu(L):
     assert p.run_host(16, 16, None, None, 16, 16, 16, None, 16, 256, raise_on_error=False) == dg.ERR_ARG
     q = dg.Plan(256, 256, 256, 1, 2, dg.AG_ROTATING_A)
     assert q.run_host(16, 16, None, None, 16, None, 16, None, 16, 256, raise_on_error=False) == dg.ERR_ARG
+
+
+@pytest.mark.parametrize("group_m", [1, 3, 8, 1000])
+@pytest.mark.parametrize("sched", [0, 1, 2, 3])
+def test_tile_order_simulator_raster_groups(L, sched, group_m):
+    # any raster group height walks every tile of every block exactly once
+    m, n, k, l, tp = 1280, 1536, 512, 2, 4
+    plan = dg.Plan(m, n, k, l, tp, sched, 1.0, 0.5)
+    plan.set_option(dg.OPT_GROUP_M, group_m)
+    _simulate(plan, m, n, k, l, tp, sched)
+    with pytest.raises(dg.DGError):
+        plan.set_option(dg.OPT_GROUP_M, -1)
+
+
+def test_rs_reduce_and_epilogue_option_rules(L):
+    p = dg.Plan(1024, 1024, 1024, 1, 8, dg.RS_TILING_A_ROTATING_C)
+    assert p.info()["epilogue"] == 1                  # one loading step in eight: per-CTA staging
+    flags_staged = p.info()["n_flags"]
+    p.set_option(dg.OPT_RS_REDUCE, 1)
+    assert p.info()["n_flags"] == flags_staged
+    p.set_option(dg.OPT_EPILOGUE, 2)                  # per-warp epilogue:
+    assert p.info()["n_flags"] == 4 * flags_staged    # hand-offs are flagged per warp quarter
+    with pytest.raises(dg.DGError):
+        p.set_option(dg.OPT_RS_REDUCE, 2)
+    p.set_option(dg.OPT_RS_REDUCE, -1)
+    # the per-warp epilogue where at least half the steps load a source
+    assert dg.Plan(1024, 1024, 1024, 1, 4, dg.RS_TILING_B_ROTATING_C, 0.5, 1.0).info()["epilogue"] == 2
+    assert dg.Plan(1024, 1024, 1024, 1, 4, dg.RS_TILING_B_ROTATING_C, 0.5, 0.0).info()["epilogue"] == 1
+    assert dg.Plan(1024, 1024, 1024, 1, 2, dg.RS_TILING_A_ROTATING_C).info()["epilogue"] == 2
+    d = dg.Plan(1024, 1024, 1024, 1, 4, dg.RS_TILING_A_ROTATING_C)
+    d.set_option(dg.OPT_EPILOGUE, 0)
+    d.set_option(dg.OPT_RS_REDUCE, 1)                 # the reduction needs a staged epilogue
+    assert d.info()["epilogue"] == 1
+    q = dg.Plan(1024, 1024, 1024, 1, 4, dg.AG_ROTATING_A)
+    with pytest.raises(dg.DGError):
+        q.set_option(dg.OPT_RS_REDUCE, 1)
+    for v in (0, 1, 2):
+        q.set_option(dg.OPT_EPILOGUE, v)
+    with pytest.raises(dg.DGError):
+        q.set_option(dg.OPT_EPILOGUE, 3)

@@ -179,7 +179,7 @@ def test_single_sm_tiles_vs_oracle(sched, tp):
         assert torch.equal(D.view(torch.int16), ref.view(torch.int16))
 
 
-@pytest.mark.parametrize("epi", [0, 1])
+@pytest.mark.parametrize("epi", [0, 1, 2])
 @pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
 @pytest.mark.parametrize("shape", [(1024, 2048, 512, 2), (392, 776, 320, 2)], ids=lambda s: "x".join(map(str, s)))
 def test_both_epilogues_vs_oracle(sched, epi, shape):
@@ -202,7 +202,7 @@ def test_both_epilogues_vs_oracle(sched, epi, shape):
 
 @pytest.mark.parametrize("sched", [dg.RS_TILING_A_ROTATING_C, dg.RS_TILING_B_ROTATING_C],
                          ids=lambda s: dg.SCHEDULE_NAMES[s])
-@pytest.mark.parametrize("epi", [0, 1])
+@pytest.mark.parametrize("epi", [0, 1, 2])
 def test_rs_nonfused_baseline_vs_oracle(sched, epi):
     # SERIAL on an RS plan: per-rank partial GEMMs, then the separate reduction
     m, n, k, l, tp = 1024, 1024, 1024, 2, 4
@@ -331,3 +331,69 @@ def test_one_row_and_eight_column_shards(sched, cg):
     if sched in (dg.AG_ROTATING_A, dg.AG_ROTATING_B):
         ref, _ = Runner(m, n, k, l, 1, sched, 0.5, 1.0, options={dg.OPT_CTA_GROUP: cg}).run(A, B, C)
         assert torch.equal(D.view(torch.int16), ref.view(torch.int16))
+
+
+@pytest.mark.parametrize("cg", [1, 2])
+@pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_per_warp_epilogue_same_bits_as_staged(sched, cg):
+    # the per-warp epilogue computes every element the same way (one fmaf of the accumulator and
+    # its source, the same hand-off order), so D matches the per-CTA staged epilogue bit for bit,
+    # on full and ragged tiles, with and without C
+    for m, n, k, l in [(1024, 2048, 512, 2), (392, 776, 320, 2), (1000, 1096, 256, 1)]:
+        for tp in (1, 4):
+            if not _shape_ok(sched, m, n, k, tp):
+                continue
+            a, b, c = host_inputs(m, n, k, l, seed=90 + tp + 10 * sched)
+            A, B, C = to_dev(a), to_dev(b), to_dev(c)
+            for alpha, beta in [(1.0, 0.0), (0.5, 1.0)]:
+                out = {}
+                for epi in (1, 2):
+                    r = Runner(m, n, k, l, tp, sched, alpha, beta,
+                               options={dg.OPT_EPILOGUE: epi, dg.OPT_CTA_GROUP: cg})
+                    out[epi], _ = r.run(A, B, C if beta else None)
+                assert torch.equal(out[1].view(torch.int16), out[2].view(torch.int16)), (m, n, tp, alpha, beta)
+                assert rel_err(out[2], oracle_full(a, b, c, alpha, beta)) <= TOL
+
+
+@pytest.mark.parametrize("epi", [1, 2])
+@pytest.mark.parametrize("cg", [1, 2])
+@pytest.mark.parametrize("sched", [dg.RS_TILING_A_ROTATING_C, dg.RS_TILING_B_ROTATING_C],
+                         ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_rs_reduction_into_the_partial_vs_oracle(sched, cg, epi):
+    # middle steps add their product into the rotating partial by TMA reductions; ragged boxes
+    # load, add and store directly; repeated runs give the same bits (the hand-off order is fixed)
+    for m, n, k, l in [(1024, 2048, 512, 2), (392, 776, 320, 2), (1000, 1096, 256, 1)]:
+        for tp in (2, 4, 8):
+            if not _shape_ok(sched, m, n, k, tp):
+                continue
+            a, b, c = host_inputs(m, n, k, l, seed=95 + tp + 10 * sched)
+            A, B, C = to_dev(a), to_dev(b), to_dev(c)
+            for alpha, beta in [(1.0, 0.0), (0.5, 1.0)]:
+                r = Runner(m, n, k, l, tp, sched, alpha, beta,
+                           options={dg.OPT_RS_REDUCE: 1, dg.OPT_CTA_GROUP: cg, dg.OPT_EPILOGUE: epi})
+                D, _ = r.run(A, B, C if beta else None)
+                assert rel_err(D, oracle_full(a, b, c, alpha, beta)) <= TOL, (m, n, tp, alpha, beta)
+                D2, _ = r.run(A, B, C if beta else None)
+                assert torch.equal(D.view(torch.int16), D2.view(torch.int16))
+
+
+@pytest.mark.parametrize("epi", [1, 2])
+@pytest.mark.parametrize("sched", [dg.RS_TILING_A_ROTATING_C, dg.RS_TILING_B_ROTATING_C],
+                         ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_rs_reduction_same_bits_when_alpha_is_a_power_of_two(sched, epi):
+    # alpha' * acc is exact for alpha' = 2^e, so the L2's round-to-nearest add of it to the
+    # partial gives the bits of fmaf(alpha', acc, partial): the automatic choice relies on it
+    for m, n, k, l in [(1024, 2048, 1024, 2), (392, 776, 320, 2)]:
+        for tp in (4, 8):
+            if not _shape_ok(sched, m, n, k, tp):
+                continue
+            a, b, c = host_inputs(m, n, k, l, seed=97 + tp + 10 * sched)
+            A, B, C = to_dev(a), to_dev(b), to_dev(c)
+            for alpha, beta in [(1.0, 0.0), (0.5, 1.0), (-0.25, 0.75)]:
+                out = {}
+                for red in (0, 1, -1):
+                    r = Runner(m, n, k, l, tp, sched, alpha, beta,
+                               options={dg.OPT_RS_REDUCE: red, dg.OPT_EPILOGUE: epi})
+                    out[red], _ = r.run(A, B, C if beta else None)
+                for red in (1, -1):
+                    assert torch.equal(out[0].view(torch.int16), out[red].view(torch.int16)), (m, tp, alpha, red)
