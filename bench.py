@@ -362,6 +362,15 @@ def timed_loop(run, steps, warmup, stream, flush=None):
     return sum(s.elapsed_time(e) for s, e in ev) / steps
 
 
+def copy_in_pieces(dst, src, piece_bytes=64 << 20):
+    """dst.copy_(src) as copies of at most ``piece_bytes`` (flat views): copy engines take
+    copies in issue order, so one multi-GB host copy would hold up the shard transfers."""
+    d, s_ = dst.view(-1), src.view(-1)
+    step = max(1, piece_bytes // d.element_size())
+    for i in range(0, d.numel(), step):
+        d[i:i + step].copy_(s_[i:i + step], non_blocking=True)
+
+
 def e2e_pipelined(plan, ws, main, copy, A_h, B_h, C_h, A0, B0, C0, D0, steps):
     """End-to-end with two buffer sets: every step uploads its inputs from
     pinned host memory, runs, and downloads its D, but step i+1's upload and
@@ -388,10 +397,10 @@ def e2e_pipelined(plan, ws, main, copy, A_h, B_h, C_h, A0, B0, C0, D0, steps):
         A, B, C, D = bufs[b]
         up.wait_event(ran[b])
         with torch.cuda.stream(up):
-            A.copy_(A_h, non_blocking=True)
-            B.copy_(B_h, non_blocking=True)
+            copy_in_pieces(A, A_h)
+            copy_in_pieces(B, B_h)
             if C is not None:
-                C.copy_(C_h, non_blocking=True)
+                copy_in_pieces(C, C_h)
         landed[b].record(up)
         main.wait_event(landed[b])
         main.wait_event(fetched[b])
@@ -399,7 +408,7 @@ def e2e_pipelined(plan, ws, main, copy, A_h, B_h, C_h, A0, B0, C0, D0, steps):
         ran[b].record(main)
         down.wait_event(ran[b])
         with torch.cuda.stream(down):
-            D_h[b].copy_(D, non_blocking=True)
+            copy_in_pieces(D_h[b], D)
         fetched[b].record(down)
     main.wait_event(fetched[0])
     main.wait_event(fetched[1])
@@ -530,8 +539,13 @@ def run_dg(args, rank, world, dist):
             plan.run_host(A_h, B_h, C_h, None, D_h, A, B, C, D, ws, main, copy)
 
         e2e_steps = max(2, min(args.steps, 5))
-        ms_e2e = timed_loop(run_e2e, e2e_steps, 3, main)
-        plan.check(ws, main)
+        with ClockSampler(local) as clk_e2e:
+            ms_e2e = timed_loop(run_e2e, e2e_steps, 3, main)
+            plan.check(ws, main)
+            # the device-only run right after, in the same thermal and power state: what the
+            # end-to-end call adds beyond the kernel is the host link's share
+            ms_dev_after = timed_loop(run, e2e_steps, 0, main)
+            plan.check(ws, main)
         # the machine's host link on these buffers (it differs between boxes and sets the e2e floor)
         link = {}
         for name, dst, src in (("h2d_gbs", B, B_h), ("d2h_gbs", D_h, D)):
@@ -539,6 +553,7 @@ def run_dg(args, rank, world, dist):
             link[name] = round(src.numel() * src.element_size() / t / 1e6, 1)
         e2e = {"value": None, "unit": "TFLOP/s", "ms_per_step": ms_e2e, "steps": e2e_steps,
                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": D.numel() * D.element_size(), "link": link,
+               "clocks": clk_e2e.summary(), "device_ms_after": round(ms_dev_after, 4),
                "mode": "one dg_run_host call per step: inputs uploaded and D downloaded inside the call "
                        "(per-rank uploads gate the kernel's tiles, finished D blocks download during the run)"}
         if not args.no_e2e_pipelined:

@@ -311,8 +311,10 @@ int layout(dg_plan_s* p) {
 }
 
 // Wave gate (auto): AG plans whose wave of co-resident tiles touches more
-// full-K operand strips than about three quarters of L2 holds.  Tiles that
-// share a strip then drift apart by more than its L2 lifetime unless the CTAs
+// full-K operand strips than about three quarters of L2 holds, or more than
+// about three eighths when a wave spans every tile row of its block (then
+// every wave re-reads all of the block's row strips).  Tiles that share a
+// strip otherwise drift apart by more than its L2 lifetime unless the CTAs
 // start each wave together.
 bool wave_sync_on(const dg_plan_s* p) {
   if (p->wave_sync >= 0) return p->wave_sync == 1;
@@ -324,7 +326,8 @@ bool wave_sync_on(const dg_plan_s* p) {
   const double wn = std::min((double)g.tiles_n * g.L, (double)units / wm);
   const double strip = (double)g.BN * (double)p->k * (double)p->esz;  // 256 rows x K elements
   const double footprint = (wm + wn) * strip;
-  return footprint > 96.0 * 1024 * 1024;
+  const double mib = 1024.0 * 1024.0;
+  return footprint > 96.0 * mib || (g.tiles_m <= g.group_m && footprint > 48.0 * mib);
 }
 
 int rt_init(dg_plan_s* p) {
@@ -875,11 +878,22 @@ int ensure_io(dg_plan_s* p) {
   return DG_OK;
 }
 
-// `rows` rows of `width` bytes at row pitch `pitch` (the same on both sides).
+// `rows` rows of `width` bytes at row pitch `pitch` (the same on both sides),
+// as copies of at most kHostCopyBytes each.  Copy engines take copies in the
+// order they were issued, so a shard transfer (or a download) queued behind
+// one host copy of hundreds of MB waits for all of it while the kernel waits
+// for that transfer; bounded pieces let the others in between.
+constexpr size_t kHostCopyBytes = size_t(64) << 20;
+
 int copy_rows(void* dst, const void* src, size_t pitch, size_t width, size_t rows, cudaMemcpyKind kind,
               cudaStream_t st) {
   if (width == 0 || rows == 0) return DG_OK;
-  DG_CUDA(cudaMemcpy2DAsync(dst, pitch, src, pitch, width, rows, kind, st));
+  const size_t step = std::max<size_t>(1, kHostCopyBytes / std::max<size_t>(pitch, 1));
+  for (size_t r0 = 0; r0 < rows; r0 += step) {
+    const size_t n = std::min(step, rows - r0);
+    DG_CUDA(cudaMemcpy2DAsync(static_cast<uint8_t*>(dst) + r0 * pitch, pitch,
+                              static_cast<const uint8_t*>(src) + r0 * pitch, pitch, width, n, kind, st));
+  }
   return DG_OK;
 }
 
