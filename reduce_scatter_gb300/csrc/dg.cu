@@ -356,6 +356,10 @@ int rt_init(dg_plan_s* p) {
   DG_SMEM_ATTR(2, 2, 0);
   DG_SMEM_ATTR(1, 2, 1);
   DG_SMEM_ATTR(2, 2, 1);
+  DG_SMEM_ATTR(1, 3, 0);
+  DG_SMEM_ATTR(2, 3, 0);
+  DG_SMEM_ATTR(1, 3, 1);
+  DG_SMEM_ATTR(2, 3, 1);
 #undef DG_SMEM_ATTR
   {
     cudaLaunchConfig_t cfg = {};
@@ -376,7 +380,10 @@ int rt_init(dg_plan_s* p) {
     int ncl2 = 0;
     cfg.dynamicSmemBytes = dg::Cfg<2, 2>::SMEM_BYTES;
     DG_CUDA(cudaOccupancyMaxActiveClusters(&ncl2, dg::dg_gemm_kernel<2, 2, 0>, &cfg));
-    p->max_pairs = std::min(std::min(ncl0, ncl1), ncl2);
+    int ncl3 = 0;
+    cfg.dynamicSmemBytes = dg::Cfg<2, 3>::SMEM_BYTES;
+    DG_CUDA(cudaOccupancyMaxActiveClusters(&ncl3, dg::dg_gemm_kernel<2, 3, 0>, &cfg));
+    p->max_pairs = std::min(std::min(ncl0, ncl1), std::min(ncl2, ncl3));
   }
   DG_CUDA(cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming));
   DG_CUDA(cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming));
@@ -663,7 +670,11 @@ int launch_kp(dg_plan_s* p, const dg::KParams& kp, cudaStream_t st) {
     grid = std::min<int64_t>(grid, tiles);
     if (grid <= 0) return DG_OK;
     const bool f8 = p->esz == 1;
-    if (p->epi == 2 && f8)
+    if (p->epi == 3 && f8)
+      dg::dg_gemm_kernel<1, 3, 1><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 3>::SMEM_BYTES, st>>>(kp);
+    else if (p->epi == 3)
+      dg::dg_gemm_kernel<1, 3, 0><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 3>::SMEM_BYTES, st>>>(kp);
+    else if (p->epi == 2 && f8)
       dg::dg_gemm_kernel<1, 2, 1><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 2>::SMEM_BYTES, st>>>(kp);
     else if (p->epi == 2)
       dg::dg_gemm_kernel<1, 2, 0><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 2>::SMEM_BYTES, st>>>(kp);
@@ -690,14 +701,19 @@ int launch_kp(dg_plan_s* p, const dg::KParams& kp, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
   cfg.blockDim = dim3(dg::NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = p->epi == 2   ? dg::Cfg<2, 2>::SMEM_BYTES
+  cfg.dynamicSmemBytes = p->epi == 3   ? dg::Cfg<2, 3>::SMEM_BYTES
+                         : p->epi == 2 ? dg::Cfg<2, 2>::SMEM_BYTES
                          : p->epi == 1 ? dg::Cfg<2, 1>::SMEM_BYTES
                                        : dg::Cfg<2, 0>::SMEM_BYTES;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const bool f8 = p->esz == 1;
-  if (p->epi == 2 && f8)
+  if (p->epi == 3 && f8)
+    DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 3, 1>, kp));
+  else if (p->epi == 3)
+    DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 3, 0>, kp));
+  else if (p->epi == 2 && f8)
     DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 2, 1>, kp));
   else if (p->epi == 2)
     DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 2, 0>, kp));
@@ -1307,7 +1323,11 @@ int dg_plan_scaled(dg_plan_t* out, int64_t m, int64_t n, int64_t k, int64_t l, i
   // (the last step the partial, the first beta * C) take the per-warp staged
   // epilogue, whose loads run further ahead; with fewer such steps the
   // per-CTA one, whose larger boxes store the others' results faster.
-  if (is_ag(schedule))
+  // bf16 AG plans with beta = 0 read no source at all: staging for the stores
+  // alone leaves room for one more operand stage.
+  if (is_ag(schedule) && esz == 2 && beta == 0.f)
+    p->epi = 3;
+  else if (is_ag(schedule))
     p->epi = (esz == 1 || k >= 16384) ? 1 : 0;
   else
     p->epi = (1 + (beta != 0.f ? 1 : 0)) * 2 >= tp ? 2 : 1;
@@ -1430,8 +1450,9 @@ int dg_set_option(dg_plan_t p, int option, int64_t value) {
       p->l2_hint = (uint32_t)value;
       return DG_OK;
     case DG_OPT_EPILOGUE:
-      if (value < 0 || value > 2)
-        return fail(DG_ERR_ARG, "epilogue must be 0 (direct), 1 (staged) or 2 (staged per warp)");
+      if (value < 0 || value > 3)
+        return fail(DG_ERR_ARG,
+                    "epilogue must be 0 (direct), 1 (staged), 2 (staged per warp) or 3 (staged stores only)");
       if (p->epoch != 0) return fail(DG_ERR_STATE, "the epilogue is fixed after the first run");
       p->epi = (int)value;
       layout(p);

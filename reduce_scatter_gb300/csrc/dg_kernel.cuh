@@ -91,8 +91,13 @@ struct Cfg {
   static constexpr uint32_t A_BYTES = A_ROWS * KROW_BYTES;
   static constexpr uint32_t B_BYTES = B_ROWS * KROW_BYTES;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = CG == 1 ? (EPI ? 3 : 4) : (EPI ? 5 : 6);
-  static constexpr uint32_t STAGING_BYTES = EPI ? 4 * XBUF : 0;  // 2 source + 2 destination chunks
+  // EPI = 3 (staged stores only): the staged epilogue without its source
+  // chunks (plans that read no source: AG with beta = 0), which gives their
+  // 32 KB back to the operand ring.
+  static constexpr bool SRC_STAGING = EPI == 1 || EPI == 2;
+  static constexpr int STAGES = CG == 1 ? (SRC_STAGING ? 3 : 4) : (SRC_STAGING ? 5 : 6);
+  static constexpr uint32_t STAGING_BYTES =
+      SRC_STAGING ? 4 * XBUF : (EPI == 3 ? 2 * XBUF : 0);  // [2 source +] 2 destination chunks
   static constexpr uint32_t SMEM_BYTES =
       STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 512 /*barriers*/;
 };
@@ -800,8 +805,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   // staged epilogue: source chunks [2] then destination chunks [2], 1024-aligned
+  // (stores-only staging: destination chunks alone)
   uint8_t* xsrc = smem + STAGES * C::STAGE_BYTES;
-  uint8_t* xdst = xsrc + 2 * XBUF;
+  uint8_t* xdst = EPI == 3 ? xsrc : xsrc + 2 * XBUF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES + C::STAGING_BYTES);
   // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, xfull[2], wfull[16]
   const uint32_t bar_full = smem_u32(bars);
@@ -1311,7 +1317,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
       const int nch = (tl.cols_valid + XCOLS - 1) / XCOLS;
       // Staged tiles need 16-byte aligned TMA column coordinates (8 bf16); fp8
       // results go out by direct stores.
-      const bool staged = EPI == 1 && (tl.out_col & 7) == 0 && !(p.out_fp8 && tl.dst == DST_D);
+      // (stores-only staging takes no source: a tile with one goes the direct way)
+      const bool staged = (EPI == 1 || (EPI == 3 && tl.src == SRC_NONE)) && (tl.out_col & 7) == 0 &&
+                          !(p.out_fp8 && tl.dst == DST_D);
       // a middle step of an in-place RS run may add its product into the
       // partial by TMA reduction instead of loading, adding and storing it
       const bool red = p.rs_reduce != 0 && staged && p.g.ce_partials == 0 && tl.src == SRC_X && tl.dst == DST_X;
@@ -1471,11 +1479,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
       if (p.d_done && tl.dst == DST_D) {
         // count this half tile of D as finished: its bulk and plain stores
         // complete and fenced first (the device-to-host stream waits on it)
-        if (EPI == 1 && et == 0) bulk_wait<0>();
+        if (EPI != 0 && et == 0) bulk_wait<0>();
         __threadfence();
         named_bar_sync(1, EPI_THREADS);
         if (et == 0) {
-          if (EPI == 1) fence_proxy_async_global();
+          if (EPI != 0) fence_proxy_async_global();
           __threadfence();
           atomicAdd(p.d_done + (int64_t)tl.s * p.g.P + tl.r, 1u);
         }
@@ -1503,18 +1511,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           pend_val = val;
         } else {
           // plain stores from every thread: fence, gather, release now
-          if (EPI == 1 && et == 0) bulk_wait<0>();
+          if (EPI != 0 && et == 0) bulk_wait<0>();
           __threadfence();
           named_bar_sync(1, EPI_THREADS);
           if (et == 0) {
-            if (EPI == 1) fence_proxy_async_global();
+            if (EPI != 0) fence_proxy_async_global();
             st_release_u32(p.flags + tflag, val);
           }
         }
       }
     }
     if (et == 0 && pend_flag >= 0) release_partial(p, pend_flag, pend_val);
-    if (EPI == 1 && et == 0) {
+    if (EPI != 0 && et == 0) {
       bulk_wait<0>();  // no bulk store may outlive the CTA
       if (aborted)     // nor a source load that was issued but never consumed
         for (uint32_t idx = nsrc > 2u ? nsrc - 2u : 0u; idx < nsrc; ++idx)

@@ -412,7 +412,7 @@ def test_rs_reduce_and_epilogue_option_rules(L):
     q = dg.Plan(1024, 1024, 1024, 1, 4, dg.AG_ROTATING_A)
     with pytest.raises(dg.DGError):
         q.set_option(dg.OPT_RS_REDUCE, 1)
-    for v in (0, 1, 2):
+    for v in (0, 1, 2, 3):
         q.set_option(dg.OPT_EPILOGUE, v)
     with pytest.raises(dg.DGError):
-        q.set_option(dg.OPT_EPILOGUE, 3)
+        q.set_option(dg.OPT_EPILOGUE, 4)

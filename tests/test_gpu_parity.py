@@ -179,7 +179,7 @@ def test_single_sm_tiles_vs_oracle(sched, tp):
         assert torch.equal(D.view(torch.int16), ref.view(torch.int16))
 
 
-@pytest.mark.parametrize("epi", [0, 1, 2])
+@pytest.mark.parametrize("epi", [0, 1, 2, 3])
 @pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
 @pytest.mark.parametrize("shape", [(1024, 2048, 512, 2), (392, 776, 320, 2)], ids=lambda s: "x".join(map(str, s)))
 def test_both_epilogues_vs_oracle(sched, epi, shape):
@@ -202,7 +202,7 @@ def test_both_epilogues_vs_oracle(sched, epi, shape):
 
 @pytest.mark.parametrize("sched", [dg.RS_TILING_A_ROTATING_C, dg.RS_TILING_B_ROTATING_C],
                          ids=lambda s: dg.SCHEDULE_NAMES[s])
-@pytest.mark.parametrize("epi", [0, 1, 2])
+@pytest.mark.parametrize("epi", [0, 1, 2, 3])
 def test_rs_nonfused_baseline_vs_oracle(sched, epi):
     # SERIAL on an RS plan: per-rank partial GEMMs, then the separate reduction
     m, n, k, l, tp = 1024, 1024, 1024, 2, 4
@@ -336,9 +336,9 @@ def test_one_row_and_eight_column_shards(sched, cg):
 @pytest.mark.parametrize("cg", [1, 2])
 @pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
 def test_per_warp_epilogue_same_bits_as_staged(sched, cg):
-    # the per-warp epilogue computes every element the same way (one fmaf of the accumulator and
-    # its source, the same hand-off order), so D matches the per-CTA staged epilogue bit for bit,
-    # on full and ragged tiles, with and without C
+    # the per-warp and the stores-only epilogues compute every element the same way (one fmaf of
+    # the accumulator and its source, the same hand-off order), so D matches the per-CTA staged
+    # epilogue bit for bit, on full and ragged tiles, with and without C
     for m, n, k, l in [(1024, 2048, 512, 2), (392, 776, 320, 2), (1000, 1096, 256, 1)]:
         for tp in (1, 4):
             if not _shape_ok(sched, m, n, k, tp):
@@ -347,11 +347,12 @@ def test_per_warp_epilogue_same_bits_as_staged(sched, cg):
             A, B, C = to_dev(a), to_dev(b), to_dev(c)
             for alpha, beta in [(1.0, 0.0), (0.5, 1.0)]:
                 out = {}
-                for epi in (1, 2):
+                for epi in (1, 2, 3):
                     r = Runner(m, n, k, l, tp, sched, alpha, beta,
                                options={dg.OPT_EPILOGUE: epi, dg.OPT_CTA_GROUP: cg})
                     out[epi], _ = r.run(A, B, C if beta else None)
-                assert torch.equal(out[1].view(torch.int16), out[2].view(torch.int16)), (m, n, tp, alpha, beta)
+                for epi in (2, 3):
+                    assert torch.equal(out[1].view(torch.int16), out[epi].view(torch.int16)), (m, n, tp, alpha, epi)
                 assert rel_err(out[2], oracle_full(a, b, c, alpha, beta)) <= TOL
 
 

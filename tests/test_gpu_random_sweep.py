@@ -31,7 +31,7 @@ def _case(i):
     if sched == 3 and (n // tp) % 8:
         n = 8 * tp * max(1, n // (8 * tp))
     cep = sched >= 2 and tp > 1 and (sched == 2 or (n // tp) % 8 == 0) and bool(rng.integers(0, 2))
-    opts = {dg.OPT_CTA_GROUP: int(rng.integers(1, 3)), dg.OPT_EPILOGUE: int(rng.integers(1, 3)) if cep else int(rng.integers(0, 3))}
+    opts = {dg.OPT_CTA_GROUP: int(rng.integers(1, 3)), dg.OPT_EPILOGUE: int(rng.integers(1, 3)) if cep else int(rng.integers(0, 4))}
     if cep:
         opts[dg.OPT_RS_CE_PARTIALS] = 1
     alpha = float(rng.choice([1.0, 0.5, -1.25]))
