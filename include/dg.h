@@ -215,7 +215,7 @@ enum dg_option {
   DG_OPT_GROUP_M = 18,        /* raster of the tiles inside one (step, rank, batch) block: groups
                                  of this many tile rows, each swept column by column (so the
                                  tiles in flight share operand strips in L2); 0 (default) = auto */
-  DG_OPT_RS_REDUCE = 19       /* RS plans, before the first run: how the tiles of the middle steps
+  DG_OPT_RS_REDUCE = 19,      /* RS plans, before the first run: how the tiles of the middle steps
                                  (0 < s < tp - 1) update the rotating partial.  1 = add
                                  alpha' * product into it by TMA reductions (fp32 adds performed
                                  at the L2; alpha' = alpha * scale_a * scale_b, / tp for the
@@ -226,6 +226,14 @@ enum dg_option {
                                  a power of two the partial takes two roundings per step.
                                  0 = load, fmaf, store.  -1 (default) = 1 where it gives the
                                  same bits as 0 (alpha' a power of two or zero, no bias), else 0 */
+  DG_OPT_MULTICAST = 20       /* 256 x 256 pair tiles: 1 = clusters of two CTA pairs that take
+                                 vertically adjacent tiles and share their B rows, each CTA
+                                 loading half of its B rows for both pairs (TMA multicast), a
+                                 quarter less operand traffic from L2 into shared memory; where
+                                 the tile order allows it (every pair of consecutive tiles in one
+                                 block with the same B rows), else as 0; same bits either way.
+                                 0 = independent pairs.  -1 (default) = 1 for AG plans with
+                                 K >= 16384, else 0 */
 };
 
 /* Plan geometry and workspace layout, for callers and tests. */
@@ -248,6 +256,7 @@ typedef struct dg_plan_info {
   int32_t reduce_op;                 /* dg_reduce_op */
   int32_t epilogue;                  /* DG_OPT_EPILOGUE in effect: 0 direct, 1 staged, 2 staged per warp */
   int32_t flag_parts;                /* RS hand-off flags per CTA half tile (4 with the per-warp epilogue) */
+  int32_t multicast;                 /* DG_OPT_MULTICAST in effect and the step-major tile order allows it */
 } dg_plan_info;
 
 /* One tile of the step-major rotation order (host decoder, for tests). */

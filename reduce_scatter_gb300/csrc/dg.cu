@@ -162,6 +162,10 @@ struct dg_plan_s {
   int tile_order = -1;   // DG_OPT_TILE_ORDER: -1 auto, 0 step-major, 1 upload frontier (AG)
   int64_t ce_bands = 0;  // DG_OPT_RS_CE_BANDS: 256-row bands per hand-off copy, 0 auto
   int64_t group_m_req = 0;  // DG_OPT_GROUP_M: tile rows per raster group, 0 auto
+  int multicast = -1;       // DG_OPT_MULTICAST: two CTA pairs per cluster share their B rows (-1 auto)
+  int mc_ok[2] = {-1, -1};  // per block order: every tile pair (2i, 2i + 1) may share (-1 not yet known)
+  int max_quads = 0;        // co-resident clusters of four of the CG = 2 kernels
+  bool map_mc = false;      // the cached B maps have the multicast boxes
   int rs_reduce = -1;       // DG_OPT_RS_REDUCE: middle RS steps add into the partial by TMA reduction
                             // (-1 auto: where that gives the same bits as load, fmaf, store)
   uint64_t id = 0;
@@ -210,6 +214,7 @@ int epi_box_rows(const dg_plan_s* p) { return p->epi == 2 ? dg::WROWS : dg::ROWS
 
 int layout(dg_plan_s* p) {
   dg::Geom& g = p->g;
+  p->mc_ok[0] = p->mc_ok[1] = -1;
   const int64_t P = p->tp;
   g.sched = p->schedule;
   g.P = (int32_t)P;
@@ -330,6 +335,32 @@ bool wave_sync_on(const dg_plan_s* p) {
   return footprint > 96.0 * mib || (g.tiles_m <= g.group_m && footprint > 48.0 * mib);
 }
 
+// Multicast of B rows between the two CTA pairs of a cluster of four: the
+// pairs take tiles 2i and 2i + 1 of the order, so every such pair of tiles
+// must lie in one (step, rank, batch) block and read the same B rows (the
+// grouped raster sweeps even-height groups of tile rows column by column).
+bool multicast_ok(dg_plan_s* p, const dg::Geom& g) {
+  int& ok = p->mc_ok[g.order == 1 ? 1 : 0];
+  if (ok < 0) {
+    ok = p->cg == 2 && g.total_tiles % 2 == 0 && g.tiles_block % 2 == 0;
+    for (int64_t i = 0; ok && i < g.total_tiles / 2; ++i) {
+      const dg::Tile a = dg::decode_tile(g, 2 * i), b = dg::decode_tile(g, 2 * i + 1);
+      ok = a.s == b.s && a.r == b.r && a.l == b.l && a.b_map == b.b_map && a.b_row == b.b_row &&
+           a.k_blocks == b.k_blocks && (g.sched != dg::SCHED_AG_B || a.flag == b.flag);
+    }
+  }
+  return ok == 1;
+}
+
+// Automatic for AG plans with K >= 16384: their long tiles keep the two pairs
+// of a cluster in step cheaply, and their long runs are held to the power
+// limit, where a quarter less L2-to-SM traffic buys clock (+1.5 % on the TP=8
+// AG workloads) that outweighs the SMs clusters of four leave idle (the TP=2
+// shape and the RS plans measured 2-7 % slower with it).
+bool multicast_wanted(const dg_plan_s* p) {
+  return p->multicast == 1 || (p->multicast < 0 && is_ag(p->schedule) && p->k >= 16384);
+}
+
 int rt_init(dg_plan_s* p) {
   if (p->rt) return DG_OK;
   int dev = 0;
@@ -384,6 +415,18 @@ int rt_init(dg_plan_s* p) {
     cfg.dynamicSmemBytes = dg::Cfg<2, 3>::SMEM_BYTES;
     DG_CUDA(cudaOccupancyMaxActiveClusters(&ncl3, dg::dg_gemm_kernel<2, 3, 0>, &cfg));
     p->max_pairs = std::min(std::min(ncl0, ncl1), std::min(ncl2, ncl3));
+    attr[0].val.clusterDim.x = 4;
+    cfg.gridDim = dim3(4 * 256, 1, 1);
+    int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+    cfg.dynamicSmemBytes = dg::Cfg<2, 0>::SMEM_BYTES;
+    DG_CUDA(cudaOccupancyMaxActiveClusters(&q0, dg::dg_gemm_kernel<2, 0, 0>, &cfg));
+    cfg.dynamicSmemBytes = dg::Cfg<2, 1>::SMEM_BYTES;
+    DG_CUDA(cudaOccupancyMaxActiveClusters(&q1, dg::dg_gemm_kernel<2, 1, 0>, &cfg));
+    cfg.dynamicSmemBytes = dg::Cfg<2, 2>::SMEM_BYTES;
+    DG_CUDA(cudaOccupancyMaxActiveClusters(&q2, dg::dg_gemm_kernel<2, 2, 0>, &cfg));
+    cfg.dynamicSmemBytes = dg::Cfg<2, 3>::SMEM_BYTES;
+    DG_CUDA(cudaOccupancyMaxActiveClusters(&q3, dg::dg_gemm_kernel<2, 3, 0>, &cfg));
+    p->max_quads = std::min(std::min(q0, q1), std::min(q2, q3));
   }
   DG_CUDA(cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming));
   DG_CUDA(cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming));
@@ -465,8 +508,8 @@ int build_epi_maps(dg_plan_s* p, const Driver& drv, const void* C, void* D, uint
   return DG_OK;
 }
 
-int build_maps(dg_plan_s* p, const Driver& drv, const void* A, const void* B, uint8_t* ws) {
-  if (p->map_key[0] == A && p->map_key[1] == B && p->map_key[2] == ws) return DG_OK;
+int build_maps(dg_plan_s* p, const Driver& drv, const void* A, const void* B, uint8_t* ws, bool mc) {
+  if (p->map_key[0] == A && p->map_key[1] == B && p->map_key[2] == ws && p->map_mc == mc) return DG_OK;
   std::memset(p->kp.tmA, 0, sizeof(p->kp.tmA));
   std::memset(p->kp.tmB, 0, sizeof(p->kp.tmB));
   const dg::Geom& g = p->g;
@@ -475,7 +518,8 @@ int build_maps(dg_plan_s* p, const Driver& drv, const void* A, const void* B, ui
   p->n_maps = 0;
   // each CTA loads its own rows of the tile: 128 of A; 256 (CG = 1) or 128 (CG = 2) of B
   const int a_box = dg::Cfg<1>::A_ROWS;
-  const int b_box = p->cg == 2 ? dg::Cfg<2>::B_ROWS : dg::Cfg<1>::B_ROWS;
+  // (with multicast each CTA loads half of its B rows for both pairs)
+  const int b_box = mc ? dg::Cfg<2>::B_ROWS / 2 : p->cg == 2 ? dg::Cfg<2>::B_ROWS : dg::Cfg<1>::B_ROWS;
   static_assert(dg::Cfg<2, 0>::B_ROWS == dg::Cfg<2, 1>::B_ROWS, "box rows do not depend on the epilogue");
   if (p->k > 0) {
     if (is_ag(p->schedule)) {
@@ -511,6 +555,7 @@ int build_maps(dg_plan_s* p, const Driver& drv, const void* A, const void* B, ui
   p->map_key[0] = A;
   p->map_key[1] = B;
   p->map_key[2] = ws;
+  p->map_mc = mc;
   return DG_OK;
 }
 
@@ -689,17 +734,19 @@ int launch_kp(dg_plan_s* p, const dg::KParams& kp, cudaStream_t st) {
     DG_CUDA(cudaGetLastError());
     return DG_OK;
   }
-  // CTA pairs: every pair must be co-resident (RS tiles wait on earlier tiles)
-  int64_t pairs = p->grid_req > 0 ? p->grid_req / 2 : p->max_pairs;
-  pairs = std::min<int64_t>(std::min<int64_t>(pairs, p->max_pairs), tiles);
-  if (pairs <= 0) return tiles > 0 ? fail(DG_ERR_UNSUPPORTED, "no co-resident CTA pair") : DG_OK;
+  // CTA pairs: every pair must be co-resident (RS tiles wait on earlier tiles).
+  // With multicast, clusters of two pairs, each cluster taking two tiles at a time.
+  const int csize = kp.mc ? 4 : 2;
+  int64_t units = p->grid_req > 0 ? p->grid_req / csize : (kp.mc ? p->max_quads : p->max_pairs);
+  units = std::min<int64_t>(std::min<int64_t>(units, kp.mc ? p->max_quads : p->max_pairs), kp.mc ? tiles / 2 : tiles);
+  if (units <= 0) return tiles > 0 ? fail(DG_ERR_UNSUPPORTED, "no co-resident CTA cluster") : DG_OK;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = (unsigned)csize;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+  cfg.gridDim = dim3((unsigned)(csize * units), 1, 1);
   cfg.blockDim = dim3(dg::NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = p->epi == 3   ? dg::Cfg<2, 3>::SMEM_BYTES
                          : p->epi == 2 ? dg::Cfg<2, 2>::SMEM_BYTES
@@ -836,6 +883,7 @@ int run_rs_ce(dg_plan_s* p, const Driver& drv, uint8_t* ws, cudaStream_t ms, cud
 int run_rs_serial(dg_plan_s* p, const Driver& drv, const void* C, void* D, uint8_t* ws, cudaStream_t st) {
   p->kser = p->kp;
   p->kser.g = p->gser;
+  p->kser.mc = 0;
   p->kser.X = reinterpret_cast<float*>(ws + p->off_serial);
   p->kser.wait_flags = 0;
   std::memset(&p->kser.tmX, 0, sizeof(CUtensorMap));
@@ -1104,15 +1152,18 @@ int run_impl(dg_plan_s* p, const void* A, const void* B, const dg_bf16_t* C, con
   if (wrap) p->epoch = 0;
   p->epoch += 1;
 
-  rc = build_maps(p, drv, A, B, ws);
-  if (rc) return rc;
-  rc = build_epi_maps(p, drv, C, D, ws);
-  if (rc) return rc;
   dg::KParams& kp = p->kp;
   kp.g = p->g;
   // Upload-frontier block order (AG): asked for, or automatic when this run
   // uploads its inputs rank by rank.
   kp.g.order = is_ag(p->schedule) && (p->tile_order == 1 || (p->tile_order < 0 && io)) ? 1 : 0;
+  // B multicast between pairs (not for the RS baseline's per-rank GEMMs)
+  const bool mc = multicast_wanted(p) && !rs_serial && p->max_quads > 0 && multicast_ok(p, kp.g);
+  kp.mc = mc ? 1u : 0u;
+  rc = build_maps(p, drv, A, B, ws, mc);
+  if (rc) return rc;
+  rc = build_epi_maps(p, drv, C, D, ws);
+  if (rc) return rc;
   kp.C = reinterpret_cast<const __nv_bfloat16*>(C);
   kp.D = D;
   kp.bias = reinterpret_cast<const __nv_bfloat16*>(bias);
@@ -1407,6 +1458,10 @@ int dg_set_option(dg_plan_t p, int option, int64_t value) {
                     "copy kind must be -1 (auto), 0 (copy engine), 1 (1D memcpy) or 2 (copy engine, tall copies)");
       p->copy_kind = (int)value;
       return DG_OK;
+    case DG_OPT_MULTICAST:
+      if (value < -1 || value > 1) return fail(DG_ERR_ARG, "multicast must be -1 (auto), 0 or 1");
+      p->multicast = (int)value;
+      return DG_OK;
     case DG_OPT_RS_REDUCE:
       if (value < -1 || value > 1) return fail(DG_ERR_ARG, "RS reduction must be -1 (auto), 0 or 1");
       if (p->epoch != 0) return fail(DG_ERR_STATE, "the RS reduction is fixed after the first run");
@@ -1500,6 +1555,7 @@ int dg_plan_info_get(dg_plan_t p, dg_plan_info* o) {
   o->a_type = p->a_type, o->b_type = p->b_type, o->elem_bytes = p->esz;
   o->out_type = p->out_type, o->reduce_op = p->reduce_op;
   o->epilogue = p->epi, o->flag_parts = epi_parts(p);
+  o->multicast = multicast_wanted(p) && multicast_ok(p, p->g) ? 1 : 0;
   return DG_OK;
 }
 

@@ -137,6 +137,9 @@ struct KParams {
   uint32_t* wave_ctr;   // per-run counter of tiles whose loads are issued (zeroed per run)
   uint32_t* progress;   // AG copy pacing: progress[s] set to 1 once a producer reaches step s, or null
   uint32_t rs_reduce;   // staged epilogues, in-place RS: middle steps add into the partial by TMA reduction
+  uint32_t mc;          // CTA pairs in clusters of four: the two pairs take tiles 2i and 2i + 1, which
+                        // share their B rows, and each CTA loads half of its B rows for both pairs
+                        // (multicast); B maps then have 64-row boxes
   // Runs that upload their inputs and download D themselves (host buffers):
   // the inputs of a tile are on the device once up_flags[upload_unit(tile)]
   // >= epoch, and d_done[s * P + r] counts the half tiles of D finished for
@@ -381,6 +384,17 @@ __device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtens
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster), "l"(policy)
+      : "memory");
+}
+// The same load multicast to every CTA of `mask` (the same shared-memory
+// offset in each); each destination's bytes are counted on the barrier at
+// mbar's offset in that destination's even (MMA-issuing) CTA.
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                    int32_t x, int32_t y, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster), "h"(mask)
       : "memory");
 }
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
@@ -819,22 +833,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
   const uint32_t bar_wfull = smem_u32(bars + 2 * STAGES + 7);  // [EPI_WARPS * WSLOTS] (EPI = 2)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 7 + EPI_WARPS * WSLOTS);
   volatile uint32_t* s_go = s_tmem + 1;  // [2] epilogue go/abort, by tile parity
-  // [2] K-block loads each CTA of a pair issued (kept in the even CTA's
+  // [4] K-block loads each CTA of the cluster issued (kept in the even CTAs'
   // shared memory, for the exit: every load must land before its CTA exits)
   volatile uint32_t* s_kcnt = s_tmem + 3;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // CTA rank inside the pair (0 for CG = 1); the even CTA issues the MMAs.
+  // CTA rank in the cluster; `half`: which half of the pair's tile this CTA
+  // holds (0 for CG = 1); the even CTA of a pair (`lead`) issues the MMAs.
+  // With multicast (clusters of four) pair `pq` of the cluster takes tile
+  // 2i + pq of the cluster's slot i.
   const uint32_t crank = CG == 2 ? cluster_ctarank() : 0u;
-  const bool leader = crank == 0;
-  const int64_t unit = CG == 2 ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;
-  const int64_t nunits = CG == 2 ? (int64_t)(gridDim.x >> 1) : (int64_t)gridDim.x;
+  const uint32_t half = crank & 1u;
+  const uint32_t lead = crank & ~1u;
+  const bool leader = half == 0;
+  const bool mc = CG == 2 && p.mc != 0;
+  const uint32_t pq = mc ? (crank >> 1) : 0u;
+  const int64_t unit = mc ? (int64_t)(blockIdx.x >> 2) : CG == 2 ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;
+  const int64_t nunits = mc ? (int64_t)(gridDim.x >> 2) : CG == 2 ? (int64_t)(gridDim.x >> 1) : (int64_t)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(bar_full + 8 * i, 1);
-      mbar_init(bar_empty + 8 * i, 1);
+      mbar_init(bar_empty + 8 * i, mc ? 2 : 1);  // with multicast both pairs free a stage
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_tfull + 8 * i, 1);
@@ -865,6 +886,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
   const uint32_t tmem_base = *s_tmem;
 
   const int64_t T = p.g.total_tiles;
+  const int64_t TI = mc ? T / 2 : T;  // tile slots (the host allows multicast only for even T)
   const uint32_t smem_base = smem_u32(smem);
   bool aborted = false;
 
@@ -884,7 +906,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
       uint32_t wave = 0;
       int32_t step_seen = -1;
       uint32_t up_ok = 0;  // ranks whose uploaded inputs this producer has seen
-      for (int64_t t = unit; t < T && ok; t += nunits, ++wave) {
+      for (int64_t i = unit; i < TI && ok; i += nunits, ++wave) {
+        const int64_t t = mc ? 2 * i + pq : i;
         const Tile tl = decode_tile(p.g, t);
         if (p.progress && tl.s != step_seen) {
           // the copies of step s + 1 may start now (paced shard transfers);
@@ -917,8 +940,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
         }
         const CUtensorMap* ma = &p.tmA[tl.a_map];
         const CUtensorMap* mb = &p.tmB[tl.b_map];
-        const int32_t a_row = (int32_t)(tl.a_row + (int64_t)crank * C::A_ROWS);
-        const int32_t b_row = (int32_t)(tl.b_row + (int64_t)crank * C::B_ROWS);
+        const int32_t a_row = (int32_t)(tl.a_row + (int64_t)half * C::A_ROWS);
+        const int32_t b_row = (int32_t)(tl.b_row + (int64_t)half * C::B_ROWS);
         for (int kb = 0; kb < tl.k_blocks; ++kb) {
           if (!mbar_wait(p, bar_empty + 8 * stage, phase ^ 1, 0x100000u | stage)) {
             ok = false;
@@ -927,13 +950,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           const uint32_t fb = bar_full + 8 * stage;
           const uint32_t sa = smem_base + stage * C::STAGE_BYTES;
           if (CG == 2) {
-            const uint32_t fb_lead = mapa_shared(fb, 0);
+            const uint32_t fb_lead = mapa_shared(fb, lead);
             if (leader) mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);  // both CTAs' bytes
             if (hint_a)
               tma_load_2d_pair_hint(sa, ma, fb_lead, kb * kblk, a_row, pol_a);
             else
               tma_load_2d_pair(sa, ma, fb_lead, kb * kblk, a_row);
-            if (hint_b)
+            if (mc)  // this pair's half of the CTA's B rows, for this CTA and its counterpart
+              tma_load_2d_pair_mc(sa + C::A_BYTES + pq * (C::B_BYTES / 2), mb, fb_lead, kb * kblk,
+                                  b_row + (int32_t)(pq * (C::B_ROWS / 2)),
+                                  (uint16_t)((1u << crank) | (1u << (crank ^ 2u))));
+            else if (hint_b)
               tma_load_2d_pair_hint(sa + C::A_BYTES, mb, fb_lead, kb * kblk, b_row, pol_b);
             else
               tma_load_2d_pair(sa + C::A_BYTES, mb, fb_lead, kb * kblk, b_row);
@@ -964,9 +991,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           for (uint32_t n = nloads > (uint32_t)STAGES ? nloads - STAGES : 0u; n < nloads; ++n)
             mbar_settle(bar_full + 8 * (n % STAGES), (n / STAGES) & 1u);
       } else {
-        // the loads of both CTAs are counted on the even CTA's barriers: hand
-        // it this CTA's count (it waits for them before either CTA exits)
-        st_shared_cluster_u32(mapa_shared(smem_u32((const void*)(s_kcnt + crank)), 0), nloads);
+        // the loads landing in a pair are counted on its even CTA's barriers:
+        // hand this CTA's count to the even CTA(s) its loads land in (they
+        // wait for them before any CTA exits)
+        st_shared_cluster_u32(mapa_shared(smem_u32((const void*)(s_kcnt + crank)), lead), nloads);
+        if (mc) st_shared_cluster_u32(mapa_shared(smem_u32((const void*)(s_kcnt + crank)), lead ^ 2u), nloads);
       }
     }
   } else if (warp == 1) {
@@ -975,7 +1004,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
       const uint32_t IDESC = p.idesc;
       uint32_t stage = 0, phase = 0, it = 0;
       bool ok = true;
-      for (int64_t t = unit; t < T && ok; t += nunits, ++it) {
+      for (int64_t i = unit; i < TI && ok; i += nunits, ++it) {
+        const int64_t t = mc ? 2 * i + pq : i;
         const Tile tl = decode_tile(p.g, t);
         const uint32_t buf = it & 1, use = it >> 1;
         if (!mbar_wait(p, bar_tempty + 8 * buf, (use & 1) ^ 1, 0x200000u | buf)) {
@@ -1011,8 +1041,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
                 tc_mma_bf16(d_tmem, ad, bd, IDESC, acc);
             }
           }
-          if (CG == 2)
-            tc_commit_pair_mc(bar_empty + 8 * stage, 0x3);
+          if (CG == 2)  // the stage is free in both CTAs of the pair (of both pairs, with multicast)
+            tc_commit_pair_mc(bar_empty + 8 * stage, mc ? (uint16_t)0xF : (uint16_t)(0x3u << lead));
           else
             tc_commit(bar_empty + 8 * stage);
           if (++stage == STAGES) {
@@ -1022,14 +1052,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
         }
         if (!ok) break;
         if (CG == 2)
-          tc_commit_pair_mc(bar_tfull + 8 * buf, 0x3);
+          tc_commit_pair_mc(bar_tfull + 8 * buf, (uint16_t)(0x3u << lead));
         else
           tc_commit(bar_tfull + 8 * buf);
       }
       if (!ok) {
         aborted = true;
         if (CG == 2)
-          tc_commit_pair_mc(bar_drain, 0x1);
+          tc_commit_pair_mc(bar_drain, (uint16_t)(0x1u << lead));
         else
           tc_commit(bar_drain);
         const uint64_t t0 = globaltimer();
@@ -1054,12 +1084,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
     uint32_t pend_val = 0;
     uint32_t up_ok = 0;
     uint32_t it = 0;
-    for (int64_t t = unit; t < T; t += nunits, ++it) {
+    for (int64_t i = unit; i < TI; i += nunits, ++it) {
       __syncwarp();  // every lane is done with the previous tile's slots before lane 0 reloads them
+      const int64_t t = mc ? 2 * i + pq : i;
       const Tile tl = decode_tile(p.g, t);
       const uint32_t buf = it & 1, use = it >> 1;
-      const int64_t tflag = tl.tile_flag >= 0 ? (tl.tile_flag * CG + crank) * EPI_WARPS + q : -1;
-      const int64_t wrow = (int64_t)crank * ROWS_PER_CTA + q * WROWS;  // this warp's first row in the tile
+      const int64_t tflag = tl.tile_flag >= 0 ? (tl.tile_flag * CG + half) * EPI_WARPS + q : -1;
+      const int64_t wrow = (int64_t)half * ROWS_PER_CTA + q * WROWS;  // this warp's first row in the tile
       int rows_here = tl.rows_valid - (int)wrow;
       rows_here = rows_here < 0 ? 0 : (rows_here > WROWS ? WROWS : rows_here);
       const int64_t row0 = tl.out_row + wrow;
@@ -1172,7 +1203,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           __syncwarp();
           if (lane == 0) {
             if (CG == 2)
-              mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * buf, 0));  // the even CTA's barrier
+              mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * buf, lead));  // the even CTA's barrier
             else
               mbar_arrive(bar_tempty + 8 * buf);
           }
@@ -1308,12 +1339,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
     uint32_t nstore = 0;  // staged destination chunks stored so far (buffer idx & 1)
     uint32_t up_ok = 0;   // ranks whose uploaded C this thread has seen (thread 0)
     uint32_t it = 0;
-    for (int64_t t = unit; t < T; t += nunits, ++it) {
+    for (int64_t i = unit; i < TI; i += nunits, ++it) {
+      const int64_t t = mc ? 2 * i + pq : i;
       const Tile tl = decode_tile(p.g, t);
       const uint32_t buf = it & 1, use = it >> 1;
-      const int64_t tflag = tl.tile_flag >= 0 ? tl.tile_flag * CG + crank : -1;
-      const int rows_here = tl.rows_valid - (int)crank * ROWS_PER_CTA;
-      const int64_t row0 = tl.out_row + (int64_t)crank * ROWS_PER_CTA;
+      const int64_t tflag = tl.tile_flag >= 0 ? tl.tile_flag * CG + half : -1;
+      const int rows_here = tl.rows_valid - (int)half * ROWS_PER_CTA;
+      const int64_t row0 = tl.out_row + (int64_t)half * ROWS_PER_CTA;
       const int nch = (tl.cols_valid + XCOLS - 1) / XCOLS;
       // Staged tiles need 16-byte aligned TMA column coordinates (8 bf16); fp8
       // results go out by direct stores.
@@ -1331,9 +1363,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
       const CUtensorMap* src_map = cep ? &p.tmR : &p.tmX;
       const CUtensorMap* xdst_map = cep ? &p.tmS : &p.tmX;
       const int64_t src_col0 = cep ? tl.x_col : tl.out_col;
-      const int64_t src_row0 = cep ? tl.xr_row + (int64_t)crank * ROWS_PER_CTA : row0;
+      const int64_t src_row0 = cep ? tl.xr_row + (int64_t)half * ROWS_PER_CTA : row0;
       const int64_t xd_col0 = cep ? tl.x_col : tl.out_col;
-      const int64_t xd_row0 = cep ? tl.xs_row + (int64_t)crank * ROWS_PER_CTA : row0;
+      const int64_t xd_row0 = cep ? tl.xs_row + (int64_t)half * ROWS_PER_CTA : row0;
       const int64_t xd_pitch = cep ? p.g.blk_n : p.g.N;
       if (et == 0) {
         if (cep && tl.s > 0) {
@@ -1411,7 +1443,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           __syncwarp();
           if (lane == 0) {
             if (CG == 2)
-              mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * buf, 0));  // the even CTA's barrier
+              mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * buf, lead));  // the even CTA's barrier
             else
               mbar_arrive(bar_tempty + 8 * buf);
           }
@@ -1531,31 +1563,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
   }
 
   if (CG == 2) {
-    // Both CTAs' operand loads complete on the even CTA's barriers, so the
-    // even CTA waits for all of them before either CTA may exit.  After an
-    // abort the two producers may have stopped at different loads (they
-    // differ by at most one ring of stages: a load is issued only once the
-    // MMA consumed the stage's previous load, which needed both CTAs' bytes),
-    // so first the phases only one CTA loaded are balanced: a load of the odd
-    // CTA alone is armed for its bytes, a missing load of the odd CTA is
-    // counted as arrived.  Without an abort both counts are equal and every
-    // phase has already completed.
+    // The operand loads that land in a pair complete on its even CTA's
+    // barriers: both CTAs' own loads, and with multicast the other pair's
+    // halves of the B rows.  So each even CTA waits for all of them before any
+    // CTA may exit.  After an abort the producers may have stopped at
+    // different loads (at most one ring of stages apart: a load is issued only
+    // once the MMAs consumed the stage's previous load, which needed every
+    // contributor's bytes), so first the phases not every contributor loaded
+    // are balanced: a phase the even CTA never armed is armed for the bytes
+    // that were issued, a missing contribution to an armed phase is counted as
+    // arrived.  Without an abort all counts are equal and every phase has
+    // already completed.
     tc_fence_before();
     __syncwarp();
-    cluster_sync_all();  // both producers' counts are in the even CTA's shared memory
+    cluster_sync_all();  // the producers' counts are in the even CTAs' shared memory
     tc_fence_after();
     if (leader && warp == 0 && lane == 0) {
-      const uint32_t kl = s_kcnt[0], ko = s_kcnt[1];
-      const uint32_t kmin = kl < ko ? kl : ko, kmax = kl < ko ? ko : kl;
+      const uint32_t own_bytes = mc ? C::A_BYTES + C::B_BYTES / 2 : C::STAGE_BYTES;
+      const uint32_t oth_bytes = C::B_BYTES / 2;
+      const uint32_t k0 = s_kcnt[lead], k1 = s_kcnt[lead + 1];
+      const uint32_t k2 = mc ? s_kcnt[lead ^ 2u] : k0, k3 = mc ? s_kcnt[(lead ^ 2u) + 1] : k0;
+      const uint32_t kmin = min(min(k0, k1), min(k2, k3)), kmax = max(max(k0, k1), max(k2, k3));
+      auto bytes_in = [&](uint32_t n) {
+        uint32_t b = (k0 > n ? own_bytes : 0u) + (k1 > n ? own_bytes : 0u);
+        if (mc) b += (k2 > n ? oth_bytes : 0u) + (k3 > n ? oth_bytes : 0u);
+        return b;
+      };
       for (uint32_t n = kmin; n < kmax; ++n) {
-        const uint32_t fb = bar_full + 8 * (n % STAGES);
-        if (n >= kl)
-          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-        else
-          mbar_complete_tx(fb, C::STAGE_BYTES);
+        const uint32_t fb = bar_full + 8 * (n % STAGES), b = bytes_in(n);
+        if (n < k0) {
+          if (b < 2 * C::STAGE_BYTES) mbar_complete_tx(fb, 2 * C::STAGE_BYTES - b);
+        } else if (b > 0) {
+          mbar_arrive_expect_tx(fb, b);
+        }
       }
       for (uint32_t n = kmax > (uint32_t)STAGES ? kmax - STAGES : 0u; n < kmax; ++n)
-        mbar_settle(bar_full + 8 * (n % STAGES), (n / STAGES) & 1u);
+        if (n < k0 || bytes_in(n) > 0) mbar_settle(bar_full + 8 * (n % STAGES), (n / STAGES) & 1u);
     }
   }
   tc_fence_before();

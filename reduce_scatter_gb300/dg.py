@@ -71,6 +71,7 @@ OPT_TILE_ORDER = 16
 OPT_RS_CE_BANDS = 17
 OPT_GROUP_M = 18
 OPT_RS_REDUCE = 19
+OPT_MULTICAST = 20
 
 # Every symbol include/dg.h declares.
 EXPORTS = ("dg_plan", "dg_workspace_bytes", "dg_run_mode", "dg_set_option", "dg_run", "dg_check",
@@ -98,7 +99,7 @@ class PlanInfo(ctypes.Structure):
         ("copies_per_run", ctypes.c_int64),
         ("a_type", ctypes.c_int32), ("b_type", ctypes.c_int32), ("elem_bytes", ctypes.c_int32),
         ("out_type", ctypes.c_int32), ("reduce_op", ctypes.c_int32),
-        ("epilogue", ctypes.c_int32), ("flag_parts", ctypes.c_int32),
+        ("epilogue", ctypes.c_int32), ("flag_parts", ctypes.c_int32), ("multicast", ctypes.c_int32),
     ]
 
     def as_dict(self):

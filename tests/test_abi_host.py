@@ -416,3 +416,23 @@ def test_rs_reduce_and_epilogue_option_rules(L):
         q.set_option(dg.OPT_EPILOGUE, v)
     with pytest.raises(dg.DGError):
         q.set_option(dg.OPT_EPILOGUE, 4)
+
+
+def test_multicast_eligibility(L):
+    # tiles 2i and 2i + 1 must share their B rows inside one block
+    for sched, shape, want in [(dg.AG_ROTATING_A, (16384, 106496, 16384, 1, 8), 1),
+                               (dg.AG_ROTATING_B, (8192, 53248, 8192, 2, 4), 1),
+                               (dg.RS_TILING_A_ROTATING_C, (16384, 8192, 28672, 1, 8), 1),
+                               (dg.RS_TILING_B_ROTATING_C, (8192, 53248, 8192, 2, 4), 1),
+                               (dg.AG_ROTATING_A, (512, 512, 256, 1, 2), 0),      # one tile per block
+                               (dg.AG_ROTATING_A, (1536, 512, 256, 1, 2), 0)]:    # three tile rows
+        m, n, k, l, tp = shape
+        p = dg.Plan(m, n, k, l, tp, sched)
+        auto = want if sched in (dg.AG_ROTATING_A, dg.AG_ROTATING_B) and k >= 16384 else 0
+        assert p.info()["multicast"] == auto              # automatic for AG with K >= 16384
+        p.set_option(dg.OPT_MULTICAST, 0)
+        assert p.info()["multicast"] == 0
+        p.set_option(dg.OPT_MULTICAST, 1)
+        assert p.info()["multicast"] == want, (sched, shape)
+    p.set_option(dg.OPT_CTA_GROUP, 1)
+    assert p.info()["multicast"] == 0                     # pair tiles only

@@ -398,3 +398,24 @@ def test_rs_reduction_same_bits_when_alpha_is_a_power_of_two(sched, epi):
                     out[red], _ = r.run(A, B, C if beta else None)
                 for red in (1, -1):
                     assert torch.equal(out[0].view(torch.int16), out[red].view(torch.int16)), (m, tp, alpha, red)
+
+
+@pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_b_multicast_between_pairs_same_bits(sched):
+    # clusters of two CTA pairs sharing their B rows compute every tile with the same MMAs:
+    # the same bits as independent pairs, and within tolerance of the oracle
+    for m, n, k, l in [(1024, 2048, 512, 2), (2048, 1024, 1024, 1), (512, 1536, 256, 1)]:
+        for tp in (1, 2, 4):
+            if not _shape_ok(sched, m, n, k, tp):
+                continue
+            a, b, c = host_inputs(m, n, k, l, seed=99 + tp + 10 * sched)
+            A, B, C = to_dev(a), to_dev(b), to_dev(c)
+            for alpha, beta in [(1.0, 0.0), (0.5, 1.0)]:
+                out = {}
+                for mc in (0, 1):
+                    r = Runner(m, n, k, l, tp, sched, alpha, beta,
+                               options={dg.OPT_MULTICAST: mc, dg.OPT_TIMEOUT_MS: 500})
+                    out[mc], rc = r.run(A, B, C if beta else None, check=False)
+                    assert rc == dg.OK, (m, n, tp, mc, dg.last_error())
+                assert torch.equal(out[0].view(torch.int16), out[1].view(torch.int16)), (m, n, tp, alpha)
+                assert rel_err(out[1], oracle_full(a, b, c, alpha, beta)) <= TOL
