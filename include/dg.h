@@ -143,17 +143,20 @@ enum dg_option {
                                  1 = 128 x 256 tiles on one SM */
   DG_OPT_EPILOGUE = 7,        /* epilogue, before the first run (all give the same bits):
                                  1 = source and result chunks staged in shared memory and moved
-                                 by TMA (default for RS plans with tp > 4, or tp > 2 and
-                                 beta == 0, and for AG plans with fp8 inputs, or with beta != 0
-                                 and K >= 16384); 0 = direct per-row global accesses (one more
-                                 operand stage; default for the other bf16 AG plans with
-                                 beta != 0); 2 = staged per warp (each epilogue warp moves its
-                                 own 32-row boxes, three source loads ahead, with no barrier
-                                 between the warps; default for RS plans where at least half
-                                 the steps load a source: tp <= 2, or tp <= 4 with beta != 0);
-                                 3 = result chunks staged, sources read directly (one more
-                                 operand stage than 1; default for bf16 AG plans with beta == 0,
-                                 which read no source) */
+                                 by TMA (default for AG plans with fp8 inputs, or with beta != 0
+                                 and K >= 16384, and for RS plans not covered below); 0 = direct
+                                 per-row global accesses (one more operand stage; default for the
+                                 other bf16 AG plans with beta != 0); 2 = staged per warp (each
+                                 epilogue warp moves its own 32-row boxes, three source loads
+                                 ahead, with no barrier between the warps; default for RS plans
+                                 where at least half the steps load a source: tp <= 2, or
+                                 tp <= 4 with beta != 0); 3 = result chunks staged, sources read
+                                 directly (one more operand stage than 1; default for bf16 AG
+                                 plans with beta == 0, which read no source); 4 = staged per warp
+                                 with two slots, one load ahead, and one more operand stage
+                                 (default for the other RS plans whose alpha * scale_a * scale_b
+                                 is a power of two, where the middle steps load nothing,
+                                 DG_OPT_RS_REDUCE) */
   DG_OPT_L2_HINT = 8,         /* L2 eviction policy of the operand loads: bits 0-1 for A,
                                  bits 2-3 for B; 0 = none, 1 = evict first, 2 = evict last */
   DG_OPT_RS_CE_PARTIALS = 10, /* RS plans with tp > 1, before the first run: 1 = hand the

@@ -206,11 +206,12 @@ namespace {
 
 bool is_ag(int s) { return s == DG_AG_ROTATING_A || s == DG_AG_ROTATING_B; }
 
-// Epilogue variant: 0 direct, 1 staged per CTA, 2 staged per warp.  The
-// per-warp epilogue hands partials on, and counts finished tiles, per warp
-// quarter of a CTA's half tile.
-int epi_parts(const dg_plan_s* p) { return p->epi == 2 ? dg::EPI_WARPS : 1; }
-int epi_box_rows(const dg_plan_s* p) { return p->epi == 2 ? dg::WROWS : dg::ROWS_PER_CTA; }
+// Epilogue variant: 0 direct, 1 staged per CTA, 2 staged per warp, 3 stores
+// staged only, 4 staged per warp with two slots.  The per-warp epilogues hand
+// partials on, and count finished tiles, per warp quarter of a CTA's half tile.
+bool epi_per_warp(const dg_plan_s* p) { return p->epi == 2 || p->epi == 4; }
+int epi_parts(const dg_plan_s* p) { return epi_per_warp(p) ? dg::EPI_WARPS : 1; }
+int epi_box_rows(const dg_plan_s* p) { return epi_per_warp(p) ? dg::WROWS : dg::ROWS_PER_CTA; }
 
 int layout(dg_plan_s* p) {
   dg::Geom& g = p->g;
@@ -391,6 +392,10 @@ int rt_init(dg_plan_s* p) {
   DG_SMEM_ATTR(2, 3, 0);
   DG_SMEM_ATTR(1, 3, 1);
   DG_SMEM_ATTR(2, 3, 1);
+  DG_SMEM_ATTR(1, 4, 0);
+  DG_SMEM_ATTR(2, 4, 0);
+  DG_SMEM_ATTR(1, 4, 1);
+  DG_SMEM_ATTR(2, 4, 1);
 #undef DG_SMEM_ATTR
   {
     cudaLaunchConfig_t cfg = {};
@@ -414,7 +419,10 @@ int rt_init(dg_plan_s* p) {
     int ncl3 = 0;
     cfg.dynamicSmemBytes = dg::Cfg<2, 3>::SMEM_BYTES;
     DG_CUDA(cudaOccupancyMaxActiveClusters(&ncl3, dg::dg_gemm_kernel<2, 3, 0>, &cfg));
-    p->max_pairs = std::min(std::min(ncl0, ncl1), std::min(ncl2, ncl3));
+    int ncl4 = 0;
+    cfg.dynamicSmemBytes = dg::Cfg<2, 4>::SMEM_BYTES;
+    DG_CUDA(cudaOccupancyMaxActiveClusters(&ncl4, dg::dg_gemm_kernel<2, 4, 0>, &cfg));
+    p->max_pairs = std::min(std::min(std::min(ncl0, ncl1), std::min(ncl2, ncl3)), ncl4);
     attr[0].val.clusterDim.x = 4;
     cfg.gridDim = dim3(4 * 256, 1, 1);
     int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
@@ -426,7 +434,10 @@ int rt_init(dg_plan_s* p) {
     DG_CUDA(cudaOccupancyMaxActiveClusters(&q2, dg::dg_gemm_kernel<2, 2, 0>, &cfg));
     cfg.dynamicSmemBytes = dg::Cfg<2, 3>::SMEM_BYTES;
     DG_CUDA(cudaOccupancyMaxActiveClusters(&q3, dg::dg_gemm_kernel<2, 3, 0>, &cfg));
-    p->max_quads = std::min(std::min(q0, q1), std::min(q2, q3));
+    int q4 = 0;
+    cfg.dynamicSmemBytes = dg::Cfg<2, 4>::SMEM_BYTES;
+    DG_CUDA(cudaOccupancyMaxActiveClusters(&q4, dg::dg_gemm_kernel<2, 4, 0>, &cfg));
+    p->max_quads = std::min(std::min(std::min(q0, q1), std::min(q2, q3)), q4);
   }
   DG_CUDA(cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming));
   DG_CUDA(cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming));
@@ -715,7 +726,11 @@ int launch_kp(dg_plan_s* p, const dg::KParams& kp, cudaStream_t st) {
     grid = std::min<int64_t>(grid, tiles);
     if (grid <= 0) return DG_OK;
     const bool f8 = p->esz == 1;
-    if (p->epi == 3 && f8)
+    if (p->epi == 4 && f8)
+      dg::dg_gemm_kernel<1, 4, 1><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 4>::SMEM_BYTES, st>>>(kp);
+    else if (p->epi == 4)
+      dg::dg_gemm_kernel<1, 4, 0><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 4>::SMEM_BYTES, st>>>(kp);
+    else if (p->epi == 3 && f8)
       dg::dg_gemm_kernel<1, 3, 1><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 3>::SMEM_BYTES, st>>>(kp);
     else if (p->epi == 3)
       dg::dg_gemm_kernel<1, 3, 0><<<(unsigned)grid, dg::NUM_THREADS, dg::Cfg<1, 3>::SMEM_BYTES, st>>>(kp);
@@ -748,7 +763,8 @@ int launch_kp(dg_plan_s* p, const dg::KParams& kp, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3((unsigned)(csize * units), 1, 1);
   cfg.blockDim = dim3(dg::NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = p->epi == 3   ? dg::Cfg<2, 3>::SMEM_BYTES
+  cfg.dynamicSmemBytes = p->epi == 4   ? dg::Cfg<2, 4>::SMEM_BYTES
+                         : p->epi == 3 ? dg::Cfg<2, 3>::SMEM_BYTES
                          : p->epi == 2 ? dg::Cfg<2, 2>::SMEM_BYTES
                          : p->epi == 1 ? dg::Cfg<2, 1>::SMEM_BYTES
                                        : dg::Cfg<2, 0>::SMEM_BYTES;
@@ -756,7 +772,11 @@ int launch_kp(dg_plan_s* p, const dg::KParams& kp, cudaStream_t st) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const bool f8 = p->esz == 1;
-  if (p->epi == 3 && f8)
+  if (p->epi == 4 && f8)
+    DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 4, 1>, kp));
+  else if (p->epi == 4)
+    DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 4, 0>, kp));
+  else if (p->epi == 3 && f8)
     DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 3, 1>, kp));
   else if (p->epi == 3)
     DG_CUDA(cudaLaunchKernelEx(&cfg, dg::dg_gemm_kernel<2, 3, 0>, kp));
@@ -1375,13 +1395,24 @@ int dg_plan_scaled(dg_plan_t* out, int64_t m, int64_t n, int64_t k, int64_t l, i
   // epilogue, whose loads run further ahead; with fewer such steps the
   // per-CTA one, whose larger boxes store the others' results faster.
   // bf16 AG plans with beta = 0 read no source at all: staging for the stores
-  // alone leaves room for one more operand stage.
+  // alone leaves room for one more operand stage.  RS plans whose middle steps
+  // add by TMA reduction (alpha * scale_a * scale_b a power of two, so the
+  // reduction is exact) load a source only at the last step and, with beta,
+  // the first: with fewer than half the steps loading, two slots per warp and
+  // one more operand stage (the per-CTA staging where the reduction is off).
+  const float a_eff = alpha * scale_a * scale_b;
+  int a_exp = 0;
+  const float a_fr = std::frexp(a_eff, &a_exp);
+  const bool exact_red = a_eff == 0.f || a_fr == 0.5f || a_fr == -0.5f;
+  const int loading = 1 + (beta != 0.f ? 1 : 0);
   if (is_ag(schedule) && esz == 2 && beta == 0.f)
     p->epi = 3;
   else if (is_ag(schedule))
     p->epi = (esz == 1 || k >= 16384) ? 1 : 0;
+  else if (loading * 2 >= tp)
+    p->epi = 2;
   else
-    p->epi = (1 + (beta != 0.f ? 1 : 0)) * 2 >= tp ? 2 : 1;
+    p->epi = exact_red ? 4 : 1;
   {
     std::lock_guard<std::mutex> lk(g_ws_mu);
     p->id = g_next_plan_id++;
@@ -1505,9 +1536,10 @@ int dg_set_option(dg_plan_t p, int option, int64_t value) {
       p->l2_hint = (uint32_t)value;
       return DG_OK;
     case DG_OPT_EPILOGUE:
-      if (value < 0 || value > 3)
+      if (value < 0 || value > 4)
         return fail(DG_ERR_ARG,
-                    "epilogue must be 0 (direct), 1 (staged), 2 (staged per warp) or 3 (staged stores only)");
+                    "epilogue must be 0 (direct), 1 (staged), 2 (staged per warp), 3 (staged stores only) "
+                    "or 4 (staged per warp, two slots)");
       if (p->epoch != 0) return fail(DG_ERR_STATE, "the epilogue is fixed after the first run");
       p->epi = (int)value;
       layout(p);

@@ -94,10 +94,14 @@ struct Cfg {
   // EPI = 3 (staged stores only): the staged epilogue without its source
   // chunks (plans that read no source: AG with beta = 0), which gives their
   // 32 KB back to the operand ring.
+  // EPI = 4: the per-warp epilogue with two slots per warp (one load ahead),
+  // which also leaves room for one more operand stage.
   static constexpr bool SRC_STAGING = EPI == 1 || EPI == 2;
   static constexpr int STAGES = CG == 1 ? (SRC_STAGING ? 3 : 4) : (SRC_STAGING ? 5 : 6);
   static constexpr uint32_t STAGING_BYTES =
-      SRC_STAGING ? 4 * XBUF : (EPI == 3 ? 2 * XBUF : 0);  // [2 source +] 2 destination chunks
+      SRC_STAGING ? 4 * XBUF : (EPI == 3 || EPI == 4 ? 2 * XBUF : 0);  // [2 source +] 2 destination chunks
+  static constexpr int WSL = EPI == 4 ? 2 : WSLOTS;  // per-warp slots in use
+  static constexpr int WPR = WSL - 1;                // per-warp source loads ahead
   static constexpr uint32_t SMEM_BYTES =
       STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 512 /*barriers*/;
 };
@@ -1067,16 +1071,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
         }
       }
     }
-  } else if constexpr (EPI == 2) {
+  } else if constexpr (EPI == 2 || EPI == 4) {
     // ------------------------------------------------- epilogue, per warp
     // Warp q owns TMEM lanes 32q..32q+31 (rows of the CTA's half tile).  Lane
     // 0 issues this warp's TMA loads and stores and its flag operations; the
     // chunk slots, their load barriers and the bulk groups are the warp's own.
     const int q = warp & 3;
-    uint8_t* wb = xsrc + (uint32_t)q * (WSLOTS * WBUF);
+    uint8_t* wb = xsrc + (uint32_t)q * (C::WSL * WBUF);
     const uint32_t wb_addr = smem_u32(wb);
-    const uint32_t wbar = bar_wfull + 8u * (uint32_t)(WSLOTS * q);
-    uint32_t seq = 0;       // chunks of staged tiles so far: chunk g uses slot g % WSLOTS and
+    const uint32_t wbar = bar_wfull + 8u * (uint32_t)(C::WSL * q);
+    uint32_t seq = 0;       // chunks of staged tiles so far: chunk g uses slot g % WSL and
                             // commits bulk group g (lane 0), so a slot's last store is a group index
     uint32_t ph = 0;        // per slot: parity of its next load completion
     uint32_t inflight = 0;  // slots whose load is issued and not yet consumed
@@ -1111,7 +1115,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
       const int64_t dst_col0 = tl.dst == DST_X && cep ? tl.x_col : tl.out_col;
       const int64_t dst_row0 = tl.dst == DST_X && cep ? tl.xs_row + wrow : row0;
       const int64_t xd_pitch = cep ? p.g.blk_n : p.g.N;
-      const int npre = has_src ? (nch < WPRE ? nch : WPRE) : 0;
+      const int npre = has_src ? (nch < C::WPR ? nch : C::WPR) : 0;
       uint32_t go = 1;
       if (lane == 0) {
         if (cep && tl.s > 0) {
@@ -1143,17 +1147,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
         }
         if (npre > 0) {
           // the source needs only the previous step: load it while the MMAs run.
-          // Chunk seq + c reuses the slot of chunk seq + c - WSLOTS, whose store
-          // is bulk group seq + c - WSLOTS of seq committed ones.
+          // Chunk seq + c reuses the slot of chunk seq + c - WSL, whose store
+          // is bulk group seq + c - WSL of seq committed ones.
           fence_proxy_async_global();
           for (int c = 0; c < npre; ++c) {
             if (c == 0)
-              bulk_wait_read<WSLOTS - 1>();
+              bulk_wait_read<C::WSL - 1>();
             else if (c == 1)
-              bulk_wait_read<WSLOTS - 2>();
+              bulk_wait_read<(C::WSL >= 2 ? C::WSL - 2 : 0)>();
             else
-              bulk_wait_read<WSLOTS - 3>();
-            const uint32_t sl = (seq + (uint32_t)c) % WSLOTS;
+              bulk_wait_read<(C::WSL >= 3 ? C::WSL - 3 : 0)>();
+            const uint32_t sl = (seq + (uint32_t)c) % C::WSL;
             mbar_arrive_expect_tx(wbar + 8 * sl, src_f32 ? WBUF : WBUF / 2);
             tma_load_2d(wb_addr + sl * WBUF, src_map, wbar + 8 * sl, (int32_t)(src_col0 + c * XCOLS),
                         (int32_t)src_row0);
@@ -1173,7 +1177,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           pend_flag = -1;
         }
       }
-      for (int c = 0; c < npre; ++c) inflight |= 1u << ((seq + (uint32_t)c) % WSLOTS);
+      for (int c = 0; c < npre; ++c) inflight |= 1u << ((seq + (uint32_t)c) % C::WSL);
       go = __shfl_sync(0xffffffffu, go, 0);
       __syncwarp();  // lane 0's acquires are seen by the lanes that read C or the partial directly
       if (go == 0) {
@@ -1218,12 +1222,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           }
           continue;
         }
-        const uint32_t g = seq + (uint32_t)c, sl = g % WSLOTS;
+        const uint32_t g = seq + (uint32_t)c, sl = g % C::WSL;
         // a box whose rows and columns are all inside the tile (and its shard) goes out by TMA
         const bool tma_ok = rows_here == WROWS && ncols == XCOLS;
         float src[32];
         if (has_src) {
-          mbar_wait(p, wbar + 8 * sl, (ph >> sl) & 1u, 0x500000u | (uint32_t)(q * WSLOTS) | sl);
+          mbar_wait(p, wbar + 8 * sl, (ph >> sl) & 1u, 0x500000u | (uint32_t)(q * C::WSL) | sl);
           ph ^= 1u << sl;
           inflight &= ~(1u << sl);
           staged_read_row(wb + sl * WBUF, lane, src_f32, p.beta, src);
@@ -1242,8 +1246,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
         if (p.bias) add_bias(p, tl.out_col + c * XCOLS, ncols, out);
         if (tma_ok) {
           // the slot is free: every lane has read its source row, or (no source)
-          // the store of chunk g - WSLOTS, bulk group g - WSLOTS, has read it
-          if (!has_src && lane == 0) bulk_wait_read<WSLOTS - 1>();
+          // the store of chunk g - WSL, bulk group g - WSL, has read it
+          if (!has_src && lane == 0) bulk_wait_read<C::WSL - 1>();
           __syncwarp();
           staged_write_row(wb + sl * WBUF, lane, dst_f32, out);
           fence_proxy_async_smem();
@@ -1260,15 +1264,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           store_row_chunk(p, tl, grow, tl.out_col + c * XCOLS, ncols, out, xp);
         }
         if (lane == 0) bulk_commit();  // bulk group g (empty when the chunk went out by plain stores)
-        if (has_src && c + WPRE < nch) {
-          // chunk c + WPRE goes to the slot of chunk c - 1, whose store is the
+        if (has_src && c + C::WPR < nch) {
+          // chunk c + WPR goes to the slot of chunk c - 1, whose store is the
           // group before the one just committed
-          const uint32_t sn = (g + WPRE) % WSLOTS;
+          const uint32_t sn = (g + C::WPR) % C::WSL;
           __syncwarp();  // every lane has read chunk c - 1's source from that slot
           if (lane == 0) {
             bulk_wait_read<1>();
             mbar_arrive_expect_tx(wbar + 8 * sn, src_f32 ? WBUF : WBUF / 2);
-            tma_load_2d(wb_addr + sn * WBUF, src_map, wbar + 8 * sn, (int32_t)(src_col0 + (c + WPRE) * XCOLS),
+            tma_load_2d(wb_addr + sn * WBUF, src_map, wbar + 8 * sn, (int32_t)(src_col0 + (c + C::WPR) * XCOLS),
                         (int32_t)src_row0);
           }
           inflight |= 1u << sn;
@@ -1322,7 +1326,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
       if (pend_flag >= 0) release_partial(p, pend_flag, pend_val);
       bulk_wait<0>();  // no bulk store may outlive the CTA
       if (aborted)     // nor a source load that was issued but never consumed
-        for (uint32_t sl = 0; sl < (uint32_t)WSLOTS; ++sl)
+        for (uint32_t sl = 0; sl < (uint32_t)C::WSL; ++sl)
           if ((inflight >> sl) & 1u) mbar_settle(wbar + 8 * sl, (ph >> sl) & 1u);
     }
   } else {

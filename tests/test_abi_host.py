@@ -178,7 +178,7 @@ def test_tile_order_simulator(L, sched, tp, shape, cg):
     _simulate(plan, m, n, k, l, tp, sched)
     if sched >= 2 and tp > 1:
         info = plan.info()
-        assert info["flag_parts"] == (4 if info["epilogue"] == 2 else 1)
+        assert info["flag_parts"] == (4 if info["epilogue"] in (2, 4) else 1)
         assert info["n_flags"] == l * tp * info["tiles_m"] * info["tiles_n"] * cg * info["flag_parts"]
 
 
@@ -391,8 +391,10 @@ def test_tile_order_simulator_raster_groups(L, sched, group_m):
 
 
 def test_rs_reduce_and_epilogue_option_rules(L):
+    assert dg.Plan(1024, 1024, 1024, 1, 8, dg.RS_TILING_A_ROTATING_C).info()["epilogue"] == 4   # reduction exact
+    assert dg.Plan(1024, 1024, 1024, 1, 8, dg.RS_TILING_A_ROTATING_C, 0.75).info()["epilogue"] == 1  # it is not
     p = dg.Plan(1024, 1024, 1024, 1, 8, dg.RS_TILING_A_ROTATING_C)
-    assert p.info()["epilogue"] == 1                  # one loading step in eight: per-CTA staging
+    p.set_option(dg.OPT_EPILOGUE, 1)
     flags_staged = p.info()["n_flags"]
     p.set_option(dg.OPT_RS_REDUCE, 1)
     assert p.info()["n_flags"] == flags_staged
@@ -403,7 +405,7 @@ def test_rs_reduce_and_epilogue_option_rules(L):
     p.set_option(dg.OPT_RS_REDUCE, -1)
     # the per-warp epilogue where at least half the steps load a source
     assert dg.Plan(1024, 1024, 1024, 1, 4, dg.RS_TILING_B_ROTATING_C, 0.5, 1.0).info()["epilogue"] == 2
-    assert dg.Plan(1024, 1024, 1024, 1, 4, dg.RS_TILING_B_ROTATING_C, 0.5, 0.0).info()["epilogue"] == 1
+    assert dg.Plan(1024, 1024, 1024, 1, 4, dg.RS_TILING_B_ROTATING_C, 0.5, 0.0).info()["epilogue"] == 4
     assert dg.Plan(1024, 1024, 1024, 1, 2, dg.RS_TILING_A_ROTATING_C).info()["epilogue"] == 2
     d = dg.Plan(1024, 1024, 1024, 1, 4, dg.RS_TILING_A_ROTATING_C)
     d.set_option(dg.OPT_EPILOGUE, 0)
@@ -412,10 +414,10 @@ def test_rs_reduce_and_epilogue_option_rules(L):
     q = dg.Plan(1024, 1024, 1024, 1, 4, dg.AG_ROTATING_A)
     with pytest.raises(dg.DGError):
         q.set_option(dg.OPT_RS_REDUCE, 1)
-    for v in (0, 1, 2, 3):
+    for v in (0, 1, 2, 3, 4):
         q.set_option(dg.OPT_EPILOGUE, v)
     with pytest.raises(dg.DGError):
-        q.set_option(dg.OPT_EPILOGUE, 4)
+        q.set_option(dg.OPT_EPILOGUE, 5)
 
 
 def test_multicast_eligibility(L):

@@ -59,7 +59,7 @@ def _want(a, b, c, bias, alpha, beta, sched, tp, op):
                          reduce_op=None if sched <= 1 else op, bias=None if bias is None else f(bias))
 
 
-@pytest.mark.parametrize("epi", [0, 1, 2, 3])
+@pytest.mark.parametrize("epi", [0, 1, 2, 3, 4])
 @pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
 @pytest.mark.parametrize("shape", [(1024, 2048, 512, 2), (392, 776, 320, 2)], ids=lambda s: "x".join(map(str, s)))
 def test_bias_f32_out_and_reduce_op_vs_oracle(sched, epi, shape):
@@ -166,7 +166,7 @@ def _fp8_close(got_codes, want_codes, fmt):
 
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
-@pytest.mark.parametrize("epi", [0, 1, 2, 3])
+@pytest.mark.parametrize("epi", [0, 1, 2, 3, 4])
 @pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
 def test_fp8_out_with_result_scale_vs_oracle(sched, epi, fmt):
     m, n, k, l = 392, 776, 320, 2

@@ -55,7 +55,7 @@ def test_fp8_allgather_bit_exact_vs_unsharded(sched):
         assert torch.equal(D.view(torch.int16), ref.view(torch.int16)), tp
 
 
-@pytest.mark.parametrize("epi", [0, 1, 2, 3])
+@pytest.mark.parametrize("epi", [0, 1, 2, 3, 4])
 @pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
 def test_fp8_all_ones_and_both_epilogues(sched, epi):
     m, n, l, tp = 512, 512, 1, 4

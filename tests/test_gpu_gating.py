@@ -120,12 +120,12 @@ def test_transfers_over_several_copy_streams(ns):
         assert torch.equal(D.view(torch.int16), D2.view(torch.int16))
 
 
-@pytest.mark.parametrize("epi", [1, 2, 3, 4])
+@pytest.mark.parametrize("epi", [1, 2, 3, 4, 5])
 @pytest.mark.parametrize("tp", [2, 4])
 @pytest.mark.parametrize("sched", [dg.RS_TILING_A_ROTATING_C, dg.RS_TILING_B_ROTATING_C],
                          ids=lambda s: dg.SCHEDULE_NAMES[s])
 def test_rs_grid_equal_to_step_distance(sched, tp, epi):
-    # epi 3, 4: the staged and the per-warp epilogue with the middle steps' TMA reductions
+    # epi 3, 4, 5: the staged and the two per-warp epilogues with the middle steps' TMA reductions
     # With as many CTA pairs as tiles between a tile and its next step, every
     # pair's next tile waits on the hand-off it made itself; the kernel must
     # release it first (a missed release shows up as a timeout, not a hang).
@@ -136,7 +136,7 @@ def test_rs_grid_equal_to_step_distance(sched, tp, epi):
     a, b, c = host_inputs(m, n, k, l, seed=26)
     A, B, C = to_dev(a), to_dev(b), to_dev(c)
     r = Runner(m, n, k, l, tp, sched, 0.5, 1.0,
-               options={dg.OPT_GRID: 2 * pairs, dg.OPT_TIMEOUT_MS: 500, dg.OPT_EPILOGUE: (0, 1, 2, 1, 2)[epi],
+               options={dg.OPT_GRID: 2 * pairs, dg.OPT_TIMEOUT_MS: 500, dg.OPT_EPILOGUE: (0, 1, 2, 1, 2, 4)[epi],
                         dg.OPT_RS_REDUCE: int(epi >= 3)})
     D, rc = r.run(A, B, C, check=False)
     assert rc == dg.OK, dg.last_error()

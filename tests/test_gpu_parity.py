@@ -179,7 +179,7 @@ def test_single_sm_tiles_vs_oracle(sched, tp):
         assert torch.equal(D.view(torch.int16), ref.view(torch.int16))
 
 
-@pytest.mark.parametrize("epi", [0, 1, 2, 3])
+@pytest.mark.parametrize("epi", [0, 1, 2, 3, 4])
 @pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
 @pytest.mark.parametrize("shape", [(1024, 2048, 512, 2), (392, 776, 320, 2)], ids=lambda s: "x".join(map(str, s)))
 def test_both_epilogues_vs_oracle(sched, epi, shape):
@@ -202,7 +202,7 @@ def test_both_epilogues_vs_oracle(sched, epi, shape):
 
 @pytest.mark.parametrize("sched", [dg.RS_TILING_A_ROTATING_C, dg.RS_TILING_B_ROTATING_C],
                          ids=lambda s: dg.SCHEDULE_NAMES[s])
-@pytest.mark.parametrize("epi", [0, 1, 2, 3])
+@pytest.mark.parametrize("epi", [0, 1, 2, 3, 4])
 def test_rs_nonfused_baseline_vs_oracle(sched, epi):
     # SERIAL on an RS plan: per-rank partial GEMMs, then the separate reduction
     m, n, k, l, tp = 1024, 1024, 1024, 2, 4
@@ -347,16 +347,16 @@ def test_per_warp_epilogue_same_bits_as_staged(sched, cg):
             A, B, C = to_dev(a), to_dev(b), to_dev(c)
             for alpha, beta in [(1.0, 0.0), (0.5, 1.0)]:
                 out = {}
-                for epi in (1, 2, 3):
+                for epi in (1, 2, 3, 4):
                     r = Runner(m, n, k, l, tp, sched, alpha, beta,
                                options={dg.OPT_EPILOGUE: epi, dg.OPT_CTA_GROUP: cg})
                     out[epi], _ = r.run(A, B, C if beta else None)
-                for epi in (2, 3):
+                for epi in (2, 3, 4):
                     assert torch.equal(out[1].view(torch.int16), out[epi].view(torch.int16)), (m, n, tp, alpha, epi)
                 assert rel_err(out[2], oracle_full(a, b, c, alpha, beta)) <= TOL
 
 
-@pytest.mark.parametrize("epi", [1, 2])
+@pytest.mark.parametrize("epi", [1, 2, 4])
 @pytest.mark.parametrize("cg", [1, 2])
 @pytest.mark.parametrize("sched", [dg.RS_TILING_A_ROTATING_C, dg.RS_TILING_B_ROTATING_C],
                          ids=lambda s: dg.SCHEDULE_NAMES[s])
