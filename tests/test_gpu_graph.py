@@ -81,3 +81,41 @@ def test_graph_of_a_host_buffer_run(sched):
         assert cap.plan.check(cap.ws, torch.cuda.current_stream(), raise_on_error=False) == dg.OK
         want, _ = ref.run(to_dev(a2), to_dev(b2), to_dev(c2))
         assert torch.equal(D_h, want.view(torch.int16).cpu()), i
+
+
+@pytest.mark.parametrize("sched", [dg.AG_ROTATING_A, dg.AG_ROTATING_B], ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_multicast_runs_in_graphs_and_with_host_buffers(sched):
+    # clusters of two pairs sharing B rows: a captured run replayed with new inputs over poisoned
+    # slots, and a dg_run_host call (upload-frontier block order), bit-equal to independent pairs
+    m, n, k, l, tp = 2048, 2048, 512, 1, 4
+    mc = Runner(m, n, k, l, tp, sched, options={dg.OPT_MULTICAST: 1})
+    ref = Runner(m, n, k, l, tp, sched, options={dg.OPT_MULTICAST: 0})
+    assert mc.plan.info()["multicast"] == 1
+    a, b, c = host_inputs(m, n, k, l, seed=520 + sched)
+    A, B = to_dev(a), to_dev(b)
+    D = torch.empty((l, m, n), dtype=torch.bfloat16, device="cuda")
+    mc.run(A, B, None, D)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        mc.plan.run(A, B, None, D, mc.ws, torch.cuda.current_stream(), mc.copy)
+    info = mc.plan.info()
+    for i in range(2):
+        a2, b2, _ = host_inputs(m, n, k, l, seed=530 + 7 * i + sched)
+        A.copy_(to_dev(a2)); B.copy_(to_dev(b2))
+        n_slots = tp * (tp - 1) * l
+        mc.ws[info["off_slots"]:info["off_slots"] + info["slot_bytes"] * n_slots].view(torch.int16).fill_(0x7FC0)
+        D.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert mc.plan.check(mc.ws, torch.cuda.current_stream(), raise_on_error=False) == dg.OK
+        want, _ = ref.run(A, B, None)
+        assert torch.equal(D.view(torch.int16), want.view(torch.int16)), i
+    del g
+    A_h, B_h = A.cpu().pin_memory(), B.cpu().pin_memory()
+    D_h = torch.empty((l, m, n), dtype=torch.bfloat16).pin_memory()
+    A_d, B_d = torch.full_like(A, float("nan")), torch.full_like(B, float("nan"))
+    D_d = torch.full_like(D, float("nan"))
+    mc.plan.run_host(A_h, B_h, None, None, D_h, A_d, B_d, None, D_d, mc.ws, mc.main, mc.copy)
+    assert mc.plan.check(mc.ws, mc.main, raise_on_error=False) == dg.OK
+    want, _ = ref.run(A, B, None)
+    assert torch.equal(D_h.view(torch.int16), want.cpu().view(torch.int16))
