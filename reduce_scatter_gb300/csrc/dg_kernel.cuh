@@ -1,8 +1,10 @@
 // dg_kernel.cuh -- persistent tcgen05 GEMM with shard-rotation tile order,
 // flag-gated TMA producer and rotating-partial (RotatingC) epilogue, sm_103a.
 //
-// One CTA per SM, 192 threads; with CG = 2 the CTAs of a cluster pair share
-// each 256 x 256 tile (the even CTA issues the MMAs for both SMs):
+// One CTA per SM, 192 threads; with CG = 2 the two CTAs of a pair share each
+// 256 x 256 tile (the even CTA issues the MMAs for both SMs), and with
+// multicast two pairs form a cluster of four that take vertically adjacent
+// tiles, each CTA loading half of its B rows for both pairs:
 //   warp 0      TMA producer: for each tile, waits (acquire, bounded) on the
 //               ready flag of the shard chunk the tile reads (and, in runs that
 //               upload their inputs, on the flag of the upload unit holding
@@ -26,9 +28,10 @@
 // Ordering across proxies:
 //   copy engine -> shard data, then stream write of the ready flag;
 //   producer: ld.acquire.gpu(flag) -> fence.proxy.async.global -> TMA loads.
-//   RS epilogue: partial stores -> fence (gpu) -> named barrier ->
-//   st.release.gpu(tile flag); the next step's epilogue acquires the flag and
-//   reads the partial with L1-bypassing loads.
+//   RS epilogue: partial stores (or TMA reductions into it) complete ->
+//   fence.proxy.async.global / fence (gpu) -> named barrier or warp sync ->
+//   st.release.gpu(tile flag); the next step's epilogue acquires the flag
+//   and reads the partial by TMA (or L1-bypassing loads).
 //
 // Every wait is bounded: flag waits by a timeout (on expiry the kernel records
 // DG timeout in the workspace status word and carries on with whatever the
@@ -77,6 +80,11 @@ constexpr int WROWS = ROWS_PER_CTA / EPI_WARPS;   // 32 rows per warp
 constexpr uint32_t WBUF = WROWS * XCOLS * 4;      // 4 KB: one fp32 box
 constexpr int WSLOTS = 4;                         // slots per warp (64 KB in all)
 constexpr int WPRE = 3;                           // source loads issued ahead
+//   EPI = 3 (staged stores): as 1 without source staging, for plans that
+//           read no source; one more operand stage.
+//   EPI = 4 (per-warp staged, two slots): as 2 with two slots per warp and one
+//           load ahead, for RS plans whose middle steps load nothing (TMA
+//           reductions); one more operand stage.
 
 // Tile configuration per CTA group.
 //   CG = 1: one SM, tile 128 x 256, tcgen05.mma.cta_group::1 (M=128, N=256).
