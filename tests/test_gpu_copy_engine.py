@@ -1,6 +1,6 @@
 """The shard transfers rely on two-dimensional device-to-device copies
 running on a copy engine: they must progress while a kernel occupies every
-SM.  Checked with a small probe program (tests/probes/copy_engine_probe.cu)
+SM.  Checked with a small probe program (tests/fixtures/copy_engine_probe.cu)
 built with nvcc; the one-dimensional form is reported, not asserted (on
 GB300 it runs as a copy kernel on SMs and waits for the SMs to free up)."""
 
@@ -19,7 +19,7 @@ def test_two_dimensional_copies_progress_beside_a_full_sm_kernel(tmp_path):
     nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
     exe = str(tmp_path / "copy_engine_probe")
     subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O2", "-o", exe,
-                    os.path.join(HERE, "probes", "copy_engine_probe.cu")], check=True)
+                    os.path.join(HERE, "fixtures", "copy_engine_probe.cu")], check=True)
     out = subprocess.run([exe], check=True, capture_output=True, text=True, timeout=120).stdout
     res = dict(line.split() for line in out.strip().splitlines())
     print(res)
