@@ -229,7 +229,7 @@ enum dg_option {
                                  a power of two the partial takes two roundings per step.
                                  0 = load, fmaf, store.  -1 (default) = 1 where it gives the
                                  same bits as 0 (alpha' a power of two or zero, no bias), else 0 */
-  DG_OPT_MULTICAST = 20       /* 256 x 256 pair tiles: 1 = clusters of two CTA pairs that take
+  DG_OPT_MULTICAST = 20       /* AG plans with 256 x 256 pair tiles: 1 = clusters of two CTA pairs that take
                                  vertically adjacent tiles and share their B rows, each CTA
                                  loading half of its B rows for both pairs (TMA multicast), a
                                  quarter less operand traffic from L2 into shared memory; where

@@ -340,10 +340,15 @@ bool wave_sync_on(const dg_plan_s* p) {
 // pairs take tiles 2i and 2i + 1 of the order, so every such pair of tiles
 // must lie in one (step, rank, batch) block and read the same B rows (the
 // grouped raster sweeps even-height groups of tile rows column by column).
+//
+// AG plans only: the two pairs of a cluster run their operand stages in step,
+// so a pair's MMAs depend on the other pair's epilogue having freed its
+// accumulator; an RS epilogue may wait there for a hand-off that the other
+// pair's epilogue still holds.
 bool multicast_ok(dg_plan_s* p, const dg::Geom& g) {
   int& ok = p->mc_ok[g.order == 1 ? 1 : 0];
   if (ok < 0) {
-    ok = p->cg == 2 && g.total_tiles % 2 == 0 && g.tiles_block % 2 == 0;
+    ok = p->cg == 2 && is_ag(p->schedule) && g.total_tiles % 2 == 0 && g.tiles_block % 2 == 0;
     for (int64_t i = 0; ok && i < g.total_tiles / 2; ++i) {
       const dg::Tile a = dg::decode_tile(g, 2 * i), b = dg::decode_tile(g, 2 * i + 1);
       ok = a.s == b.s && a.r == b.r && a.l == b.l && a.b_map == b.b_map && a.b_row == b.b_row &&

@@ -424,8 +424,8 @@ def test_multicast_eligibility(L):
     # tiles 2i and 2i + 1 must share their B rows inside one block
     for sched, shape, want in [(dg.AG_ROTATING_A, (16384, 106496, 16384, 1, 8), 1),
                                (dg.AG_ROTATING_B, (8192, 53248, 8192, 2, 4), 1),
-                               (dg.RS_TILING_A_ROTATING_C, (16384, 8192, 28672, 1, 8), 1),
-                               (dg.RS_TILING_B_ROTATING_C, (8192, 53248, 8192, 2, 4), 1),
+                               (dg.RS_TILING_A_ROTATING_C, (16384, 8192, 28672, 1, 8), 0),   # AG only
+                               (dg.RS_TILING_B_ROTATING_C, (8192, 53248, 8192, 2, 4), 0),
                                (dg.AG_ROTATING_A, (512, 512, 256, 1, 2), 0),      # one tile per block
                                (dg.AG_ROTATING_A, (1536, 512, 256, 1, 2), 0)]:    # three tile rows
         m, n, k, l, tp = shape
