@@ -1,6 +1,7 @@
 """A seeded random sweep over the configuration space against the CPU oracle:
-schedule, TP, tile configuration, epilogue, input type, RS hand-off, batch,
-alpha / beta / scales and ragged shapes (within the shape rules)."""
+schedule, TP, tile configuration, epilogue, middle-step reduction, B
+multicast, input type, RS hand-off, batch, alpha / beta / scales and ragged
+shapes (within the shape rules)."""
 
 import numpy as np
 import pytest
@@ -31,7 +32,9 @@ def _case(i):
     if sched == 3 and (n // tp) % 8:
         n = 8 * tp * max(1, n // (8 * tp))
     cep = sched >= 2 and tp > 1 and (sched == 2 or (n // tp) % 8 == 0) and bool(rng.integers(0, 2))
-    opts = {dg.OPT_CTA_GROUP: int(rng.integers(1, 3)), dg.OPT_EPILOGUE: int(rng.integers(1, 3)) if cep else int(rng.integers(0, 4))}
+    # the reduction may be forced on RS plans only (an AG plan rejects it)
+    opts = {dg.OPT_CTA_GROUP: int(rng.integers(1, 3)), dg.OPT_EPILOGUE: int(rng.integers(0, 5)),
+            dg.OPT_RS_REDUCE: int(rng.integers(-1, 2 if sched >= 2 else 1)), dg.OPT_MULTICAST: int(rng.integers(-1, 2))}
     if cep:
         opts[dg.OPT_RS_CE_PARTIALS] = 1
     alpha = float(rng.choice([1.0, 0.5, -1.25]))
@@ -154,6 +157,24 @@ def test_random_configuration_from_host_buffers(i):
     assert torch.equal(D_h, want.view(torch.int16).cpu()), (sched, tp, m, n, k, l, ta, tb, opts, pinned)
 
 
+def _medium_case(i):
+    rng = np.random.default_rng(6000 + i)
+    sched = int(rng.integers(0, 4))
+    tp = int(rng.choice([2, 4, 8]))
+    m = int(rng.integers(2048 // (8 * tp), 8192 // (8 * tp) + 1)) * 8 * tp
+    n = int(rng.integers(2048 // (8 * tp), 8192 // (8 * tp) + 1)) * 8 * tp
+    k = int(rng.integers(512 // (16 * tp), 4096 // (16 * tp) + 1)) * 16 * tp
+    l = int(rng.integers(1, 3))
+    alpha, beta = float(rng.choice([1.0, 0.5])), float(rng.choice([0.0, 1.0]))
+    opts = {dg.OPT_CTA_GROUP: int(rng.integers(1, 3)), dg.OPT_WAVE_SYNC: int(rng.integers(-1, 2)),
+            dg.OPT_MULTICAST: int(rng.integers(-1, 2)), dg.OPT_EPILOGUE: int(rng.integers(0, 5))}
+    if sched >= 2:
+        opts[dg.OPT_RS_REDUCE] = int(rng.integers(-1, 2))
+        if rng.integers(0, 2):
+            opts[dg.OPT_RS_CE_PARTIALS] = 1
+    return rng, sched, tp, m, n, k, l, alpha, beta, opts
+
+
 @pytest.mark.parametrize("i", range(24))
 def test_random_medium_configuration(i):
     # shapes of 2048-8192 rows and columns: many waves of the persistent grid, the
@@ -163,17 +184,7 @@ def test_random_medium_configuration(i):
 
     from oracle import gemm as og
     from reduce_scatter_gb300 import synth
-    rng = np.random.default_rng(6000 + i)
-    sched = int(rng.integers(0, 4))
-    tp = int(rng.choice([2, 4, 8]))
-    m = int(rng.integers(2048 // (8 * tp), 8192 // (8 * tp) + 1)) * 8 * tp
-    n = int(rng.integers(2048 // (8 * tp), 8192 // (8 * tp) + 1)) * 8 * tp
-    k = int(rng.integers(512 // (16 * tp), 4096 // (16 * tp) + 1)) * 16 * tp
-    l = int(rng.integers(1, 3))
-    alpha, beta = float(rng.choice([1.0, 0.5])), float(rng.choice([0.0, 1.0]))
-    opts = {dg.OPT_CTA_GROUP: int(rng.integers(1, 3)), dg.OPT_WAVE_SYNC: int(rng.integers(-1, 2))}
-    if sched >= 2 and rng.integers(0, 2):
-        opts[dg.OPT_RS_CE_PARTIALS] = 1
+    rng, sched, tp, m, n, k, l, alpha, beta, opts = _medium_case(i)
     seed, dist = 100 + i, ("normal", 0.0, 1.0)
     A = synth.tensor_bits_torch(seed, synth.STREAM_A, (l, m, k), dist, device="cuda").view(torch.bfloat16)
     B = synth.tensor_bits_torch(seed, synth.STREAM_B, (l, n, k), dist, device="cuda").view(torch.bfloat16)

@@ -99,7 +99,7 @@ def test_serial_baseline_unaffected_by_ce_option(sched):
 
 
 @pytest.mark.parametrize("sched", RS, ids=lambda s: dg.SCHEDULE_NAMES[s])
-@pytest.mark.parametrize("epi", [0, 1, 2])
+@pytest.mark.parametrize("epi", [0, 1, 2, 3, 4])
 def test_ce_handoff_direct_paths_and_fp8_out(sched, epi):
     # tiles that leave the staged path (fp8 D at the last step; every tile with EPILOGUE=0 set
     # after the hand-off option) read the partial from the receive buffer and write the send buffer
