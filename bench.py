@@ -87,8 +87,9 @@ def measured_peaks():
 
 
 def kernel_source_hash() -> str:
+    # the kernel and the host code that picks its variant and options
     h = hashlib.sha256()
-    for name in ("dg_kernel.cuh", "dg_geom.h"):
+    for name in ("dg_kernel.cuh", "dg_geom.h", "dg.cu"):
         with open(os.path.join(ROOT, "reduce_scatter_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

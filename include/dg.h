@@ -157,8 +157,12 @@ enum dg_option {
                                  (default for the other RS plans whose alpha * scale_a * scale_b
                                  is a power of two, where the middle steps load nothing,
                                  DG_OPT_RS_REDUCE) */
-  DG_OPT_L2_HINT = 8,         /* L2 eviction policy of the operand loads: bits 0-1 for A,
-                                 bits 2-3 for B; 0 = none, 1 = evict first, 2 = evict last */
+  DG_OPT_L2_HINT = 8,         /* L2 eviction policies of the kernel's TMA traffic: bits 0-1
+                                 for the A loads, bits 2-3 for the B loads, bits 4-5 for the
+                                 epilogue's (C / partial loads, partial / D stores and
+                                 reductions); each 0 = none, 1 = evict first, 2 = evict last.
+                                 Default 16 (the epilogue's traffic evict-first) on RS plans
+                                 with bf16 operands, 0 otherwise */
   DG_OPT_RS_CE_PARTIALS = 10, /* RS plans with tp > 1, before the first run: 1 = hand the
                                  rotating partial from rank to rank by copy-engine transfers
                                  (each rank writes a send buffer; the copy streams wait on

@@ -11,8 +11,8 @@ the pages' benchmarks, as synthetic inputs.
   (K split 8 x 3584); A N(0,1), B N(0,0.02).
 * ``ag_b_tp4_batched`` / ``rs_b_tp4_batched``: RotatingB / TilingB RotatingC,
   TP=4, 8192 x 53248 x 8192, L=2, alpha=0.5, beta=1, C N(0,1).
-* ``rs_b_tp4_quarter``: rs_b_tp4_batched with N / 4 and L = 1, for profiler
-  captures.
+* ``rs_b_tp4_quarter`` / ``rs_b_tp4_half``: rs_b_tp4_batched with N / 4 (N / 2)
+  and L = 1, for profiler captures.
 * ``ag_a_tp8_pr_small``: ag_a_tp8_pr with M / 2 and N / 8, for profiler
   captures of the headline kernel.
 * ``ag_a_tp8_pr_e4m3`` / ``rs_a_tp8_e4m3``: the TP=8 problems with e4m3
@@ -90,6 +90,10 @@ WORKLOADS = {
         # a quarter of rs_b_tp4_batched's N and one batch: small enough (about 1 GB on the
         # device) for a full profiler capture, same per-tile work
         Workload("rs_b_tp4_quarter", 3, 4, 8192, 13312, 8192, l=1, alpha=0.5, beta=1.0, dist_a=N1,
+                 dist_b=N002, dist_c=N1),
+        # half of its N and one batch (about 2.3 GB on the device): enough column waves per
+        # raster group for the rotating partial's L2 traffic to matter, still capturable
+        Workload("rs_b_tp4_half", 3, 4, 8192, 26624, 8192, l=1, alpha=0.5, beta=1.0, dist_a=N1,
                  dist_b=N002, dist_c=N1),
     ]
 }

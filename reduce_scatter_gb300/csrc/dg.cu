@@ -152,7 +152,7 @@ struct dg_plan_s {
   bool cep = false;  // RS: hand partials on by copy-engine transfers (DG_OPT_RS_CE_PARTIALS)
   size_t off_done = 0, off_send = 0, off_recv = 0;
   int epi = 0;  // epilogue: 0 direct, 1 staged through shared memory with TMA (default: RS, fp8, K >= 16384)
-  uint32_t l2_hint = 0;  // L2 policy of operand loads (DG_OPT_L2_HINT)
+  uint32_t l2_hint = 0;  // L2 policies of the TMA traffic (DG_OPT_L2_HINT)
   int wave_sync = -1;  // DG_OPT_WAVE_SYNC: -1 auto, 0 off, 1 on
   int copy_pace = -1;  // DG_OPT_COPY_PACE: -1 auto, 0 off, 1 on
   int copy_kind = -1;  // DG_OPT_COPY_KIND: -1 auto (AG shards 0, RS hand-off 2), 0 copy engine (2D
@@ -1418,6 +1418,11 @@ int dg_plan_scaled(dg_plan_t* out, int64_t m, int64_t n, int64_t k, int64_t l, i
     p->epi = 2;
   else
     p->epi = exact_red ? 4 : 1;
+  // The RS epilogue streams the rotating partial (read once, written once per
+  // step, far more bytes than L2 holds): with bf16 operands, evict it first,
+  // so that the operand rows stay in L2 across the tiles that share them (fp8
+  // operand tiles are half the bytes; there the policy measured slower).
+  p->l2_hint = !is_ag(schedule) && esz == 2 ? 16u : 0u;
   {
     std::lock_guard<std::mutex> lk(g_ws_mu);
     p->id = g_next_plan_id++;
@@ -1536,8 +1541,8 @@ int dg_set_option(dg_plan_t p, int option, int64_t value) {
       p->wave_sync = (int)value;
       return DG_OK;
     case DG_OPT_L2_HINT:
-      if (value < 0 || value > 15 || (value & 3) == 3 || ((value >> 2) & 3) == 3)
-        return fail(DG_ERR_ARG, "L2 hint: two 2-bit fields (A, B), each 0, 1 or 2");
+      if (value < 0 || value > 63 || (value & 3) == 3 || ((value >> 2) & 3) == 3 || ((value >> 4) & 3) == 3)
+        return fail(DG_ERR_ARG, "L2 hint: three 2-bit fields (A, B, epilogue), each 0, 1 or 2");
       p->l2_hint = (uint32_t)value;
       return DG_OK;
     case DG_OPT_EPILOGUE:

@@ -143,8 +143,9 @@ struct KParams {
   uint32_t wait_flags;  // AG: 1 = wait on chunk flags
   int32_t n_maps;       // tensor maps in use (each of tmA / tmB)
   uint32_t idesc;       // tcgen05 instruction descriptor (operand formats, M, N)
-  uint32_t l2_hint;     // L2 policy of operand loads: bits 0-1 A, bits 2-3 B
-                        // (0 none, 1 evict-first, 2 evict-last)
+  uint32_t l2_hint;     // L2 policies: bits 0-1 A loads, bits 2-3 B loads, bits 4-5 the
+                        // epilogue's TMA traffic (source loads, partial / D stores and
+                        // reductions); each 0 none, 1 evict-first, 2 evict-last
   uint32_t wave_sync;   // producers start tile i only after every CTA issued tile i-1
   uint32_t* wave_ctr;   // per-run counter of tiles whose loads are issued (zeroed per run)
   uint32_t* progress;   // AG copy pacing: progress[s] set to 1 once a producer reaches step s, or null
@@ -284,19 +285,52 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(src), "r"(x), "r"(y)
-               : "memory");
+// The epilogue's L2 policy: `use` false leaves the default policy.
+struct EpiPolicy {
+  uint64_t pol;
+  bool use;
+};
+__device__ __forceinline__ EpiPolicy epi_policy(const KParams& p) {
+  const uint32_t kind = (p.l2_hint >> 4) & 3u;
+  return EpiPolicy{kind ? l2_policy(kind) : 0ull, kind != 0};
+}
+// An epilogue TMA load (source chunk into shared memory) under that policy.
+__device__ __forceinline__ void tma_load_2d_epi(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x,
+                                                int32_t y, EpiPolicy ep) {
+  if (ep.use)
+    tma_load_2d_hint(dst, map, bar, x, y, ep.pol);
+  else
+    tma_load_2d(dst, map, bar, x, y);
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y,
+                                             EpiPolicy ep) {
+  if (ep.use)
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y), "l"(ep.pol)
+                 : "memory");
+  else
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
 }
 // Element-wise add of a shared-memory box into global memory (the reduction
 // is performed at the L2; the map's element type, fp32 here, sets the add).
-__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y) {
-  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(src), "r"(x), "r"(y)
-               : "memory");
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y,
+                                                  EpiPolicy ep) {
+  if (ep.use)
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(x), "r"(y), "l"(ep.pol)
+        : "memory");
+  else
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N committed bulk stores still read their shared memory.
@@ -798,14 +832,17 @@ __device__ __forceinline__ void release_partial(const KParams& p, int64_t flag, 
 // beta*C (bf16, at the tile's output position).
 __device__ __forceinline__ void staged_load_src(const KParams& p, const Tile& tl, int64_t row0, int c,
                                                 uint32_t idx, uint32_t sbase, uint32_t bar_xfull,
-                                                const CUtensorMap* xmap, int64_t x_col0, int64_t x_row0) {
+                                                const CUtensorMap* xmap, int64_t x_col0, int64_t x_row0,
+                                                EpiPolicy ep) {
   const uint32_t sb = idx & 1;
   const bool f32 = tl.src == SRC_X;
   mbar_arrive_expect_tx(bar_xfull + 8 * sb, f32 ? XBUF : XBUF / 2);
   if (f32)
-    tma_load_2d(sbase + sb * XBUF, xmap, bar_xfull + 8 * sb, (int32_t)(x_col0 + c * XCOLS), (int32_t)x_row0);
+    tma_load_2d_epi(sbase + sb * XBUF, xmap, bar_xfull + 8 * sb, (int32_t)(x_col0 + c * XCOLS), (int32_t)x_row0,
+                    ep);
   else
-    tma_load_2d(sbase + sb * XBUF, &p.tmC, bar_xfull + 8 * sb, (int32_t)(tl.out_col + c * XCOLS), (int32_t)row0);
+    tma_load_2d_epi(sbase + sb * XBUF, &p.tmC, bar_xfull + 8 * sb, (int32_t)(tl.out_col + c * XCOLS),
+                    (int32_t)row0, ep);
 }
 
 // Upload units whose flags a tile's inputs wait on (runs with host buffers).
@@ -1096,6 +1133,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
     uint32_t pend_val = 0;
     uint32_t up_ok = 0;
     uint32_t it = 0;
+    const EpiPolicy ep = epi_policy(p);
     for (int64_t i = unit; i < TI; i += nunits, ++it) {
       __syncwarp();  // every lane is done with the previous tile's slots before lane 0 reloads them
       const int64_t t = mc ? 2 * i + pq : i;
@@ -1167,8 +1205,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
               bulk_wait_read<(C::WSL >= 3 ? C::WSL - 3 : 0)>();
             const uint32_t sl = (seq + (uint32_t)c) % C::WSL;
             mbar_arrive_expect_tx(wbar + 8 * sl, src_f32 ? WBUF : WBUF / 2);
-            tma_load_2d(wb_addr + sl * WBUF, src_map, wbar + 8 * sl, (int32_t)(src_col0 + c * XCOLS),
-                        (int32_t)src_row0);
+            tma_load_2d_epi(wb_addr + sl * WBUF, src_map, wbar + 8 * sl, (int32_t)(src_col0 + c * XCOLS),
+                            (int32_t)src_row0, ep);
           }
         }
         // No warp blocks while it holds a deferred hand-off: the accumulator
@@ -1262,9 +1300,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           __syncwarp();
           if (lane == 0) {
             if (red)
-              tma_reduce_add_2d(dst_map, wb_addr + sl * WBUF, (int32_t)(dst_col0 + c * XCOLS), (int32_t)dst_row0);
+              tma_reduce_add_2d(dst_map, wb_addr + sl * WBUF, (int32_t)(dst_col0 + c * XCOLS), (int32_t)dst_row0,
+                                ep);
             else
-              tma_store_2d(dst_map, wb_addr + sl * WBUF, (int32_t)(dst_col0 + c * XCOLS), (int32_t)dst_row0);
+              tma_store_2d(dst_map, wb_addr + sl * WBUF, (int32_t)(dst_col0 + c * XCOLS), (int32_t)dst_row0, ep);
           }
         } else if (row_ok) {
           float* xp = nullptr;  // the partial's plain-store address (send buffer or X)
@@ -1280,8 +1319,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           if (lane == 0) {
             bulk_wait_read<1>();
             mbar_arrive_expect_tx(wbar + 8 * sn, src_f32 ? WBUF : WBUF / 2);
-            tma_load_2d(wb_addr + sn * WBUF, src_map, wbar + 8 * sn, (int32_t)(src_col0 + (c + C::WPR) * XCOLS),
-                        (int32_t)src_row0);
+            tma_load_2d_epi(wb_addr + sn * WBUF, src_map, wbar + 8 * sn,
+                            (int32_t)(src_col0 + (c + C::WPR) * XCOLS), (int32_t)src_row0, ep);
           }
           inflight |= 1u << sn;
         }
@@ -1351,6 +1390,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
     uint32_t nstore = 0;  // staged destination chunks stored so far (buffer idx & 1)
     uint32_t up_ok = 0;   // ranks whose uploaded C this thread has seen (thread 0)
     uint32_t it = 0;
+    const EpiPolicy ep = epi_policy(p);
     for (int64_t i = unit; i < TI; i += nunits, ++it) {
       const int64_t t = mc ? 2 * i + pq : i;
       const Tile tl = decode_tile(p.g, t);
@@ -1417,7 +1457,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           // the source needs only the previous step: load it while the MMAs run
           fence_proxy_async_global();
           for (int c = 0; c < nch && c < 2; ++c)
-            staged_load_src(p, tl, row0, c, nload + c, xsrc_addr, bar_xfull, src_map, src_col0, src_row0);
+            staged_load_src(p, tl, row0, c, nload + c, xsrc_addr, bar_xfull, src_map, src_col0, src_row0, ep);
           nsrc = nload + (uint32_t)(nch < 2 ? nch : 2);
         }
         bool go = mbar_wait(p, bar_tfull + 8 * buf, use & 1, 0x400000u | buf);
@@ -1501,11 +1541,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           named_bar_sync(1, EPI_THREADS);  // barrier B: the chunk is complete in shared memory
           if (et == 0) {
             if (red)
-              tma_reduce_add_2d(xdst_map, xdst_addr + db * XBUF, (int32_t)(xd_col0 + c * XCOLS), (int32_t)xd_row0);
+              tma_reduce_add_2d(xdst_map, xdst_addr + db * XBUF, (int32_t)(xd_col0 + c * XCOLS), (int32_t)xd_row0,
+                                ep);
             else if (tl.dst == DST_X)
-              tma_store_2d(xdst_map, xdst_addr + db * XBUF, (int32_t)(xd_col0 + c * XCOLS), (int32_t)xd_row0);
+              tma_store_2d(xdst_map, xdst_addr + db * XBUF, (int32_t)(xd_col0 + c * XCOLS), (int32_t)xd_row0, ep);
             else
-              tma_store_2d(&p.tmD, xdst_addr + db * XBUF, (int32_t)(tl.out_col + c * XCOLS), (int32_t)row0);
+              tma_store_2d(&p.tmD, xdst_addr + db * XBUF, (int32_t)(tl.out_col + c * XCOLS), (int32_t)row0, ep);
             bulk_commit();
           }
           ++nstore;
@@ -1515,7 +1556,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dg_gemm_kernel(const __grid_co
           store_row_chunk(p, tl, grow, tl.out_col + c * XCOLS, ncols, out, xp);
         }
         if (et == 0 && has_src && c + 2 < nch) {
-          staged_load_src(p, tl, row0, c + 2, nload + c + 2, xsrc_addr, bar_xfull, src_map, src_col0, src_row0);
+          staged_load_src(p, tl, row0, c + 2, nload + c + 2, xsrc_addr, bar_xfull, src_map, src_col0, src_row0, ep);
           nsrc = nload + (uint32_t)c + 3;
         }
       }

@@ -438,3 +438,12 @@ def test_multicast_eligibility(L):
         assert p.info()["multicast"] == want, (sched, shape)
     p.set_option(dg.OPT_CTA_GROUP, 1)
     assert p.info()["multicast"] == 0                     # pair tiles only
+
+
+def test_l2_hint_option_rules(L):
+    p = dg.Plan(1024, 2048, 512, 1, 4, 2, 1.0, 0.0)
+    for v in (0, 2, 9, 16, 32, 18, 42):
+        p.set_option(dg.OPT_L2_HINT, v)
+    for v in (-1, 3, 12, 48, 64):
+        with pytest.raises(dg.DGError):
+            p.set_option(dg.OPT_L2_HINT, v)

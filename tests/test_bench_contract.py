@@ -50,7 +50,7 @@ def test_record_traffic_parses_an_ncu_csv(tmp_path, monkeypatch):
     prof.mkdir()
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     (tmp_path / "reduce_scatter_gb300" / "csrc").mkdir(parents=True)
-    for name in ("dg_kernel.cuh", "dg_geom.h"):
+    for name in ("dg_kernel.cuh", "dg_geom.h", "dg.cu"):
         (tmp_path / "reduce_scatter_gb300" / "csrc" / name).write_text(name)
     ent = bench.record_traffic("ag_a_tp8_pr", str(csv), "ncu ...", "note")
     assert ent["dram_bytes_read"] == 56_700_000_000 and ent["dram_bytes_write"] == 3_491_002_624
@@ -58,6 +58,9 @@ def test_record_traffic_parses_an_ncu_csv(tmp_path, monkeypatch):
     assert bench.recorded_traffic("ag_a_tp8_pr") == ent["bytes_per_launch"]
     (tmp_path / "reduce_scatter_gb300" / "csrc" / "dg_geom.h").write_text("changed")
     assert bench.recorded_traffic("ag_a_tp8_pr") is None       # stale once the kernel changes
+    bench.record_traffic("ag_a_tp8_pr", str(csv), "ncu ...", "note")
+    (tmp_path / "reduce_scatter_gb300" / "csrc" / "dg.cu").write_text("changed")
+    assert bench.recorded_traffic("ag_a_tp8_pr") is None       # or the host code that picks its variant
 
 
 def test_parity_check_of_the_timed_sample():

@@ -230,15 +230,18 @@ def test_rs_serial_needs_the_serial_workspace():
     assert rc == dg.ERR_STATE
 
 
-@pytest.mark.parametrize("hint", [2, 6, 9])
+@pytest.mark.parametrize("hint", [2, 6, 9, 16, 32, 18])
 def test_l2_hints_do_not_change_results(hint):
+    # operand policies (bits 0-3) and the epilogue's (bits 4-5, in every staged epilogue)
     m, n, k, l, tp = 1024, 2048, 512, 1, 4
     a, b, c = host_inputs(m, n, k, l, seed=90)
     A, B, C = to_dev(a), to_dev(b), to_dev(c)
     for sched in SCHEDS:
-        ref, _ = Runner(m, n, k, l, tp, sched, 0.5, 1.0).run(A, B, C)
-        D, _ = Runner(m, n, k, l, tp, sched, 0.5, 1.0, options={dg.OPT_L2_HINT: hint}).run(A, B, C)
-        assert torch.equal(D.view(torch.int16), ref.view(torch.int16)), sched
+        for epi in ([None] if hint < 16 else [None, 1, 2, 3, 4]):
+            extra = {} if epi is None else {dg.OPT_EPILOGUE: epi}
+            ref, _ = Runner(m, n, k, l, tp, sched, 0.5, 1.0, options=extra).run(A, B, C)
+            D, _ = Runner(m, n, k, l, tp, sched, 0.5, 1.0, options={dg.OPT_L2_HINT: hint, **extra}).run(A, B, C)
+            assert torch.equal(D.view(torch.int16), ref.view(torch.int16)), (sched, epi)
 
 
 @pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
