@@ -141,18 +141,20 @@ enum dg_option {
   DG_OPT_CTA_GROUP = 6,       /* tile configuration, before the first run: 2 (default) =
                                  256 x 256 tiles on an SM pair (tcgen05 cta_group::2),
                                  1 = 128 x 256 tiles on one SM */
-  DG_OPT_EPILOGUE = 7,        /* epilogue, before the first run (all give the same bits):
+  DG_OPT_EPILOGUE = 7,        /* epilogue, before the first run (all give the same bits, except
+                                 in RS plans whose middle steps reduce with alpha * scale_a *
+                                 scale_b not a power of two, DG_OPT_RS_REDUCE):
                                  1 = source and result chunks staged in shared memory and moved
-                                 by TMA (default for AG plans with fp8 inputs, or with beta != 0
-                                 and K >= 16384, and for RS plans not covered below); 0 = direct
+                                 by TMA (default for AG plans with beta != 0 and fp8 inputs or
+                                 K >= 16384, and for RS plans not covered below); 0 = direct
                                  per-row global accesses (one more operand stage; default for the
                                  other bf16 AG plans with beta != 0); 2 = staged per warp (each
                                  epilogue warp moves its own 32-row boxes, three source loads
                                  ahead, with no barrier between the warps; default for RS plans
                                  where at least half the steps load a source: tp <= 2, or
                                  tp <= 4 with beta != 0); 3 = result chunks staged, sources read
-                                 directly (one more operand stage than 1; default for bf16 AG
-                                 plans with beta == 0, which read no source); 4 = staged per warp
+                                 directly (one more operand stage than 1; default for AG plans
+                                 with beta == 0, which read no source); 4 = staged per warp
                                  with two slots, one load ahead, and one more operand stage
                                  (default for the other RS plans whose alpha * scale_a * scale_b
                                  is a power of two, where the middle steps load nothing,
@@ -228,11 +230,12 @@ enum dg_option {
                                  at the L2; alpha' = alpha * scale_a * scale_b, / tp for the
                                  mean) instead of loading it and storing fmaf(alpha', product,
                                  partial); needs a staged epilogue (selects it if the direct one
-                                 is set); no effect with DG_OPT_RS_CE_PARTIALS.  The product is
-                                 then rounded before the add, so with a bias or with alpha' not
-                                 a power of two the partial takes two roundings per step.
-                                 0 = load, fmaf, store.  -1 (default) = 1 where it gives the
-                                 same bits as 0 (alpha' a power of two or zero, no bias), else 0 */
+                                 is set); chunks that are not whole and the copy-engine hand-off
+                                 still load, fmaf and store.  The product is rounded before the
+                                 add, so where alpha' is not a power of two (or with a bias) the
+                                 partial takes two roundings per step and the bits differ from
+                                 0's in the last places (and between epilogue variants).
+                                 0 = load, fmaf, store.  -1 (default) = 1 without a bias, else 0 */
   DG_OPT_MULTICAST = 20       /* AG plans with 256 x 256 pair tiles: 1 = clusters of two CTA pairs that take
                                  vertically adjacent tiles and share their B rows, each CTA
                                  loading half of its B rows for both pairs (TMA multicast), a

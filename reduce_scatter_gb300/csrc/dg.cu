@@ -909,6 +909,7 @@ int run_rs_serial(dg_plan_s* p, const Driver& drv, const void* C, void* D, uint8
   p->kser = p->kp;
   p->kser.g = p->gser;
   p->kser.mc = 0;
+  p->kser.rs_reduce = 0;
   p->kser.X = reinterpret_cast<float*>(ws + p->off_serial);
   p->kser.wait_flags = 0;
   std::memset(&p->kser.tmX, 0, sizeof(CUtensorMap));
@@ -1221,13 +1222,13 @@ int run_impl(dg_plan_s* p, const void* A, const void* B, const dg_bf16_t* C, con
   {
     // Middle RS steps may add alpha' * acc into the partial by TMA reduction
     // (a round-to-nearest fp32 add at the L2) instead of loading the partial
-    // and storing fmaf(alpha', acc, partial).  With alpha' a power of two (or
-    // zero) and no bias, alpha' * acc is exact, so both round the same exact
-    // sum once: the same bits.  Automatic only then.
-    int e = 0;
-    const float fr = std::frexp(kp.alpha, &e);
-    const bool exact = kp.alpha == 0.f || fr == 0.5f || fr == -0.5f;
-    const bool want = p->rs_reduce == 1 || (p->rs_reduce < 0 && exact && bias == nullptr);
+    // and storing fmaf(alpha', acc, partial).  That rounds the product, then
+    // the sum.  With alpha' a power of two (or zero) the product is exact and
+    // both give the same bits; otherwise they differ in the last bits of the
+    // partial.  Automatic without a bias (the product is then all that is
+    // added); chunks that are not whole, the direct epilogue and the
+    // copy-engine hand-off still load, fmaf and store.
+    const bool want = p->rs_reduce == 1 || (p->rs_reduce < 0 && bias == nullptr);
     kp.rs_reduce = want && p->epi != 0 && !is_ag(p->schedule) && !p->cep ? 1u : 0u;
   }
   kp.wave_ctr = reinterpret_cast<uint32_t*>(ws + p->off_status + 64);
@@ -1399,18 +1400,19 @@ int dg_plan_scaled(dg_plan_t* out, int64_t m, int64_t n, int64_t k, int64_t l, i
   // (the last step the partial, the first beta * C) take the per-warp staged
   // epilogue, whose loads run further ahead; with fewer such steps the
   // per-CTA one, whose larger boxes store the others' results faster.
-  // bf16 AG plans with beta = 0 read no source at all: staging for the stores
-  // alone leaves room for one more operand stage.  RS plans whose middle steps
-  // add by TMA reduction (alpha * scale_a * scale_b a power of two, so the
-  // reduction is exact) load a source only at the last step and, with beta,
-  // the first: with fewer than half the steps loading, two slots per warp and
-  // one more operand stage (the per-CTA staging where the reduction is off).
+  // AG plans with beta = 0 read no source at all: staging for the stores alone
+  // leaves room for one more operand stage.  RS plans, whose middle steps add
+  // by TMA reduction, load a source only at the last step and, with beta, the
+  // first: with fewer than half the steps loading, two slots per warp and one
+  // more operand stage where alpha * scale_a * scale_b is a power of two, the
+  // per-CTA staging otherwise (measured faster on the fp8 plans, whose scales
+  // rarely multiply to a power of two).
   const float a_eff = alpha * scale_a * scale_b;
   int a_exp = 0;
   const float a_fr = std::frexp(a_eff, &a_exp);
   const bool exact_red = a_eff == 0.f || a_fr == 0.5f || a_fr == -0.5f;
   const int loading = 1 + (beta != 0.f ? 1 : 0);
-  if (is_ag(schedule) && esz == 2 && beta == 0.f)
+  if (is_ag(schedule) && beta == 0.f)
     p->epi = 3;
   else if (is_ag(schedule))
     p->epi = (esz == 1 || k >= 16384) ? 1 : 0;

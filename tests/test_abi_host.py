@@ -447,3 +447,13 @@ def test_l2_hint_option_rules(L):
     for v in (-1, 3, 12, 48, 64):
         with pytest.raises(dg.DGError):
             p.set_option(dg.OPT_L2_HINT, v)
+
+
+def test_ag_epilogue_defaults(L):
+    # AG with beta == 0 reads no source: stores-only staging, bf16 and fp8 alike
+    assert dg.Plan(1024, 1024, 1024, 1, 4, dg.AG_ROTATING_A).info()["epilogue"] == 3
+    assert dg.Plan(1024, 1024, 1024, 1, 4, dg.AG_ROTATING_A, 1.0, 0.0, dg.TYPE_E4M3, dg.TYPE_E4M3).info()["epilogue"] == 3
+    # with a source: staged for fp8 or long K, direct otherwise
+    assert dg.Plan(1024, 1024, 1024, 1, 4, dg.AG_ROTATING_B, 1.0, 1.0, dg.TYPE_E4M3, dg.TYPE_E5M2).info()["epilogue"] == 1
+    assert dg.Plan(1024, 1024, 16384, 1, 4, dg.AG_ROTATING_A, 1.0, 1.0).info()["epilogue"] == 1
+    assert dg.Plan(1024, 1024, 1024, 1, 4, dg.AG_ROTATING_A, 1.0, 1.0).info()["epilogue"] == 0

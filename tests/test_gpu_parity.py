@@ -340,8 +340,9 @@ def test_one_row_and_eight_column_shards(sched, cg):
 @pytest.mark.parametrize("sched", SCHEDS, ids=lambda s: dg.SCHEDULE_NAMES[s])
 def test_per_warp_epilogue_same_bits_as_staged(sched, cg):
     # the per-warp and the stores-only epilogues compute every element the same way (one fmaf of
-    # the accumulator and its source, the same hand-off order), so D matches the per-CTA staged
-    # epilogue bit for bit, on full and ragged tiles, with and without C
+    # the accumulator and its source, or with alpha a power of two its exact equivalent by
+    # reduction, the same hand-off order), so D matches the per-CTA staged epilogue bit for bit,
+    # on full and ragged tiles, with and without C
     for m, n, k, l in [(1024, 2048, 512, 2), (392, 776, 320, 2), (1000, 1096, 256, 1)]:
         for tp in (1, 4):
             if not _shape_ok(sched, m, n, k, tp):
@@ -401,6 +402,36 @@ def test_rs_reduction_same_bits_when_alpha_is_a_power_of_two(sched, epi):
                     out[red], _ = r.run(A, B, C if beta else None)
                 for red in (1, -1):
                     assert torch.equal(out[0].view(torch.int16), out[red].view(torch.int16)), (m, tp, alpha, red)
+
+
+@pytest.mark.parametrize("sched", [dg.RS_TILING_A_ROTATING_C, dg.RS_TILING_B_ROTATING_C],
+                         ids=lambda s: dg.SCHEDULE_NAMES[s])
+def test_rs_reduction_by_default_with_alpha_not_a_power_of_two(sched):
+    # without a bias the middle steps reduce by default whatever alpha' is: the product is
+    # rounded, then added (two roundings); the staged epilogues agree bit for bit on whole
+    # tiles, and every variant, the one-rounding path (RS_REDUCE=0) and the copy-engine
+    # hand-off included, stays within tolerance of the oracle
+    for m, n, k, l in [(1024, 2048, 1024, 2), (392, 776, 320, 2)]:
+        whole = m == 1024
+        for tp in (4, 8):
+            if not _shape_ok(sched, m, n, k, tp):
+                continue
+            a, b, c = host_inputs(m, n, k, l, seed=98 + tp + 10 * sched)
+            A, B, C = to_dev(a), to_dev(b), to_dev(c)
+            for alpha, beta in [(0.75, 1.0), (-1.3, 0.0)]:
+                want = oracle_full(a, b, c, alpha, beta)
+                ref, _ = Runner(m, n, k, l, tp, sched, alpha, beta, options={dg.OPT_EPILOGUE: 1}).run(
+                    A, B, C if beta else None)
+                assert rel_err(ref, want) <= TOL
+                variants = [{dg.OPT_EPILOGUE: e} for e in (0, 2, 3, 4)] + [{dg.OPT_CTA_GROUP: 1},
+                                                                           {dg.OPT_RS_REDUCE: 0}]
+                if sched == dg.RS_TILING_A_ROTATING_C or (n // tp) % 8 == 0:
+                    variants += [{dg.OPT_RS_CE_PARTIALS: 1}]
+                for opts in variants:
+                    D, _ = Runner(m, n, k, l, tp, sched, alpha, beta, options=opts).run(A, B, C if beta else None)
+                    assert rel_err(D, want) <= TOL, (m, tp, alpha, opts)
+                    if whole and opts.get(dg.OPT_EPILOGUE) in (2, 4):
+                        assert torch.equal(D.view(torch.int16), ref.view(torch.int16)), (m, tp, alpha, opts)
 
 
 @pytest.mark.parametrize("sched", [dg.AG_ROTATING_A, dg.AG_ROTATING_B], ids=lambda s: dg.SCHEDULE_NAMES[s])
