@@ -391,8 +391,8 @@ def test_tile_order_simulator_raster_groups(L, sched, group_m):
 
 
 def test_rs_reduce_and_epilogue_option_rules(L):
-    assert dg.Plan(1024, 1024, 1024, 1, 8, dg.RS_TILING_A_ROTATING_C).info()["epilogue"] == 4   # reduction exact
-    assert dg.Plan(1024, 1024, 1024, 1, 8, dg.RS_TILING_A_ROTATING_C, 0.75).info()["epilogue"] == 1  # it is not
+    assert dg.Plan(1024, 1024, 1024, 1, 8, dg.RS_TILING_A_ROTATING_C).info()["epilogue"] == 4   # alpha' = 2^0
+    assert dg.Plan(1024, 1024, 1024, 1, 8, dg.RS_TILING_A_ROTATING_C, 0.75).info()["epilogue"] == 1  # not 2^e
     p = dg.Plan(1024, 1024, 1024, 1, 8, dg.RS_TILING_A_ROTATING_C)
     p.set_option(dg.OPT_EPILOGUE, 1)
     flags_staged = p.info()["n_flags"]

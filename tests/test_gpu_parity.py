@@ -387,7 +387,8 @@ def test_rs_reduction_into_the_partial_vs_oracle(sched, cg, epi):
                          ids=lambda s: dg.SCHEDULE_NAMES[s])
 def test_rs_reduction_same_bits_when_alpha_is_a_power_of_two(sched, epi):
     # alpha' * acc is exact for alpha' = 2^e, so the L2's round-to-nearest add of it to the
-    # partial gives the bits of fmaf(alpha', acc, partial): the automatic choice relies on it
+    # partial gives the bits of fmaf(alpha', acc, partial): for such alpha' the reduction, on by
+    # default, changes no bit
     for m, n, k, l in [(1024, 2048, 1024, 2), (392, 776, 320, 2)]:
         for tp in (4, 8):
             if not _shape_ok(sched, m, n, k, tp):
